@@ -1,0 +1,423 @@
+"""Benchmark: one CSA2 decode step over decoder layers 20..39 (1 Full index pass, 4 Reindex
+passes, 15 Reuse inherits, 20 sparse-attention calls) for a batch of 32 independent requests
+at 131,072 visible positions, FP4 main KV + FP4 indexer K, one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hsa|reference]
+
+Prints one JSON line (rank 0). `value` is decode steps/s summed over ranks (weak scaling: each
+rank runs its own batch of 32 requests; no collective on the data path). The step runs through
+hsa_schedule_step, captured once in a CUDA graph and replayed. Inputs are resident in HBM and
+larger than L2 (the 1.49 GB cache). `e2e` repeats the measurement through the same public call,
+with the step's per-layer inputs copied from pinned host memory and the outputs copied back
+inside the timed region. `--impl reference` times the fp64 CPU oracle on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from hierarchical_sparse_attention_index_gb300 import synth  # noqa: E402
+
+METRIC = "decode steps/s (20 decoder layers) at 128K ctx, batch 32"
+CFG = synth.CFG1
+LAYERS = list(range(20, 40))
+MODES_BY_LAYER = {20: 0, 24: 1, 28: 1, 32: 1, 36: 1}     # Full / Reindex; the rest Reuse
+INDEX_LAYERS = [20, 24, 28, 32, 36]
+
+# algorithmic bytes (per request, per step)
+SCAN_B = 68                                   # indexer-K entry
+ATTN_B_PER_REQ = 512 * 288 + 128 * 512 + 64 * 512 * 2 + 64 * 512 * 4    # 409,600
+ATTN_FLOP_PER_REQ = 2 * 2 * 64 * 640 * 512                                # QK + PV
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p.get("bf16_tflops"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (200 ms period)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def build_inputs(H, torch, seed, rank):
+    """Device-resident step inputs for one rank (its own batch of 32 requests)."""
+    B, T, nq = CFG.batch, CFG.T, CFG.nq
+    s = seed + 7919 * rank
+    cache = H.Cache(B, T, 1)
+    W = torch.from_numpy(synth.w_idx_bf16(s, 20).view(np.int16)).cuda().view(torch.bfloat16)
+    for b in range(B):
+        lat = synth.latents_bf16(s, 20, b, T)
+        x = torch.from_numpy(lat.view(np.int16)).pin_memory().cuda(non_blocking=True).view(torch.bfloat16)
+        sub = H.Cache(1, T, 1, tensors=(cache.kv_q[b:b + 1], cache.kv_s[b:b + 1], cache.ik_q[b:b + 1],
+                                        cache.ik_s[b:b + 1]))
+        H.hsa_cache_write_compress(sub, x[None], None, W, T, None)
+    torch.cuda.synchronize()
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0, ("cache write", code, flags)
+
+    host = {}
+    for l in INDEX_LAYERS:
+        host[("qi", l)] = synth.index_q_bf16(s, l, B, nq)
+        host[("wi", l)] = synth.index_w(s, l, B, nq)
+    for l in LAYERS:
+        host[("qa", l)] = synth.attn_q_bf16(s, l, B, nq)
+        host[("sw", l)] = synth.swa_e4m3(s, l, B, nq)
+    dev = {}
+    for k, v in host.items():
+        t = torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda()
+        dev[k] = t.view(torch.bfloat16) if v.dtype == np.uint16 else t
+    vis = torch.from_numpy(synth.visibility(B, nq, T)).cuda()
+    outs = [torch.empty(B, nq, 64, 512, device="cuda") for _ in LAYERS]
+    topk = [torch.empty(B, nq, 512, dtype=torch.int32, device="cuda") if l in INDEX_LAYERS else None
+            for l in LAYERS]
+    pool = torch.empty(B, nq, 16384, dtype=torch.int32, device="cuda")
+    ws = H.new_workspace(B, nq, T)
+    modes = [MODES_BY_LAYER.get(l, 2) for l in LAYERS]
+    step = H.StepArgs(modes, [dev.get(("qi", l)) for l in LAYERS], [dev.get(("wi", l)) for l in LAYERS],
+                      [dev[("qa", l)] for l in LAYERS], [dev[("sw", l)] for l in LAYERS], outs, topk, pool,
+                      vis, nq, T, 1.0)
+    return dict(cache=cache, dev=dev, host=host, vis=vis, outs=outs, topk=topk, pool=pool, ws=ws, step=step)
+
+
+def per_kernel_times(H, torch, I, reps=5):
+    """Average duration of each API call of the step, with CUDA events on the launching stream."""
+    st = torch.cuda.current_stream()
+    B, T, nq = CFG.batch, CFG.T, CFG.nq
+    d, ws = I["dev"], I["ws"]
+    acc = {"index_full": [], "index_reindex": [], "sparse_attn_decode": []}
+    for _ in range(reps):
+        latest = None
+        for j, l in enumerate(LAYERS):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            mode = MODES_BY_LAYER.get(l, 2)
+            if mode != 2:
+                e0.record(st)
+                if mode == 0:
+                    H.hsa_index_full(I["cache"], d[("qi", l)], d[("wi", l)], I["vis"], nq, T, I["topk"][j], I["pool"], ws)
+                    acc_key = "index_full"
+                else:
+                    H.hsa_index_reindex(I["cache"], d[("qi", l)], d[("wi", l)], I["vis"], nq, T, I["pool"],
+                                        I["topk"][j], ws)
+                    acc_key = "index_reindex"
+                e1.record(st)
+                acc[acc_key].append((e0, e1))
+                latest = I["topk"][j]
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(st)
+            H.hsa_sparse_attn_decode(I["cache"], d[("qa", l)], latest, d[("sw", l)], I["vis"], nq, T, 1.0,
+                                     I["outs"][j], ws)
+            a1.record(st)
+            acc["sparse_attn_decode"].append((a0, a1))
+    torch.cuda.synchronize()
+    return {k: 1e-3 * statistics.mean(e0.elapsed_time(e1) for e0, e1 in v) for k, v in acc.items()}  # seconds
+
+
+def run_hsa(args):
+    import torch
+    import torch.distributed as dist
+
+    import hierarchical_sparse_attention_index_gb300 as H
+    rank, world, local = env_rank()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    H.load_library()
+    I = build_inputs(H, torch, CFG.seed, rank)
+
+    st = torch.cuda.current_stream()
+    # one eager step (sets up per-device state), then capture the step as a CUDA graph
+    H.hsa_schedule_step(I["cache"], I["step"], I["ws"])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream()
+    s2.wait_stream(st)
+    with torch.cuda.stream(s2):
+        with torch.cuda.graph(g, stream=s2):
+            H.hsa_schedule_step(I["cache"], I["step"], I["ws"], stream=s2)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        g.replay()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(st)
+    barrier()
+    clocks = sampler.stop()
+    t = e0.elapsed_time(e1) * 1e-3
+    code, flags = H.hsa_get_device_status()
+    if code != 0 or flags != 0:
+        raise RuntimeError(f"device status after the timed region: code {code} flags {flags}")
+    tmax = t
+    if world > 1:
+        tt = torch.tensor([t], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        tmax = float(tt.item())
+    value = world * args.steps / tmax
+
+    # per-kernel durations (eager, same work) for the roofline of the dominant kernel
+    kt = per_kernel_times(H, torch, I)
+    hbm_peak, tflops_peak, peak_src = load_peaks()
+    B, T = CFG.batch, CFG.T
+    attn_bytes = B * ATTN_B_PER_REQ
+    attn_calls = len(LAYERS)
+    scan_bytes = B * T * SCAN_B + B * T * 4
+    shares = {"sparse_attn_decode": attn_calls * kt["sparse_attn_decode"], "index_full": kt["index_full"],
+              "index_reindex": 4 * kt["index_reindex"]}
+    dominant = max(shares, key=shares.get)
+    if dominant == "sparse_attn_decode":
+        ach = attn_bytes / kt["sparse_attn_decode"] / 1e9
+    elif dominant == "index_full":
+        ach = scan_bytes / kt["index_full"] / 1e9
+    else:
+        ach = B * 16384 * SCAN_B / kt["index_reindex"] / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
+                "peak_source": peak_src,
+                "per_call_us": {k: round(v * 1e6, 2) for k, v in kt.items()},
+                "step_share": {k: round(v / sum(shares.values()), 3) for k, v in shares.items()}}
+
+    # end to end through the same public call with host buffers (pinned), copies in the timed region
+    hin = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
+           for k, v in I["host"].items()}
+    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in I["outs"]]
+    htopk = [torch.empty(t_.shape, dtype=t_.dtype).pin_memory() if t_ is not None else None for t_ in I["topk"]]
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(o.numel() * o.element_size() for o in hout) + sum(x.numel() * 4 for x in htopk if x is not None)
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for k, v in hin.items():
+            dst = I["dev"][k]
+            (dst.view(torch.int16) if dst.dtype == torch.bfloat16 else dst).copy_(v, non_blocking=True)
+        H.hsa_schedule_step(I["cache"], I["step"], I["ws"])
+        for o, h in zip(I["outs"], hout):
+            h.copy_(o, non_blocking=True)
+        for x, h in zip(I["topk"], htopk):
+            if x is not None:
+                h.copy_(x, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(st)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(st)
+    barrier()
+    te = max(f0.elapsed_time(f1) * 1e-3, 1e-9)
+    e2e = {"value": round(world * e2e_steps / te, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "wall_s": round(time.perf_counter() - t0, 4)}
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * tmax / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp4-e2m1 cache; f16 tensor-core MMA, fp32 accumulate",
+            "data": "synthetic (seeded N(0,1) latents through the m=1 cache writer; bf16 queries)",
+            "config": {"workload": CFG.name, "batch_per_gpu": B, "ctx": T, "nq": CFG.nq,
+                       "layers": "20..39 (1 Full, 4 Reindex, 15 Reuse, 20 attention)",
+                       "parallelism": f"replicas x{world} (requests sharded, no collective)",
+                       "l2": "inputs larger than L2 (1.49 GB FP4 cache per step)",
+                       "step": "hsa_schedule_step captured in one CUDA graph"},
+            "clocks": clocks, "gpu_launches": args.steps * 35,
+            "e2e": e2e, "roofline": roofline}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, sample_requests=2, steps=20)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _threads_used():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(args, sample_requests=2, steps=1):
+    """The fp64 oracle, as it stands, on a bounded sample: `sample_requests` of the 32 requests of
+    the same workload for `steps` decode steps; reported per full batch-32 step."""
+    import oracle as O
+    B, T, nq, s = CFG.batch, CFG.T, CFG.nq, CFG.seed
+    f32 = synth.bf16_bits_to_f32
+    modes = O.layer_modes()
+    W = f32(synth.w_idx_bf16(s, 20))
+    per = []
+    for b in range(sample_requests):
+        lat = synth.latents_bf16(s, 20, b, T)
+        kv_q, kv_s, ik_q, ik_s, _, _ = O.cache_write_compress(f32(lat), None, W, 1)
+        Ki = O.index_k_dequant(ik_q, ik_s)
+        Km = O.main_kv_dequant(kv_q, kv_s)
+        qi = {l: f32(synth.index_q_bf16(s, l, B, nq))[b, 0] for l in INDEX_LAYERS}
+        wi = {l: synth.index_w(s, l, B, nq)[b, 0] for l in INDEX_LAYERS}
+        qa = {l: f32(synth.attn_q_bf16(s, l, B, nq))[b, 0] for l in LAYERS}
+        sw = {l: O.swa_decode(synth.swa_e4m3(s, l, B, nq)[b]) for l in LAYERS}
+        for _ in range(steps):
+            t0 = time.perf_counter()
+            O.decode_step(LAYERS, modes, Ki, Km, qi, wi, qa, sw, T, 0, 1.0)
+            per.append(time.perf_counter() - t0)
+    t_req = statistics.mean(per)
+    return {"value": round(1.0 / (B * t_req), 4), "unit": "steps/s", "cores": _threads_used(), "kind": "oracle",
+            "sample": f"{sample_requests} of {B} requests x {steps} step(s) of the same workload; "
+                      f"{t_req:.3f} s per request-step, scaled to a batch-32 step"}
+
+
+class OracleStepper:
+    """Advances the oracle through the 20-slot schedule one layer slot per call, for one request."""
+
+    def __init__(self, request=0):
+        import oracle as O
+        self.O = O
+        B, T, nq, s = CFG.batch, CFG.T, CFG.nq, CFG.seed
+        f32 = synth.bf16_bits_to_f32
+        self.modes = O.layer_modes()
+        W = f32(synth.w_idx_bf16(s, 20))
+        lat = synth.latents_bf16(s, 20, request, T)
+        kv_q, kv_s, ik_q, ik_s, _, _ = O.cache_write_compress(f32(lat), None, W, 1)
+        self.Ki, self.Km = O.index_k_dequant(ik_q, ik_s), O.main_kv_dequant(kv_q, kv_s)
+        self.qi = {l: f32(synth.index_q_bf16(s, l, B, nq))[request, 0] for l in INDEX_LAYERS}
+        self.wi = {l: synth.index_w(s, l, B, nq)[request, 0] for l in INDEX_LAYERS}
+        self.qa = {l: f32(synth.attn_q_bf16(s, l, B, nq))[request, 0] for l in LAYERS}
+        self.sw = {l: O.swa_decode(synth.swa_e4m3(s, l, B, nq)[request]) for l in LAYERS}
+        self.i, self.topk, self.pool, self.T = 0, None, None, T
+
+    def slot(self):
+        O, l, T = self.O, LAYERS[self.i % len(LAYERS)], self.T
+        if self.modes[l] == "Full":
+            self.topk, self.pool, _, _ = O.index_full(self.qi[l], self.wi[l], self.Ki, T)
+        elif self.modes[l] == "Reindex":
+            self.topk, _ = O.index_reindex(self.qi[l], self.wi[l], self.Ki, self.pool, T)
+        rows = O.attention_rows(self.Km, self.topk, self.sw[l], 0, T)
+        O.sparse_attention(self.qa[l], rows, 1.0)
+        self.i += 1
+
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    # Each timed step is one layer slot of one request (the oracle as it stands), cycling
+    # through the 20-slot schedule; 20 steps make one request-step, scaled to batch 32.
+    B = CFG.batch
+    st = OracleStepper(0)
+    for _ in range(len(LAYERS)):          # one untimed request-step
+        st.slot()
+    st.i = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.slot()
+    t = time.perf_counter() - t0
+    req_steps = args.steps / len(LAYERS)
+    value = req_steps / t / B
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / value, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same seeded workload)",
+            "config": {"workload": CFG.name, "batch_per_gpu": B, "ctx": CFG.T, "nq": CFG.nq,
+                       "layers": "20..39 (1 Full, 4 Reindex, 15 Reuse, 20 attention)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "steps/s", "cores": _threads_used(),
+                             "kind": "oracle",
+                             "sample": f"request 0 of {B}, one layer slot per step over {args.steps} steps "
+                                       f"({req_steps:.2f} request-steps), scaled to a batch-{B} step"},
+            "e2e": {"value": round(value, 4), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["hsa", "reference"], default="hsa")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_hsa(args)
+
+
+if __name__ == "__main__":
+    main()

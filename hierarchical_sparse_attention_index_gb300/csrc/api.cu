@@ -1,0 +1,337 @@
+// C ABI of libhsa (include/hsa.h): argument validation, workspace carve-up, launches and the
+// decode-step schedule. Everything here is host code; it launches kernels only.
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "hsa_common.cuh"
+#include "hsa_internal.h"
+
+namespace hsa {
+
+// Per-device status word (HSA_FLAG_*), written by kernels with atomicOr.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+int g_cc_major[kMaxDevices];
+
+// Device pointer of the status word and the SM count of the current device (set up once per device).
+bool device_info(uint32_t** status, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return false;
+    cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&g_cc_major[dev], cudaDevAttrComputeCapabilityMajor, dev);
+    g_status_ptr[dev] = static_cast<uint32_t*>(ptr);
+  }
+  *status = g_status_ptr[dev];
+  *sms = g_num_sms[dev];
+  return g_cc_major[dev] == 10;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+hsa_status check_cache(const hsa_cache* c) {
+  if (!c || !c->kv_q || !c->kv_s || !c->ik_q || !c->ik_s) return HSA_ERR_INVALID_ARG;
+  if (c->batch < 1 || c->capacity < 8 || (c->capacity & 7)) return HSA_ERR_SHAPE;
+  if (c->capacity > (int64_t)INT32_MAX) return HSA_ERR_SHAPE;
+  if (c->ratio != 1 && c->ratio != 2) return HSA_ERR_INVALID_ARG;
+  if (c->kv_scale_fmt != HSA_SCALE_E8M0 && c->kv_scale_fmt != HSA_SCALE_E4M3) return HSA_ERR_INVALID_ARG;
+  if (!aligned16(c->kv_q) || !aligned16(c->kv_s) || !aligned16(c->ik_q) || !aligned16(c->ik_s)) return HSA_ERR_ALIGN;
+  return HSA_OK;
+}
+
+hsa_status check_query(const hsa_cache* c, int32_t nq, int64_t max_vis) {
+  if (nq < 1 || nq > HSA_MAX_NQ) return HSA_ERR_SHAPE;
+  if (max_vis < 0 || max_vis > c->capacity || max_vis > HSA_MAX_VIS) return HSA_ERR_SHAPE;
+  return HSA_OK;
+}
+
+}  // namespace
+
+bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
+  if (batch < 1 || nq < 1 || nq > HSA_MAX_NQ || max_vis < 0 || max_vis > HSA_MAX_VIS) return false;
+  const int64_t rows = (int64_t)batch * nq;
+  L->rows = (int32_t)rows;
+  L->ld_s = round_up(std::max(max_vis, (int64_t)1), 256);
+  L->ld_b = L->ld_s / 8;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += (bytes + 255) & ~(size_t)255;
+    return at;
+  };
+  // zero-between-calls region first
+  L->zero_begin = 0;
+  L->off_hist_full = take((size_t)rows * 2 * kHistBins * 4);
+  L->off_state_full = take((size_t)rows * 2 * sizeof(SelState));
+  L->off_done_full = take((size_t)batch * 4);
+  L->off_hist_pool = take((size_t)rows * kHistBins * 4);
+  L->off_state_pool = take((size_t)rows * sizeof(SelState));
+  L->off_done_pool = take((size_t)rows * 4);
+  L->zero_end = o;
+  L->off_scores = take((size_t)rows * L->ld_s * 4);
+  L->off_blkmax = take((size_t)rows * L->ld_b * 4);
+  L->off_cand_full = take((size_t)rows * (L->ld_s + L->ld_b) * 4);
+  L->off_sure_full = take((size_t)rows * (kTopK + kCandBlocks) * 4);
+  L->off_pscores = take((size_t)rows * kPool * 4);
+  L->off_cand_pool = take((size_t)rows * kPool * 4);
+  L->off_sure_pool = take((size_t)rows * kTopK * 4);
+  L->attn_bytes = 0;
+  L->off_attn = take(0);
+  L->total = o;
+  return true;
+}
+
+}  // namespace hsa
+
+using namespace hsa;
+
+extern "C" {
+
+int32_t hsa_abi_version(void) { return HSA_ABI_VERSION; }
+
+const char* hsa_status_string(hsa_status s) {
+  switch (s) {
+    case HSA_OK: return "HSA_OK";
+    case HSA_ERR_INVALID_ARG: return "HSA_ERR_INVALID_ARG: a pointer is NULL or an enum/size is invalid";
+    case HSA_ERR_SHAPE: return "HSA_ERR_SHAPE: a size is out of range";
+    case HSA_ERR_ALIGN: return "HSA_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case HSA_ERR_WORKSPACE: return "HSA_ERR_WORKSPACE: workspace missing or too small";
+    case HSA_ERR_CUDA: return "HSA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case HSA_ERR_TIMEOUT: return "HSA_ERR_TIMEOUT: a bounded device wait gave up";
+    case HSA_ERR_UNSUPPORTED: return "HSA_ERR_UNSUPPORTED: needs an sm_100-family GPU (GB300 / sm_103a)";
+  }
+  return "HSA_ERR_UNKNOWN";
+}
+
+size_t hsa_workspace_bytes(int32_t batch, int32_t nq, int64_t max_vis) {
+  WsLayout L;
+  if (!make_ws_layout(batch, nq, max_vis, &L)) return 0;
+  return L.total;
+}
+
+hsa_status hsa_workspace_init(void* ws, size_t ws_bytes, hsa_stream_t stream) {
+  if (!ws) return HSA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
+}
+
+hsa_status hsa_cache_write_compress(const hsa_cache* cache, const void* wkv, const void* wgate, const void* w_idx,
+                                    int64_t n_tokens, const int64_t* start_entry, hsa_stream_t stream) {
+  hsa_status st = check_cache(cache);
+  if (st != HSA_OK) return st;
+  if (!wkv || !w_idx) return HSA_ERR_INVALID_ARG;
+  if ((cache->ratio == 2) != (wgate != nullptr)) return HSA_ERR_INVALID_ARG;
+  if (n_tokens < 0) return HSA_ERR_SHAPE;
+  if (!aligned16(wkv) || !aligned16(w_idx) || (wgate && !aligned16(wgate))) return HSA_ERR_ALIGN;
+  uint32_t* status;
+  int sms;
+  if (!device_info(&status, &sms)) return HSA_ERR_UNSUPPORTED;
+  WriteParams p;
+  memset(&p, 0, sizeof(p));
+  p.batch = cache->batch;
+  p.ratio = cache->ratio;
+  p.scale_fmt = cache->kv_scale_fmt;
+  p.cap = cache->capacity;
+  p.n_tokens = n_tokens;
+  p.n_entries = n_tokens / cache->ratio;
+  p.wkv = static_cast<const uint16_t*>(wkv);
+  p.wgate = static_cast<const uint16_t*>(wgate);
+  p.w_idx = static_cast<const uint16_t*>(w_idx);
+  p.start_entry = start_entry;
+  p.kv_q = cache->kv_q;
+  p.kv_s = cache->kv_s;
+  p.ik_q = cache->ik_q;
+  p.ik_s = cache->ik_s;
+  p.status = status;
+  if (p.n_entries == 0) return HSA_OK;
+  return launch_cache_write(p, (cudaStream_t)stream) == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
+}
+
+static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const void* q, const float* w,
+                               const int32_t* vis, int32_t nq, int64_t max_vis, const int32_t* pool,
+                               int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
+                               hsa_stream_t stream) {
+  hsa_status st = check_cache(cache);
+  if (st != HSA_OK) return st;
+  st = check_query(cache, nq, max_vis);
+  if (st != HSA_OK) return st;
+  if (!q || !w || !vis || !topk_out || (pool_mode ? !pool : !pool_out)) return HSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(topk_out) || (pool_out && !aligned16(pool_out))) return HSA_ERR_ALIGN;
+  WsLayout L;
+  if (!make_ws_layout(cache->batch, nq, max_vis, &L)) return HSA_ERR_SHAPE;
+  if (!ws || ws_bytes < L.total) return HSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return HSA_ERR_ALIGN;
+  uint32_t* status;
+  int sms;
+  if (!device_info(&status, &sms)) return HSA_ERR_UNSUPPORTED;
+  uint8_t* W = static_cast<uint8_t*>(ws);
+  const cudaStream_t s = (cudaStream_t)stream;
+
+  ScanParams sp;
+  memset(&sp, 0, sizeof(sp));
+  sp.pool_mode = pool_mode ? 1 : 0;
+  sp.batch = cache->batch;
+  sp.nq = nq;
+  sp.cap = cache->capacity;
+  sp.ik_q = cache->ik_q;
+  sp.ik_s = cache->ik_s;
+  sp.q = static_cast<const uint16_t*>(q);
+  sp.w = w;
+  sp.vis = vis;
+  sp.pool = pool;
+  sp.status = status;
+  SelectParams se;
+  memset(&se, 0, sizeof(se));
+  se.pool_mode = sp.pool_mode;
+  se.batch = cache->batch;
+  se.nq = nq;
+  se.max_vis = max_vis;
+  se.vis = vis;
+  se.pool = pool;
+  se.topk_out = topk_out;
+  se.pool_out = pool_out;
+  se.status = status;
+  if (!pool_mode) {
+    sp.n_seg = cache->batch;
+    sp.chunks_per_seg = (int32_t)((std::max(max_vis, (int64_t)1) + 255) / 256);
+    sp.scores = reinterpret_cast<float*>(W + L.off_scores);
+    sp.ld_s = L.ld_s;
+    sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
+    sp.ld_b = L.ld_b;
+    sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_full);
+    sp.state = reinterpret_cast<SelState*>(W + L.off_state_full);
+    sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_full);
+    se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_full);
+    se.ld_cand = L.ld_s + L.ld_b;
+    se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_full);
+    se.ld_sure = kTopK + kCandBlocks;
+  } else {
+    sp.n_seg = L.rows;
+    sp.chunks_per_seg = kPool / 256;
+    sp.scores = reinterpret_cast<float*>(W + L.off_pscores);
+    sp.ld_s = kPool;
+    sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_pool);
+    sp.state = reinterpret_cast<SelState*>(W + L.off_state_pool);
+    sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_pool);
+    se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_pool);
+    se.ld_cand = kPool;
+    se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_pool);
+    se.ld_sure = kTopK;
+  }
+  sp.total_items = sp.n_seg * sp.chunks_per_seg;
+  se.scores = sp.scores;
+  se.ld_s = sp.ld_s;
+  se.blkmax = sp.blkmax;
+  se.ld_b = sp.ld_b;
+  se.hist = sp.hist;
+  se.state = sp.state;
+  if (launch_index_scan(sp, sms, s) != cudaSuccess) return HSA_ERR_CUDA;
+  if (launch_select(se, s) != cudaSuccess) return HSA_ERR_CUDA;
+  return HSA_OK;
+}
+
+hsa_status hsa_index_full(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,
+                          int64_t max_vis, int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
+                          hsa_stream_t stream) {
+  return index_common(false, cache, q, w, vis, nq, max_vis, nullptr, topk_out, pool_out, ws, ws_bytes, stream);
+}
+
+hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,
+                             int64_t max_vis, const int32_t* pool, int32_t* topk_out, void* ws, size_t ws_bytes,
+                             hsa_stream_t stream) {
+  return index_common(true, cache, q, w, vis, nq, max_vis, pool, topk_out, nullptr, ws, ws_bytes, stream);
+}
+
+hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const int32_t* topk, const uint8_t* swa,
+                                  const int32_t* vis, int32_t nq, int64_t max_vis, float sm_scale, float* out,
+                                  void* ws, size_t ws_bytes, hsa_stream_t stream) {
+  hsa_status st = check_cache(cache);
+  if (st != HSA_OK) return st;
+  st = check_query(cache, nq, max_vis);
+  if (st != HSA_OK) return st;
+  if (!q || !topk || !swa || !vis || !out) return HSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(swa) || !aligned16(out)) return HSA_ERR_ALIGN;
+  (void)ws;
+  (void)ws_bytes;
+  uint32_t* status;
+  int sms;
+  if (!device_info(&status, &sms)) return HSA_ERR_UNSUPPORTED;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.batch = cache->batch;
+  p.nq = nq;
+  p.cap = cache->capacity;
+  p.scale_fmt = cache->kv_scale_fmt;
+  p.kv_q = cache->kv_q;
+  p.kv_s = cache->kv_s;
+  p.q = static_cast<const uint16_t*>(q);
+  p.topk = topk;
+  p.swa = swa;
+  p.vis = vis;
+  p.sm_scale = sm_scale;
+  p.out = out;
+  p.status = status;
+  return launch_attention(p, (cudaStream_t)stream) == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
+}
+
+hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, void* ws, size_t ws_bytes,
+                             hsa_stream_t stream) {
+  hsa_status st = check_cache(cache);
+  if (st != HSA_OK) return st;
+  if (!a || !a->modes || !a->q_attn || !a->swa || !a->out || !a->topk || !a->pool || !a->vis)
+    return HSA_ERR_INVALID_ARG;
+  if (a->n_layers < 1) return HSA_ERR_SHAPE;
+  if (a->modes[0] != HSA_MODE_FULL) return HSA_ERR_INVALID_ARG;
+  for (int l = 0; l < a->n_layers; ++l) {
+    const int m = a->modes[l];
+    if (m != HSA_MODE_FULL && m != HSA_MODE_REINDEX && m != HSA_MODE_REUSE) return HSA_ERR_INVALID_ARG;
+    if (m != HSA_MODE_REUSE && (!a->q_idx || !a->w_idx || !a->q_idx[l] || !a->w_idx[l] || !a->topk[l]))
+      return HSA_ERR_INVALID_ARG;
+    if (!a->q_attn[l] || !a->swa[l] || !a->out[l]) return HSA_ERR_INVALID_ARG;
+  }
+  const int32_t* latest = nullptr;
+  for (int l = 0; l < a->n_layers; ++l) {
+    const int m = a->modes[l];
+    if (m == HSA_MODE_FULL) {
+      st = hsa_index_full(cache, a->q_idx[l], a->w_idx[l], a->vis, a->nq, a->max_vis, a->topk[l], a->pool, ws,
+                          ws_bytes, stream);
+      latest = a->topk[l];
+    } else if (m == HSA_MODE_REINDEX) {
+      st = hsa_index_reindex(cache, a->q_idx[l], a->w_idx[l], a->vis, a->nq, a->max_vis, a->pool, a->topk[l], ws,
+                             ws_bytes, stream);
+      latest = a->topk[l];
+    }
+    if (st != HSA_OK) return st;
+    st = hsa_sparse_attn_decode(cache, a->q_attn[l], latest, a->swa[l], a->vis, a->nq, a->max_vis, a->sm_scale,
+                                a->out[l], ws, ws_bytes, stream);
+    if (st != HSA_OK) return st;
+  }
+  return HSA_OK;
+}
+
+hsa_status hsa_get_device_status(hsa_stream_t stream, uint32_t* flags) {
+  if (!flags) return HSA_ERR_INVALID_ARG;
+  uint32_t* status;
+  int sms;
+  device_info(&status, &sms);
+  if (!status) return HSA_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return HSA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return HSA_ERR_CUDA;
+  if (cudaMemset(status, 0, 4) != cudaSuccess) return HSA_ERR_CUDA;
+  *flags = v;
+  return (v & HSA_FLAG_TIMEOUT) ? HSA_ERR_TIMEOUT : HSA_OK;
+}
+
+}  // extern "C"

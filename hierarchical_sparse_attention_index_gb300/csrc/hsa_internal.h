@@ -1,0 +1,122 @@
+// Host-side declarations shared by the libhsa translation units: workspace layout, kernel
+// parameter blocks and launchers. Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/hsa.h"
+
+namespace hsa {
+
+// Per selection row (one top-k over one array) state kept in the workspace. All counters are
+// zero between calls.
+struct SelState {
+  int32_t thr_bin;   // threshold histogram bin; -1 = every valid element is taken
+  int32_t above;     // elements in bins above thr_bin
+  int32_t nvalid;    // valid elements of the row
+  int32_t nsure;     // collect: elements appended to the sure list
+  int32_t ncand;     // collect: elements appended to the candidate list
+  int32_t ready;     // 1 once thr_bin/above/nvalid are written for this call
+  int32_t pad[2];
+};
+
+// Workspace carve-up for hsa_index_full / hsa_index_reindex / hsa_sparse_attn_decode.
+struct WsLayout {
+  int32_t rows;        // batch * nq
+  int64_t ld_s;        // score row stride (positions), a multiple of 256
+  int64_t ld_b;        // block-max row stride (blocks) = ld_s / 8
+  size_t off_scores, off_blkmax, off_hist_full, off_cand_full, off_sure_full, off_state_full, off_done_full;
+  size_t off_pscores, off_hist_pool, off_cand_pool, off_sure_pool, off_state_pool, off_done_pool;
+  size_t off_attn;     // attention partials
+  size_t attn_bytes;
+  size_t zero_begin, zero_end;   // region that must be zero between calls (hist + state + counters)
+  size_t total;
+};
+
+bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L);
+
+// ------------------------------------------------------------------ index scoring
+struct ScanParams {
+  int32_t pool_mode;     // 0: Full (segment = request, nq queries share K); 1: Reindex (segment = (b,q))
+  int32_t batch, nq;
+  int64_t cap;
+  const uint8_t* ik_q;
+  const uint8_t* ik_s;
+  const uint16_t* q;     // bf16 [B][nq][16][128]
+  const float* w;        // [B][nq][16]
+  const int32_t* vis;    // [B][nq]
+  const int32_t* pool;   // Reindex: [B][nq][16384]
+  int32_t n_seg;
+  int32_t chunks_per_seg;
+  int32_t total_items;
+  float* scores;         // Full: [rows][ld_s]; Reindex: [rows][16384]
+  int64_t ld_s;
+  float* blkmax;         // Full: [rows][ld_b]
+  int64_t ld_b;
+  uint32_t* hist;        // Full: [rows][2][4096]; Reindex: [rows][4096]
+  SelState* state;       // Full: [rows][2]; Reindex: [rows]
+  uint32_t* seg_done;    // [n_seg]
+  uint32_t* status;
+};
+
+struct SelectParams {
+  int32_t pool_mode;
+  int32_t batch, nq;
+  int64_t max_vis;
+  const int32_t* vis;
+  const int32_t* pool;   // Reindex: slot -> position
+  const float* scores;
+  int64_t ld_s;
+  const float* blkmax;
+  int64_t ld_b;
+  uint32_t* hist;
+  SelState* state;
+  int32_t* cand;         // Full: [rows][ld_s + ld_b]; Reindex: [rows][16384]
+  int64_t ld_cand;
+  int32_t* sure;         // Full: [rows][512 + 2048]; Reindex: [rows][512]
+  int64_t ld_sure;
+  int32_t* topk_out;     // [rows][512]
+  int32_t* pool_out;     // Full: [rows][16384]
+  uint32_t* status;
+};
+
+cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_select(const SelectParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------------ attention
+struct AttnParams {
+  int32_t batch, nq;
+  int64_t cap;
+  int32_t scale_fmt;
+  const uint8_t* kv_q;
+  const uint8_t* kv_s;
+  const uint16_t* q;      // bf16 [B][nq][64][512]
+  const int32_t* topk;    // [B][nq][512]
+  const uint8_t* swa;     // [B][W+nq-1][512]
+  const int32_t* vis;     // [B][nq]
+  float sm_scale;
+  float* out;             // [B][nq][64][512]
+  float* partial;         // workspace: [B*nq][5][64][512 + 2]
+  uint32_t* status;
+};
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------------ cache write
+struct WriteParams {
+  int32_t batch, ratio, scale_fmt;
+  int64_t cap, n_tokens, n_entries;
+  const uint16_t* wkv;
+  const uint16_t* wgate;
+  const uint16_t* w_idx;
+  const int64_t* start_entry;
+  uint8_t* kv_q;
+  uint8_t* kv_s;
+  uint8_t* ik_q;
+  uint8_t* ik_s;
+  uint32_t* status;
+};
+cudaError_t launch_cache_write(const WriteParams& p, cudaStream_t s);
+
+}  // namespace hsa

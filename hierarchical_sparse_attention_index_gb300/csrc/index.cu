@@ -1,0 +1,854 @@
+// Indexer kernels: FP4 indexer-K scoring (Full scan and Reindex pool rescoring) and the exact
+// top-k selection behind both ([CED] Figure 5; [ARCH] §3.3; [COST] §3.2; [10100] 层次化稀疏索引器).
+//
+// Scoring, s_t = sum_h w_h ReLU(q_h . k_t):
+//  - One producer warp streams 256-entry stages of indexer K into a 4-deep shared-memory ring
+//    with bulk async copies (contiguous rows for Full; 8-entry runs gathered through the pool
+//    for Reindex). Eight consumer warps score them.
+//  - Each consumer thread reads its 16-byte chunk of an entry with one shared load. That chunk
+//    holds the entry's bytes in "fragment order" (include/hsa.h). The thread converts E2M1 pairs
+//    to f16x2 with the hardware cvt and feeds them straight into m16n8k16 tensor-core MMAs as
+//    the A operand (rows = entries, k = dims, n = heads).
+//  - Every k-step lies inside one 32-dim scale group, so the E8M0 scale is applied exactly in
+//    fp32 to the per-group accumulator. The query is converted once per segment to f16, after a
+//    per-head power-of-two shift that keeps its largest element in [2^14, 2^15). The shift is
+//    folded back into the head weight.
+//  - The epilogue fuses the ReLU-weighted head sum, the visibility mask, the 8-entry block max
+//    ([ARCH] §3.3 块 max 是上界) and a 4096-bin histogram of the top 12 bits of each score's
+//    order key. The last CTA to finish a request turns the histograms into the threshold bins
+//    of the position top-512 and the block top-2048.
+// Selection (exact; ties to the lower index):
+//  - collect: elements above the threshold bin are taken, elements in it become candidates.
+//  - finish: an 11-bit-digit radix select over (low key bits, inverted index) composites picks
+//    the remaining candidates. A bitmap over the index space then emits the result in
+//    ascending order, expands blocks into the candidate pool, and clears the workspace state.
+#include "hsa_common.cuh"
+#include "hsa_internal.h"
+
+namespace hsa {
+namespace {
+
+constexpr int kChunk = 256;
+constexpr int kMaxStages = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kScanThreads = kConsumers + 32;
+constexpr int kCodesBytes = kChunk * 64;
+constexpr int kScaleBytes = kChunk * 4;
+constexpr int kFlushItems = 240;   // packed 16-bit histogram counters: flush before 65536 entries
+
+struct ScanSmemLayout {
+  int nst, nlr;
+  size_t codes, scales, slotpos, bfrag, wsc, hist, bars, misc, total;
+};
+
+__host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq) {
+  ScanSmemLayout L;
+  const int nql = pool_mode ? 1 : nq;
+  L.nst = (nql <= 5) ? 4 : 2;
+  L.nlr = pool_mode ? 1 : 2 * nq;
+  size_t o = 0;
+  L.codes = o;   o += (size_t)L.nst * kCodesBytes;
+  L.scales = o;  o += (size_t)L.nst * kScaleBytes;
+  L.slotpos = o; o += (size_t)L.nst * kChunk * 4;
+  L.bfrag = o;   o += (size_t)nql * 2 * 8 * 32 * 2 * 4;
+  L.wsc = o;     o += (size_t)nql * 16 * 4;
+  L.hist = o;    o += (size_t)L.nlr * (kHistBins / 2) * 4;
+  L.bars = o;    o += 2 * kMaxStages * 8;
+  L.misc = o;    o += 256;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Exclusive prefix sum over the first `nthreads` threads (a multiple of 32); scratch holds 32 ints.
+// The caller's threads must all call it (named barrier `bar_id` over `nthreads`).
+__device__ __forceinline__ int excl_scan(int v, int* scratch, int bar_id, int nthreads, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  named_bar_sync(bar_id, nthreads);
+  const int nw = nthreads >> 5;
+  if (warp == 0) {
+    int t = (lane < nw) ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < nw) scratch[lane] = t;   // inclusive warp totals
+  }
+  named_bar_sync(bar_id, nthreads);
+  const int before = (warp > 0) ? scratch[warp - 1] : 0;
+  *total = scratch[nw - 1];
+  named_bar_sync(bar_id, nthreads);
+  return before + x - v;
+}
+
+// Threshold bin for a top-K over a 4096-bin histogram; 256 consumer threads (named barrier 1).
+__device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, int* scratch) {
+  const int tid = threadIdx.x;
+  uint32_t cnt[16];
+  int local = 0;
+  const int top = kHistBins - 16 * (tid + 1);   // this thread owns bins [top, top+16), high first
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    cnt[i] = __ldcg(ghist + top + 15 - i);
+    local += (int)cnt[i];
+  }
+  int total;
+  const int excl = excl_scan(local, scratch, 1, kConsumers, &total);
+  if (total <= K) {
+    if (tid == 0) {
+      st->thr_bin = -1;
+      st->above = total;
+      st->nvalid = total;
+      __threadfence();
+      st->ready = 1;
+    }
+  } else if (excl < K && excl + local >= K) {
+    int run = excl;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (run + (int)cnt[i] >= K) {
+        st->thr_bin = top + 15 - i;
+        st->above = run;
+        st->nvalid = total;
+        __threadfence();
+        st->ready = 1;
+        break;
+      }
+      run += (int)cnt[i];
+    }
+  }
+  named_bar_sync(1, kConsumers);
+}
+
+__global__ void __launch_bounds__(kScanThreads) index_scan_kernel(const ScanParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const ScanSmemLayout L = scan_smem_layout(p.pool_mode, p.nq);
+  const int nql = p.pool_mode ? 1 : p.nq;
+  const int nst = L.nst;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last flag, [2..9] vis, [16..48) scratch
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // contiguous item range of this CTA
+  const int64_t per = ((int64_t)p.total_items + gridDim.x - 1) / gridDim.x;
+  const int i0 = (int)imin64((int64_t)blockIdx.x * per, p.total_items);
+  const int i1 = (int)imin64((int64_t)i0 + per, p.total_items);
+
+  if (tid == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    misc[0] = 0;
+    fence_mbar_init();
+  }
+  {
+    uint32_t* h = reinterpret_cast<uint32_t*>(smem + L.hist);
+    for (int i = tid; i < L.nlr * (kHistBins / 2); i += kScanThreads) h[i] = 0;
+  }
+  __syncthreads();
+  if (i0 >= i1) return;
+
+  const int cps = p.chunks_per_seg;
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer warp
+    for (int it = i0, k = 0; it < i1; ++it, ++k) {
+      const int s = k % nst;
+      if (k >= nst) {
+        if (!mbar_wait(empty0 + 8 * s, ((k / nst) - 1) & 1)) {
+          flag_status(p.status, HSA_FLAG_TIMEOUT);
+          misc[0] = 1;
+          return;
+        }
+      }
+      const int seg = it / cps, c = it % cps;
+      const uint32_t full = full0 + 8 * s;
+      const uint32_t dcodes = smem_u32(smem + L.codes + (size_t)s * kCodesBytes);
+      const uint32_t dscales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
+      if (!p.pool_mode) {
+        int vmax = 0;
+        for (int q = 0; q < p.nq; ++q) vmax = max(vmax, __ldg(p.vis + seg * p.nq + q));
+        vmax = (int)imin64(vmax, p.cap);
+        const int p0 = c * kChunk;
+        const int n = max(0, min(kChunk, vmax - p0));
+        if (lane == 0) {
+          if (n > 0) {
+            const int nc = (int)imin64((n + 7) & ~7, p.cap - p0);
+            mbar_arrive_expect_tx(full, (uint32_t)nc * 68u);
+            const int64_t e0 = (int64_t)seg * p.cap + p0;
+            bulk_g2s(dcodes, p.ik_q + e0 * 64, (uint32_t)nc * 64u, full);
+            bulk_g2s(dscales, p.ik_s + e0 * 4, (uint32_t)nc * 4u, full);
+          } else {
+            mbar_arrive(full);
+          }
+        }
+      } else {
+        // pool gather: lane handles the 8-slot run `lane` of this 256-slot chunk
+        const int row = seg;
+        const int b = row / p.nq;
+        const int vis = __ldg(p.vis + row);
+        const int* pr = p.pool + (int64_t)row * kPool + c * kChunk + lane * 8;
+        int* sp = reinterpret_cast<int*>(smem + L.slotpos) + s * kChunk + lane * 8;
+        const int base = __ldg(pr);
+        bool ok = (base >= 0) && ((base & 7) == 0) && (base < p.cap);
+        if (base >= 0 && !ok) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+        for (int j = 0; j < 8; ++j) {
+          const int v = __ldg(pr + j);
+          int outv = -1;
+          if (ok && v >= 0) {
+            if (v == base + j && v < vis) outv = v;
+            else if (v != base + j || v >= p.cap) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+          }
+          sp[j] = outv;
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, ok);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(m) * (512u + 32u));
+        __syncwarp();
+        if (ok) {
+          const int64_t e0 = (int64_t)b * p.cap + base;
+          bulk_g2s(dcodes + lane * 512, p.ik_q + e0 * 64, 512u, full);
+          bulk_g2s(dscales + lane * 32, p.ik_s + e0 * 4, 32u, full);
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumer warps
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t* hist_sm = reinterpret_cast<uint32_t*>(smem + L.hist);
+  uint32_t* bfrag = reinterpret_cast<uint32_t*>(smem + L.bfrag);
+  float* wsc = reinterpret_cast<float*>(smem + L.wsc);
+  int* svis = misc + 2;
+  int* scratch = misc + 16;
+
+  uint32_t B[2][8][2];   // query fragments of the current query (registers)
+  float wr[2][2];
+  int cur_seg = -1, seg_items = 0, since_flush = 0;
+
+  auto flush_hist = [&](int seg) {
+    named_bar_sync(1, kConsumers);
+    for (int lr = 0; lr < L.nlr; ++lr) {
+      int grow;
+      if (p.pool_mode) grow = seg;
+      else grow = (seg * p.nq + (lr >> 1)) * 2 + (lr & 1);
+      uint32_t* gh = p.hist + (size_t)grow * kHistBins;
+      uint32_t* sh = hist_sm + lr * (kHistBins / 2);
+      for (int i = tid; i < kHistBins / 2; i += kConsumers) {
+        const uint32_t v = sh[i];
+        if (v) {
+          if (v & 0xFFFFu) atomicAdd(gh + 2 * i, v & 0xFFFFu);
+          if (v >> 16) atomicAdd(gh + 2 * i + 1, v >> 16);
+          sh[i] = 0;
+        }
+      }
+    }
+    __threadfence();
+    named_bar_sync(1, kConsumers);
+  };
+
+  auto finish_segment = [&](int seg, int nitems) {
+    flush_hist(seg);
+    if (tid == 0) {
+      const unsigned old = atomicAdd(p.seg_done + seg, (unsigned)nitems);
+      misc[1] = (old + (unsigned)nitems == (unsigned)cps) ? 1 : 0;
+    }
+    named_bar_sync(1, kConsumers);
+    if (misc[1]) {
+      __threadfence();
+      if (p.pool_mode) {
+        compute_threshold(p.hist + (size_t)seg * kHistBins, kTopK, p.state + seg, scratch);
+      } else {
+        for (int q = 0; q < p.nq; ++q) {
+          const int row = seg * p.nq + q;
+          compute_threshold(p.hist + (size_t)(2 * row) * kHistBins, kTopK, p.state + 2 * row, scratch);
+          compute_threshold(p.hist + (size_t)(2 * row + 1) * kHistBins, kCandBlocks, p.state + 2 * row + 1,
+                            scratch);
+        }
+      }
+      if (tid == 0) p.seg_done[seg] = 0;
+    }
+    named_bar_sync(1, kConsumers);
+  };
+
+  auto load_segment = [&](int seg) {
+    named_bar_sync(1, kConsumers);
+    for (int ql = 0; ql < nql; ++ql) {
+      const int row = p.pool_mode ? seg : seg * p.nq + ql;
+      const int h = tid >> 4, d0 = (tid & 15) * 8;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHIdx + h) * kDIdx + d0));
+      float x[8];
+      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(rw[i] << 16);
+        x[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      int sh = 0;
+      if (amax > 0.f) {
+        int e;
+        frexpf(amax, &e);          // amax = m * 2^e, m in [0.5, 1)
+        sh = 15 - e;               // amax * 2^sh in [2^14, 2^15)
+      }
+      uint32_t pk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half lo = __float2half_rn(ldexpf(x[2 * i], sh));
+        const __half hi = __float2half_rn(ldexpf(x[2 * i + 1], sh));
+        pk[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+      }
+      // dims d0..d0+7 -> k-step s = d0/16, t' = (d0%16)/4 and t'+1
+      const int ks = d0 >> 4, tp = (d0 & 15) >> 2;
+      const int nt = h >> 3, gp = h & 7;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int ln = 4 * gp + tp + u;
+        uint32_t* dst = bfrag + ((((size_t)ql * 2 + nt) * 8 + ks) * 32 + ln) * 2;
+        dst[0] = pk[2 * u];
+        dst[1] = pk[2 * u + 1];
+      }
+      if ((tid & 15) == 0) wsc[ql * 16 + h] = ldexpf(__ldg(p.w + (size_t)row * kHIdx + h), -sh);
+      if (tid < 8 && !p.pool_mode && tid == ql) svis[ql] = __ldg(p.vis + row);
+    }
+    if (p.pool_mode && tid == 0) svis[0] = __ldg(p.vis + seg);
+    named_bar_sync(1, kConsumers);
+  };
+
+  auto load_query_regs = [&](int ql) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint2 v = *reinterpret_cast<const uint2*>(bfrag + ((((size_t)ql * 2 + nt) * 8 + s) * 32 + lane) * 2);
+        B[nt][s][0] = v.x;
+        B[nt][s][1] = v.y;
+      }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) wr[nt][j] = wsc[ql * 16 + nt * 8 + 2 * t + j];
+  };
+
+  for (int it = i0, k = 0; it < i1; ++it, ++k) {
+    const int seg = it / cps, c = it % cps;
+    if (seg != cur_seg) {
+      if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
+      cur_seg = seg;
+      seg_items = 0;
+      since_flush = 0;
+      load_segment(seg);
+      if (nql == 1) load_query_regs(0);
+    } else if (since_flush >= kFlushItems) {
+      flush_hist(seg);
+      since_flush = 0;
+    }
+    ++seg_items;
+    ++since_flush;
+    named_bar_sync(1, kConsumers);
+    if (misc[0]) break;
+
+    const int s = k % nst;
+    if (!mbar_wait(full0 + 8 * s, (k / nst) & 1)) {
+      flag_status(p.status, HSA_FLAG_TIMEOUT);
+      misc[0] = 1;
+      continue;
+    }
+    int nrows;   // rows of this stage that hold data
+    if (!p.pool_mode) {
+      int vmax = 0;
+      for (int q = 0; q < p.nq; ++q) vmax = max(vmax, svis[q]);
+      vmax = (int)imin64(vmax, p.cap);
+      nrows = max(0, min(kChunk, vmax - c * kChunk));
+    } else {
+      nrows = kChunk;
+    }
+    const uint32_t codes = smem_u32(smem + L.codes + (size_t)s * kCodesBytes);
+    const uint32_t scales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
+    const int* slotpos = reinterpret_cast<const int*>(smem + L.slotpos) + s * kChunk;
+
+    if (nrows > 0) {
+#pragma unroll 1
+      for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = warp * 32 + mt * 16 + g, r1 = r0 + 8;
+        if (warp * 32 + mt * 16 >= nrows) break;
+        const uint4 A0 = lds128(codes + r0 * 64 + 16 * t);
+        const uint4 A1 = lds128(codes + r1 * 64 + 16 * t);
+        const uint32_t S0 = lds32(scales + r0 * 4), S1 = lds32(scales + r1 * 4);
+        uint32_t a0[16], a1[16];
+        e2m1x8_to_f16x2x4(A0.x, a0[0], a0[1], a0[2], a0[3]);
+        e2m1x8_to_f16x2x4(A0.y, a0[4], a0[5], a0[6], a0[7]);
+        e2m1x8_to_f16x2x4(A0.z, a0[8], a0[9], a0[10], a0[11]);
+        e2m1x8_to_f16x2x4(A0.w, a0[12], a0[13], a0[14], a0[15]);
+        e2m1x8_to_f16x2x4(A1.x, a1[0], a1[1], a1[2], a1[3]);
+        e2m1x8_to_f16x2x4(A1.y, a1[4], a1[5], a1[6], a1[7]);
+        e2m1x8_to_f16x2x4(A1.z, a1[8], a1[9], a1[10], a1[11]);
+        e2m1x8_to_f16x2x4(A1.w, a1[12], a1[13], a1[14], a1[15]);
+        float sc0[4], sc1[4];
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          sc0[gi] = e8m0_to_f32(S0 >> (8 * gi));
+          sc1[gi] = e8m0_to_f32(S1 >> (8 * gi));
+        }
+        int pos0, pos1;
+        bool in0 = true, in1 = true;
+        if (!p.pool_mode) {
+          pos0 = c * kChunk + r0;
+          pos1 = c * kChunk + r1;
+        } else {
+          pos0 = slotpos[r0];
+          pos1 = slotpos[r1];
+          in0 = pos0 >= 0;
+          in1 = pos1 >= 0;
+        }
+        for (int ql = 0; ql < nql; ++ql) {
+          if (nql > 1) load_query_regs(ql);
+          float tot[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tot[nt][j] = 0.f;
+#pragma unroll
+          for (int gi = 0; gi < 4; ++gi) {
+            float tmp[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tmp[nt][j] = 0.f;
+#pragma unroll
+            for (int ss = 0; ss < 2; ++ss) {
+              const int ks = 2 * gi + ss;
+              const uint32_t x0 = a0[4 * gi + 2 * ss], x2 = a0[4 * gi + 2 * ss + 1];
+              const uint32_t x1 = a1[4 * gi + 2 * ss], x3 = a1[4 * gi + 2 * ss + 1];
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) mma_f16_16816(tmp[nt], x0, x1, x2, x3, B[nt][ks][0], B[nt][ks][1]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              tot[nt][0] = fmaf(sc0[gi], tmp[nt][0], tot[nt][0]);
+              tot[nt][1] = fmaf(sc0[gi], tmp[nt][1], tot[nt][1]);
+              tot[nt][2] = fmaf(sc1[gi], tmp[nt][2], tot[nt][2]);
+              tot[nt][3] = fmaf(sc1[gi], tmp[nt][3], tot[nt][3]);
+            }
+          }
+          float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              v0 = fmaf(wr[nt][j], fmaxf(tot[nt][j], 0.f), v0);
+              v1 = fmaf(wr[nt][j], fmaxf(tot[nt][2 + j], 0.f), v1);
+            }
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+          bool ok0, ok1;
+          if (!p.pool_mode) {
+            const int vq = imin64(svis[ql], p.cap);
+            ok0 = pos0 < vq;
+            ok1 = pos1 < vq;
+          } else {
+            ok0 = in0;
+            ok1 = in1;
+          }
+          v0 = ok0 ? v0 : -INFINITY;
+          v1 = ok1 ? v1 : -INFINITY;
+          if (!p.pool_mode) {
+            const int row = cur_seg * p.nq + ql;
+            float* srow = p.scores + (size_t)row * p.ld_s;
+            if (t == 0) srow[pos0] = v0;
+            if (t == 1) srow[pos1] = v1;
+            uint32_t* hp = hist_sm + (2 * ql) * (kHistBins / 2);
+            if (t == 0 && ok0) {
+              const uint32_t bin = order_key(v0) >> kHistShift;
+              atomicAdd(hp + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
+            }
+            if (t == 1 && ok1) {
+              const uint32_t bin = order_key(v1) >> kHistShift;
+              atomicAdd(hp + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
+            }
+            // block maxima over the 8 rows g = 0..7 (block A) and 8..15 (block B)
+            float bA = v0, bB = v1;
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+              bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, o));
+              bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, o));
+            }
+            const int jA = (c * kChunk + warp * 32 + mt * 16) >> 3;
+            const int vq = imin64(svis[ql], p.cap);
+            uint32_t* hb = hist_sm + (2 * ql + 1) * (kHistBins / 2);
+            if (lane == 0 && jA * 8 < vq) {
+              p.blkmax[(size_t)row * p.ld_b + jA] = bA;
+              const uint32_t bin = order_key(bA) >> kHistShift;
+              atomicAdd(hb + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
+            }
+            if (lane == 1 && (jA + 1) * 8 < vq) {
+              p.blkmax[(size_t)row * p.ld_b + jA + 1] = bB;
+              const uint32_t bin = order_key(bB) >> kHistShift;
+              atomicAdd(hb + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
+            }
+          } else {
+            float* srow = p.scores + (size_t)cur_seg * kPool + c * kChunk;
+            if (t == 0) srow[r0] = v0;
+            if (t == 1) srow[r1] = v1;
+            if (t == 0 && ok0) {
+              const uint32_t bin = order_key(v0) >> kHistShift;
+              atomicAdd(hist_sm + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
+            }
+            if (t == 1 && ok1) {
+              const uint32_t bin = order_key(v1) >> kHistShift;
+              atomicAdd(hist_sm + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+  if (cur_seg >= 0 && !misc[0]) finish_segment(cur_seg, seg_items);
+}
+
+// ------------------------------------------------------------------ collect
+constexpr int kCollectThreads = 256;
+constexpr int kCollectChunk = 8192;
+
+__device__ __forceinline__ void warp_append(bool pred, int value, int* counter, int* list, int cap,
+                                            uint32_t* status) {
+  const uint32_t m = __ballot_sync(0xffffffffu, pred);
+  if (!m) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (pred) {
+    const int off = base + __popc(m & ((1u << lane) - 1u));
+    if (off < cap) list[off] = value;
+    else flag_status(status, HSA_FLAG_INDEX_RANGE);
+  }
+}
+
+__global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectParams p) {
+  const int row = blockIdx.y, which = blockIdx.z;
+  const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
+  const float* data;
+  int n;
+  int64_t cand_off = 0, sure_off = 0;
+  int sure_cap;
+  if (p.pool_mode) {
+    data = p.scores + (size_t)row * kPool;
+    n = kPool;
+    sure_cap = kTopK;
+  } else if (which == 0) {
+    data = p.scores + (size_t)row * p.ld_s;
+    n = vis;
+    sure_cap = kTopK;
+  } else {
+    data = p.blkmax + (size_t)row * p.ld_b;
+    n = (vis + kBlk - 1) / kBlk;
+    cand_off = p.ld_s;
+    sure_off = kTopK;
+    sure_cap = kCandBlocks;
+  }
+  const int e0 = blockIdx.x * kCollectChunk;
+  if (e0 >= n) return;
+  SelState* st = p.state + (p.pool_mode ? row : 2 * row + which);
+  const int thr = *reinterpret_cast<volatile int*>(&st->thr_bin);
+  int* cand = p.cand + (size_t)row * p.ld_cand + cand_off;
+  int* sure = p.sure + (size_t)row * p.ld_sure + sure_off;
+  const int e1 = min(n, e0 + kCollectChunk);
+  for (int base = e0; base < e1; base += kCollectThreads) {
+    const int e = base + threadIdx.x;
+    bool is_sure = false, is_cand = false;
+    if (e < e1) {
+      const float v = __ldcg(data + e);
+      if (v != -INFINITY) {
+        const int bin = (int)(order_key(v) >> kHistShift);
+        is_sure = (thr < 0) || (bin > thr);
+        is_cand = (thr >= 0) && (bin == thr);
+      }
+    }
+    warp_append(is_sure, e, &st->nsure, sure, sure_cap, p.status);
+    warp_append(is_cand, e, &st->ncand, cand, (int)(which == 0 ? (p.pool_mode ? kPool : p.ld_s) : p.ld_b),
+                p.status);
+  }
+}
+
+// ------------------------------------------------------------------ finish
+constexpr int kFinishThreads = 1024;
+
+__device__ __forceinline__ int block_excl_scan_1024(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int tt = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, tt, o);
+      if (lane >= o) tt += y;
+    }
+    scratch[lane] = tt;
+  }
+  __syncthreads();
+  const int before = warp ? scratch[warp - 1] : 0;
+  *total = scratch[31];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) uint32_t fsm[];
+  const int row = blockIdx.x, which = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
+  const float* data;
+  int n, K;
+  int64_t cand_off = 0, sure_off = 0;
+  if (p.pool_mode) {
+    data = p.scores + (size_t)row * kPool;
+    n = kPool;
+    K = kTopK;
+  } else if (which == 0) {
+    data = p.scores + (size_t)row * p.ld_s;
+    n = vis;
+    K = kTopK;
+  } else {
+    data = p.blkmax + (size_t)row * p.ld_b;
+    n = (vis + kBlk - 1) / kBlk;
+    K = kCandBlocks;
+    cand_off = p.ld_s;
+    sure_off = kTopK;
+  }
+  SelState* st = p.state + (p.pool_mode ? row : 2 * row + which);
+  const int nwords = (max(n, 1) + 31) >> 5;
+  uint32_t* bitmap = fsm;                       // [nwords]
+  uint32_t* shist = fsm + ((nwords + 3) & ~3);  // [2048]
+  int* scratch = reinterpret_cast<int*>(shist + 2048);   // [64]
+
+  __shared__ int s_thr, s_nvalid, s_nsure, s_ncand, s_ready;
+  __shared__ int s_digit, s_above, s_cnt;
+  if (tid == 0) {
+    volatile SelState* vs = st;
+    s_ready = vs->ready;
+    s_thr = vs->thr_bin;
+    s_nvalid = vs->nvalid;
+    s_nsure = vs->nsure;
+    s_ncand = vs->ncand;
+  }
+  for (int i = tid; i < nwords; i += kFinishThreads) bitmap[i] = 0;
+  __syncthreads();
+  const int thr = s_ready ? s_thr : -1;
+  const int nvalid = s_ready ? s_nvalid : 0;
+  const int Keff = min(K, nvalid);
+  const int nsure = min(s_nsure, K);
+  const int cand_cap = (int)(p.pool_mode ? kPool : (which == 0 ? p.ld_s : p.ld_b));
+  const int ncand = min(s_ncand, cand_cap);
+  const int* cand = p.cand + (size_t)row * p.ld_cand + cand_off;
+  const int* sure = p.sure + (size_t)row * p.ld_sure + sure_off;
+
+  for (int i = tid; i < nsure; i += kFinishThreads) {
+    const int e = __ldcg(sure + i);
+    if (e >= 0 && e < n) atomicOr(bitmap + (e >> 5), 1u << (e & 31));
+  }
+  int need = Keff - nsure;
+  if (thr >= 0 && need > 0 && ncand > 0) {
+    uint64_t prefix = 0, mask = 0;
+    int remaining = need;
+    const int shifts[5] = {41, 30, 19, 8, 0};
+    const int widths[5] = {11, 11, 11, 11, 8};
+    for (int d = 0; d < 5; ++d) {
+      const int sh = shifts[d];
+      const uint32_t wm = (1u << widths[d]) - 1u;
+      for (int i = tid; i < 2048; i += kFinishThreads) shist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < ncand; i += kFinishThreads) {
+        const int e = __ldcg(cand + i);
+        const uint32_t key = order_key(__ldcg(data + e));
+        const uint64_t comp = ((uint64_t)(key & 0xFFFFFu) << 32) | (uint64_t)(~(uint32_t)e);
+        if ((comp & mask) == prefix) atomicAdd(shist + ((comp >> sh) & wm), 1u);
+      }
+      __syncthreads();
+      // 2048 bins, 2 per thread, highest first
+      const int hi_bin = 2047 - 2 * tid;
+      const int c_hi = (int)shist[hi_bin], c_lo = (int)shist[hi_bin - 1];
+      int tot;
+      const int excl = block_excl_scan_1024(c_hi + c_lo, scratch, &tot);
+      if (excl < remaining && excl + c_hi + c_lo >= remaining) {
+        if (excl + c_hi >= remaining) {
+          s_digit = hi_bin;
+          s_above = excl;
+          s_cnt = c_hi;
+        } else {
+          s_digit = hi_bin - 1;
+          s_above = excl + c_hi;
+          s_cnt = c_lo;
+        }
+      }
+      __syncthreads();
+      remaining -= s_above;
+      prefix |= (uint64_t)s_digit << sh;
+      mask |= (uint64_t)wm << sh;
+      const bool all_in = (s_cnt == remaining);
+      __syncthreads();
+      if (all_in) break;
+    }
+    for (int i = tid; i < ncand; i += kFinishThreads) {
+      const int e = __ldcg(cand + i);
+      const uint32_t key = order_key(__ldcg(data + e));
+      const uint64_t comp = ((uint64_t)(key & 0xFFFFFu) << 32) | (uint64_t)(~(uint32_t)e);
+      if ((comp & mask) >= prefix) atomicOr(bitmap + (e >> 5), 1u << (e & 31));
+    }
+  }
+  __syncthreads();
+
+  // ascending emission
+  const int per = (nwords + kFinishThreads - 1) / kFinishThreads;
+  const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
+  int cnt = 0;
+  for (int i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
+  int total;
+  int o = block_excl_scan_1024(cnt, scratch, &total);
+  if (p.pool_mode) {
+    int32_t* out = p.topk_out + (size_t)row * kTopK;
+    const int32_t* pl = p.pool + (size_t)row * kPool;
+    for (int i = w0; i < w1; ++i) {
+      uint32_t m = bitmap[i];
+      while (m) {
+        const int b = __ffs(m) - 1;
+        m &= m - 1;
+        if (o < kTopK) out[o] = __ldg(pl + i * 32 + b);
+        ++o;
+      }
+    }
+    for (int j = total + tid; j < kTopK; j += kFinishThreads) out[j] = -1;
+  } else if (which == 0) {
+    int32_t* out = p.topk_out + (size_t)row * kTopK;
+    for (int i = w0; i < w1; ++i) {
+      uint32_t m = bitmap[i];
+      while (m) {
+        const int b = __ffs(m) - 1;
+        m &= m - 1;
+        if (o < kTopK) out[o] = i * 32 + b;
+        ++o;
+      }
+    }
+    for (int j = total + tid; j < kTopK; j += kFinishThreads) out[j] = -1;
+  } else {
+    int32_t* out = p.pool_out + (size_t)row * kPool;
+    for (int i = w0; i < w1; ++i) {
+      uint32_t m = bitmap[i];
+      while (m) {
+        const int b = __ffs(m) - 1;
+        m &= m - 1;
+        const int blk = i * 32 + b;
+        if (o < kCandBlocks) {
+          int4 lo, hi;
+          const int q0 = blk * 8;
+          lo.x = (q0 + 0 < vis) ? q0 + 0 : -1;
+          lo.y = (q0 + 1 < vis) ? q0 + 1 : -1;
+          lo.z = (q0 + 2 < vis) ? q0 + 2 : -1;
+          lo.w = (q0 + 3 < vis) ? q0 + 3 : -1;
+          hi.x = (q0 + 4 < vis) ? q0 + 4 : -1;
+          hi.y = (q0 + 5 < vis) ? q0 + 5 : -1;
+          hi.z = (q0 + 6 < vis) ? q0 + 6 : -1;
+          hi.w = (q0 + 7 < vis) ? q0 + 7 : -1;
+          reinterpret_cast<int4*>(out + 8 * o)[0] = lo;
+          reinterpret_cast<int4*>(out + 8 * o)[1] = hi;
+        }
+        ++o;
+      }
+    }
+    for (int j = 8 * min(total, kCandBlocks) + tid; j < kPool; j += kFinishThreads) out[j] = -1;
+  }
+  // clear this row's histogram and state for the next call
+  uint32_t* gh = p.hist + (size_t)(p.pool_mode ? row : 2 * row + which) * kHistBins;
+  for (int i = tid; i < kHistBins; i += kFinishThreads) gh[i] = 0;
+  if (tid == 0) {
+    st->thr_bin = 0;
+    st->above = 0;
+    st->nvalid = 0;
+    st->nsure = 0;
+    st->ncand = 0;
+    st->ready = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s) {
+  const ScanSmemLayout L = scan_smem_layout(p.pool_mode, p.nq);
+  static int set_bytes = 0;        // the attribute is per function, set to the largest size seen
+  if ((int)L.total > set_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(index_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L.total);
+    if (e != cudaSuccess) return e;
+    set_bytes = (int)L.total;
+  }
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_scan_kernel, kScanThreads, L.total) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  int grid = num_sms * per_sm;
+  if (grid > p.total_items) grid = p.total_items;
+  if (grid < 1) grid = 1;
+  index_scan_kernel<<<grid, kScanThreads, L.total, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
+  const int rows = p.batch * p.nq;
+  const int nsel = p.pool_mode ? 1 : 2;
+  const int64_t nmax = p.pool_mode ? kPool : p.max_vis;
+  dim3 cg((unsigned)((nmax + kCollectChunk - 1) / kCollectChunk), (unsigned)rows, (unsigned)nsel);
+  collect_kernel<<<cg, kCollectThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t nwords = (nmax + 31) / 32;
+  const size_t smem = (size_t)((nwords + 3) & ~3) * 4 + 2048 * 4 + 64 * 4;
+  static size_t set_bytes = 0;
+  if (smem > set_bytes) {
+    e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    set_bytes = smem;
+  }
+  finish_kernel<<<dim3((unsigned)rows, (unsigned)nsel), kFinishThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace hsa

@@ -178,9 +178,36 @@ def main_kv_dequant(kv_q, kv_s, scale_fmt=SCALE_E8M0):
     return dequant_groups(kv_q, kv_s, MAIN_GROUP, scale_fmt)
 
 
+# Indexer-K byte order (a layout choice; the pages fix the value format only). The stored
+# byte 16t + 2s + i holds the logical byte 8s + 2t + i, whose low nibble is element
+# 2(8s + 2t + i) and high nibble the next element.
+def _fragment_perm():
+    perm = np.empty(64, np.int64)          # perm[stored] = logical
+    for t in range(4):
+        for s in range(8):
+            for i in range(2):
+                perm[16 * t + 2 * s + i] = 8 * s + 2 * t + i
+    return perm
+
+
+def index_k_to_stored(packed_natural):
+    """Natural packing (byte j = elements 2j, 2j+1) -> stored fragment order."""
+    packed_natural = np.asarray(packed_natural, np.uint8)
+    return packed_natural[:, _fragment_perm()]
+
+
+def index_k_to_natural(stored):
+    """Stored fragment order -> natural packing."""
+    stored = np.asarray(stored, np.uint8)
+    out = np.empty_like(stored)
+    out[:, _fragment_perm()] = stored
+    return out
+
+
 def index_k_dequant(ik_q, ik_s):
-    """Indexer-K entry: 128 x E2M1 + one E8M0 per 32 channels = 68 B ([890B] §三 事实二)."""
-    return dequant_groups(ik_q, ik_s, INDEX_GROUP, SCALE_E8M0)
+    """Indexer-K entry: 128 x E2M1 in fragment order + one E8M0 per 32 channels = 68 B
+    ([890B] §三 事实二)."""
+    return dequant_groups(index_k_to_natural(ik_q), ik_s, INDEX_GROUP, SCALE_E8M0)
 
 
 def swa_decode(rows_u8):
@@ -418,8 +445,8 @@ def cache_write_compress(wkv, wgate, w_idx, m, scale_fmt=SCALE_E8M0):
     lat = rms_norm(compress_pool(wkv, wgate, m))
     kv_q, kv_s = quantise_groups(lat.astype(np.float32), MAIN_GROUP, scale_fmt)
     K = lat @ np.asarray(w_idx, np.float64)
-    ik_q, ik_s = quantise_groups(K.astype(np.float32), INDEX_GROUP, SCALE_E8M0)
-    return kv_q, kv_s, ik_q, ik_s, lat, K
+    ik_nat, ik_s = quantise_groups(K.astype(np.float32), INDEX_GROUP, SCALE_E8M0)
+    return kv_q, kv_s, index_k_to_stored(ik_nat), ik_s, lat, K
 
 
 # ---------------------------------------------------------------------------------------

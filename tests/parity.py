@@ -1,0 +1,137 @@
+"""Shared helpers of the parity tests: oracle-side inputs and comparisons.
+
+Inputs come from the seeded generator module. The FP4 caches that both sides read are
+produced by the oracle's own writer, so no oracle input ever comes from the CUDA path.
+Tolerances:
+- indices match exactly, except positions whose oracle score lies within TOPK_REL (1e-4,
+  relative) of the k-th threshold (the required band);
+- attention: max|o - o_ref| / max|o_ref| <= ATTN_REL (2e-3, the required bound);
+- cache write: codes equal, except elements within WRITE_REL of a rounding midpoint or a
+  scale boundary. The fp32 pipeline (expf, a correctly rounded sqrt and division, 512-term
+  fp32 sums) stays within about 1e-6 of the fp64 values, so 1e-5 leaves a 10x margin.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+from hierarchical_sparse_attention_index_gb300 import synth
+
+TOPK_REL = 1e-4
+ATTN_REL = 2e-3
+WRITE_REL = 1e-5
+E2M1_MIDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def f32(bits):
+    return synth.bf16_bits_to_f32(bits)
+
+
+def oracle_cache(seed, layer, batch, T, cap, planted=0, q_plant=None, w_plant=None, scale_fmt=O.SCALE_E8M0):
+    """Per-request m=1 cache written by the oracle from seeded N(0,1) latents.
+
+    Returns packed arrays [B][cap][...] (zero padded past T), the dequantised keys per request
+    and the planted positions."""
+    W = synth.w_idx_bf16(seed, layer)
+    kv_q = np.zeros((batch, cap, 256), np.uint8)
+    kv_s = np.zeros((batch, cap, 32), np.uint8)
+    ik_q = np.zeros((batch, cap, 64), np.uint8)
+    ik_s = np.zeros((batch, cap, 4), np.uint8)
+    planted_pos = []
+    for b in range(batch):
+        lat = synth.latents_bf16(seed, layer, b, T)
+        if planted:
+            planted_pos.append(synth.plant_clusters(lat, W, q_plant[b], w_plant[b], planted, seed, b))
+        a, s_, c, d, _, _ = O.cache_write_compress(f32(lat), None, f32(W), 1, scale_fmt)
+        kv_q[b, :T], kv_s[b, :T], ik_q[b, :T], ik_s[b, :T] = a, s_, c, d
+    return dict(kv_q=kv_q, kv_s=kv_s, ik_q=ik_q, ik_s=ik_s, W=W, planted=planted_pos)
+
+
+def dequant_index(cache, b, n):
+    return O.index_k_dequant(cache["ik_q"][b, :n], cache["ik_s"][b, :n])
+
+
+def dequant_main(cache, b, n, scale_fmt=O.SCALE_E8M0):
+    return O.main_kv_dequant(cache["kv_q"][b, :n], cache["kv_s"][b, :n], scale_fmt)
+
+
+def check_set_band(gpu_sel, oracle_sel, score, name):
+    """Sets may differ only at elements whose oracle score is within TOPK_REL of the threshold."""
+    g = set(int(x) for x in gpu_sel)
+    o = set(int(x) for x in oracle_sel)
+    if g == o:
+        return 0
+    key = score.astype(np.float32).astype(np.float64)
+    tau = min(key[list(o)])
+    bad = [x for x in g ^ o if abs(score[x] - tau) > TOPK_REL * abs(tau)]
+    assert not bad, f"{name}: {len(g ^ o)} differing, {len(bad)} outside the band (tau={tau}): {bad[:8]}"
+    return len(g ^ o)
+
+
+def check_topk(gpu_row, s, vis, k=512, name="topk"):
+    """gpu_row: the kernel's [k] output; s: oracle fp64 scores over positions (>= vis: -inf)."""
+    kk = min(k, vis)
+    g = gpu_row[gpu_row >= 0]
+    assert len(g) == kk, f"{name}: {len(g)} indices, expected {kk}"
+    assert np.all(gpu_row[kk:] == -1) and np.all(np.diff(g) > 0), f"{name}: not ascending/-1 padded"
+    assert g.min() >= 0 and g.max() < vis
+    o = O.topk_ascending(s, vis, k)
+    return check_set_band(g, o, s, name)
+
+
+def check_pool(gpu_pool, s, vis, name="pool"):
+    """Structure of the pool plus block-set parity under the band on block maxima."""
+    m = O.block_maxima(s, vis)
+    nblk = len(m)
+    nsel = min(2048, nblk)
+    runs = gpu_pool[:8 * nsel].reshape(nsel, 8)
+    blocks = runs[:, 0] // 8
+    assert np.all(runs[:, 0] >= 0), f"{name}: empty run"
+    assert np.all(np.diff(blocks) > 0), f"{name}: blocks not ascending"
+    expect = blocks[:, None] * 8 + np.arange(8)[None, :]
+    expect = np.where(expect < vis, expect, -1)
+    assert np.array_equal(runs, expect), f"{name}: run contents"
+    assert np.all(gpu_pool[8 * nsel:] == -1)
+    o = O.topk_ascending(m, nblk, 2048)
+    return check_set_band(blocks, o, m, name)
+
+
+def check_attention(o_gpu, o_ref, name="attn"):
+    denom = np.max(np.abs(o_ref))
+    err = np.max(np.abs(o_gpu.astype(np.float64) - o_ref)) / (denom if denom > 0 else 1.0)
+    assert err <= ATTN_REL, f"{name}: rel err {err:.3e} > {ATTN_REL}"
+    return err
+
+
+def _near_mid(v, tol):
+    a = np.abs(v)
+    return np.any(np.abs(a[..., None] - E2M1_MIDS) <= tol * np.maximum(1.0, a[..., None]), axis=-1)
+
+
+def unpack_codes(packed):
+    packed = np.asarray(packed, np.uint8)
+    out = np.empty(packed.shape[:-1] + (packed.shape[-1] * 2,), np.uint8)
+    out[..., 0::2] = packed & 0xF
+    out[..., 1::2] = packed >> 4
+    return out
+
+
+def write_exclusions(x64, group, scale_fmt, err_abs):
+    """Mask of elements [N, D] whose code the oracle cannot fix to within err_abs of the value:
+    near a rounding midpoint of x/s, or in a group whose scale choice is near a boundary."""
+    N, D = x64.shape
+    g = x64.reshape(N, D // group, group)
+    amax = np.abs(g).max(axis=2)
+    err = np.broadcast_to(err_abs, x64.shape).reshape(N, D // group, group)
+    gerr = err.max(axis=2)
+    if scale_fmt == O.SCALE_E8M0:
+        cand = 6.0 * O.e8m0_decode(np.arange(255))
+    else:
+        cand = 6.0 * O.e4m3_decode(np.arange(1, 127))
+    near_b = np.min(np.abs(amax[..., None] - cand[None, None, :]), axis=-1) <= gerr
+    sb = O.e8m0_scale_byte(amax) if scale_fmt == O.SCALE_E8M0 else O.e4m3_scale_byte(amax)
+    s = O.e8m0_decode(sb) if scale_fmt == O.SCALE_E8M0 else O.e4m3_decode(sb)
+    v = g / s[..., None]
+    near_m = _near_mid(v, 0.0) | (np.min(np.abs(np.abs(v)[..., None] - E2M1_MIDS), axis=-1) <= err / s[..., None])
+    mask = near_m | near_b[..., None]
+    return mask.reshape(N, D)

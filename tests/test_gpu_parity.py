@@ -1,0 +1,312 @@
+"""GPU parity: every entry point of include/hsa.h, called through the C ABI, against the fp64
+oracle on the same seeded inputs. Sizes span several tiles and a ragged tail, and the edge
+cases (tiny and non-multiple contexts, contexts shorter than the window, multi-query verify
+blocks, out-of-range indices) are covered. Downstream checks are conditional: reindex is
+checked with the kernel's own pool and attention with the kernel's own indices, so a legal
+near-tie upstream cannot cascade."""
+import numpy as np
+import pytest
+
+import oracle as O
+from hierarchical_sparse_attention_index_gb300 import synth
+from tests import parity as P
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hsa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from hierarchical_sparse_attention_index_gb300 import build
+    build.build()
+    import hierarchical_sparse_attention_index_gb300 as H
+    H.load_library()
+    return H
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def gpu_cache(H, oc, cap, fmt=O.SCALE_E8M0):
+    B = oc["kv_q"].shape[0]
+    return H.Cache(B, cap, 1, fmt, tensors=(dev(oc["kv_q"]), dev(oc["kv_s"]), dev(oc["ik_q"]), dev(oc["ik_s"])))
+
+
+def round8(n):
+    return max(8, (n + 7) // 8 * 8)
+
+
+# ------------------------------------------------------------------ cache write
+def _check_write(H, oc_lat, oc_bytes, gpu, entries, fmt, name):
+    """oc_lat: oracle fp64 latents [n,512]; oc_bytes: oracle (kv_q, kv_s, ik_q, ik_s); gpu: same from device."""
+    lat, K, W = oc_lat
+    n = lat.shape[0]
+    # main KV
+    ex = P.write_exclusions(lat, 16, fmt, P.WRITE_REL * np.maximum(1.0, np.abs(lat)))
+    gc = P.unpack_codes(gpu[0][entries])
+    oc = P.unpack_codes(oc_bytes[0])
+    grp_ex = ex.reshape(n, 32, 16).any(axis=2)
+    bad = (gc != oc) & ~ex
+    assert not bad.any(), f"{name}: {bad.sum()} main-KV codes differ outside the band"
+    bad_s = (gpu[1][entries] != oc_bytes[1]) & ~grp_ex
+    assert not bad_s.any(), f"{name}: {bad_s.sum()} main-KV scales differ"
+    assert ex.mean() < 1e-3, f"{name}: band excludes {ex.mean():.2e} of the elements"
+    # indexer K (compare element codes in natural order)
+    kerr = 4e-6 * (np.abs(lat) @ np.abs(W)) + P.WRITE_REL * np.abs(K)
+    exk = P.write_exclusions(K, 32, O.SCALE_E8M0, kerr)
+    gk = P.unpack_codes(O.index_k_to_natural(gpu[2][entries]))
+    ok_ = P.unpack_codes(O.index_k_to_natural(oc_bytes[2]))
+    bad = (gk != ok_) & ~exk
+    assert not bad.any(), f"{name}: {bad.sum()} indexer-K codes differ outside the band"
+    bad_s = (gpu[3][entries] != oc_bytes[3]) & ~exk.reshape(n, 4, 32).any(axis=2)
+    assert not bad_s.any(), f"{name}: {bad_s.sum()} indexer-K scales differ"
+    assert exk.mean() < 1e-2
+
+
+@pytest.mark.parametrize("fmt", [O.SCALE_E8M0, O.SCALE_E4M3])
+def test_cache_write_m1(hsa, fmt):
+    H = hsa
+    seed, B, n, cap = 11, 2, 777, 1024
+    starts = np.array([0, 100], np.int64)
+    wkv = np.stack([synth.latents_bf16(seed, 20, b, n) for b in range(B)])
+    W = synth.w_idx_bf16(seed, 20)
+    cache = H.Cache(B, cap, 1, fmt)
+    H.hsa_cache_write_compress(cache, dev_bf16(wkv), None, dev_bf16(W), n, dev(starts))
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    g = [t.cpu().numpy() for t in (cache.kv_q, cache.kv_s, cache.ik_q, cache.ik_s)]
+    for b in range(B):
+        kv_q, kv_s, ik_q, ik_s, lat, K = O.cache_write_compress(P.f32(wkv[b]), None, P.f32(W), 1, fmt)
+        ent = np.arange(starts[b], starts[b] + n)
+        _check_write(H, (lat, K, P.f32(W).astype(np.float64)), (kv_q, kv_s, ik_q, ik_s),
+                     [x[b] for x in g], ent, fmt, f"m1 b{b}")
+        untouched = np.setdiff1d(np.arange(cap), ent)
+        assert not g[0][b][untouched].any() and not g[2][b][untouched].any()
+
+
+@pytest.mark.parametrize("fmt", [O.SCALE_E8M0, O.SCALE_E4M3])
+def test_cache_write_m2(hsa, fmt):
+    H = hsa
+    seed, n = 12, 4097                       # odd: the trailing token is not written
+    wkv = synth.latents_bf16(seed, 2, 0, n)[None]
+    wg = synth.gates_bf16(seed, 2, 0, n)[None]
+    W = synth.w_idx_bf16(seed, 2)
+    cache = H.Cache(1, 2056, 2, fmt)
+    H.hsa_cache_write_compress(cache, dev_bf16(wkv), dev_bf16(wg), dev_bf16(W), n, None)
+    g = [t.cpu().numpy()[0] for t in (cache.kv_q, cache.kv_s, cache.ik_q, cache.ik_s)]
+    kv_q, kv_s, ik_q, ik_s, lat, K = O.cache_write_compress(P.f32(wkv[0]), P.f32(wg[0]), P.f32(W), 2, fmt)
+    assert lat.shape[0] == 2048
+    _check_write(H, (lat, K, P.f32(W).astype(np.float64)), (kv_q, kv_s, ik_q, ik_s), g, np.arange(2048), fmt, "m2")
+    assert not g[0][2048:].any()
+
+
+def test_cache_write_rejects_bad_args(hsa):
+    H = hsa
+    cache = H.Cache(1, 64, 2)
+    x = torch.zeros(1, 16, 512, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(512, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(H.HsaError):          # ratio 2 needs wgate
+        H.hsa_cache_write_compress(cache, x, None, W, 16)
+    starts = torch.tensor([60], dtype=torch.int64, device="cuda")
+    H.hsa_cache_write_compress(cache, x, x, W, 16, starts)   # entries 60..67: 64..67 are past capacity
+    code, flags = H.hsa_get_device_status()
+    assert flags & H.HSA_FLAG_WRITE_RANGE
+
+
+# ------------------------------------------------------------------ Full indexer
+FULL_CASES = [  # (B, T, nq)
+    (1, 32768, 1), (3, 5000, 1), (1, 1, 1), (1, 7, 1), (1, 9, 1), (1, 511, 1), (1, 513, 1),
+    (1, 16385, 1), (2, 4100, 5), (1, 20000, 2),
+]
+
+
+def _full_case(H, B, T, nq, seed=0):
+    cap = round8(T)
+    oc = P.oracle_cache(seed, 20, B, T, cap)
+    q = synth.index_q_bf16(seed, 20, B, nq)
+    w = synth.index_w(seed, 20, B, nq)
+    vis = synth.visibility(B, nq, T)
+    cache = gpu_cache(H, oc, cap)
+    ws = H.new_workspace(B, nq, T)
+    topk = torch.full((B, nq, 512), -7, dtype=torch.int32, device="cuda")
+    pool = torch.full((B, nq, 16384), -7, dtype=torch.int32, device="cuda")
+    H.hsa_index_full(cache, dev_bf16(q), dev(w), dev(vis), nq, T, topk, pool, ws)
+    return oc, q, w, vis, cache, ws, topk, pool
+
+
+@pytest.mark.parametrize("B,T,nq", FULL_CASES)
+def test_index_full(hsa, B, T, nq):
+    H = hsa
+    oc, q, w, vis, cache, ws, topk, pool = _full_case(H, B, T, nq)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    topk, pool = topk.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        K = P.dequant_index(oc, b, T)
+        for i in range(nq):
+            s = O.index_scores(P.f32(q[b, i]), w[b, i], K, int(vis[b, i]))
+            P.check_topk(topk[b, i], s, int(vis[b, i]), name=f"topk b{b} q{i}")
+            P.check_pool(pool[b, i], s, int(vis[b, i]), name=f"pool b{b} q{i}")
+
+
+def test_index_full_repeatable(hsa):
+    """The workspace is left clean: a second call gives the same indices."""
+    H = hsa
+    oc, q, w, vis, cache, ws, topk, pool = _full_case(H, 2, 9000, 1)
+    t1, p1 = topk.clone(), pool.clone()
+    H.hsa_index_full(cache, dev_bf16(q), dev(w), dev(vis), 1, 9000, topk, pool, ws)
+    assert torch.equal(t1, topk) and torch.equal(p1, pool)
+
+
+def test_index_full_ties(hsa):
+    """All-equal scores (a zero query): the lowest positions and blocks win."""
+    H = hsa
+    T = 40000
+    oc = P.oracle_cache(5, 20, 1, T, T)
+    cache = gpu_cache(H, oc, T)
+    q = torch.zeros(1, 1, 16, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(1, 1, 16, device="cuda")
+    vis = torch.tensor([[T]], dtype=torch.int32, device="cuda")
+    ws = H.new_workspace(1, 1, T)
+    topk = torch.empty(1, 1, 512, dtype=torch.int32, device="cuda")
+    pool = torch.empty(1, 1, 16384, dtype=torch.int32, device="cuda")
+    H.hsa_index_full(cache, q, w, vis, 1, T, topk, pool, ws)
+    assert topk.cpu().numpy()[0, 0].tolist() == list(range(512))
+    assert pool.cpu().numpy()[0, 0].tolist() == list(range(16384))
+
+
+# ------------------------------------------------------------------ Reindex
+@pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 3000, 1), (1, 200000, 1)])
+def test_index_reindex(hsa, B, T, nq):
+    H = hsa
+    oc, q, w, vis, cache, ws, topk, pool = _full_case(H, B, T, nq)
+    q2 = synth.index_q_bf16(0, 24, B, nq)
+    w2 = synth.index_w(0, 24, B, nq)
+    out = torch.full((B, nq, 512), -7, dtype=torch.int32, device="cuda")
+    H.hsa_index_reindex(cache, dev_bf16(q2), dev(w2), dev(vis), nq, T, pool, out, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    out, pool = out.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        K = P.dequant_index(oc, b, T)
+        for i in range(nq):
+            v = int(vis[b, i])
+            ref, _ = O.index_reindex(P.f32(q2[b, i]), w2[b, i], K, pool[b, i], v)
+            s = O.index_scores(P.f32(q2[b, i]), w2[b, i], K, v)
+            g = out[b, i]
+            kk = min(512, int(((pool[b, i] >= 0) & (pool[b, i] < v)).sum()))
+            assert (g >= 0).sum() == kk and np.all(g[kk:] == -1) and np.all(np.diff(g[:kk]) > 0)
+            assert set(g[:kk].tolist()) <= set(pool[b, i].tolist())
+            P.check_set_band(g[:kk], ref[ref >= 0], s, f"reindex b{b} q{i}")
+            if -(-v // 8) <= 2048:    # the pool is the whole context: reindex == full top-k
+                P.check_topk(g, s, v, name="reindex-as-full")
+
+
+# ------------------------------------------------------------------ attention
+def _attn_ref(oc, b, i, T, topk_row, swa_rows, q, vis, scale, fmt=O.SCALE_E8M0):
+    Km = P.dequant_main(oc, b, T, fmt)
+    rows = O.attention_rows(Km, topk_row, O.swa_decode(swa_rows), i, vis)
+    return O.sparse_attention(P.f32(q), rows, scale)
+
+
+@pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 300, 1), (1, 50, 1), (3, 2000, 2)])
+def test_sparse_attention(hsa, B, T, nq):
+    H = hsa
+    oc, q, w, vis, cache, ws, topk, pool = _full_case(H, B, T, nq)
+    qa = synth.attn_q_bf16(0, 20, B, nq)
+    swa = synth.swa_e4m3(0, 20, B, nq)
+    out = torch.full((B, nq, 64, 512), float("nan"), device="cuda")
+    H.hsa_sparse_attn_decode(cache, dev_bf16(qa), topk, dev(swa), dev(vis), nq, T, 1.0, out, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    out, topk = out.cpu().numpy(), topk.cpu().numpy()
+    for b in range(B):
+        for i in range(nq):
+            ref = _attn_ref(oc, b, i, T, topk[b, i], swa[b], qa[b, i], int(vis[b, i]), 1.0)
+            P.check_attention(out[b, i], ref, f"attn b{b} q{i}")
+
+
+def test_sparse_attention_scale_and_e4m3_scales(hsa):
+    H = hsa
+    T, fmt = 6000, O.SCALE_E4M3
+    oc = P.oracle_cache(3, 20, 1, T, T, scale_fmt=fmt)
+    cache = gpu_cache(H, oc, T, fmt)
+    rng = np.random.default_rng(0)
+    topk = np.sort(rng.choice(T, 512, replace=False)).astype(np.int32)[None, None]
+    qa = synth.attn_q_bf16(3, 21, 1, 1)
+    swa = synth.swa_e4m3(3, 21, 1, 1)
+    vis = np.array([[T]], np.int32)
+    out = torch.empty(1, 1, 64, 512, device="cuda")
+    ws = H.new_workspace(1, 1, T)
+    H.hsa_sparse_attn_decode(cache, dev_bf16(qa), dev(topk), dev(swa), dev(vis), 1, T, 3.0, out, ws)
+    ref = _attn_ref(oc, 0, 0, T, topk[0, 0], swa[0], qa[0, 0], T, 3.0, fmt)
+    P.check_attention(out.cpu().numpy()[0, 0], ref, "attn e4m3 scale 3")
+
+
+def test_sparse_attention_flags_bad_index(hsa):
+    H = hsa
+    T = 1000
+    oc = P.oracle_cache(4, 20, 1, T, T)
+    cache = gpu_cache(H, oc, T)
+    topk = np.full((1, 1, 512), -1, np.int32)
+    topk[0, 0, :3] = [5, 999, 1200]          # 1200 >= vis: skipped and flagged
+    qa = synth.attn_q_bf16(4, 20, 1, 1)
+    swa = synth.swa_e4m3(4, 20, 1, 1)
+    out = torch.empty(1, 1, 64, 512, device="cuda")
+    ws = H.new_workspace(1, 1, T)
+    H.hsa_sparse_attn_decode(cache, dev_bf16(qa), dev(topk), dev(swa), dev(np.array([[T]], np.int32)), 1, T, 1.0,
+                             out, ws)
+    code, flags = H.hsa_get_device_status()
+    assert flags & H.HSA_FLAG_INDEX_RANGE
+    ref = _attn_ref(oc, 0, 0, T, np.array([5, 999]), swa[0], qa[0, 0], T, 1.0)
+    P.check_attention(out.cpu().numpy()[0, 0], ref, "attn bad index")
+
+
+# ------------------------------------------------------------------ schedule
+def test_schedule_step(hsa):
+    H = hsa
+    B, T, nq, seed = 2, 12345, 1, 0
+    layers = [20, 21, 24, 25]
+    modes = [H.HSA_MODE_FULL, H.HSA_MODE_REUSE, H.HSA_MODE_REINDEX, H.HSA_MODE_REUSE]
+    cap = round8(T)
+    oc = P.oracle_cache(seed, 20, B, T, cap)
+    cache = gpu_cache(H, oc, cap)
+    vis = synth.visibility(B, nq, T)
+    qi = {l: synth.index_q_bf16(seed, l, B, nq) for l in (20, 24)}
+    wi = {l: synth.index_w(seed, l, B, nq) for l in (20, 24)}
+    qa = {l: synth.attn_q_bf16(seed, l, B, nq) for l in layers}
+    sw = {l: synth.swa_e4m3(seed, l, B, nq) for l in layers}
+    d_qi = [dev_bf16(qi[l]) if l in qi else None for l in layers]
+    d_wi = [dev(wi[l]) if l in wi else None for l in layers]
+    d_qa = [dev_bf16(qa[l]) for l in layers]
+    d_sw = [dev(sw[l]) for l in layers]
+    outs = [torch.empty(B, nq, 64, 512, device="cuda") for _ in layers]
+    tk = [torch.empty(B, nq, 512, dtype=torch.int32, device="cuda") if l in qi else None for l in layers]
+    pool = torch.empty(B, nq, 16384, dtype=torch.int32, device="cuda")
+    d_vis = dev(vis)
+    ws = H.new_workspace(B, nq, T)
+    step = H.StepArgs(modes, d_qi, d_wi, d_qa, d_sw, outs, tk, pool, d_vis, nq, T, 1.0)
+    H.hsa_schedule_step(cache, step, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    pool_h = pool.cpu().numpy()
+    t20, t24 = tk[0].cpu().numpy(), tk[2].cpu().numpy()
+    for b in range(B):
+        K = P.dequant_index(oc, b, T)
+        s20 = O.index_scores(P.f32(qi[20][b, 0]), wi[20][b, 0], K, T)
+        P.check_topk(t20[b, 0], s20, T, name="step L20")
+        P.check_pool(pool_h[b, 0], s20, T, name="step pool")
+        ref24, _ = O.index_reindex(P.f32(qi[24][b, 0]), wi[24][b, 0], K, pool_h[b, 0], T)
+        s24 = O.index_scores(P.f32(qi[24][b, 0]), wi[24][b, 0], K, T)
+        P.check_set_band(t24[b, 0][t24[b, 0] >= 0], ref24[ref24 >= 0], s24, "step L24")
+        for j, l in enumerate(layers):
+            idx = t20 if l < 24 else t24
+            ref = _attn_ref(oc, b, 0, T, idx[b, 0], sw[l][b], qa[l][b, 0], T, 1.0)
+            P.check_attention(outs[j].cpu().numpy()[b, 0], ref, f"step attn L{l}")

@@ -121,6 +121,21 @@ def test_quantise_bounds_and_roundtrip(fmt, group):
     assert np.all(deq[0] == 0)
 
 
+def test_index_k_fragment_order():
+    for stored, t, s_, i, lo, hi in read_golden("index_k_fragment_order.txt"):
+        stored = int(stored)
+        assert stored == 16 * int(t) + 2 * int(s_) + int(i)
+        row = np.zeros((1, 64), np.uint8)
+        row[0, stored] = 0x21                      # low nibble 1 (+0.5), high nibble 2 (+1.0)
+        vals = O.index_k_dequant(row, np.full((1, 4), 127, np.uint8))[0]
+        nz = np.nonzero(vals)[0].tolist()
+        assert nz == [int(lo), int(hi)] and vals[int(lo)] == 0.5 and vals[int(hi)] == 1.0
+    # the stored order is a permutation: natural -> stored -> natural is the identity
+    rng = np.random.default_rng(0)
+    x = rng.integers(0, 256, (5, 64)).astype(np.uint8)
+    assert np.array_equal(O.index_k_to_natural(O.index_k_to_stored(x)), x)
+
+
 def test_nibble_order_low_first():
     x = np.zeros((1, 32), np.float32)
     x[0, 0] = 6.0     # element 0 -> low nibble of byte 0
@@ -177,7 +192,7 @@ def test_score_worked_example():
     want = []
     for i, (_, b0, b16, s0, s1, s2, s3, exp) in enumerate(rows):
         ik_q[i, 0] = int(b0, 16)
-        ik_q[i, 16] = int(b16, 16)
+        ik_q[i, 4] = int(b16, 16)
         ik_s[i] = [int(s0), int(s1), int(s2), int(s3)]
         want.append(float(exp))
     K = O.index_k_dequant(ik_q, ik_s)
