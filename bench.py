@@ -249,6 +249,20 @@ def run_hsa(args):
                 "per_call_us": {k: round(v * 1e6, 2) for k, v in kt.items()},
                 "step_share": {k: round(v / sum(shares.values()), 3) for k, v in shares.items()}}
 
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(H, torch, I, args, world, barrier, st)
+    line = make_line(args, world, value, tmax, clocks, e2e, roofline)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, sample_requests=2, steps=20)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(H, torch, I, args, world, barrier, st):
     # end to end through the same public call with host buffers (pinned), copies in the timed region
     hin = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
            for k, v in I["host"].items()}
@@ -280,10 +294,13 @@ def run_hsa(args):
     f1.record(st)
     barrier()
     te = max(f0.elapsed_time(f1) * 1e-3, 1e-9)
-    e2e = {"value": round(world * e2e_steps / te, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "wall_s": round(time.perf_counter() - t0, 4)}
+    return {"value": round(world * e2e_steps / te, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": e2e_steps, "wall_s": round(time.perf_counter() - t0, 4)}
 
-    line = {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+
+def make_line(args, world, value, tmax, clocks, e2e, roofline):
+    B, T = CFG.batch, CFG.T
+    return {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * tmax / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp4-e2m1 cache; f16 tensor-core MMA, fp32 accumulate",
             "data": "synthetic (seeded N(0,1) latents through the m=1 cache writer; bf16 queries)",
@@ -292,15 +309,7 @@ def run_hsa(args):
                        "parallelism": f"replicas x{world} (requests sharded, no collective)",
                        "l2": "inputs larger than L2 (1.49 GB FP4 cache per step)",
                        "step": "hsa_schedule_step captured in one CUDA graph"},
-            "clocks": clocks, "gpu_launches": args.steps * 35,
-            "e2e": e2e, "roofline": roofline}
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args, sample_requests=2, steps=20)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+            "clocks": clocks, "gpu_launches": args.steps * 35, "e2e": e2e, "roofline": roofline}
 
 
 def _threads_used():
@@ -404,15 +413,22 @@ def run_reference(args):
 
 
 def main():
+    global CFG
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["hsa", "reference"], default="hsa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=CFG.batch, help="requests per GPU (profiling runs)")
+    ap.add_argument("--ctx", type=int, default=CFG.T, help="visible positions (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.batch != CFG.batch or args.ctx != CFG.T:
+        CFG = synth.DecodeConfig(f"b{args.batch}_t{args.ctx}_20layers", CFG.seed, args.batch, args.ctx, CFG.nq,
+                                 CFG.layers)
     if args.impl == "reference":
         run_reference(args)
     else:

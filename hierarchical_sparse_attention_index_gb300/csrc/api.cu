@@ -167,7 +167,8 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
   st = check_query(cache, nq, max_vis);
   if (st != HSA_OK) return st;
   if (!q || !w || !vis || !topk_out || (pool_mode ? !pool : !pool_out)) return HSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(topk_out) || (pool_out && !aligned16(pool_out))) return HSA_ERR_ALIGN;
+  if (!aligned16(q) || !aligned16(topk_out) || (pool_out && !aligned16(pool_out)) || (pool && !aligned16(pool)))
+    return HSA_ERR_ALIGN;
   WsLayout L;
   if (!make_ws_layout(cache->batch, nq, max_vis, &L)) return HSA_ERR_SHAPE;
   if (!ws || ws_bytes < L.total) return HSA_ERR_WORKSPACE;

@@ -143,20 +143,56 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     fence_mbar_init();
   }
 
+  // ---------------------------------------------------------------- issue every global load up front
+  // K rows: warp = 64-dim segment kb, 4 keys per thread (r = lane + 32 i)
+  const int kb = warp;
+  uint4 krow[4][4];
+  uint32_t rsc[4];
+  bool valid[4];
+  if (rank < 4) {
+    int idx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) idx[i] = __ldg(p.topk + (size_t)row * kTopK + rank * kKeys + lane + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      valid[i] = (idx[i] >= 0) && (idx[i] < vis) && (idx[i] < p.cap);
+      if (idx[i] >= 0 && !valid[i] && kb == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+      const size_t e = (size_t)b * p.cap + (valid[i] ? idx[i] : 0);
+      const uint4* cs = reinterpret_cast<const uint4*>(p.kv_q + e * 256 + kb * 32);
+      krow[i][0] = __ldg(cs);
+      krow[i][1] = __ldg(cs + 1);
+      rsc[i] = __ldg(reinterpret_cast<const uint32_t*>(p.kv_s + e * 32 + kb * 4));
+    }
+  } else {
+    // SWA row r holds position vis - 128 + r for this query (rows [qi, qi+128) of the buffer)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane + 32 * i;
+      valid[i] = (vis - kSwa + r) >= 0;
+      const uint4* cs = reinterpret_cast<const uint4*>(
+          p.swa + ((size_t)b * (kSwa + p.nq - 1) + qi + r) * kDLat + kb * 64);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) krow[i][j] = __ldg(cs + j);
+    }
+  }
+  // Q: 4 threads per head, 128 dims each
+  const int qh = tid >> 2, qk = tid & 3;
+  uint4 qraw[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHAtt + qh) * kDLat + qk * 128);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qraw[i] = __ldg(src + i);
+  }
+
   // ---------------------------------------------------------------- Q: bf16 -> f16 with per-head shift
   {
-    const int h = tid >> 2, qk = tid & 3;       // 4 threads per head, 128 dims each
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHAtt + h) * kDLat + qk * 128);
     float amax = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-      const uint4 v = __ldg(src + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
-      }
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                                           fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
@@ -164,82 +200,64 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     if (amax > 0.f) {
       int e;
       frexpf(amax, &e);
-      sh = 15 - e;
+      sh = max(-126, min(127, 15 - e));     // amax * 2^sh in [2^14, 2^15)
     }
-    if (qk == 0) s_scale[h] = ldexpf(p.sm_scale, -sh);
-#pragma unroll 2
+    const float mul = __uint_as_float((uint32_t)(127 + sh) << 23);   // exact power of two
+    if (qk == 0) s_scale[qh] = p.sm_scale * __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const uint4 v = __ldg(src + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __half lo = __float2half_rn(ldexpf(__uint_as_float(w[j] << 16), sh));
-        const __half hi = __float2half_rn(ldexpf(__uint_as_float(w[j] & 0xFFFF0000u), sh));
+        const __half lo = __float2half_rn(__uint_as_float(w[j] << 16) * mul);
+        const __half hi = __float2half_rn(__uint_as_float(w[j] & 0xFFFF0000u) * mul);
         o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
       }
       const int d = qk * 128 + i * 8;            // first dim of this 8-dim chunk
-      const uint32_t addr = sQ + (uint32_t)(d >> 6) * (kHAtt * 128u) + sw128(h, (d & 63) >> 3);
+      const uint32_t addr = sQ + (uint32_t)(d >> 6) * (kHAtt * 128u) + sw128(qh, (d & 63) >> 3);
       sts128(addr, o[0], o[1], o[2], o[3]);
     }
   }
 
-  // ---------------------------------------------------------------- K tile: gather + dequantise
-  {
-    const int kb = warp;                         // 64-dim segment handled by this warp
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane + 32 * i;
-      uint32_t o[32];
-      bool valid = false;
-      if (rank < 4) {
-        const int idx = __ldg(p.topk + (size_t)row * kTopK + rank * kKeys + r);
-        valid = (idx >= 0) && (idx < vis) && (idx < p.cap);
-        if (idx >= 0 && !valid && kb == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-        if (valid) {
-          const size_t e = (size_t)b * p.cap + idx;
-          const uint4* cs = reinterpret_cast<const uint4*>(p.kv_q + e * 256 + kb * 32);
-          const uint4 c0 = __ldg(cs), c1 = __ldg(cs + 1);
-          const uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(p.kv_s + e * 32 + kb * 4));
-          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  // ---------------------------------------------------------------- K tile: dequantise into the swizzled tile
 #pragma unroll
-          for (int j = 0; j < 8; ++j) e2m1x8_to_f16x2x4(cw[j], o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+  for (int i = 0; i < 4; ++i) {
+    const int r = lane + 32 * i;
+    uint32_t o[32];
+    if (rank < 4) {
+      const uint32_t cw[8] = {krow[i][0].x, krow[i][0].y, krow[i][0].z, krow[i][0].w,
+                              krow[i][1].x, krow[i][1].y, krow[i][1].z, krow[i][1].w};
 #pragma unroll
-          for (int gi = 0; gi < 4; ++gi) {
-            const uint32_t sb = (sc4 >> (8 * gi)) & 0xFFu;
-            const float sf = (p.scale_fmt == HSA_SCALE_E8M0) ? e8m0_to_f32(sb) : e4m3_to_f32(sb);
-            const __half hs = __float2half_rn(sf);
-            const uint32_t s2 = (uint32_t)__half_as_ushort(hs) * 0x10001u;
+      for (int j = 0; j < 8; ++j) e2m1x8_to_f16x2x4(cw[j], o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[8 * gi + j] = hmul2_u32(o[8 * gi + j], s2);
-          }
-        }
-      } else {
-        // SWA row r holds position vis - 128 + r for this query (rows [qi, qi+128) of the buffer)
-        valid = (vis - kSwa + r) >= 0;
-        if (valid) {
-          const uint8_t* srow = p.swa + ((size_t)b * (kSwa + p.nq - 1) + qi + r) * kDLat + kb * 64;
-          const uint4* cs = reinterpret_cast<const uint4*>(srow);
+      for (int gi = 0; gi < 4; ++gi) {
+        const uint32_t sb = (rsc[i] >> (8 * gi)) & 0xFFu;
+        const float sf = (p.scale_fmt == HSA_SCALE_E8M0) ? e8m0_to_f32(sb) : e4m3_to_f32(sb);
+        const __half hs = __float2half_rn(sf);
+        const uint32_t s2 = (uint32_t)__half_as_ushort(hs) * 0x10001u;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = __ldg(cs + j);
-            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        for (int j = 0; j < 8; ++j) o[8 * gi + j] = hmul2_u32(o[8 * gi + j], s2);
+      }
+    } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              o[8 * j + 2 * u] = e4m3x2_to_f16x2((uint16_t)(vw[u] & 0xFFFFu));
-              o[8 * j + 2 * u + 1] = e4m3x2_to_f16x2((uint16_t)(vw[u] >> 16));
-            }
-          }
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t vw[4] = {krow[i][j].x, krow[i][j].y, krow[i][j].z, krow[i][j].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          o[8 * j + 2 * u] = e4m3x2_to_f16x2((uint16_t)(vw[u] & 0xFFFFu));
+          o[8 * j + 2 * u + 1] = e4m3x2_to_f16x2((uint16_t)(vw[u] >> 16));
         }
       }
-      if (!valid) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = 0u;
-      }
-      if (kb == 0) s_valid[r] = valid ? 1 : 0;
-      const uint32_t blk = sK + (uint32_t)kb * (kKeys * 128u);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) sts128(blk + sw128(r, c), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
     }
+    if (!valid[i]) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = 0u;
+    }
+    if (kb == 0) s_valid[r] = valid[i] ? 1 : 0;
+    const uint32_t blk = sK + (uint32_t)kb * (kKeys * 128u);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) sts128(blk + sw128(r, c), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
   }
   fence_async_smem();
   tc_fence_before();

@@ -139,7 +139,7 @@ __device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, in
   named_bar_sync(1, kConsumers);
 }
 
-__global__ void __launch_bounds__(kScanThreads) index_scan_kernel(const ScanParams p) {
+__global__ void __maxnreg__(112) index_scan_kernel(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const ScanSmemLayout L = scan_smem_layout(p.pool_mode, p.nq);
   const int nql = p.pool_mode ? 1 : p.nq;
@@ -210,11 +210,15 @@ __global__ void __launch_bounds__(kScanThreads) index_scan_kernel(const ScanPara
         const int vis = __ldg(p.vis + row);
         const int* pr = p.pool + (int64_t)row * kPool + c * kChunk + lane * 8;
         int* sp = reinterpret_cast<int*>(smem + L.slotpos) + s * kChunk + lane * 8;
-        const int base = __ldg(pr);
+        const int4 pa = __ldg(reinterpret_cast<const int4*>(pr));
+        const int4 pb = __ldg(reinterpret_cast<const int4*>(pr) + 1);
+        const int pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        const int base = pv[0];
         bool ok = (base >= 0) && ((base & 7) == 0) && (base < p.cap);
         if (base >= 0 && !ok) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+#pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int v = __ldg(pr + j);
+          const int v = pv[j];
           int outv = -1;
           if (ok && v >= 0) {
             if (v == base + j && v < vis) outv = v;
@@ -401,21 +405,7 @@ __global__ void __launch_bounds__(kScanThreads) index_scan_kernel(const ScanPara
         const uint4 A0 = lds128(codes + r0 * 64 + 16 * t);
         const uint4 A1 = lds128(codes + r1 * 64 + 16 * t);
         const uint32_t S0 = lds32(scales + r0 * 4), S1 = lds32(scales + r1 * 4);
-        uint32_t a0[16], a1[16];
-        e2m1x8_to_f16x2x4(A0.x, a0[0], a0[1], a0[2], a0[3]);
-        e2m1x8_to_f16x2x4(A0.y, a0[4], a0[5], a0[6], a0[7]);
-        e2m1x8_to_f16x2x4(A0.z, a0[8], a0[9], a0[10], a0[11]);
-        e2m1x8_to_f16x2x4(A0.w, a0[12], a0[13], a0[14], a0[15]);
-        e2m1x8_to_f16x2x4(A1.x, a1[0], a1[1], a1[2], a1[3]);
-        e2m1x8_to_f16x2x4(A1.y, a1[4], a1[5], a1[6], a1[7]);
-        e2m1x8_to_f16x2x4(A1.z, a1[8], a1[9], a1[10], a1[11]);
-        e2m1x8_to_f16x2x4(A1.w, a1[12], a1[13], a1[14], a1[15]);
-        float sc0[4], sc1[4];
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-          sc0[gi] = e8m0_to_f32(S0 >> (8 * gi));
-          sc1[gi] = e8m0_to_f32(S1 >> (8 * gi));
-        }
+        const uint32_t aw0[4] = {A0.x, A0.y, A0.z, A0.w}, aw1[4] = {A1.x, A1.y, A1.z, A1.w};
         int pos0, pos1;
         bool in0 = true, in1 = true;
         if (!p.pool_mode) {
@@ -436,25 +426,27 @@ __global__ void __launch_bounds__(kScanThreads) index_scan_kernel(const ScanPara
             for (int j = 0; j < 4; ++j) tot[nt][j] = 0.f;
 #pragma unroll
           for (int gi = 0; gi < 4; ++gi) {
+            // group gi = word gi of each row's chunk = k-steps 2gi (bytes 0,1) and 2gi+1 (bytes 2,3)
+            uint32_t f0, f1, f2, f3, h0, h1, h2, h3;
+            e2m1x8_to_f16x2x4(aw0[gi], f0, f1, f2, f3);
+            e2m1x8_to_f16x2x4(aw1[gi], h0, h1, h2, h3);
+            // E8M0 scale as a float: 2^(b-127) for b in 1..254; b = 0 only occurs with all-zero
+            // codes (amax = 0), where 0 * 0 = 0 either way
+            const float sc0 = __uint_as_float(((S0 >> (8 * gi)) & 0xFFu) << 23);
+            const float sc1 = __uint_as_float(((S1 >> (8 * gi)) & 0xFFu) << 23);
             float tmp[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) tmp[nt][j] = 0.f;
-#pragma unroll
-            for (int ss = 0; ss < 2; ++ss) {
-              const int ks = 2 * gi + ss;
-              const uint32_t x0 = a0[4 * gi + 2 * ss], x2 = a0[4 * gi + 2 * ss + 1];
-              const uint32_t x1 = a1[4 * gi + 2 * ss], x3 = a1[4 * gi + 2 * ss + 1];
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) mma_f16_16816(tmp[nt], x0, x1, x2, x3, B[nt][ks][0], B[nt][ks][1]);
+            for (int nt = 0; nt < 2; ++nt) {
+              tmp[nt][0] = tmp[nt][1] = tmp[nt][2] = tmp[nt][3] = 0.f;
+              mma_f16_16816(tmp[nt], f0, h0, f1, h1, B[nt][2 * gi][0], B[nt][2 * gi][1]);
+              mma_f16_16816(tmp[nt], f2, h2, f3, h3, B[nt][2 * gi + 1][0], B[nt][2 * gi + 1][1]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-              tot[nt][0] = fmaf(sc0[gi], tmp[nt][0], tot[nt][0]);
-              tot[nt][1] = fmaf(sc0[gi], tmp[nt][1], tot[nt][1]);
-              tot[nt][2] = fmaf(sc1[gi], tmp[nt][2], tot[nt][2]);
-              tot[nt][3] = fmaf(sc1[gi], tmp[nt][3], tot[nt][3]);
+              tot[nt][0] = fmaf(sc0, tmp[nt][0], tot[nt][0]);
+              tot[nt][1] = fmaf(sc0, tmp[nt][1], tot[nt][1]);
+              tot[nt][2] = fmaf(sc1, tmp[nt][2], tot[nt][2]);
+              tot[nt][3] = fmaf(sc1, tmp[nt][3], tot[nt][3]);
             }
           }
           float v0 = 0.f, v1 = 0.f;
@@ -538,7 +530,7 @@ __global__ void __launch_bounds__(kScanThreads) index_scan_kernel(const ScanPara
 
 // ------------------------------------------------------------------ collect
 constexpr int kCollectThreads = 256;
-constexpr int kCollectChunk = 8192;
+constexpr int kCollectChunk = 2048;   // 8 elements per thread, all loads issued first
 
 __device__ __forceinline__ void warp_append(bool pred, int value, int* counter, int* list, int cap,
                                             uint32_t* status) {
@@ -585,25 +577,31 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectPa
   int* cand = p.cand + (size_t)row * p.ld_cand + cand_off;
   int* sure = p.sure + (size_t)row * p.ld_sure + sure_off;
   const int e1 = min(n, e0 + kCollectChunk);
-  for (int base = e0; base < e1; base += kCollectThreads) {
-    const int e = base + threadIdx.x;
+  constexpr int kPer = kCollectChunk / kCollectThreads;
+  float v[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = e0 + j * kCollectThreads + threadIdx.x;
+    v[j] = (e < e1) ? __ldcg(data + e) : -INFINITY;
+  }
+  const int cand_cap = (int)(which == 0 ? (p.pool_mode ? kPool : p.ld_s) : p.ld_b);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = e0 + j * kCollectThreads + threadIdx.x;
     bool is_sure = false, is_cand = false;
-    if (e < e1) {
-      const float v = __ldcg(data + e);
-      if (v != -INFINITY) {
-        const int bin = (int)(order_key(v) >> kHistShift);
-        is_sure = (thr < 0) || (bin > thr);
-        is_cand = (thr >= 0) && (bin == thr);
-      }
+    if (v[j] != -INFINITY) {
+      const int bin = (int)(order_key(v[j]) >> kHistShift);
+      is_sure = (thr < 0) || (bin > thr);
+      is_cand = (thr >= 0) && (bin == thr);
     }
     warp_append(is_sure, e, &st->nsure, sure, sure_cap, p.status);
-    warp_append(is_cand, e, &st->ncand, cand, (int)(which == 0 ? (p.pool_mode ? kPool : p.ld_s) : p.ld_b),
-                p.status);
+    warp_append(is_cand, e, &st->ncand, cand, cand_cap, p.status);
   }
 }
 
 // ------------------------------------------------------------------ finish
 constexpr int kFinishThreads = 1024;
+constexpr int kFinStage = 8192;   // candidates staged in shared memory
 
 __device__ __forceinline__ int block_excl_scan_1024(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -659,6 +657,8 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
   uint32_t* bitmap = fsm;                       // [nwords]
   uint32_t* shist = fsm + ((nwords + 3) & ~3);  // [2048]
   int* scratch = reinterpret_cast<int*>(shist + 2048);   // [64]
+  int* s_cidx = scratch + 64;                   // [kFinStage]
+  uint32_t* s_ckey = reinterpret_cast<uint32_t*>(s_cidx + kFinStage);   // [kFinStage]
 
   __shared__ int s_thr, s_nvalid, s_nsure, s_ncand, s_ready;
   __shared__ int s_digit, s_above, s_cnt;
@@ -687,6 +687,28 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
   }
   int need = Keff - nsure;
   if (thr >= 0 && need > 0 && ncand > 0) {
+    // stage the candidates (index, low 20 key bits) in shared memory when they fit
+    const bool staged = ncand <= kFinStage;
+    if (staged) {
+      for (int i = tid; i < ncand; i += kFinishThreads) {
+        const int e = __ldcg(cand + i);
+        s_cidx[i] = e;
+        s_ckey[i] = order_key(__ldcg(data + e)) & 0xFFFFFu;
+      }
+      __syncthreads();
+    }
+    auto comp_of = [&](int i) -> uint64_t {
+      int e;
+      uint32_t k20;
+      if (staged) {
+        e = s_cidx[i];
+        k20 = s_ckey[i];
+      } else {
+        e = __ldcg(cand + i);
+        k20 = order_key(__ldcg(data + e)) & 0xFFFFFu;
+      }
+      return ((uint64_t)k20 << 32) | (uint64_t)(~(uint32_t)e);
+    };
     uint64_t prefix = 0, mask = 0;
     int remaining = need;
     const int shifts[5] = {41, 30, 19, 8, 0};
@@ -697,9 +719,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
       for (int i = tid; i < 2048; i += kFinishThreads) shist[i] = 0;
       __syncthreads();
       for (int i = tid; i < ncand; i += kFinishThreads) {
-        const int e = __ldcg(cand + i);
-        const uint32_t key = order_key(__ldcg(data + e));
-        const uint64_t comp = ((uint64_t)(key & 0xFFFFFu) << 32) | (uint64_t)(~(uint32_t)e);
+        const uint64_t comp = comp_of(i);
         if ((comp & mask) == prefix) atomicAdd(shist + ((comp >> sh) & wm), 1u);
       }
       __syncthreads();
@@ -728,10 +748,11 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
       if (all_in) break;
     }
     for (int i = tid; i < ncand; i += kFinishThreads) {
-      const int e = __ldcg(cand + i);
-      const uint32_t key = order_key(__ldcg(data + e));
-      const uint64_t comp = ((uint64_t)(key & 0xFFFFFu) << 32) | (uint64_t)(~(uint32_t)e);
-      if ((comp & mask) >= prefix) atomicOr(bitmap + (e >> 5), 1u << (e & 31));
+      const uint64_t comp = comp_of(i);
+      if ((comp & mask) >= prefix) {
+        const int e = (int)(~(uint32_t)(comp & 0xFFFFFFFFull));
+        atomicOr(bitmap + (e >> 5), 1u << (e & 31));
+      }
     }
   }
   __syncthreads();
@@ -840,7 +861,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t nwords = (nmax + 31) / 32;
-  const size_t smem = (size_t)((nwords + 3) & ~3) * 4 + 2048 * 4 + 64 * 4;
+  const size_t smem = (size_t)((nwords + 3) & ~3) * 4 + 2048 * 4 + 64 * 4 + (size_t)kFinStage * 8;
   static size_t set_bytes = 0;
   if (smem > set_bytes) {
     e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
