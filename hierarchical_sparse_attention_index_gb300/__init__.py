@@ -26,7 +26,7 @@ STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_SHAPE", 3: "HSA_ERR
 
 EXPORTS = ("hsa_abi_version", "hsa_status_string", "hsa_workspace_bytes", "hsa_workspace_init",
            "hsa_cache_write_compress", "hsa_index_full", "hsa_index_reindex", "hsa_sparse_attn_decode",
-           "hsa_schedule_step", "hsa_get_device_status")
+           "hsa_schedule_step", "hsa_get_device_status", "hsa_index_reindex_noalloc")
 
 
 class HsaError(RuntimeError):
@@ -76,6 +76,7 @@ def load_library(path: str = LIB_PATH):
         "hsa_sparse_attn_decode": (I32, [C, P, P, P, P, I32, I64, F, P, P, SZ, P]),
         "hsa_schedule_step": (I32, [C, ctypes.POINTER(hsa_step_args), P, SZ, P]),
         "hsa_get_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32)]),
+        "hsa_index_reindex_noalloc": (I32, [C, P, P, P, I32, I64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -172,6 +173,13 @@ def hsa_index_reindex(cache: Cache, q, w, vis, nq, max_vis, pool, topk_out, ws, 
     _check("hsa_index_reindex", load_library().hsa_index_reindex(
         cache.ref, _ptr(q), _ptr(w), _ptr(vis), nq, max_vis, _ptr(pool), _ptr(topk_out), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def hsa_index_reindex_noalloc(cache: Cache, q, w, vis, nq, max_vis, pool, topk_out, stream=None):
+    """Reindex without a caller workspace: the scratch is a fixed array inside the library
+    (batch * nq <= 32). For callers that cannot allocate device memory."""
+    _check("hsa_index_reindex_noalloc", load_library().hsa_index_reindex_noalloc(
+        cache.ref, _ptr(q), _ptr(w), _ptr(vis), nq, max_vis, _ptr(pool), _ptr(topk_out), _stream(stream)))
 
 
 def hsa_sparse_attn_decode(cache: Cache, q, topk, swa, vis, nq, max_vis, sm_scale, out, ws, stream=None):

@@ -59,6 +59,8 @@ hsa_status check_query(const hsa_cache* c, int32_t nq, int64_t max_vis) {
 
 }  // namespace
 
+bool device_status_ptr(uint32_t** status, int* sms) { return device_info(status, sms); }
+
 bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   if (batch < 1 || nq < 1 || nq > HSA_MAX_NQ || max_vis < 0 || max_vis > HSA_MAX_VIS) return false;
   const int64_t rows = (int64_t)batch * nq;

@@ -37,6 +37,10 @@ struct WsLayout {
 
 bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L);
 
+// Device address of the per-device status word and the SM count of the current device;
+// false on a non-sm_100-family device.
+bool device_status_ptr(uint32_t** status, int* sms);
+
 // ------------------------------------------------------------------ index scoring
 struct ScanParams {
   int32_t pool_mode;     // 0: Full (segment = request, nq queries share K); 1: Reindex (segment = (b,q))

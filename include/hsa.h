@@ -184,6 +184,25 @@ HSA_API hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, cons
                              int32_t nq, int64_t max_vis, const int32_t* pool, int32_t* topk_out,
                              void* ws, size_t ws_bytes, hsa_stream_t stream);
 
+/* Reindex without a workspace. The pages have no counterpart for this entry point; it is a
+ * convenience of this library. Some callers cannot allocate device memory at all: a plugin
+ * that may only touch the buffers it is handed, code running inside an arena planned by an
+ * inference server, or a latency-critical loop that must never wait on an allocator. They call
+ * this instead of hsa_index_reindex. Arguments, outputs and errors are those of
+ * hsa_index_reindex, without ws/ws_bytes. The scratch it needs (about 4.7 MB) is a fixed array
+ * in the library's own device memory, which every GPU that loads the library holds until the
+ * process exits.
+ *  - batch * nq must be at most 32; larger requests return HSA_ERR_SHAPE and launch nothing.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *    make that first call before capturing a stream into a CUDA graph.
+ *  - Every call shares the one array and clears the part that must start at zero
+ *    (cudaMemsetAsync on `stream`). Calls that overlap on the GPU (different streams, or
+ *    different host threads without ordering) race on it and give undefined results.
+ *  - It calls no cudaMalloc/cudaFree and no allocating library routine. */
+HSA_API hsa_status hsa_index_reindex_noalloc(const hsa_cache* cache, const void* q, const float* w,
+                                             const int32_t* vis, int32_t nq, int64_t max_vis, const int32_t* pool,
+                                             int32_t* topk_out, hsa_stream_t stream);
+
 /* Sparse attention ([CED] Figure 4: Selected Main KV ⊕ SWA KV -> Core Attention;
  * [890B] 注意力实际有多稀: 512 + 128 = 640 positions; [ARCH] §7: dequantise before attention).
  * For request b, query i and head h:
