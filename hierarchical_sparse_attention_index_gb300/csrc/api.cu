@@ -1,5 +1,7 @@
 // C ABI of libhsa (include/hsa.h): argument validation, workspace carve-up, launches and the
 // decode-step schedule. Everything here is host code; it launches kernels only.
+#include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -39,6 +41,14 @@ bool device_info(uint32_t** status, int* sms) {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Map a CUDA error to HSA_ERR_CUDA; with HSA_DEBUG set in the environment, name it on stderr.
+hsa_status cuda_fail(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return HSA_OK;
+  static const bool dbg = getenv("HSA_DEBUG") != nullptr;
+  if (dbg) fprintf(stderr, "hsa: %s: %s\n", where, cudaGetErrorString(e));
+  return HSA_ERR_CUDA;
+}
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 hsa_status check_cache(const hsa_cache* c) {
@@ -65,7 +75,7 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   if (batch < 1 || nq < 1 || nq > HSA_MAX_NQ || max_vis < 0 || max_vis > HSA_MAX_VIS) return false;
   const int64_t rows = (int64_t)batch * nq;
   L->rows = (int32_t)rows;
-  L->ld_s = round_up(std::max(max_vis, (int64_t)1), 256);
+  L->ld_s = round_up(std::max(max_vis, (int64_t)1), kScanChunk);
   L->ld_b = L->ld_s / 8;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -157,7 +167,7 @@ hsa_status hsa_cache_write_compress(const hsa_cache* cache, const void* wkv, con
   p.ik_s = cache->ik_s;
   p.status = status;
   if (p.n_entries == 0) return HSA_OK;
-  return launch_cache_write(p, (cudaStream_t)stream) == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
+  return cuda_fail(launch_cache_write(p, (cudaStream_t)stream), "cache write launch");
 }
 
 static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const void* q, const float* w,
@@ -207,7 +217,7 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
   se.status = status;
   if (!pool_mode) {
     sp.n_seg = cache->batch;
-    sp.chunks_per_seg = (int32_t)((std::max(max_vis, (int64_t)1) + 255) / 256);
+    sp.chunks_per_seg = (int32_t)((std::max(max_vis, (int64_t)1) + kScanChunk - 1) / kScanChunk);
     sp.scores = reinterpret_cast<float*>(W + L.off_scores);
     sp.ld_s = L.ld_s;
     sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
@@ -221,7 +231,7 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
     se.ld_sure = kTopK + kCandBlocks;
   } else {
     sp.n_seg = L.rows;
-    sp.chunks_per_seg = kPool / 256;
+    sp.chunks_per_seg = kPool / kScanChunk;
     sp.scores = reinterpret_cast<float*>(W + L.off_pscores);
     sp.ld_s = kPool;
     sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_pool);
@@ -239,9 +249,9 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
   se.ld_b = sp.ld_b;
   se.hist = sp.hist;
   se.state = sp.state;
-  if (launch_index_scan(sp, sms, s) != cudaSuccess) return HSA_ERR_CUDA;
-  if (launch_select(se, s) != cudaSuccess) return HSA_ERR_CUDA;
-  return HSA_OK;
+  hsa_status r = cuda_fail(launch_index_scan(sp, sms, s), "index scan launch");
+  if (r != HSA_OK) return r;
+  return cuda_fail(launch_select(se, s), "select launch");
 }
 
 hsa_status hsa_index_full(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,
@@ -285,7 +295,7 @@ hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const i
   p.sm_scale = sm_scale;
   p.out = out;
   p.status = status;
-  return launch_attention(p, (cudaStream_t)stream) == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
+  return cuda_fail(launch_attention(p, (cudaStream_t)stream), "attention launch");
 }
 
 hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, void* ws, size_t ws_bytes,

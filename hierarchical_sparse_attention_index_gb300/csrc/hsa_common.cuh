@@ -23,6 +23,7 @@ constexpr int kPool = HSA_POOL_SLOTS;
 constexpr int kSwa = HSA_SWA_W;
 constexpr int kMaxNq = HSA_MAX_NQ;
 constexpr int kHistBins = 4096;        // top 12 bits of the order key
+constexpr int kScanChunk = 512;        // entries per pipeline stage of the scoring kernel
 constexpr int kHistShift = 20;
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
@@ -138,6 +139,30 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Programmatic dependent launch: wait for the preceding kernel in the stream (and its memory),
+// and let the next kernel start its own setup early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialisation: the kernel may start while its predecessor
+// drains, and must call griddep_wait() before reading anything the predecessor wrote.
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bit) {

@@ -25,7 +25,7 @@ struct SelState {
 // Workspace carve-up for hsa_index_full / hsa_index_reindex / hsa_sparse_attn_decode.
 struct WsLayout {
   int32_t rows;        // batch * nq
-  int64_t ld_s;        // score row stride (positions), a multiple of 256
+  int64_t ld_s;        // score row stride (positions), a multiple of kScanChunk
   int64_t ld_b;        // block-max row stride (blocks) = ld_s / 8
   size_t off_scores, off_blkmax, off_hist_full, off_cand_full, off_sure_full, off_state_full, off_done_full;
   size_t off_pscores, off_hist_pool, off_cand_pool, off_sure_pool, off_state_pool, off_done_pool;

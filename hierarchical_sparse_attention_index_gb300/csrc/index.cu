@@ -28,14 +28,14 @@
 namespace hsa {
 namespace {
 
-constexpr int kChunk = 256;
+constexpr int kChunk = kScanChunk;
 constexpr int kMaxStages = 4;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kScanThreads = kConsumers + 32;
 constexpr int kCodesBytes = kChunk * 64;
 constexpr int kScaleBytes = kChunk * 4;
-constexpr int kFlushItems = 240;   // packed 16-bit histogram counters: flush before 65536 entries
+constexpr int kFlushItems = 120;   // packed 16-bit histogram counters: flush before 65536 entries
 
 struct ScanSmemLayout {
   int nst, nlr;
@@ -45,7 +45,7 @@ struct ScanSmemLayout {
 __host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq) {
   ScanSmemLayout L;
   const int nql = pool_mode ? 1 : nq;
-  L.nst = (nql <= 5) ? 4 : 2;
+  L.nst = (nql <= 2) ? 3 : (nql <= 5 ? 2 : 1);
   L.nlr = pool_mode ? 1 : 2 * nq;
   size_t o = 0;
   L.codes = o;   o += (size_t)L.nst * kCodesBytes;
@@ -103,12 +103,13 @@ __device__ __forceinline__ int excl_scan(int v, int* scratch, int bar_id, int nt
 // Threshold bin for a top-K over a 4096-bin histogram; 256 consumer threads (named barrier 1).
 __device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, int* scratch) {
   const int tid = threadIdx.x;
-  uint32_t cnt[16];
+  constexpr int kPerT = kHistBins / kConsumers;   // bins per thread
+  uint32_t cnt[kPerT];
   int local = 0;
-  const int top = kHistBins - 16 * (tid + 1);   // this thread owns bins [top, top+16), high first
+  const int top = kHistBins - kPerT * (tid + 1);   // this thread owns bins [top, top+kPerT), high first
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    cnt[i] = __ldcg(ghist + top + 15 - i);
+  for (int i = 0; i < kPerT; ++i) {
+    cnt[i] = __ldcg(ghist + top + kPerT - 1 - i);
     local += (int)cnt[i];
   }
   int total;
@@ -124,9 +125,9 @@ __device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, in
   } else if (excl < K && excl + local >= K) {
     int run = excl;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kPerT; ++i) {
       if (run + (int)cnt[i] >= K) {
-        st->thr_bin = top + 15 - i;
+        st->thr_bin = top + kPerT - 1 - i;
         st->above = run;
         st->nvalid = total;
         __threadfence();
@@ -139,7 +140,7 @@ __device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, in
   named_bar_sync(1, kConsumers);
 }
 
-__global__ void __maxnreg__(112) index_scan_kernel(const ScanParams p) {
+__global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const ScanSmemLayout L = scan_smem_layout(p.pool_mode, p.nq);
   const int nql = p.pool_mode ? 1 : p.nq;
@@ -167,6 +168,8 @@ __global__ void __maxnreg__(112) index_scan_kernel(const ScanParams p) {
     for (int i = tid; i < L.nlr * (kHistBins / 2); i += kScanThreads) h[i] = 0;
   }
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
   if (i0 >= i1) return;
 
   const int cps = p.chunks_per_seg;
@@ -204,36 +207,46 @@ __global__ void __maxnreg__(112) index_scan_kernel(const ScanParams p) {
           }
         }
       } else {
-        // pool gather: lane handles the 8-slot run `lane` of this 256-slot chunk
+        // pool gather: lane handles the 8-slot runs `lane` and `lane + 32` of this 512-slot chunk
         const int row = seg;
         const int b = row / p.nq;
         const int vis = __ldg(p.vis + row);
-        const int* pr = p.pool + (int64_t)row * kPool + c * kChunk + lane * 8;
-        int* sp = reinterpret_cast<int*>(smem + L.slotpos) + s * kChunk + lane * 8;
-        const int4 pa = __ldg(reinterpret_cast<const int4*>(pr));
-        const int4 pb = __ldg(reinterpret_cast<const int4*>(pr) + 1);
-        const int pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-        const int base = pv[0];
-        bool ok = (base >= 0) && ((base & 7) == 0) && (base < p.cap);
-        if (base >= 0 && !ok) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+        bool ok[2];
+        int base[2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int v = pv[j];
-          int outv = -1;
-          if (ok && v >= 0) {
-            if (v == base + j && v < vis) outv = v;
-            else if (v != base + j || v >= p.cap) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+        for (int u = 0; u < 2; ++u) {
+          const int bi = lane + 32 * u;
+          const int* pr = p.pool + (int64_t)row * kPool + c * kChunk + bi * 8;
+          int* sp = reinterpret_cast<int*>(smem + L.slotpos) + s * kChunk + bi * 8;
+          const int4 pa = __ldg(reinterpret_cast<const int4*>(pr));
+          const int4 pb = __ldg(reinterpret_cast<const int4*>(pr) + 1);
+          const int pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+          base[u] = pv[0];
+          ok[u] = (base[u] >= 0) && ((base[u] & 7) == 0) && (base[u] < p.cap);
+          if (base[u] >= 0 && !ok[u]) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int v = pv[j];
+            int outv = -1;
+            if (ok[u] && v >= 0) {
+              if (v == base[u] + j && v < vis) outv = v;
+              else if (v != base[u] + j || v >= p.cap) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+            }
+            sp[j] = outv;
           }
-          sp[j] = outv;
         }
-        const uint32_t m = __ballot_sync(0xffffffffu, ok);
+        const uint32_t m0 = __ballot_sync(0xffffffffu, ok[0]), m1 = __ballot_sync(0xffffffffu, ok[1]);
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(m) * (512u + 32u));
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(__popc(m0) + __popc(m1)) * (512u + 32u));
         __syncwarp();
-        if (ok) {
-          const int64_t e0 = (int64_t)b * p.cap + base;
-          bulk_g2s(dcodes + lane * 512, p.ik_q + e0 * 64, 512u, full);
-          bulk_g2s(dscales + lane * 32, p.ik_s + e0 * 4, 32u, full);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (ok[u]) {
+            const int bi = lane + 32 * u;
+            const int64_t e0 = (int64_t)b * p.cap + base[u];
+            bulk_g2s(dcodes + bi * 512, p.ik_q + e0 * 64, 512u, full);
+            bulk_g2s(dscales + bi * 32, p.ik_s + e0 * 4, 32u, full);
+          }
         }
       }
     }
@@ -299,7 +312,7 @@ __global__ void __maxnreg__(112) index_scan_kernel(const ScanParams p) {
 
   auto load_segment = [&](int seg) {
     named_bar_sync(1, kConsumers);
-    for (int ql = 0; ql < nql; ++ql) {
+    for (int ql = 0; ql < nql && tid < 256; ++ql) {
       const int row = p.pool_mode ? seg : seg * p.nq + ql;
       const int h = tid >> 4, d0 = (tid & 15) * 8;
       const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHIdx + h) * kDIdx + d0));
@@ -549,6 +562,8 @@ __device__ __forceinline__ void warp_append(bool pred, int value, int* counter, 
 }
 
 __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int row = blockIdx.y, which = blockIdx.z;
   const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
   const float* data;
@@ -633,6 +648,8 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
   extern __shared__ __align__(16) uint32_t fsm[];
   const int row = blockIdx.x, which = blockIdx.y;
   const int tid = threadIdx.x;
+  griddep_wait();
+  griddep_launch_dependents();
   const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
   const float* data;
   int n, K;
@@ -848,8 +865,7 @@ cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s) 
   int grid = num_sms * per_sm;
   if (grid > p.total_items) grid = p.total_items;
   if (grid < 1) grid = 1;
-  index_scan_kernel<<<grid, kScanThreads, L.total, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(index_scan_kernel, dim3(grid), dim3(kScanThreads), L.total, s, p);
 }
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
@@ -857,8 +873,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
   const int nsel = p.pool_mode ? 1 : 2;
   const int64_t nmax = p.pool_mode ? kPool : p.max_vis;
   dim3 cg((unsigned)((nmax + kCollectChunk - 1) / kCollectChunk), (unsigned)rows, (unsigned)nsel);
-  collect_kernel<<<cg, kCollectThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(collect_kernel, cg, dim3(kCollectThreads), 0, s, p);
   if (e != cudaSuccess) return e;
   const int64_t nwords = (nmax + 31) / 32;
   const size_t smem = (size_t)((nwords + 3) & ~3) * 4 + 2048 * 4 + 64 * 4 + (size_t)kFinStage * 8;
@@ -868,8 +883,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     set_bytes = smem;
   }
-  finish_kernel<<<dim3((unsigned)rows, (unsigned)nsel), kFinishThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(finish_kernel, dim3((unsigned)rows, (unsigned)nsel), dim3(kFinishThreads), smem, s, p);
 }
 
 }  // namespace hsa

@@ -99,7 +99,7 @@ extern "C" HSA_API hsa_status hsa_index_reindex_noalloc(const hsa_cache* cache, 
   sp.vis = vis;
   sp.pool = pool;
   sp.n_seg = rows;
-  sp.chunks_per_seg = kPool / 256;
+  sp.chunks_per_seg = kPool / kScanChunk;
   sp.total_items = sp.n_seg * sp.chunks_per_seg;
   sp.scores = reinterpret_cast<float*>(W + kOffScores);
   sp.ld_s = kPool;

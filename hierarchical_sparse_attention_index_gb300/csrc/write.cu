@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
   uint16_t* W = reinterpret_cast<uint16_t*>(wsm + kOffW);
   float* Ks = reinterpret_cast<float*>(wsm + kOffK);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();
+  griddep_launch_dependents();
 
   for (int i = tid; i < kDLat * kDIdx / 8; i += kWThreads)
     reinterpret_cast<uint4*>(W)[i] = __ldg(reinterpret_cast<const uint4*>(p.w_idx) + i);
@@ -283,8 +285,7 @@ cudaError_t launch_cache_write(const WriteParams& p, cudaStream_t s) {
   const int64_t ntiles = ((int64_t)p.batch * p.n_entries + kEnt - 1) / kEnt;
   int grid = (int)imin64(ntiles, (int64_t)sms);
   if (grid < 1) return cudaSuccess;
-  cache_write_kernel<<<grid, kWThreads, kWSmem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(cache_write_kernel, dim3(grid), dim3(kWThreads), kWSmem, s, p);
 }
 
 }  // namespace hsa
