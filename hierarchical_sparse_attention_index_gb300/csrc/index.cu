@@ -352,7 +352,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
         dst[1] = pk[2 * u + 1];
       }
       if ((tid & 15) == 0) wsc[ql * 16 + h] = ldexpf(__ldg(p.w + (size_t)row * kHIdx + h), -sh);
-      if (tid < 8 && !p.pool_mode && tid == ql) svis[ql] = __ldg(p.vis + row);
+      if (tid < 8 && !p.pool_mode && tid == ql) svis[ql] = (int)imin64(__ldg(p.vis + row), p.cap);
     }
     if (p.pool_mode && tid == 0) svis[0] = __ldg(p.vis + seg);
     named_bar_sync(1, kConsumers);
@@ -410,56 +410,65 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     const uint32_t scales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
     const int* slotpos = reinterpret_cast<const int*>(smem + L.slotpos) + s * kChunk;
 
-    if (nrows > 0) {
-#pragma unroll 1
+    if (warp * 32 < nrows) {
+      // per-stage constants of this warp
+      float* const score_base = p.pool_mode ? p.scores + (size_t)cur_seg * kPool + c * kChunk : nullptr;
+#pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
+        if (mt == 1 && warp * 32 + 16 >= nrows) break;
         const int r0 = warp * 32 + mt * 16 + g, r1 = r0 + 8;
-        if (warp * 32 + mt * 16 >= nrows) break;
         const uint4 A0 = lds128(codes + r0 * 64 + 16 * t);
         const uint4 A1 = lds128(codes + r1 * 64 + 16 * t);
         const uint32_t S0 = lds32(scales + r0 * 4), S1 = lds32(scales + r1 * 4);
         const uint32_t aw0[4] = {A0.x, A0.y, A0.z, A0.w}, aw1[4] = {A1.x, A1.y, A1.z, A1.w};
-        int pos0, pos1;
+        // row of this lane for the stores: lanes t = 0 and t = 1 own rows r0 and r1
+        const int myr = (t & 1) ? r1 : r0;
+        int mypos;                       // Full: position; Reindex: slot position (or -1)
         bool in0 = true, in1 = true;
-        if (!p.pool_mode) {
-          pos0 = c * kChunk + r0;
-          pos1 = c * kChunk + r1;
+        if (p.pool_mode) {
+          const int s0 = slotpos[r0], s1 = slotpos[r1];
+          in0 = s0 >= 0;
+          in1 = s1 >= 0;
+          mypos = (t & 1) ? s1 : s0;
         } else {
-          pos0 = slotpos[r0];
-          pos1 = slotpos[r1];
-          in0 = pos0 >= 0;
-          in1 = pos1 >= 0;
+          mypos = c * kChunk + myr;
         }
         for (int ql = 0; ql < nql; ++ql) {
           if (nql > 1) load_query_regs(ql);
           float tot[2][4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tot[nt][j] = 0.f;
 #pragma unroll
           for (int gi = 0; gi < 4; ++gi) {
             // group gi = word gi of each row's chunk = k-steps 2gi (bytes 0,1) and 2gi+1 (bytes 2,3)
             uint32_t f0, f1, f2, f3, h0, h1, h2, h3;
             e2m1x8_to_f16x2x4(aw0[gi], f0, f1, f2, f3);
             e2m1x8_to_f16x2x4(aw1[gi], h0, h1, h2, h3);
-            // E8M0 scale as a float: 2^(b-127) for b in 1..254; b = 0 only occurs with all-zero
-            // codes (amax = 0), where 0 * 0 = 0 either way
-            const float sc0 = __uint_as_float(((S0 >> (8 * gi)) & 0xFFu) << 23);
-            const float sc1 = __uint_as_float(((S1 >> (8 * gi)) & 0xFFu) << 23);
+            // E8M0 scale as a float, 2^(b-127): byte gi moved to the exponent field. b = 0 only
+            // occurs with all-zero codes (amax = 0), where 0 * 0 = 0 either way
+            const int sh = 23 - 8 * gi;
+            const float sc0 = __uint_as_float((sh >= 0 ? (S0 << sh) : (S0 >> -sh)) & 0x7F800000u);
+            const float sc1 = __uint_as_float((sh >= 0 ? (S1 << sh) : (S1 >> -sh)) & 0x7F800000u);
             float tmp[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-              tmp[nt][0] = tmp[nt][1] = tmp[nt][2] = tmp[nt][3] = 0.f;
-              mma_f16_16816(tmp[nt], f0, h0, f1, h1, B[nt][2 * gi][0], B[nt][2 * gi][1]);
+              mma_f16_16816_zc(tmp[nt], f0, h0, f1, h1, B[nt][2 * gi][0], B[nt][2 * gi][1]);
               mma_f16_16816(tmp[nt], f2, h2, f3, h3, B[nt][2 * gi + 1][0], B[nt][2 * gi + 1][1]);
             }
+            if (gi == 0) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              tot[nt][0] = fmaf(sc0, tmp[nt][0], tot[nt][0]);
-              tot[nt][1] = fmaf(sc0, tmp[nt][1], tot[nt][1]);
-              tot[nt][2] = fmaf(sc1, tmp[nt][2], tot[nt][2]);
-              tot[nt][3] = fmaf(sc1, tmp[nt][3], tot[nt][3]);
+              for (int nt = 0; nt < 2; ++nt) {
+                tot[nt][0] = sc0 * tmp[nt][0];
+                tot[nt][1] = sc0 * tmp[nt][1];
+                tot[nt][2] = sc1 * tmp[nt][2];
+                tot[nt][3] = sc1 * tmp[nt][3];
+              }
+            } else {
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                tot[nt][0] = fmaf(sc0, tmp[nt][0], tot[nt][0]);
+                tot[nt][1] = fmaf(sc0, tmp[nt][1], tot[nt][1]);
+                tot[nt][2] = fmaf(sc1, tmp[nt][2], tot[nt][2]);
+                tot[nt][3] = fmaf(sc1, tmp[nt][3], tot[nt][3]);
+              }
             }
           }
           float v0 = 0.f, v1 = 0.f;
@@ -471,66 +480,46 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
               v1 = fmaf(wr[nt][j], fmaxf(tot[nt][2 + j], 0.f), v1);
             }
           v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-          v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
           v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
           v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
           bool ok0, ok1;
           if (!p.pool_mode) {
-            const int vq = imin64(svis[ql], p.cap);
-            ok0 = pos0 < vq;
-            ok1 = pos1 < vq;
+            const int vq = svis[ql];
+            ok0 = c * kChunk + r0 < vq;
+            ok1 = c * kChunk + r1 < vq;
           } else {
             ok0 = in0;
             ok1 = in1;
           }
           v0 = ok0 ? v0 : -INFINITY;
           v1 = ok1 ? v1 : -INFINITY;
+          const float myv = (t & 1) ? v1 : v0;
+          const bool myok = (t & 1) ? ok1 : ok0;
+          const uint32_t mybin = order_key(myv) >> kHistShift;
+          const uint32_t myinc = (mybin & 1) ? 0x10000u : 1u;
           if (!p.pool_mode) {
             const int row = cur_seg * p.nq + ql;
-            float* srow = p.scores + (size_t)row * p.ld_s;
-            if (t == 0) srow[pos0] = v0;
-            if (t == 1) srow[pos1] = v1;
+            if (t < 2) p.scores[(size_t)row * p.ld_s + mypos] = myv;
             uint32_t* hp = hist_sm + (2 * ql) * (kHistBins / 2);
-            if (t == 0 && ok0) {
-              const uint32_t bin = order_key(v0) >> kHistShift;
-              atomicAdd(hp + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
-            }
-            if (t == 1 && ok1) {
-              const uint32_t bin = order_key(v1) >> kHistShift;
-              atomicAdd(hp + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
-            }
-            // block maxima over the 8 rows g = 0..7 (block A) and 8..15 (block B)
+            if (t < 2 && myok) atomicAdd(hp + (mybin >> 1), myinc);
+            // block maxima over rows g = 0..7 (block A) and 8..15 (block B); lanes 0/1 store them
             float bA = v0, bB = v1;
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) {
               bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, o));
               bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, o));
             }
-            const int jA = (c * kChunk + warp * 32 + mt * 16) >> 3;
-            const int vq = imin64(svis[ql], p.cap);
+            const int jb = ((c * kChunk + warp * 32 + mt * 16) >> 3) + (lane & 1);
+            const float bv = (lane & 1) ? bB : bA;
+            const bool bok = (lane < 2) && (jb * 8 < svis[ql]);
+            const uint32_t bbin = order_key(bv) >> kHistShift;
+            if (bok) p.blkmax[(size_t)row * p.ld_b + jb] = bv;
             uint32_t* hb = hist_sm + (2 * ql + 1) * (kHistBins / 2);
-            if (lane == 0 && jA * 8 < vq) {
-              p.blkmax[(size_t)row * p.ld_b + jA] = bA;
-              const uint32_t bin = order_key(bA) >> kHistShift;
-              atomicAdd(hb + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
-            }
-            if (lane == 1 && (jA + 1) * 8 < vq) {
-              p.blkmax[(size_t)row * p.ld_b + jA + 1] = bB;
-              const uint32_t bin = order_key(bB) >> kHistShift;
-              atomicAdd(hb + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
-            }
+            if (bok) atomicAdd(hb + (bbin >> 1), (bbin & 1) ? 0x10000u : 1u);
           } else {
-            float* srow = p.scores + (size_t)cur_seg * kPool + c * kChunk;
-            if (t == 0) srow[r0] = v0;
-            if (t == 1) srow[r1] = v1;
-            if (t == 0 && ok0) {
-              const uint32_t bin = order_key(v0) >> kHistShift;
-              atomicAdd(hist_sm + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
-            }
-            if (t == 1 && ok1) {
-              const uint32_t bin = order_key(v1) >> kHistShift;
-              atomicAdd(hist_sm + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
-            }
+            if (t < 2) score_base[myr] = myv;
+            if (t < 2 && myok) atomicAdd(hist_sm + (mybin >> 1), myinc);
           }
         }
       }
