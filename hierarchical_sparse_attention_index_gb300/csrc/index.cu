@@ -140,10 +140,13 @@ __device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, in
   named_bar_sync(1, kConsumers);
 }
 
+// kPoolMode: Reindex (segment = one (request, query) row, entries gathered through the pool);
+// kOneQuery: one query per segment (always in Reindex; nq == 1 in Full).
+template <bool kPoolMode, bool kOneQuery>
 __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const ScanSmemLayout L = scan_smem_layout(p.pool_mode, p.nq);
-  const int nql = p.pool_mode ? 1 : p.nq;
+  const ScanSmemLayout L = scan_smem_layout(kPoolMode, p.nq);
+  const int nql = kOneQuery ? 1 : p.nq;
   const int nst = L.nst;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last flag, [2..9] vis, [16..48) scratch
@@ -189,7 +192,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       const uint32_t full = full0 + 8 * s;
       const uint32_t dcodes = smem_u32(smem + L.codes + (size_t)s * kCodesBytes);
       const uint32_t dscales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
-      if (!p.pool_mode) {
+      if (!kPoolMode) {
         int vmax = 0;
         for (int q = 0; q < p.nq; ++q) vmax = max(vmax, __ldg(p.vis + seg * p.nq + q));
         vmax = (int)imin64(vmax, p.cap);
@@ -269,7 +272,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     named_bar_sync(1, kConsumers);
     for (int lr = 0; lr < L.nlr; ++lr) {
       int grow;
-      if (p.pool_mode) grow = seg;
+      if (kPoolMode) grow = seg;
       else grow = (seg * p.nq + (lr >> 1)) * 2 + (lr & 1);
       uint32_t* gh = p.hist + (size_t)grow * kHistBins;
       uint32_t* sh = hist_sm + lr * (kHistBins / 2);
@@ -295,7 +298,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     named_bar_sync(1, kConsumers);
     if (misc[1]) {
       __threadfence();
-      if (p.pool_mode) {
+      if (kPoolMode) {
         compute_threshold(p.hist + (size_t)seg * kHistBins, kTopK, p.state + seg, scratch);
       } else {
         for (int q = 0; q < p.nq; ++q) {
@@ -313,7 +316,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   auto load_segment = [&](int seg) {
     named_bar_sync(1, kConsumers);
     for (int ql = 0; ql < nql && tid < 256; ++ql) {
-      const int row = p.pool_mode ? seg : seg * p.nq + ql;
+      const int row = kPoolMode ? seg : seg * p.nq + ql;
       const int h = tid >> 4, d0 = (tid & 15) * 8;
       const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHIdx + h) * kDIdx + d0));
       float x[8];
@@ -352,9 +355,9 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
         dst[1] = pk[2 * u + 1];
       }
       if ((tid & 15) == 0) wsc[ql * 16 + h] = ldexpf(__ldg(p.w + (size_t)row * kHIdx + h), -sh);
-      if (tid < 8 && !p.pool_mode && tid == ql) svis[ql] = (int)imin64(__ldg(p.vis + row), p.cap);
+      if (tid < 8 && !kPoolMode && tid == ql) svis[ql] = (int)imin64(__ldg(p.vis + row), p.cap);
     }
-    if (p.pool_mode && tid == 0) svis[0] = __ldg(p.vis + seg);
+    if (kPoolMode && tid == 0) svis[0] = __ldg(p.vis + seg);
     named_bar_sync(1, kConsumers);
   };
 
@@ -398,9 +401,9 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       continue;
     }
     int nrows;   // rows of this stage that hold data
-    if (!p.pool_mode) {
+    if (!kPoolMode) {
       int vmax = 0;
-      for (int q = 0; q < p.nq; ++q) vmax = max(vmax, svis[q]);
+      for (int q = 0; q < nql; ++q) vmax = max(vmax, svis[q]);
       vmax = (int)imin64(vmax, p.cap);
       nrows = max(0, min(kChunk, vmax - c * kChunk));
     } else {
@@ -412,8 +415,8 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
 
     if (warp * 32 < nrows) {
       // per-stage constants of this warp
-      float* const score_base = p.pool_mode ? p.scores + (size_t)cur_seg * kPool + c * kChunk : nullptr;
-#pragma unroll
+      float* const score_base = kPoolMode ? p.scores + (size_t)cur_seg * kPool + c * kChunk : nullptr;
+#pragma unroll 1
       for (int mt = 0; mt < 2; ++mt) {
         if (mt == 1 && warp * 32 + 16 >= nrows) break;
         const int r0 = warp * 32 + mt * 16 + g, r1 = r0 + 8;
@@ -425,7 +428,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
         const int myr = (t & 1) ? r1 : r0;
         int mypos;                       // Full: position; Reindex: slot position (or -1)
         bool in0 = true, in1 = true;
-        if (p.pool_mode) {
+        if (kPoolMode) {
           const int s0 = slotpos[r0], s1 = slotpos[r1];
           in0 = s0 >= 0;
           in1 = s1 >= 0;
@@ -484,7 +487,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
           v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
           v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
           bool ok0, ok1;
-          if (!p.pool_mode) {
+          if (!kPoolMode) {
             const int vq = svis[ql];
             ok0 = c * kChunk + r0 < vq;
             ok1 = c * kChunk + r1 < vq;
@@ -498,7 +501,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
           const bool myok = (t & 1) ? ok1 : ok0;
           const uint32_t mybin = order_key(myv) >> kHistShift;
           const uint32_t myinc = (mybin & 1) ? 0x10000u : 1u;
-          if (!p.pool_mode) {
+          if (!kPoolMode) {
             const int row = cur_seg * p.nq + ql;
             if (t < 2) p.scores[(size_t)row * p.ld_s + mypos] = myv;
             uint32_t* hp = hist_sm + (2 * ql) * (kHistBins / 2);
@@ -837,24 +840,30 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
 
 }  // namespace
 
-cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s) {
-  const ScanSmemLayout L = scan_smem_layout(p.pool_mode, p.nq);
+template <bool kPoolMode, bool kOneQuery>
+cudaError_t launch_scan_variant(const ScanParams& p, int num_sms, cudaStream_t s) {
+  const ScanSmemLayout L = scan_smem_layout(kPoolMode, p.nq);
+  auto kern = index_scan_kernel<kPoolMode, kOneQuery>;
   static int set_bytes = 0;        // the attribute is per function, set to the largest size seen
   if ((int)L.total > set_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(index_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L.total);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
     if (e != cudaSuccess) return e;
     set_bytes = (int)L.total;
   }
   int per_sm = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_scan_kernel, kScanThreads, L.total) !=
-          cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kScanThreads, L.total) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   int grid = num_sms * per_sm;
   if (grid > p.total_items) grid = p.total_items;
   if (grid < 1) grid = 1;
-  return launch_pdl(index_scan_kernel, dim3(grid), dim3(kScanThreads), L.total, s, p);
+  return launch_pdl(kern, dim3(grid), dim3(kScanThreads), L.total, s, p);
+}
+
+cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s) {
+  if (p.pool_mode) return launch_scan_variant<true, true>(p, num_sms, s);
+  if (p.nq == 1) return launch_scan_variant<false, true>(p, num_sms, s);
+  return launch_scan_variant<false, false>(p, num_sms, s);
 }
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
