@@ -99,8 +99,9 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   L->off_pscores = take((size_t)rows * kPool * 4);
   L->off_cand_pool = take((size_t)rows * kPool * 4);
   L->off_sure_pool = take((size_t)rows * kTopK * 4);
-  L->attn_bytes = 0;
-  L->off_attn = take(0);
+  // attention partials: per row, 4 CTAs x (64 x 512 unnormalised outputs + 64 (max, sum) pairs)
+  L->attn_bytes = (size_t)rows * kAttnSplit * (kHAtt * kDLat + 2 * kHAtt) * 4;
+  L->off_attn = take(L->attn_bytes);
   L->total = o;
   return true;
 }
@@ -275,8 +276,10 @@ hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const i
   if (st != HSA_OK) return st;
   if (!q || !topk || !swa || !vis || !out) return HSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(swa) || !aligned16(out)) return HSA_ERR_ALIGN;
-  (void)ws;
-  (void)ws_bytes;
+  WsLayout L;
+  if (!make_ws_layout(cache->batch, nq, max_vis, &L)) return HSA_ERR_SHAPE;
+  if (!ws || ws_bytes < L.total) return HSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return HSA_ERR_ALIGN;
   uint32_t* status;
   int sms;
   if (!device_info(&status, &sms)) return HSA_ERR_UNSUPPORTED;
@@ -294,6 +297,7 @@ hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const i
   p.vis = vis;
   p.sm_scale = sm_scale;
   p.out = out;
+  p.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.off_attn);
   p.status = status;
   return cuda_fail(launch_attention(p, (cudaStream_t)stream), "attention launch");
 }

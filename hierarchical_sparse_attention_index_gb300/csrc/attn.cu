@@ -11,12 +11,14 @@
 //     per-head power-of-two shift (exact within f16), in the same layout;
 //  2. tcgen05: S^T = K . Q^T in two M=128 passes (rows 0..127, then rows 32..159, of which only
 //     keys 128..159 are used), accumulated in TMEM;
-//  3. exchanges per-head max and sum through distributed shared memory, so every CTA
-//     normalises against the global max. It writes P^T (f16) as the next B operand;
+//  3. runs a softmax local to its 160 keys (own max m_c and sum l_c per head) and writes
+//     P^T (f16) as the next B operand; no cluster exchange is needed before PV;
 //  4. tcgen05: O^T[512 dims][64 heads] = V^T . P^T, reading the same tile as an MN-major
 //     A operand (K = V = the 512-d latent), 4 M-tiles of 128 dims x 10 k-steps;
-//  5. scales by 1/sum, stages its partial in shared memory, and sums its 16-head slice over
-//     the 4 CTAs through DSMEM in a fixed order (deterministic).
+//  5. writes its unnormalised partial O_c and (m_c, l_c) to the workspace (L2) straight from
+//     TMEM. After one cluster barrier each CTA forms its 16 heads as
+//     sum_c exp(m_c - M) O_c / sum_c exp(m_c - M) l_c over c in rank order (deterministic).
+//     L2 moves these 128 KB per CTA several times faster than distributed shared memory.
 // Setup (TMEM allocation, barrier init) runs before the programmatic-dependency wait, so it
 // overlaps the tail of the previous kernel in the stream. Every wait is bounded.
 #include "hsa_common.cuh"
@@ -26,7 +28,7 @@ namespace hsa {
 namespace {
 
 constexpr int kAttnThreads = 256;
-constexpr int kCluster = 4;
+constexpr int kCluster = kAttnSplit;
 constexpr int kRows = 160;                               // keys per CTA
 constexpr int kTopRows = 128;
 constexpr uint32_t kKbStride = kRows * 128u;             // bytes per 64-dim block of the tile
@@ -35,6 +37,7 @@ constexpr uint32_t kQBytes = kHAtt * kDLat * 2;          // 64 KB f16 Q (then lo
 constexpr uint32_t kOffK = 0, kOffQ = kTileBytes, kOffMisc = kOffQ + kQBytes;
 constexpr uint32_t kMiscBytes = 1792;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;   // + alignment slack
+constexpr size_t kPartFloats = (size_t)kHAtt * kDLat + 2 * kHAtt;   // one CTA's partial in the workspace
 constexpr int kSStride = 164;                            // fp32 staging row stride (conflict-free)
 constexpr int kTmemCols = 512;
 constexpr int kColS0 = 0, kColS1 = 64, kColO = 256;
@@ -86,23 +89,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -118,21 +104,6 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t s2) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// 32 FP4 codes (two uint4) x four scale bytes -> 32 f16x2 (element 2j in the low half)
-__device__ __forceinline__ void dequant_fp4_64(const uint4 c0, const uint4 c1, uint32_t sc4, int fmt, uint32_t* o) {
-  const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-  for (int j = 0; j < 8; ++j) e2m1x8_to_f16x2x4(cw[j], o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    const uint32_t sb = (sc4 >> (8 * gi)) & 0xFFu;
-    const float sf = (fmt == HSA_SCALE_E8M0) ? e8m0_to_f32(sb) : e4m3_to_f32(sb);
-    const uint32_t s2 = (uint32_t)__half_as_ushort(__float2half_rn(sf)) * 0x10001u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) o[8 * gi + j] = hmul2_u32(o[8 * gi + j], s2);
-  }
-}
-
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads, 1)
     sparse_attn_kernel(const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -144,7 +115,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   float* s_scale = misc;              // [64] logit scale per head
   float* s_m = misc + 64;             // [64] local max (read remotely)
   float* s_l = misc + 128;            // [64] local sum (read remotely)
-  float* s_invl = misc + 192;         // [64]
+  float* s_w = misc + 192;            // [4][16] combine weights of this CTA's heads
   int* s_valid = reinterpret_cast<int*>(misc + 256);      // [160]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 416);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(misc + 418);
@@ -170,77 +141,55 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const int vis = __ldg(p.vis + row);
 
   // ---------------------------------------------------------------- issue every global load up front
-  // warp = 64-dim segment kb; top-k rows r = lane + 32 i (i < 4), SWA row 128 + lane
-  const int kb = warp;
-  uint4 kr[4][2];
-  uint32_t ksc[4];
-  bool kval[4];
-  {
-    int idx[4];
+  // Lane = 8 q + rr. One warp-wide load covers 8 rows (rr) x 64 contiguous bytes (4 lanes q x
+  // 16 B), so every sector fetched is used whole, and in the shared-memory stores that follow,
+  // the 8 lanes of each store phase write 8 different rows (distinct swizzled 16-byte units).
+  const int rr = lane & 7, qq = lane >> 3;
+  // the row indices go first: the row loads depend on them
+  int kidx[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) idx[i] = __ldg(p.topk + (size_t)row * kTopK + rank * kTopRows + lane + 32 * i);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kval[i] = (idx[i] >= 0) && (idx[i] < vis) && (idx[i] < p.cap);
-      if (idx[i] >= 0 && !kval[i] && kb == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-      const size_t e = (size_t)b * p.cap + (kval[i] ? idx[i] : 0);
-      const uint4* cs = reinterpret_cast<const uint4*>(p.kv_q + e * 256 + kb * 32);
-      kr[i][0] = __ldg(cs);
-      kr[i][1] = __ldg(cs + 1);
-      ksc[i] = __ldg(reinterpret_cast<const uint32_t*>(p.kv_s + e * 32 + kb * 4));
-    }
-  }
-  // SWA: window row w = 32 rank + lane of this query holds position vis - 128 + w
-  const int wrow = 32 * (int)rank + lane;
-  const bool sval = (vis - kSwa + wrow) >= 0;
-  uint4 sr[4];
-  {
-    const uint4* cs = reinterpret_cast<const uint4*>(
-        p.swa + ((size_t)b * (kSwa + p.nq - 1) + qi + wrow) * kDLat + kb * 64);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) sr[j] = __ldg(cs + j);
-  }
-  const int qh = tid >> 2, qk = tid & 3;    // Q: 4 threads per head, 128 dims each
+  for (int gsel = 0; gsel < 2; ++gsel)
+    kidx[gsel] = __ldg(p.topk + (size_t)row * kTopK + rank * kTopRows + 8 * (2 * warp + gsel) + rr);
+  // Q: warp w owns heads 8w + rr; step s takes 8-dim chunk 4 s + qq (s = 0..15)
   uint4 qraw[16];
+  const int qh = 8 * warp + rr;
   {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHAtt + qh) * kDLat + qk * 128);
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHAtt + qh) * kDLat);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) qraw[i] = __ldg(src + i);
+    for (int s4 = 0; s4 < 16; ++s4) qraw[s4] = __ldg(src + 4 * s4 + qq);
   }
 
-  // ---------------------------------------------------------------- K tile rows
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = lane + 32 * i;
-    uint32_t o[32];
-    dequant_fp4_64(kr[i][0], kr[i][1], ksc[i], p.scale_fmt, o);
-    if (!kval[i]) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = 0u;
-    }
-    if (kb == 0) s_valid[r] = kval[i] ? 1 : 0;
-    const uint32_t blk = sK + (uint32_t)kb * kKbStride;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) sts128(blk + sw128(r, c), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-  }
+  // SWA: this CTA's 32 window rows (w = 32 rank + r, position vis - 128 + w) are one contiguous
+  // 16 KB block; warp w takes rows 8 (w >> 1) + rr, FP8 chunks jj = 4 (4 (w & 1) + s) + qq
+  uint4 sc[4];
+  const int srow = 8 * (warp >> 1) + rr;
+  const bool sval = (vis - kSwa + 32 * (int)rank + srow) >= 0;
   {
-    const int r = kTopRows + lane;
-    uint32_t o[32];
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.swa + ((size_t)b * (kSwa + p.nq - 1) + qi + 32 * (int)rank + srow) * kDLat);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t vw[4] = {sr[j].x, sr[j].y, sr[j].z, sr[j].w};
+    for (int s4 = 0; s4 < 4; ++s4) sc[s4] = __ldg(src + 4 * (4 * (warp & 1) + s4) + qq);
+  }
+  // top-k rows: warp w owns row groups 2w and 2w+1 (rows 8g + rr); step s takes code chunk
+  // j = 4 (s & 3) + qq (16 B = dims 32j .. 32j+31) of group 2w + (s >> 2)
+  uint4 kc[8];
+  uint32_t ks2[8];
+  bool kval[2];
+  {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        o[8 * j + 2 * u] = sval ? e4m3x2_to_f16x2((uint16_t)(vw[u] & 0xFFFFu)) : 0u;
-        o[8 * j + 2 * u + 1] = sval ? e4m3x2_to_f16x2((uint16_t)(vw[u] >> 16)) : 0u;
+    for (int gsel = 0; gsel < 2; ++gsel) {
+      const int idx = kidx[gsel];
+      kval[gsel] = (idx >= 0) && (idx < vis) && (idx < p.cap);
+      if (idx >= 0 && !kval[gsel] && qq == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+      const size_t e = (size_t)b * p.cap + (kval[gsel] ? idx : 0);
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const int j = 4 * s4 + qq;
+        kc[4 * gsel + s4] = __ldg(reinterpret_cast<const uint4*>(p.kv_q + e * 256) + j);
+        ks2[4 * gsel + s4] = __ldg(reinterpret_cast<const uint16_t*>(p.kv_s + e * 32) + j);
       }
     }
-    if (kb == 0) s_valid[r] = sval ? 1 : 0;
-    const uint32_t blk = sK + (uint32_t)kb * kKbStride;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) sts128(blk + sw128(r, c), o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
   }
-
   // ---------------------------------------------------------------- Q: bf16 -> f16 with per-head shift
   {
     float amax = 0.f;
@@ -251,8 +200,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       for (int j = 0; j < 4; ++j)
         amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
     int sh = 0;
     if (amax > 0.f) {
       int e;
@@ -260,7 +209,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       sh = max(-126, min(127, 15 - e));     // amax * 2^sh in [2^14, 2^15)
     }
     const float mul = __uint_as_float((uint32_t)(127 + sh) << 23);   // exact power of two
-    if (qk == 0) s_scale[qh] = p.sm_scale * __uint_as_float((uint32_t)(127 - sh) << 23);
+    if (qq == 0) s_scale[qh] = p.sm_scale * __uint_as_float((uint32_t)(127 - sh) << 23);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
@@ -271,9 +220,53 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
         const __half hi = __float2half_rn(__uint_as_float(w[j] & 0xFFFF0000u) * mul);
         o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
       }
-      const int d = qk * 128 + i * 8;
-      sts128(sQ + (uint32_t)(d >> 6) * (kHAtt * 128u) + sw128(qh, (d & 63) >> 3), o[0], o[1], o[2], o[3]);
+      const int c = 4 * i + qq;                          // 8-dim chunk: block c / 8, unit c % 8
+      sts128(sQ + (uint32_t)(c >> 3) * (kHAtt * 128u) + sw128(qh, c & 7), o[0], o[1], o[2], o[3]);
     }
+  }
+  // ---------------------------------------------------------------- K tile: SWA rows (E4M3 -> f16, exact)
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4) {
+    const int jj = 4 * (4 * (warp & 1) + s4) + qq;       // dims 16 jj .. 16 jj + 15
+    const uint32_t vw[4] = {sc[s4].x, sc[s4].y, sc[s4].z, sc[s4].w};
+    uint32_t o[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      o[2 * u] = sval ? e4m3x2_to_f16x2((uint16_t)(vw[u] & 0xFFFFu)) : 0u;
+      o[2 * u + 1] = sval ? e4m3x2_to_f16x2((uint16_t)(vw[u] >> 16)) : 0u;
+    }
+    const int r = kTopRows + srow;
+    const uint32_t blk = sK + (uint32_t)(jj >> 2) * kKbStride;
+    const int c0 = 2 * (jj & 3);
+    sts128(blk + sw128(r, c0), o[0], o[1], o[2], o[3]);
+    sts128(blk + sw128(r, c0 + 1), o[4], o[5], o[6], o[7]);
+  }
+  if ((warp & 1) == 0 && qq == 0) s_valid[kTopRows + srow] = sval ? 1 : 0;
+
+  // ---------------------------------------------------------------- K tile: top-k rows (E2M1 x scale -> f16)
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    const int gsel = st >> 2;
+    const int r = 8 * (2 * warp + gsel) + rr;
+    const int j = 4 * (st & 3) + qq;
+    const uint32_t cw[4] = {kc[st].x, kc[st].y, kc[st].z, kc[st].w};
+    uint32_t o[16];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) e2m1x8_to_f16x2x4(cw[w], o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const uint32_t sb = (ks2[st] >> (8 * gi)) & 0xFFu;
+      const float sf = (p.scale_fmt == HSA_SCALE_E8M0) ? e8m0_to_f32(sb) : e4m3_to_f32(sb);
+      const uint32_t s2 = kval[gsel] ? (uint32_t)__half_as_ushort(__float2half_rn(sf)) * 0x10001u : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o[8 * gi + u] = hmul2_u32(o[8 * gi + u], s2);
+    }
+    // dims 32j + 8w -> block kb = j / 2, 16-byte chunk 4 (j & 1) + w
+    const uint32_t blk = sK + (uint32_t)(j >> 1) * kKbStride;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      sts128(blk + sw128(r, 4 * (j & 1) + w), o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+    if (qq == 0 && (st & 3) == 0) s_valid[r] = kval[gsel] ? 1 : 0;
   }
   fence_async_smem();
   tc_fence_before();
@@ -283,17 +276,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 
   // ---------------------------------------------------------------- S^T = K . Q^T (two M=128 passes)
   if (tid == 0) {
+    // Descriptors are formed once; a k-step only moves the start-address field (address >> 4),
+    // which cannot carry out of its 14 bits because every operand lies below 256 KB.
     const uint32_t id = idesc_f16(128, 64, false, false);
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const uint32_t row0 = pass ? 32u : 0u;
-#pragma unroll 1
-      for (int k = 0; k < kDLat / 16; ++k) {
-        const uint32_t kbk = k >> 2, kk = k & 3;
-        const uint64_t a = sdesc(sK + kbk * kKbStride + row0 * 128u + kk * 32u, 16u, 1024u);
-        const uint64_t bq = sdesc(sQ + kbk * (kHAtt * 128u) + kk * 32u, 16u, 1024u);
-        umma_f16(tmem + (pass ? kColS1 : kColS0), a, bq, id, k > 0);
-      }
+    const uint64_t a0 = sdesc(sK, 16u, 1024u), a1 = sdesc(sK + 32u * 128u, 16u, 1024u);
+    const uint64_t b0 = sdesc(sQ, 16u, 1024u);
+#pragma unroll
+    for (int k = 0; k < kDLat / 16; ++k) {
+      const uint32_t ko = ((uint32_t)(k >> 2) * kKbStride + (uint32_t)(k & 3) * 32u) >> 4;
+      const uint32_t qo = ((uint32_t)(k >> 2) * (kHAtt * 128u) + (uint32_t)(k & 3) * 32u) >> 4;
+      umma_f16(tmem + kColS0, a0 + ko, b0 + qo, id, k > 0);
+      umma_f16(tmem + kColS1, a1 + ko, b0 + qo, id, k > 0);
     }
     umma_commit(bar);
   }
@@ -321,7 +314,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     }
   }
   __syncthreads();
-  // per head: 4 threads, keys 4i + kq
+  // per head: 4 threads, keys 4i + kq. The softmax is local to this CTA's 160 keys: its own
+  // max m_c and sum l_c; the cluster combine below rescales the four partials.
   const int hh = tid >> 2, kq = tid & 3;
   float x[kRows / 4];
   float mloc = -INFINITY;
@@ -332,17 +326,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   }
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-  if (kq == 0) s_m[hh] = mloc;
-  cluster_sync();               // publishes s_m; every thread has read its logits
-  float M = -INFINITY;
-#pragma unroll
-  for (uint32_t src = 0; src < kCluster; ++src) M = fmaxf(M, ld_dsmem_f32(mapa(smem_u32(s_m + hh), src)));
   float lsum = 0.f;
   // P^T (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys
 #pragma unroll
   for (int i = 0; i < kRows / 4; ++i) {
     const int key = 4 * i + kq;
-    const float pr = (M == -INFINITY) ? 0.f : exp2f((x[i] - M) * 1.4426950408889634f);
+    const float pr = (mloc == -INFINITY) ? 0.f : exp2f((x[i] - mloc) * 1.4426950408889634f);
     const __half ph = __float2half_rn(pr);
     lsum += __half2float(ph);                   // the value the tensor core will see
     sts16(sP + (uint32_t)(key >> 6) * (kHAtt * 128u) + sw128(hh, (key & 63) >> 3) + (uint32_t)(key & 7) * 2u,
@@ -350,39 +339,39 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   }
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-  if (kq == 0) s_l[hh] = lsum;
+  if (kq == 0) {
+    s_m[hh] = mloc;
+    s_l[hh] = lsum;
+  }
   fence_async_smem();
   tc_fence_before();
-  cluster_sync();               // publishes s_l; P complete
+  __syncthreads();
   tc_fence_after();
-  if (kq == 0) {
-    float L = 0.f;
-#pragma unroll
-    for (uint32_t src = 0; src < kCluster; ++src) L += ld_dsmem_f32(mapa(smem_u32(s_l + hh), src));
-    s_invl[hh] = (L > 0.f) ? 1.f / L : 0.f;
-  }
 
   // ---------------------------------------------------------------- O^T = V^T . P^T
   if (tid == 0) {
     const uint32_t id = idesc_f16(128, 64, true, false);
-#pragma unroll 1
-    for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll 1
-      for (int ks = 0; ks < kRows / 16; ++ks) {
-        const uint64_t a = sdesc(sK + (uint32_t)(2 * mt) * kKbStride + (uint32_t)(16 * ks) * 128u, kKbStride, 1024u);
-        const uint64_t bp = sdesc(sP + (uint32_t)(ks >> 2) * (kHAtt * 128u) + (uint32_t)(ks & 3) * 32u, 16u, 1024u);
-        umma_f16(tmem + kColO + 64 * mt, a, bp, id, ks > 0);
+    const uint64_t a0 = sdesc(sK, kKbStride, 1024u), b0 = sdesc(sP, 16u, 1024u);
+#pragma unroll
+    for (int ks = 0; ks < kRows / 16; ++ks) {
+      const uint32_t bo = ((uint32_t)(ks >> 2) * (kHAtt * 128u) + (uint32_t)(ks & 3) * 32u) >> 4;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const uint32_t ao = ((uint32_t)(2 * mt) * kKbStride + (uint32_t)(16 * ks) * 128u) >> 4;
+        umma_f16(tmem + kColO + 64 * mt, a0 + ao, b0 + bo, id, ks > 0);
       }
     }
     umma_commit(bar);
   }
   if (!mbar_wait(bar, 1) && tid == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
   tc_fence_after();
-  __syncthreads();              // s_invl visible
 
-  // ---------------------------------------------------------------- partial O (scaled) -> staging F[h][d] (K region)
-  float* F = reinterpret_cast<float*>(sm + kOffK);
+  // ---------------------------------------------------------------- unnormalised partial O -> L2
+  // partial[row][rank]: 64 x 512 fp32 outputs [h][d], then (m_c, l_c) for the 64 heads. The
+  // cluster peers read it right after the barrier below, so it is served from L2.
+  float* part = p.partial + ((size_t)row * kCluster) * kPartFloats;
   {
+    float* mine = part + (size_t)rank * kPartFloats;
     const int qd = warp & 3, half = warp >> 2;
 #pragma unroll 1
     for (int u = 0; u < 2; ++u) {
@@ -394,51 +383,75 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
         TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mt + 32 * hc), r);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int h = 32 * hc + j;
-          F[h * kDLat + d] = __uint_as_float(r[j]) * s_invl[h];
-        }
+        for (int j = 0; j < 32; ++j) __stcg(mine + (size_t)(32 * hc + j) * kDLat + d, __uint_as_float(r[j]));
       }
+    }
+    if (tid < kHAtt) {
+      __stcg(mine + kHAtt * kDLat + 2 * tid, s_m[tid]);
+      __stcg(mine + kHAtt * kDLat + 2 * tid + 1, s_l[tid]);
     }
   }
   tc_fence_before();
-  cluster_sync();
+  cluster_sync();               // release/acquire at cluster scope: every partial of this row is visible
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 
-  // ---------------------------------------------------------------- sum the cluster's partials for this CTA's 16 heads
+  // combine weights of this CTA's heads: w_c = exp(m_c - M) / sum_c' exp(m_c' - M) l_c'
+  if (tid < 16) {
+    const int h = 16 * (int)rank + tid;
+    float mc[kCluster], lc[kCluster];
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(part + (size_t)c * kPartFloats + kHAtt * kDLat) + h);
+      mc[c] = ml.x;
+      lc[c] = ml.y;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) M = fmaxf(M, mc[c]);
+    float e[kCluster], L = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) {
+      e[c] = (mc[c] == -INFINITY) ? 0.f : exp2f((mc[c] - M) * 1.4426950408889634f);
+      L += e[c] * lc[c];
+    }
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) s_w[c * 16 + tid] = e[c] * inv;
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- out[h] = sum_c w_c[h] O_c[h], c in rank order
   {
-    float* out = p.out + (size_t)row * kHAtt * kDLat;
-    const uint32_t Fs = smem_u32(F);
+    float* out = p.out + ((size_t)row * kHAtt + 16 * rank) * kDLat;
     constexpr int kPer = 16 * (kDLat / 4) / kAttnThreads;   // 8 float4 per thread
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
+    for (int half = 0; half < 2; ++half) {
       float4 v[kCluster][kPer / 2];
 #pragma unroll
       for (int u = 0; u < kPer / 2; ++u) {
-        const int i = tid + kAttnThreads * (hf * (kPer / 2) + u);
-        const int h = 16 * (int)rank + i / (kDLat / 4), d4 = i % (kDLat / 4);
-        const uint32_t off = Fs + (uint32_t)(h * kDLat + 4 * d4) * 4u;
+        const int i = tid + kAttnThreads * (half * (kPer / 2) + u);   // float4 index within the 16-head slice
 #pragma unroll
-        for (uint32_t src = 0; src < kCluster; ++src) v[src][u] = ld_dsmem_f32x4(mapa(off, src));
+        for (int c = 0; c < kCluster; ++c)
+          v[c][u] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)c * kPartFloats + (size_t)16 * rank * kDLat) + i);
       }
 #pragma unroll
       for (int u = 0; u < kPer / 2; ++u) {
-        float4 acc = v[0][u];
+        const int i = tid + kAttnThreads * (half * (kPer / 2) + u);
+        const int hl = i / (kDLat / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int src = 1; src < kCluster; ++src) {
-          acc.x += v[src][u].x;
-          acc.y += v[src][u].y;
-          acc.z += v[src][u].z;
-          acc.w += v[src][u].w;
+        for (int c = 0; c < kCluster; ++c) {
+          const float w = s_w[c * 16 + hl];
+          acc.x = fmaf(w, v[c][u].x, acc.x);
+          acc.y = fmaf(w, v[c][u].y, acc.y);
+          acc.z = fmaf(w, v[c][u].z, acc.z);
+          acc.w = fmaf(w, v[c][u].w, acc.w);
         }
-        const int i = tid + kAttnThreads * (hf * (kPer / 2) + u);
-        const int h = 16 * (int)rank + i / (kDLat / 4), d4 = i % (kDLat / 4);
-        reinterpret_cast<float4*>(out + (size_t)h * kDLat)[d4] = acc;
+        reinterpret_cast<float4*>(out)[i] = acc;
       }
     }
   }
-  cluster_sync();
-  tc_fence_after();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
 }  // namespace

@@ -102,7 +102,7 @@ struct AttnParams {
   const int32_t* vis;     // [B][nq]
   float sm_scale;
   float* out;             // [B][nq][64][512]
-  float* partial;         // workspace: [B*nq][5][64][512 + 2]
+  float* partial;         // workspace: [B*nq][4][64*512 outputs, then 64 (max, sum) pairs]
   uint32_t* status;
 };
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t s);

@@ -210,7 +210,10 @@ HSA_API hsa_status hsa_index_reindex_noalloc(const hsa_cache* cache, const void*
  *   topk[b][i][*] in [0, vis) and then SWA rows r in [i, i+128) of swa[b] whose position
  *   vis - 128 + (r - i) is >= 0. K = V = the 512-d latent. With no keys the output is 0.
  *   q     bf16 [B][nq][64][512]     topk  i32 [B][nq][512]     swa  e4m3 [B][128+nq-1][512]
- *   out   f32  [B][nq][64][512] */
+ *   out   f32  [B][nq][64][512]
+ *   ws    workspace of at least hsa_workspace_bytes(B, nq, max_vis) bytes, 16-byte aligned; it
+ *         carries the partial outputs of the 4 key slices of each (b, i) between the CTAs that
+ *         combine them, and needs no initialisation */
 HSA_API hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const int32_t* topk,
                                   const uint8_t* swa, const int32_t* vis, int32_t nq, int64_t max_vis,
                                   float sm_scale, float* out, void* ws, size_t ws_bytes,

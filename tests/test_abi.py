@@ -75,6 +75,13 @@ def test_host_validation_without_gpu(lib):
     assert lib.hsa_index_full(ctypes.byref(c), 0x10, 0x20, 0x30, 1, 2000, 0x40, 0x50, 0x60, 1 << 30, null) == 2
     assert lib.hsa_index_full(ctypes.byref(c), 0x11, 0x20, 0x30, 1, 10, 0x40, 0x50, 0x60, 1 << 30, null) == 3
     assert lib.hsa_index_full(ctypes.byref(c), 0x10, 0x20, 0x30, 1, 10, 0x40, 0x50, 0x60, 16, null) == 4
+    # attention: the workspace carries the partial outputs, so a missing or short one is refused
+    assert lib.hsa_sparse_attn_decode(ctypes.byref(c), 0x10, 0x20, 0x30, 0x40, 1, 10, 1.0, 0x50, null, 0,
+                                      null) == 4
+    assert lib.hsa_sparse_attn_decode(ctypes.byref(c), 0x10, 0x20, 0x30, 0x40, 1, 10, 1.0, 0x50, 0x60, 16,
+                                      null) == 4
+    assert lib.hsa_sparse_attn_decode(ctypes.byref(c), 0x10, 0x20, 0x30, 0x40, 1, 10, 1.0, 0x58, 0x60, 1 << 30,
+                                      null) == 3
     c.ratio = 3
     assert lib.hsa_index_full(ctypes.byref(c), 0x10, 0x20, 0x30, 1, 10, 0x40, 0x50, 0x60, 1 << 30, null) == 1
     c.ratio = 2
