@@ -147,7 +147,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const ScanSmemLayout L = scan_smem_layout(kPoolMode, p.nq);
   const int nql = kOneQuery ? 1 : p.nq;
-  const int nst = L.nst;
+  const int nst = kOneQuery ? 3 : L.nst;   // one query: always the 3-stage ring (see scan_smem_layout)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last flag, [2..9] vis, [16..48) scratch
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
@@ -179,16 +179,15 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
-    for (int it = i0, k = 0; it < i1; ++it, ++k) {
-      const int s = k % nst;
-      if (k >= nst) {
-        if (!mbar_wait(empty0 + 8 * s, ((k / nst) - 1) & 1)) {
+    int s = 0, round = 0, seg = i0 / cps, c = i0 % cps;
+    for (int it = i0; it < i1; ++it) {
+      if (round > 0) {
+        if (!mbar_wait(empty0 + 8 * s, (round - 1) & 1)) {
           flag_status(p.status, HSA_FLAG_TIMEOUT);
-          misc[0] = 1;
+          *reinterpret_cast<volatile int*>(misc) = 1;
           return;
         }
       }
-      const int seg = it / cps, c = it % cps;
       const uint32_t full = full0 + 8 * s;
       const uint32_t dcodes = smem_u32(smem + L.codes + (size_t)s * kCodesBytes);
       const uint32_t dscales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
@@ -251,6 +250,14 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
             bulk_g2s(dscales + bi * 32, p.ik_s + e0 * 4, 32u, full);
           }
         }
+      }
+      if (++s == nst) {
+        s = 0;
+        ++round;
+      }
+      if (++c == cps) {
+        c = 0;
+        ++seg;
       }
     }
     return;
@@ -376,8 +383,15 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       for (int j = 0; j < 2; ++j) wr[nt][j] = wsc[ql * 16 + nt * 8 + 2 * t + j];
   };
 
-  for (int it = i0, k = 0; it < i1; ++it, ++k) {
-    const int seg = it / cps, c = it % cps;
+  // Stage index, ring parity and (segment, chunk) advance incrementally. Segment changes and
+  // histogram flushes are the same for every consumer warp, so the named barriers inside them
+  // stay matched; a wait that times out flags the status and that warp skips its remaining
+  // stages (no early exit, so the barriers still match).
+  int s = 0, seg = i0 / cps, c = i0 % cps;
+  uint32_t ph = 0;
+  bool dead = false;
+  int vmax_seg = 0;                // Full: visible rows of the current request (max over its queries)
+  for (int it = i0; it < i1; ++it) {
     if (seg != cur_seg) {
       if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
       cur_seg = seg;
@@ -385,32 +399,26 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       since_flush = 0;
       load_segment(seg);
       if (nql == 1) load_query_regs(0);
+      if (!kPoolMode) {
+        int vmax = 0;
+        for (int q = 0; q < nql; ++q) vmax = max(vmax, svis[q]);
+        vmax_seg = vmax;           // svis is already capped at the capacity
+      }
     } else if (since_flush >= kFlushItems) {
       flush_hist(seg);
       since_flush = 0;
     }
     ++seg_items;
     ++since_flush;
-    named_bar_sync(1, kConsumers);
-    if (misc[0]) break;
-
-    const int s = k % nst;
-    if (!mbar_wait(full0 + 8 * s, (k / nst) & 1)) {
+    if (!dead && *reinterpret_cast<volatile int*>(misc) != 0) dead = true;
+    if (!dead && !mbar_wait(full0 + 8 * s, ph)) {
       flag_status(p.status, HSA_FLAG_TIMEOUT);
-      misc[0] = 1;
-      continue;
+      *reinterpret_cast<volatile int*>(misc) = 1;
+      dead = true;
     }
-    int nrows;   // rows of this stage that hold data
-    if (!kPoolMode) {
-      int vmax = 0;
-      for (int q = 0; q < nql; ++q) vmax = max(vmax, svis[q]);
-      vmax = (int)imin64(vmax, p.cap);
-      nrows = max(0, min(kChunk, vmax - c * kChunk));
-    } else {
-      nrows = kChunk;
-    }
-    const uint32_t codes = smem_u32(smem + L.codes + (size_t)s * kCodesBytes);
-    const uint32_t scales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
+    const int nrows = dead ? 0 : (kPoolMode ? kChunk : max(0, min(kChunk, vmax_seg - c * kChunk)));
+    const uint32_t codes = smem_u32(smem + L.codes) + (uint32_t)s * kCodesBytes;
+    const uint32_t scales = smem_u32(smem + L.scales) + (uint32_t)s * kScaleBytes;
     const int* slotpos = reinterpret_cast<const int*>(smem + L.slotpos) + s * kChunk;
 
     if (warp * 32 < nrows) {
@@ -529,8 +537,16 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (++s == nst) {
+      s = 0;
+      ph ^= 1u;
+    }
+    if (++c == cps) {
+      c = 0;
+      ++seg;
+    }
   }
-  if (cur_seg >= 0 && !misc[0]) finish_segment(cur_seg, seg_items);
+  if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
 }
 
 // ------------------------------------------------------------------ collect
