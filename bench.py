@@ -47,6 +47,26 @@ def env_rank():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def rank_seed(seed, rank):
+    """Seed of a rank's own batch: every rank scores different requests (weak scaling)."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(t, world, dist=None, device="cpu"):
+    """The slowest rank's time (a MAX all-reduce over the process group; t itself at world 1)."""
+    if world <= 1:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_value(steps, world, tmax):
+    """Decode steps per second summed over all ranks: each rank ran `steps` steps of its own batch."""
+    return world * steps / tmax
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -104,7 +124,7 @@ class ClockSampler:
 def build_inputs(H, torch, seed, rank):
     """Device-resident step inputs for one rank (its own batch of 32 requests)."""
     B, T, nq = CFG.batch, CFG.T, CFG.nq
-    s = seed + 7919 * rank
+    s = rank_seed(seed, rank)
     cache = H.Cache(B, T, 1)
     W = torch.from_numpy(synth.w_idx_bf16(s, 20).view(np.int16)).cuda().view(torch.bfloat16)
     for b in range(B):
@@ -141,37 +161,81 @@ def build_inputs(H, torch, seed, rank):
     return dict(cache=cache, dev=dev, host=host, vis=vis, outs=outs, topk=topk, pool=pool, ws=ws, step=step)
 
 
-def per_kernel_times(H, torch, I, reps=5):
-    """Average duration of each API call of the step, with CUDA events on the launching stream."""
-    st = torch.cuda.current_stream()
+def per_kernel_times(H, torch, I, reps=10):
+    """Average device duration of each API call of the step. The calls of one kind are captured
+    in a CUDA graph in step order (20 attention calls over the step's own indices, the Full pass,
+    the 4 Reindex passes) and the replays are timed with CUDA events on the launching stream, so
+    host launch latency is not counted."""
+    st = torch.cuda.Stream()
     B, T, nq = CFG.batch, CFG.T, CFG.nq
     d, ws = I["dev"], I["ws"]
-    acc = {"index_full": [], "index_reindex": [], "sparse_attn_decode": []}
-    for _ in range(reps):
-        latest = None
-        for j, l in enumerate(LAYERS):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            mode = MODES_BY_LAYER.get(l, 2)
-            if mode != 2:
-                e0.record(st)
-                if mode == 0:
-                    H.hsa_index_full(I["cache"], d[("qi", l)], d[("wi", l)], I["vis"], nq, T, I["topk"][j], I["pool"], ws)
-                    acc_key = "index_full"
-                else:
-                    H.hsa_index_reindex(I["cache"], d[("qi", l)], d[("wi", l)], I["vis"], nq, T, I["pool"],
-                                        I["topk"][j], ws)
-                    acc_key = "index_reindex"
-                e1.record(st)
-                acc[acc_key].append((e0, e1))
-                latest = I["topk"][j]
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record(st)
-            H.hsa_sparse_attn_decode(I["cache"], d[("qa", l)], latest, d[("sw", l)], I["vis"], nq, T, 1.0,
-                                     I["outs"][j], ws)
-            a1.record(st)
-            acc["sparse_attn_decode"].append((a0, a1))
-    torch.cuda.synchronize()
-    return {k: 1e-3 * statistics.mean(e0.elapsed_time(e1) for e0, e1 in v) for k, v in acc.items()}  # seconds
+    latest, att = None, []
+    for j, l in enumerate(LAYERS):
+        if MODES_BY_LAYER.get(l, 2) != 2:
+            latest = I["topk"][j]
+        att.append((l, j, latest))
+
+    def attn(s):
+        for l, j, tk in att:
+            H.hsa_sparse_attn_decode(I["cache"], d[("qa", l)], tk, d[("sw", l)], I["vis"], nq, T, 1.0,
+                                     I["outs"][j], ws, stream=s)
+
+    def full(s):
+        j = LAYERS.index(20)
+        H.hsa_index_full(I["cache"], d[("qi", 20)], d[("wi", 20)], I["vis"], nq, T, I["topk"][j], I["pool"], ws,
+                         stream=s)
+
+    def reindex(s):
+        for l in INDEX_LAYERS[1:]:
+            j = LAYERS.index(l)
+            H.hsa_index_reindex(I["cache"], d[("qi", l)], d[("wi", l)], I["vis"], nq, T, I["pool"], I["topk"][j],
+                                ws, stream=s)
+
+    out = {}
+    for key, fn, calls in (("sparse_attn_decode", attn, len(att)), ("index_full", full, 1),
+                           ("index_reindex", reindex, len(INDEX_LAYERS) - 1)):
+        st.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(g, stream=st):
+                fn(st)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            e0.record(st)
+            for _ in range(reps):
+                g.replay()
+            e1.record(st)
+        torch.cuda.synchronize()
+        out[key] = 1e-3 * e0.elapsed_time(e1) / (reps * calls)       # seconds per call
+    return out
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each kernel, from the
+# ncu captures summarised in profiles/, keyed by the SHA-256 of the kernel's source file at the
+# time of the capture: once the source changes, the figure no longer applies and is reported
+# as null.
+NCU_TRAFFIC = {
+    "sparse_attn_decode": ("attn.cu", "ca10f05583471101c92f1457ed0adaf18ac5ef4aa0abb80bd729cb394dc78a37", 10612736,
+                           "profiles/sparse_attn_b32_t128k.md"),
+}
+
+
+def ncu_traffic(kernel):
+    import hashlib
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec is None:
+        return None, None
+    fname, digest, traffic, src = rec
+    path = os.path.join(ROOT, "hierarchical_sparse_attention_index_gb300", "csrc", fname)
+    try:
+        with open(path, "rb") as f:
+            now = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None, None
+    return (traffic, src) if now == digest else (None, None)
 
 
 def run_hsa(args):
@@ -220,12 +284,8 @@ def run_hsa(args):
     code, flags = H.hsa_get_device_status()
     if code != 0 or flags != 0:
         raise RuntimeError(f"device status after the timed region: code {code} flags {flags}")
-    tmax = t
-    if world > 1:
-        tt = torch.tensor([t], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        tmax = float(tt.item())
-    value = world * args.steps / tmax
+    tmax = max_over_ranks(t, world, dist, device="cuda")
+    value = whole_job_value(args.steps, world, tmax)
 
     # per-kernel durations (eager, same work) for the roofline of the dominant kernel
     kt = per_kernel_times(H, torch, I)
@@ -243,9 +303,10 @@ def run_hsa(args):
         ach = scan_bytes / kt["index_full"] / 1e9
     else:
         ach = B * 16384 * SCAN_B / kt["index_reindex"] / 1e9
+    traffic, traffic_src = ncu_traffic(dominant)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
-                "peak_source": peak_src,
+                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": traffic,
+                "traffic_source": traffic_src, "peak_source": peak_src,
                 "per_call_us": {k: round(v * 1e6, 2) for k, v in kt.items()},
                 "step_share": {k: round(v / sum(shares.values()), 3) for k, v in shares.items()}}
 
