@@ -135,3 +135,61 @@ def write_exclusions(x64, group, scale_fmt, err_abs):
     near_m = _near_mid(v, 0.0) | (np.min(np.abs(np.abs(v)[..., None] - E2M1_MIDS), axis=-1) <= err / s[..., None])
     mask = near_m | near_b[..., None]
     return mask.reshape(N, D)
+
+
+def check_write(oc_lat, oc_bytes, gpu, entries, fmt, name):
+    """oc_lat: oracle fp64 latents [n,512]; oc_bytes: oracle (kv_q, kv_s, ik_q, ik_s); gpu: same from device."""
+    lat, K, W = oc_lat
+    n = lat.shape[0]
+    # main KV
+    ex = write_exclusions(lat, 16, fmt, WRITE_REL * np.maximum(1.0, np.abs(lat)))
+    gc = unpack_codes(gpu[0][entries])
+    oc = unpack_codes(oc_bytes[0])
+    grp_ex = ex.reshape(n, 32, 16).any(axis=2)
+    bad = (gc != oc) & ~ex
+    assert not bad.any(), f"{name}: {bad.sum()} main-KV codes differ outside the band"
+    bad_s = (gpu[1][entries] != oc_bytes[1]) & ~grp_ex
+    assert not bad_s.any(), f"{name}: {bad_s.sum()} main-KV scales differ"
+    assert ex.mean() < 1e-3, f"{name}: band excludes {ex.mean():.2e} of the elements"
+    # indexer K (compare element codes in natural order)
+    kerr = 4e-6 * (np.abs(lat) @ np.abs(W)) + WRITE_REL * np.abs(K)
+    exk = write_exclusions(K, 32, O.SCALE_E8M0, kerr)
+    gk = unpack_codes(O.index_k_to_natural(gpu[2][entries]))
+    ok_ = unpack_codes(O.index_k_to_natural(oc_bytes[2]))
+    bad = (gk != ok_) & ~exk
+    assert not bad.any(), f"{name}: {bad.sum()} indexer-K codes differ outside the band"
+    bad_s = (gpu[3][entries] != oc_bytes[3]) & ~exk.reshape(n, 4, 32).any(axis=2)
+    assert not bad_s.any(), f"{name}: {bad_s.sum()} indexer-K scales differ"
+    assert exk.mean() < 1e-2
+
+
+# ------------------------------------------------------------------ oracle writer in a process pool
+def write_chunk(args):
+    """Pool worker: the oracle's cache writer on one run of tokens. Entries depend only on their
+    own tokens (m = 1) or token pair (m = 2), so runs of tokens are independent."""
+    wkv, wg, W, m, fmt, keep = args
+    kv_q, kv_s, ik_q, ik_s, lat, K = O.cache_write_compress(f32(wkv), None if wg is None else f32(wg), f32(W), m,
+                                                            fmt)
+    return (kv_q, kv_s, ik_q, ik_s) + ((lat, K) if keep else ())
+
+
+def oracle_write(pool, wkv, wg, W, m=1, fmt=O.SCALE_E8M0, keep=False, chunk=16384):
+    """The oracle's writer over n tokens, split into runs of `chunk` tokens (even, so that m = 2
+    pairs stay whole) across a spawn process pool. Returns kv_q, kv_s, ik_q, ik_s (and the fp64
+    latent and indexer K with keep=True)."""
+    n = wkv.shape[0]
+    jobs = [(wkv[i:i + chunk], None if wg is None else wg[i:i + chunk], W, m, fmt, keep) for i in range(0, n, chunk)]
+    parts = pool.map(write_chunk, jobs)
+    return tuple(np.concatenate([p[k] for p in parts], axis=0) for k in range(len(parts[0])))
+
+
+class MainRows:
+    """Main-KV rows of one request, dequantised on demand (K_main[sel] for a list of positions),
+    so that attention references at 1M positions never dequantise the whole request."""
+
+    def __init__(self, kv_q, kv_s, fmt=O.SCALE_E8M0):
+        self.kv_q, self.kv_s, self.fmt = kv_q, kv_s, fmt
+
+    def __getitem__(self, sel):
+        sel = np.asarray(sel, np.int64)
+        return O.main_kv_dequant(self.kv_q[sel], self.kv_s[sel], self.fmt)

@@ -44,32 +44,6 @@ def round8(n):
 
 
 # ------------------------------------------------------------------ cache write
-def _check_write(H, oc_lat, oc_bytes, gpu, entries, fmt, name):
-    """oc_lat: oracle fp64 latents [n,512]; oc_bytes: oracle (kv_q, kv_s, ik_q, ik_s); gpu: same from device."""
-    lat, K, W = oc_lat
-    n = lat.shape[0]
-    # main KV
-    ex = P.write_exclusions(lat, 16, fmt, P.WRITE_REL * np.maximum(1.0, np.abs(lat)))
-    gc = P.unpack_codes(gpu[0][entries])
-    oc = P.unpack_codes(oc_bytes[0])
-    grp_ex = ex.reshape(n, 32, 16).any(axis=2)
-    bad = (gc != oc) & ~ex
-    assert not bad.any(), f"{name}: {bad.sum()} main-KV codes differ outside the band"
-    bad_s = (gpu[1][entries] != oc_bytes[1]) & ~grp_ex
-    assert not bad_s.any(), f"{name}: {bad_s.sum()} main-KV scales differ"
-    assert ex.mean() < 1e-3, f"{name}: band excludes {ex.mean():.2e} of the elements"
-    # indexer K (compare element codes in natural order)
-    kerr = 4e-6 * (np.abs(lat) @ np.abs(W)) + P.WRITE_REL * np.abs(K)
-    exk = P.write_exclusions(K, 32, O.SCALE_E8M0, kerr)
-    gk = P.unpack_codes(O.index_k_to_natural(gpu[2][entries]))
-    ok_ = P.unpack_codes(O.index_k_to_natural(oc_bytes[2]))
-    bad = (gk != ok_) & ~exk
-    assert not bad.any(), f"{name}: {bad.sum()} indexer-K codes differ outside the band"
-    bad_s = (gpu[3][entries] != oc_bytes[3]) & ~exk.reshape(n, 4, 32).any(axis=2)
-    assert not bad_s.any(), f"{name}: {bad_s.sum()} indexer-K scales differ"
-    assert exk.mean() < 1e-2
-
-
 @pytest.mark.parametrize("fmt", [O.SCALE_E8M0, O.SCALE_E4M3])
 def test_cache_write_m1(hsa, fmt):
     H = hsa
@@ -85,7 +59,7 @@ def test_cache_write_m1(hsa, fmt):
     for b in range(B):
         kv_q, kv_s, ik_q, ik_s, lat, K = O.cache_write_compress(P.f32(wkv[b]), None, P.f32(W), 1, fmt)
         ent = np.arange(starts[b], starts[b] + n)
-        _check_write(H, (lat, K, P.f32(W).astype(np.float64)), (kv_q, kv_s, ik_q, ik_s),
+        P.check_write((lat, K, P.f32(W).astype(np.float64)), (kv_q, kv_s, ik_q, ik_s),
                      [x[b] for x in g], ent, fmt, f"m1 b{b}")
         untouched = np.setdiff1d(np.arange(cap), ent)
         assert not g[0][b][untouched].any() and not g[2][b][untouched].any()
@@ -103,7 +77,7 @@ def test_cache_write_m2(hsa, fmt):
     g = [t.cpu().numpy()[0] for t in (cache.kv_q, cache.kv_s, cache.ik_q, cache.ik_s)]
     kv_q, kv_s, ik_q, ik_s, lat, K = O.cache_write_compress(P.f32(wkv[0]), P.f32(wg[0]), P.f32(W), 2, fmt)
     assert lat.shape[0] == 2048
-    _check_write(H, (lat, K, P.f32(W).astype(np.float64)), (kv_q, kv_s, ik_q, ik_s), g, np.arange(2048), fmt, "m2")
+    P.check_write((lat, K, P.f32(W).astype(np.float64)), (kv_q, kv_s, ik_q, ik_s), g, np.arange(2048), fmt, "m2")
     assert not g[0][2048:].any()
 
 
