@@ -422,30 +422,23 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     const int* slotpos = reinterpret_cast<const int*>(smem + L.slotpos) + s * kChunk;
 
     if (warp * 32 < nrows) {
-      // per-stage constants of this warp
-      float* const score_base = kPoolMode ? p.scores + (size_t)cur_seg * kPool + c * kChunk : nullptr;
-#pragma unroll 1
-      for (int mt = 0; mt < 2; ++mt) {
-        if (mt == 1 && warp * 32 + 16 >= nrows) break;
-        const int r0 = warp * 32 + mt * 16 + g, r1 = r0 + 8;
-        const uint4 A0 = lds128(codes + r0 * 64 + 16 * t);
-        const uint4 A1 = lds128(codes + r1 * 64 + 16 * t);
-        const uint32_t S0 = lds32(scales + r0 * 4), S1 = lds32(scales + r1 * 4);
-        const uint32_t aw0[4] = {A0.x, A0.y, A0.z, A0.w}, aw1[4] = {A1.x, A1.y, A1.z, A1.w};
-        // row of this lane for the stores: lanes t = 0 and t = 1 own rows r0 and r1
-        const int myr = (t & 1) ? r1 : r0;
-        int mypos;                       // Full: position; Reindex: slot position (or -1)
-        bool in0 = true, in1 = true;
-        if (kPoolMode) {
-          const int s0 = slotpos[r0], s1 = slotpos[r1];
-          in0 = s0 >= 0;
-          in1 = s1 >= 0;
-          mypos = (t & 1) ? s1 : s0;
-        } else {
-          mypos = c * kChunk + myr;
-        }
-        for (int ql = 0; ql < nql; ++ql) {
-          if (nql > 1) load_query_regs(ql);
+      const bool two = warp * 32 + 16 < nrows;        // the warp's second 16-row tile holds data
+      const uint32_t a_base = codes + (uint32_t)(warp * 32 + g) * 64u + 16u * t;
+      const uint32_t s_base = scales + (uint32_t)(warp * 32 + g) * 4u;
+      // this lane's row after the reduce-scatter below: rows 8t .. 8t+7 of the warp's 32 are
+      // the 8-entry block t, one row per lane g
+      const int r_mine = warp * 32 + 8 * t + g;
+      for (int ql = 0; ql < nql; ++ql) {
+        if (nql > 1) load_query_regs(ql);
+        // vp[mt][0/1]: ReLU-weighted sum over this lane's 4 heads for rows g / g+8 of tile mt
+        float vp[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          if (mt == 1 && !two) break;
+          const uint4 A0 = lds128(a_base + (uint32_t)mt * 1024u);
+          const uint4 A1 = lds128(a_base + (uint32_t)mt * 1024u + 512u);
+          const uint32_t S0 = lds32(s_base + (uint32_t)mt * 64u), S1 = lds32(s_base + (uint32_t)mt * 64u + 32u);
+          const uint32_t aw0[4] = {A0.x, A0.y, A0.z, A0.w}, aw1[4] = {A1.x, A1.y, A1.z, A1.w};
           float tot[2][4];
 #pragma unroll
           for (int gi = 0; gi < 4; ++gi) {
@@ -464,74 +457,54 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
               mma_f16_16816_zc(tmp[nt], f0, h0, f1, h1, B[nt][2 * gi][0], B[nt][2 * gi][1]);
               mma_f16_16816(tmp[nt], f2, h2, f3, h3, B[nt][2 * gi + 1][0], B[nt][2 * gi + 1][1]);
             }
-            if (gi == 0) {
 #pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                tot[nt][0] = sc0 * tmp[nt][0];
-                tot[nt][1] = sc0 * tmp[nt][1];
-                tot[nt][2] = sc1 * tmp[nt][2];
-                tot[nt][3] = sc1 * tmp[nt][3];
-              }
-            } else {
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                tot[nt][0] = fmaf(sc0, tmp[nt][0], tot[nt][0]);
-                tot[nt][1] = fmaf(sc0, tmp[nt][1], tot[nt][1]);
-                tot[nt][2] = fmaf(sc1, tmp[nt][2], tot[nt][2]);
-                tot[nt][3] = fmaf(sc1, tmp[nt][3], tot[nt][3]);
-              }
+            for (int nt = 0; nt < 2; ++nt) {
+              tot[nt][0] = gi ? fmaf(sc0, tmp[nt][0], tot[nt][0]) : sc0 * tmp[nt][0];
+              tot[nt][1] = gi ? fmaf(sc0, tmp[nt][1], tot[nt][1]) : sc0 * tmp[nt][1];
+              tot[nt][2] = gi ? fmaf(sc1, tmp[nt][2], tot[nt][2]) : sc1 * tmp[nt][2];
+              tot[nt][3] = gi ? fmaf(sc1, tmp[nt][3], tot[nt][3]) : sc1 * tmp[nt][3];
             }
           }
-          float v0 = 0.f, v1 = 0.f;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-              v0 = fmaf(wr[nt][j], fmaxf(tot[nt][j], 0.f), v0);
-              v1 = fmaf(wr[nt][j], fmaxf(tot[nt][2 + j], 0.f), v1);
+              vp[mt][0] = fmaf(wr[nt][j], fmaxf(tot[nt][j], 0.f), vp[mt][0]);
+              vp[mt][1] = fmaf(wr[nt][j], fmaxf(tot[nt][2 + j], 0.f), vp[mt][1]);
             }
-          v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-          v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-          v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
-          v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
-          bool ok0, ok1;
-          if (!kPoolMode) {
-            const int vq = svis[ql];
-            ok0 = c * kChunk + r0 < vq;
-            ok1 = c * kChunk + r1 < vq;
-          } else {
-            ok0 = in0;
-            ok1 = in1;
+        }
+        // Reduce-scatter over the 4 head lanes t of a row group: after it, lane (g, t) holds
+        // the full 16-head score of row 8t + g of the warp (tile t >> 1, row g + 8 (t & 1)).
+        const bool hi2 = (t & 2) != 0, hi1 = (t & 1) != 0;
+        const float k0 = (hi2 ? vp[1][0] : vp[0][0]) + __shfl_xor_sync(0xffffffffu, hi2 ? vp[0][0] : vp[1][0], 2);
+        const float k1 = (hi2 ? vp[1][1] : vp[0][1]) + __shfl_xor_sync(0xffffffffu, hi2 ? vp[0][1] : vp[1][1], 2);
+        float v = (hi1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, hi1 ? k0 : k1, 1);
+        bool ok;
+        if (!kPoolMode) {
+          ok = c * kChunk + r_mine < svis[ql];
+        } else {
+          ok = slotpos[r_mine] >= 0;
+        }
+        v = ok ? v : -INFINITY;
+        const uint32_t bin = order_key(v) >> kHistShift;
+        if (!kPoolMode) {
+          const int row = cur_seg * p.nq + ql;
+          p.scores[(size_t)row * p.ld_s + c * kChunk + r_mine] = v;
+          if (ok) atomicAdd(hist_sm + (2 * ql) * (kHistBins / 2) + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
+          // 8-entry block max: block t of the warp is held by lanes g = 0..7 of column t
+          float bm = v;
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+          const int jb = ((c * kChunk + warp * 32) >> 3) + t;
+          if (g == 0 && jb * 8 < svis[ql]) {
+            p.blkmax[(size_t)row * p.ld_b + jb] = bm;
+            const uint32_t bb = order_key(bm) >> kHistShift;
+            atomicAdd(hist_sm + (2 * ql + 1) * (kHistBins / 2) + (bb >> 1), (bb & 1) ? 0x10000u : 1u);
           }
-          v0 = ok0 ? v0 : -INFINITY;
-          v1 = ok1 ? v1 : -INFINITY;
-          const float myv = (t & 1) ? v1 : v0;
-          const bool myok = (t & 1) ? ok1 : ok0;
-          const uint32_t mybin = order_key(myv) >> kHistShift;
-          const uint32_t myinc = (mybin & 1) ? 0x10000u : 1u;
-          if (!kPoolMode) {
-            const int row = cur_seg * p.nq + ql;
-            if (t < 2) p.scores[(size_t)row * p.ld_s + mypos] = myv;
-            uint32_t* hp = hist_sm + (2 * ql) * (kHistBins / 2);
-            if (t < 2 && myok) atomicAdd(hp + (mybin >> 1), myinc);
-            // block maxima over rows g = 0..7 (block A) and 8..15 (block B); lanes 0/1 store them
-            float bA = v0, bB = v1;
-#pragma unroll
-            for (int o = 4; o <= 16; o <<= 1) {
-              bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, o));
-              bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, o));
-            }
-            const int jb = ((c * kChunk + warp * 32 + mt * 16) >> 3) + (lane & 1);
-            const float bv = (lane & 1) ? bB : bA;
-            const bool bok = (lane < 2) && (jb * 8 < svis[ql]);
-            const uint32_t bbin = order_key(bv) >> kHistShift;
-            if (bok) p.blkmax[(size_t)row * p.ld_b + jb] = bv;
-            uint32_t* hb = hist_sm + (2 * ql + 1) * (kHistBins / 2);
-            if (bok) atomicAdd(hb + (bbin >> 1), (bbin & 1) ? 0x10000u : 1u);
-          } else {
-            if (t < 2) score_base[myr] = myv;
-            if (t < 2 && myok) atomicAdd(hist_sm + (mybin >> 1), myinc);
-          }
+        } else {
+          p.scores[(size_t)cur_seg * kPool + c * kChunk + r_mine] = v;
+          if (ok) atomicAdd(hist_sm + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
         }
       }
     }
