@@ -36,6 +36,10 @@ constexpr int kScanThreads = kConsumers + 32;
 constexpr int kCodesBytes = kChunk * 64;
 constexpr int kScaleBytes = kChunk * 4;
 constexpr int kFlushItems = 120;   // packed 16-bit histogram counters: flush before 65536 entries
+// Reindex: each consumer warp gathers its own 32 pool slots (four 8-entry runs) of the stages
+// ahead into a private ring of kRing buffers with cp.async (16 bytes per lane, 512-byte runs).
+constexpr int kRing = 4;
+constexpr int kWarpCodes = 32 * 64, kWarpScales = 32 * 4, kWarpSlots = 32 * 4;
 
 struct ScanSmemLayout {
   int nst, nlr;
@@ -45,12 +49,18 @@ struct ScanSmemLayout {
 __host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq) {
   ScanSmemLayout L;
   const int nql = pool_mode ? 1 : nq;
-  L.nst = (nql <= 2) ? 3 : (nql <= 5 ? 2 : 1);
+  L.nst = pool_mode ? 1 : ((nql <= 2) ? 3 : (nql <= 5 ? 2 : 1));
   L.nlr = pool_mode ? 1 : 2 * nq;
   size_t o = 0;
-  L.codes = o;   o += (size_t)L.nst * kCodesBytes;
-  L.scales = o;  o += (size_t)L.nst * kScaleBytes;
-  L.slotpos = o; o += (size_t)L.nst * kChunk * 4;
+  if (pool_mode) {     // per-warp rings [warp][kRing][...]
+    L.codes = o;   o += (size_t)kConsumerWarps * kRing * kWarpCodes;
+    L.scales = o;  o += (size_t)kConsumerWarps * kRing * kWarpScales;
+    L.slotpos = o; o += (size_t)kConsumerWarps * kRing * kWarpSlots;
+  } else {
+    L.codes = o;   o += (size_t)L.nst * kCodesBytes;
+    L.scales = o;  o += (size_t)L.nst * kScaleBytes;
+    L.slotpos = o;
+  }
   L.bfrag = o;   o += (size_t)nql * 2 * 8 * 32 * 2 * 4;
   L.wsc = o;     o += (size_t)nql * 16 * 4;
   L.hist = o;    o += (size_t)L.nlr * (kHistBins / 2) * 4;
@@ -69,6 +79,15 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Exclusive prefix sum over the first `nthreads` threads (a multiple of 32); scratch holds 32 ints.
@@ -147,7 +166,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const ScanSmemLayout L = scan_smem_layout(kPoolMode, p.nq);
   const int nql = kOneQuery ? 1 : p.nq;
-  const int nst = kOneQuery ? 3 : L.nst;   // one query: always the 3-stage ring (see scan_smem_layout)
+  const int nst = kPoolMode ? 1 : (kOneQuery ? 3 : L.nst);   // compile-time where it can be (scan_smem_layout)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last flag, [2..9] vis, [16..48) scratch
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
@@ -178,7 +197,8 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   const int cps = p.chunks_per_seg;
 
   if (warp == kConsumerWarps) {
-    // ---------------------------------------------------------------- producer warp
+    // ---------------------------------------------------------------- producer warp (Full only)
+    if (kPoolMode) return;
     int s = 0, round = 0, seg = i0 / cps, c = i0 % cps;
     for (int it = i0; it < i1; ++it) {
       if (round > 0) {
@@ -191,7 +211,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       const uint32_t full = full0 + 8 * s;
       const uint32_t dcodes = smem_u32(smem + L.codes + (size_t)s * kCodesBytes);
       const uint32_t dscales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
-      if (!kPoolMode) {
+      {
         int vmax = 0;
         for (int q = 0; q < p.nq; ++q) vmax = max(vmax, __ldg(p.vis + seg * p.nq + q));
         vmax = (int)imin64(vmax, p.cap);
@@ -206,48 +226,6 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
             bulk_g2s(dscales, p.ik_s + e0 * 4, (uint32_t)nc * 4u, full);
           } else {
             mbar_arrive(full);
-          }
-        }
-      } else {
-        // pool gather: lane handles the 8-slot runs `lane` and `lane + 32` of this 512-slot chunk
-        const int row = seg;
-        const int b = row / p.nq;
-        const int vis = __ldg(p.vis + row);
-        bool ok[2];
-        int base[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int bi = lane + 32 * u;
-          const int* pr = p.pool + (int64_t)row * kPool + c * kChunk + bi * 8;
-          int* sp = reinterpret_cast<int*>(smem + L.slotpos) + s * kChunk + bi * 8;
-          const int4 pa = __ldg(reinterpret_cast<const int4*>(pr));
-          const int4 pb = __ldg(reinterpret_cast<const int4*>(pr) + 1);
-          const int pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-          base[u] = pv[0];
-          ok[u] = (base[u] >= 0) && ((base[u] & 7) == 0) && (base[u] < p.cap);
-          if (base[u] >= 0 && !ok[u]) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int v = pv[j];
-            int outv = -1;
-            if (ok[u] && v >= 0) {
-              if (v == base[u] + j && v < vis) outv = v;
-              else if (v != base[u] + j || v >= p.cap) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-            }
-            sp[j] = outv;
-          }
-        }
-        const uint32_t m0 = __ballot_sync(0xffffffffu, ok[0]), m1 = __ballot_sync(0xffffffffu, ok[1]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(__popc(m0) + __popc(m1)) * (512u + 32u));
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (ok[u]) {
-            const int bi = lane + 32 * u;
-            const int64_t e0 = (int64_t)b * p.cap + base[u];
-            bulk_g2s(dcodes + bi * 512, p.ik_q + e0 * 64, 512u, full);
-            bulk_g2s(dscales + bi * 32, p.ik_s + e0 * 4, 32u, full);
           }
         }
       }
@@ -391,6 +369,72 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   uint32_t ph = 0;
   bool dead = false;
   int vmax_seg = 0;                // Full: visible rows of the current request (max over its queries)
+
+  // Reindex: this warp's slots of item k are pool[seg][c * kChunk + warp * 32 + lane]; the
+  // warp gathers their four 8-entry runs itself, kRing - 1 items ahead of the one it scores.
+  int rs = 0;                      // ring buffer of the current item
+  int iseg = seg, ic = c;          // next item whose runs are gathered
+  int lseg = seg, lc = c;          // next item whose pool values are loaded
+  int pv_next = -1;                // pool value (this lane's slot) of the next item to gather
+  const uint32_t ring_codes = smem_u32(smem + L.codes) + (uint32_t)(warp * kRing * kWarpCodes);
+  const uint32_t ring_scales = smem_u32(smem + L.scales) + (uint32_t)(warp * kRing * kWarpScales);
+  int* const ring_slots = reinterpret_cast<int*>(smem + L.slotpos) + warp * kRing * 32;
+  auto pool_val = [&](int sg, int ch) -> int {
+    return __ldg(p.pool + (int64_t)sg * kPool + ch * kChunk + warp * 32 + lane);
+  };
+  auto advance = [&](int& sg, int& ch) {
+    if (++ch == cps) {
+      ch = 0;
+      ++sg;
+    }
+  };
+  auto gather = [&](int sg, int slot, int pv) {
+    // run u (slots 8u .. 8u+7 of the warp) starts at the pool value of lane 8u; a run is fetched
+    // only if that start is an 8-aligned in-range entry, and a slot is scored only if it holds
+    // start + its offset and is visible; anything else is flagged
+    const int vis = __ldg(p.vis + sg);
+    const int64_t ebase = (int64_t)(sg / p.nq) * p.cap;
+    const int j = lane & 7;
+    const int base = __shfl_sync(0xffffffffu, pv, lane & ~7);
+    const bool bok = (base >= 0) && ((base & 7) == 0) && (base < p.cap);
+    int outv = -1;
+    if (bok && pv >= 0) {
+      if (pv == base + j && pv < vis) outv = pv;
+      else if (pv != base + j || pv >= p.cap) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+    } else if (j == 0 && base >= 0 && !bok) {
+      flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+    }
+    ring_slots[slot * 32 + lane] = outv;
+    const uint32_t dc = ring_codes + (uint32_t)(slot * kWarpCodes), ds = ring_scales + (uint32_t)(slot * kWarpScales);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int bb = __shfl_sync(0xffffffffu, base, 8 * u);
+      if (bb >= 0 && (bb & 7) == 0 && bb < p.cap) cp_async16(dc + u * 512 + lane * 16, p.ik_q + (ebase + bb) * 64 + lane * 16);
+    }
+    const int us = (lane >> 1) & 3;
+    const int bs = __shfl_sync(0xffffffffu, base, 8 * us);
+    if (lane < 8 && bs >= 0 && (bs & 7) == 0 && bs < p.cap)
+      cp_async16(ds + us * 32 + (lane & 1) * 16, p.ik_s + (ebase + bs) * 4 + (lane & 1) * 16);
+    cp_async_commit();
+  };
+  if (kPoolMode) {
+    int pv0[kRing - 1], sg0[kRing - 1];
+#pragma unroll
+    for (int j = 0; j < kRing - 1; ++j) {
+      pv0[j] = (i0 + j < i1) ? pool_val(lseg, lc) : -1;
+      sg0[j] = lseg;
+      advance(lseg, lc);
+    }
+#pragma unroll
+    for (int j = 0; j < kRing - 1; ++j) {
+      if (i0 + j < i1) gather(sg0[j], j, pv0[j]);
+      else cp_async_commit();
+      advance(iseg, ic);
+    }
+    pv_next = (i0 + kRing - 1 < i1) ? pool_val(lseg, lc) : -1;
+    advance(lseg, lc);
+  }
+
   for (int it = i0; it < i1; ++it) {
     if (seg != cur_seg) {
       if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
@@ -410,21 +454,38 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     }
     ++seg_items;
     ++since_flush;
-    if (!dead && *reinterpret_cast<volatile int*>(misc) != 0) dead = true;
-    if (!dead && !mbar_wait(full0 + 8 * s, ph)) {
-      flag_status(p.status, HSA_FLAG_TIMEOUT);
-      *reinterpret_cast<volatile int*>(misc) = 1;
-      dead = true;
+    uint32_t codes, scales;
+    const int* slotpos = nullptr;
+    int row_off;                   // first row of this warp inside the buffer it reads
+    if (kPoolMode) {
+      if (it + kRing - 1 < i1) gather(iseg, rs == 0 ? kRing - 1 : rs - 1, pv_next);
+      else cp_async_commit();
+      advance(iseg, ic);
+      pv_next = (it + kRing < i1) ? pool_val(lseg, lc) : -1;
+      advance(lseg, lc);
+      cp_async_wait<kRing - 1>();  // this item's runs have landed
+      __syncwarp();
+      codes = ring_codes + (uint32_t)(rs * kWarpCodes);
+      scales = ring_scales + (uint32_t)(rs * kWarpScales);
+      slotpos = ring_slots + rs * 32;
+      row_off = 0;
+    } else {
+      if (!dead && *reinterpret_cast<volatile int*>(misc) != 0) dead = true;
+      if (!dead && !mbar_wait(full0 + 8 * s, ph)) {
+        flag_status(p.status, HSA_FLAG_TIMEOUT);
+        *reinterpret_cast<volatile int*>(misc) = 1;
+        dead = true;
+      }
+      codes = smem_u32(smem + L.codes) + (uint32_t)s * kCodesBytes;
+      scales = smem_u32(smem + L.scales) + (uint32_t)s * kScaleBytes;
+      row_off = warp * 32;
     }
     const int nrows = dead ? 0 : (kPoolMode ? kChunk : max(0, min(kChunk, vmax_seg - c * kChunk)));
-    const uint32_t codes = smem_u32(smem + L.codes) + (uint32_t)s * kCodesBytes;
-    const uint32_t scales = smem_u32(smem + L.scales) + (uint32_t)s * kScaleBytes;
-    const int* slotpos = reinterpret_cast<const int*>(smem + L.slotpos) + s * kChunk;
 
     if (warp * 32 < nrows) {
       const bool two = warp * 32 + 16 < nrows;        // the warp's second 16-row tile holds data
-      const uint32_t a_base = codes + (uint32_t)(warp * 32 + g) * 64u + 16u * t;
-      const uint32_t s_base = scales + (uint32_t)(warp * 32 + g) * 4u;
+      const uint32_t a_base = codes + (uint32_t)(row_off + g) * 64u + 16u * t;
+      const uint32_t s_base = scales + (uint32_t)(row_off + g) * 4u;
       // this lane's row after the reduce-scatter below: rows 8t .. 8t+7 of the warp's 32 are
       // the 8-entry block t, one row per lane g
       const int r_mine = warp * 32 + 8 * t + g;
@@ -483,7 +544,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
         if (!kPoolMode) {
           ok = c * kChunk + r_mine < svis[ql];
         } else {
-          ok = slotpos[r_mine] >= 0;
+          ok = slotpos[8 * t + g] >= 0;
         }
         v = ok ? v : -INFINITY;
         const uint32_t bin = order_key(v) >> kHistShift;
@@ -509,10 +570,14 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    if (++s == nst) {
-      s = 0;
-      ph ^= 1u;
+    if (!kPoolMode) {
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (++s == nst) {
+        s = 0;
+        ph ^= 1u;
+      }
+    } else if (++rs == kRing) {
+      rs = 0;
     }
     if (++c == cps) {
       c = 0;
