@@ -16,8 +16,8 @@ struct SelState {
   int32_t thr_bin;   // threshold histogram bin; -1 = every valid element is taken
   int32_t above;     // elements in bins above thr_bin
   int32_t nvalid;    // valid elements of the row
-  int32_t nsure;     // collect: elements appended to the sure list
-  int32_t ncand;     // collect: elements appended to the candidate list
+  int32_t nsure;     // unused (kept zero)
+  int32_t ncand;     // unused (kept zero)
   int32_t ready;     // 1 once thr_bin/above/nvalid are written for this call
   int32_t pad[2];
 };

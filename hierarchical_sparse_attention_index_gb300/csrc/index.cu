@@ -17,11 +17,13 @@
 //    ([ARCH] §3.3 块 max 是上界) and a 4096-bin histogram of the top 12 bits of each score's
 //    order key. The last CTA to finish a request turns the histograms into the threshold bins
 //    of the position top-512 and the block top-2048.
-// Selection (exact; ties to the lower index):
-//  - collect: elements above the threshold bin are taken, elements in it become candidates.
-//  - finish: an 11-bit-digit radix select over (low key bits, inverted index) composites picks
-//    the remaining candidates. A bitmap over the index space then emits the result in
-//    ascending order, expands blocks into the candidate pool, and clears the workspace state.
+// Selection (exact; ties to the lower index), one CTA per (row, selection): elements above the
+// threshold bin are taken, elements in it become candidates, and an 11-bit-digit radix select
+// over (low key bits, inverted index) composites picks the remaining ones. A bitmap over the
+// index space then emits the result in ascending order, expands blocks into the candidate
+// pool, and clears the workspace state.
+#include <algorithm>
+
 #include "hsa_common.cuh"
 #include "hsa_internal.h"
 
@@ -587,82 +589,9 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
 }
 
-// ------------------------------------------------------------------ collect
-constexpr int kCollectThreads = 256;
-constexpr int kCollectChunk = 2048;   // 8 elements per thread, all loads issued first
-
-__device__ __forceinline__ void warp_append(bool pred, int value, int* counter, int* list, int cap,
-                                            uint32_t* status) {
-  const uint32_t m = __ballot_sync(0xffffffffu, pred);
-  if (!m) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(m) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(m));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (pred) {
-    const int off = base + __popc(m & ((1u << lane) - 1u));
-    if (off < cap) list[off] = value;
-    else flag_status(status, HSA_FLAG_INDEX_RANGE);
-  }
-}
-
-__global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectParams p) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int row = blockIdx.y, which = blockIdx.z;
-  const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
-  const float* data;
-  int n;
-  int64_t cand_off = 0, sure_off = 0;
-  int sure_cap;
-  if (p.pool_mode) {
-    data = p.scores + (size_t)row * kPool;
-    n = kPool;
-    sure_cap = kTopK;
-  } else if (which == 0) {
-    data = p.scores + (size_t)row * p.ld_s;
-    n = vis;
-    sure_cap = kTopK;
-  } else {
-    data = p.blkmax + (size_t)row * p.ld_b;
-    n = (vis + kBlk - 1) / kBlk;
-    cand_off = p.ld_s;
-    sure_off = kTopK;
-    sure_cap = kCandBlocks;
-  }
-  const int e0 = blockIdx.x * kCollectChunk;
-  if (e0 >= n) return;
-  SelState* st = p.state + (p.pool_mode ? row : 2 * row + which);
-  const int thr = *reinterpret_cast<volatile int*>(&st->thr_bin);
-  int* cand = p.cand + (size_t)row * p.ld_cand + cand_off;
-  int* sure = p.sure + (size_t)row * p.ld_sure + sure_off;
-  const int e1 = min(n, e0 + kCollectChunk);
-  constexpr int kPer = kCollectChunk / kCollectThreads;
-  float v[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = e0 + j * kCollectThreads + threadIdx.x;
-    v[j] = (e < e1) ? __ldcg(data + e) : -INFINITY;
-  }
-  const int cand_cap = (int)(which == 0 ? (p.pool_mode ? kPool : p.ld_s) : p.ld_b);
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = e0 + j * kCollectThreads + threadIdx.x;
-    bool is_sure = false, is_cand = false;
-    if (v[j] != -INFINITY) {
-      const int bin = (int)(order_key(v[j]) >> kHistShift);
-      is_sure = (thr < 0) || (bin > thr);
-      is_cand = (thr >= 0) && (bin == thr);
-    }
-    warp_append(is_sure, e, &st->nsure, sure, sure_cap, p.status);
-    warp_append(is_cand, e, &st->ncand, cand, cand_cap, p.status);
-  }
-}
-
-// ------------------------------------------------------------------ finish
-constexpr int kFinishThreads = 1024;
-constexpr int kFinStage = 8192;   // candidates staged in shared memory
+// ------------------------------------------------------------------ select
+constexpr int kSelThreads = 1024;
+constexpr int kFinStage = 8192;   // threshold-bin candidates kept in shared memory; more spill to the workspace
 
 __device__ __forceinline__ int block_excl_scan_1024(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -690,7 +619,15 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int* scratch, int* to
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectParams p) {
+// One CTA per (row, selection): the exact top-K of one score array, emitted ascending.
+//  1. stream the row once: an element whose 12-bit key bin lies above the threshold bin the
+//     score pass found is taken at once (a bit in the index bitmap); an element in the
+//     threshold bin becomes a candidate (index + low 20 key bits, in shared memory);
+//  2. an 11-bit-digit radix select over the candidates' (low key bits, inverted index)
+//     composites takes the remaining K - above, ties to the lower index;
+//  3. the bitmap is emitted in ascending order (Reindex: through the pool; Full blocks: expanded
+//     into 8 positions each), and the row's histogram and state are cleared for the next call.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
   extern __shared__ __align__(16) uint32_t fsm[];
   const int row = blockIdx.x, which = blockIdx.y;
   const int tid = threadIdx.x;
@@ -699,7 +636,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
   const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
   const float* data;
   int n, K;
-  int64_t cand_off = 0, sure_off = 0;
+  int64_t cand_off = 0;
   if (p.pool_mode) {
     data = p.scores + (size_t)row * kPool;
     n = kPool;
@@ -713,7 +650,6 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
     n = (vis + kBlk - 1) / kBlk;
     K = kCandBlocks;
     cand_off = p.ld_s;
-    sure_off = kTopK;
   }
   SelState* st = p.state + (p.pool_mode ? row : 2 * row + which);
   const int nwords = (max(n, 1) + 31) >> 5;
@@ -722,52 +658,75 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
   int* scratch = reinterpret_cast<int*>(shist + 2048);   // [64]
   int* s_cidx = scratch + 64;                   // [kFinStage]
   uint32_t* s_ckey = reinterpret_cast<uint32_t*>(s_cidx + kFinStage);   // [kFinStage]
+  int* gcand = p.cand + (size_t)row * p.ld_cand + cand_off;              // overflow candidates
+  const int gcap = (int)(p.pool_mode ? kPool : (which == 0 ? p.ld_s : p.ld_b));
 
-  __shared__ int s_thr, s_nvalid, s_nsure, s_ncand, s_ready;
+  __shared__ int s_thr, s_nvalid, s_ready, s_ncand, s_nsure;
   __shared__ int s_digit, s_above, s_cnt;
   if (tid == 0) {
     volatile SelState* vs = st;
     s_ready = vs->ready;
     s_thr = vs->thr_bin;
     s_nvalid = vs->nvalid;
-    s_nsure = vs->nsure;
-    s_ncand = vs->ncand;
+    s_ncand = 0;
+    s_nsure = 0;
   }
-  for (int i = tid; i < nwords; i += kFinishThreads) bitmap[i] = 0;
+  for (int i = tid; i < nwords; i += kSelThreads) bitmap[i] = 0;
   __syncthreads();
   const int thr = s_ready ? s_thr : -1;
-  const int nvalid = s_ready ? s_nvalid : 0;
-  const int Keff = min(K, nvalid);
-  const int nsure = min(s_nsure, K);
-  const int cand_cap = (int)(p.pool_mode ? kPool : (which == 0 ? p.ld_s : p.ld_b));
-  const int ncand = min(s_ncand, cand_cap);
-  const int* cand = p.cand + (size_t)row * p.ld_cand + cand_off;
-  const int* sure = p.sure + (size_t)row * p.ld_sure + sure_off;
+  const int Keff = min(K, s_ready ? s_nvalid : 0);
 
-  for (int i = tid; i < nsure; i += kFinishThreads) {
-    const int e = __ldcg(sure + i);
-    if (e >= 0 && e < n) atomicOr(bitmap + (e >> 5), 1u << (e & 31));
-  }
-  int need = Keff - nsure;
-  if (thr >= 0 && need > 0 && ncand > 0) {
-    // stage the candidates (index, low 20 key bits) in shared memory when they fit
-    const bool staged = ncand <= kFinStage;
-    if (staged) {
-      for (int i = tid; i < ncand; i += kFinishThreads) {
-        const int e = __ldcg(cand + i);
-        s_cidx[i] = e;
-        s_ckey[i] = order_key(__ldcg(data + e)) & 0xFFFFFu;
-      }
-      __syncthreads();
+  // 1. one pass over the row: 8 float4 loads in flight per thread
+  const int n4 = (n + 3) >> 2;
+  for (int base = 0; base < n4; base += 8 * kSelThreads) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i4 = base + u * kSelThreads + tid;
+      v[u] = (i4 < n4) ? __ldcg(reinterpret_cast<const float4*>(data) + i4)
+                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e0 = 4 * (base + u * kSelThreads + tid);
+      const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = e0 + j;
+        if (e >= n || f[j] == -INFINITY) continue;
+        const uint32_t key = order_key(f[j]);
+        const int bin = (int)(key >> kHistShift);
+        if (thr < 0 || bin > thr) {
+          atomicOr(bitmap + (e >> 5), 1u << (e & 31));
+          atomicAdd(&s_nsure, 1);
+        } else if (bin == thr) {
+          const int slot = atomicAdd(&s_ncand, 1);
+          if (slot < kFinStage) {
+            s_cidx[slot] = e;
+            s_ckey[slot] = key & 0xFFFFFu;
+          } else if (slot - kFinStage < gcap) {
+            gcand[slot - kFinStage] = e;
+          } else {
+            flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int ncand = min(s_ncand, kFinStage + gcap);
+  const int need = Keff - s_nsure;
+
+  // 2. exact selection of the remaining `need` among the candidates
+  if (thr >= 0 && need > 0 && ncand > 0) {
     auto comp_of = [&](int i) -> uint64_t {
       int e;
       uint32_t k20;
-      if (staged) {
+      if (i < kFinStage) {
         e = s_cidx[i];
         k20 = s_ckey[i];
       } else {
-        e = __ldcg(cand + i);
+        e = __ldcg(gcand + (i - kFinStage));
         k20 = order_key(__ldcg(data + e)) & 0xFFFFFu;
       }
       return ((uint64_t)k20 << 32) | (uint64_t)(~(uint32_t)e);
@@ -779,9 +738,9 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
     for (int d = 0; d < 5; ++d) {
       const int sh = shifts[d];
       const uint32_t wm = (1u << widths[d]) - 1u;
-      for (int i = tid; i < 2048; i += kFinishThreads) shist[i] = 0;
+      for (int i = tid; i < 2048; i += kSelThreads) shist[i] = 0;
       __syncthreads();
-      for (int i = tid; i < ncand; i += kFinishThreads) {
+      for (int i = tid; i < ncand; i += kSelThreads) {
         const uint64_t comp = comp_of(i);
         if ((comp & mask) == prefix) atomicAdd(shist + ((comp >> sh) & wm), 1u);
       }
@@ -810,7 +769,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
       __syncthreads();
       if (all_in) break;
     }
-    for (int i = tid; i < ncand; i += kFinishThreads) {
+    for (int i = tid; i < ncand; i += kSelThreads) {
       const uint64_t comp = comp_of(i);
       if ((comp & mask) >= prefix) {
         const int e = (int)(~(uint32_t)(comp & 0xFFFFFFFFull));
@@ -820,8 +779,8 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
   }
   __syncthreads();
 
-  // ascending emission
-  const int per = (nwords + kFinishThreads - 1) / kFinishThreads;
+  // 3. ascending emission
+  const int per = (nwords + kSelThreads - 1) / kSelThreads;
   const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
   int cnt = 0;
   for (int i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
@@ -839,7 +798,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
         ++o;
       }
     }
-    for (int j = total + tid; j < kTopK; j += kFinishThreads) out[j] = -1;
+    for (int j = total + tid; j < kTopK; j += kSelThreads) out[j] = -1;
   } else if (which == 0) {
     int32_t* out = p.topk_out + (size_t)row * kTopK;
     for (int i = w0; i < w1; ++i) {
@@ -851,7 +810,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
         ++o;
       }
     }
-    for (int j = total + tid; j < kTopK; j += kFinishThreads) out[j] = -1;
+    for (int j = total + tid; j < kTopK; j += kSelThreads) out[j] = -1;
   } else {
     int32_t* out = p.pool_out + (size_t)row * kPool;
     for (int i = w0; i < w1; ++i) {
@@ -877,11 +836,11 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectPara
         ++o;
       }
     }
-    for (int j = 8 * min(total, kCandBlocks) + tid; j < kPool; j += kFinishThreads) out[j] = -1;
+    for (int j = 8 * min(total, kCandBlocks) + tid; j < kPool; j += kSelThreads) out[j] = -1;
   }
   // clear this row's histogram and state for the next call
   uint32_t* gh = p.hist + (size_t)(p.pool_mode ? row : 2 * row + which) * kHistBins;
-  for (int i = tid; i < kHistBins; i += kFinishThreads) gh[i] = 0;
+  for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0;
   if (tid == 0) {
     st->thr_bin = 0;
     st->above = 0;
@@ -924,18 +883,15 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
   const int rows = p.batch * p.nq;
   const int nsel = p.pool_mode ? 1 : 2;
   const int64_t nmax = p.pool_mode ? kPool : p.max_vis;
-  dim3 cg((unsigned)((nmax + kCollectChunk - 1) / kCollectChunk), (unsigned)rows, (unsigned)nsel);
-  cudaError_t e = launch_pdl(collect_kernel, cg, dim3(kCollectThreads), 0, s, p);
-  if (e != cudaSuccess) return e;
-  const int64_t nwords = (nmax + 31) / 32;
+  const int64_t nwords = (std::max<int64_t>(nmax, 1) + 31) / 32;
   const size_t smem = (size_t)((nwords + 3) & ~3) * 4 + 2048 * 4 + 64 * 4 + (size_t)kFinStage * 8;
   static size_t set_bytes = 0;
   if (smem > set_bytes) {
-    e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     set_bytes = smem;
   }
-  return launch_pdl(finish_kernel, dim3((unsigned)rows, (unsigned)nsel), dim3(kFinishThreads), smem, s, p);
+  return launch_pdl(select_kernel, dim3((unsigned)rows, (unsigned)nsel), dim3(kSelThreads), smem, s, p);
 }
 
 }  // namespace hsa
