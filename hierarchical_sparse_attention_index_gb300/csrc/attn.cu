@@ -27,7 +27,7 @@
 namespace hsa {
 namespace {
 
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 512;
 constexpr int kCluster = kAttnSplit;
 constexpr int kRows = 160;                               // keys per CTA
 constexpr int kTopRows = 128;
@@ -38,7 +38,7 @@ constexpr uint32_t kOffK = 0, kOffQ = kTileBytes, kOffMisc = kOffQ + kQBytes;
 constexpr uint32_t kMiscBytes = 1792;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;   // + alignment slack
 constexpr size_t kPartFloats = (size_t)kHAtt * kDLat + 2 * kHAtt;   // one CTA's partial in the workspace
-constexpr int kSStride = 164;                            // fp32 staging row stride (conflict-free)
+constexpr int kSStride = 168;                            // fp32 staging row stride (conflict-free)
 constexpr int kTmemCols = 512;
 constexpr int kColS0 = 0, kColS1 = 64, kColO = 256;
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -79,6 +79,12 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
         "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),             \
         "=r"(r[30]), "=r"(r[31])                                                                                \
       : "r"(taddr))
+#define TMEM_LD16(taddr, r)                                                                                     \
+  asm volatile(                                                                                                 \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"   \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),        \
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])   \
+      : "r"(taddr))
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -99,6 +105,12 @@ __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
   return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
 }
+// elementwise max(m, |x|) on bf16 pairs
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t m, uint32_t x) {
+  const __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&m),
+                                   __habs2(*reinterpret_cast<const __nv_bfloat162*>(&x)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t s2) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&s2));
   return *reinterpret_cast<const uint32_t*>(&r);
@@ -113,12 +125,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const uint32_t sK = base + kOffK, sQ = base + kOffQ, sP = base + kOffQ;
   float* misc = reinterpret_cast<float*>(sm + kOffMisc);
   float* s_scale = misc;              // [64] logit scale per head
-  float* s_m = misc + 64;             // [64] local max (read remotely)
-  float* s_l = misc + 128;            // [64] local sum (read remotely)
+  float* s_m = misc + 64;             // [64] local max
+  float* s_l = misc + 128;            // [64] local sum
   float* s_w = misc + 192;            // [4][16] combine weights of this CTA's heads
   int* s_valid = reinterpret_cast<int*>(misc + 256);      // [160]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 416);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(misc + 418);
+  float* s_qmax = misc + 64;          // [16 warps][8 heads] partial |q| maxima (before s_m / s_l are used)
   const uint32_t bar = smem_u32(s_bar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -145,89 +158,62 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   // 16 B), so every sector fetched is used whole, and in the shared-memory stores that follow,
   // the 8 lanes of each store phase write 8 different rows (distinct swizzled 16-byte units).
   const int rr = lane & 7, qq = lane >> 3;
-  // the row indices go first: the row loads depend on them
-  int kidx[2];
-#pragma unroll
-  for (int gsel = 0; gsel < 2; ++gsel)
-    kidx[gsel] = __ldg(p.topk + (size_t)row * kTopK + rank * kTopRows + 8 * (2 * warp + gsel) + rr);
-  // Q: warp w owns heads 8w + rr; step s takes 8-dim chunk 4 s + qq (s = 0..15)
-  uint4 qraw[16];
-  const int qh = 8 * warp + rr;
+  // top-k rows: warp w owns rows 8w + rr; step s takes code chunk j = 4 s + qq (dims 32j..32j+31).
+  // The row index goes first: the row loads depend on it.
+  const int krow = 8 * warp + rr;
+  const int kidx = __ldg(p.topk + (size_t)row * kTopK + rank * kTopRows + krow);
+  // q: warp w owns heads 8 (w >> 1) + rr; step s takes 8-dim chunk 4 (8 (w & 1) + s) + qq
+  uint4 qraw[8];
+  const int qh = 8 * (warp >> 1) + rr;
   {
     const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHAtt + qh) * kDLat);
 #pragma unroll
-    for (int s4 = 0; s4 < 16; ++s4) qraw[s4] = __ldg(src + 4 * s4 + qq);
+    for (int s4 = 0; s4 < 8; ++s4) qraw[s4] = __ldg(src + 4 * (8 * (warp & 1) + s4) + qq);
   }
-
   // SWA: this CTA's 32 window rows (w = 32 rank + r, position vis - 128 + w) are one contiguous
-  // 16 KB block; warp w takes rows 8 (w >> 1) + rr, FP8 chunks jj = 4 (4 (w & 1) + s) + qq
-  uint4 sc[4];
-  const int srow = 8 * (warp >> 1) + rr;
+  // 16 KB block; warp w takes rows 8 (w >> 2) + rr, FP8 chunks jj = 4 (2 (w & 3) + s) + qq
+  uint4 sc[2];
+  const int srow = 8 * (warp >> 2) + rr;
   const bool sval = (vis - kSwa + 32 * (int)rank + srow) >= 0;
   {
     const uint4* src = reinterpret_cast<const uint4*>(
         p.swa + ((size_t)b * (kSwa + p.nq - 1) + qi + 32 * (int)rank + srow) * kDLat);
 #pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) sc[s4] = __ldg(src + 4 * (4 * (warp & 1) + s4) + qq);
+    for (int s4 = 0; s4 < 2; ++s4) sc[s4] = __ldg(src + 4 * (2 * (warp & 3) + s4) + qq);
   }
-  // top-k rows: warp w owns row groups 2w and 2w+1 (rows 8g + rr); step s takes code chunk
-  // j = 4 (s & 3) + qq (16 B = dims 32j .. 32j+31) of group 2w + (s >> 2)
-  uint4 kc[8];
-  uint32_t ks2[8];
-  bool kval[2];
+  uint4 kc[4];
+  uint32_t ks2[4];
+  const bool kval = (kidx >= 0) && (kidx < vis) && (kidx < p.cap);
+  if (kidx >= 0 && !kval && qq == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
   {
+    const size_t e = (size_t)b * p.cap + (kval ? kidx : 0);
 #pragma unroll
-    for (int gsel = 0; gsel < 2; ++gsel) {
-      const int idx = kidx[gsel];
-      kval[gsel] = (idx >= 0) && (idx < vis) && (idx < p.cap);
-      if (idx >= 0 && !kval[gsel] && qq == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-      const size_t e = (size_t)b * p.cap + (kval[gsel] ? idx : 0);
-#pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) {
-        const int j = 4 * s4 + qq;
-        kc[4 * gsel + s4] = __ldg(reinterpret_cast<const uint4*>(p.kv_q + e * 256) + j);
-        ks2[4 * gsel + s4] = __ldg(reinterpret_cast<const uint16_t*>(p.kv_s + e * 32) + j);
-      }
+    for (int s4 = 0; s4 < 4; ++s4) {
+      const int j = 4 * s4 + qq;
+      kc[s4] = __ldg(reinterpret_cast<const uint4*>(p.kv_q + e * 256) + j);
+      ks2[s4] = __ldg(reinterpret_cast<const uint16_t*>(p.kv_s + e * 32) + j);
     }
   }
-  // ---------------------------------------------------------------- Q: bf16 -> f16 with per-head shift
+
+  // ---------------------------------------------------------------- q: per-head |q| max (partial)
   {
-    float amax = 0.f;
+    uint32_t m2 = 0u;                 // bf16x2 running max of |q|
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+      for (int j = 0; j < 4; ++j) m2 = bf16x2_max_abs(m2, w[j]);
     }
+    float amax = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-    int sh = 0;
-    if (amax > 0.f) {
-      int e;
-      frexpf(amax, &e);
-      sh = max(-126, min(127, 15 - e));     // amax * 2^sh in [2^14, 2^15)
-    }
-    const float mul = __uint_as_float((uint32_t)(127 + sh) << 23);   // exact power of two
-    if (qq == 0) s_scale[qh] = p.sm_scale * __uint_as_float((uint32_t)(127 - sh) << 23);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half lo = __float2half_rn(__uint_as_float(w[j] << 16) * mul);
-        const __half hi = __float2half_rn(__uint_as_float(w[j] & 0xFFFF0000u) * mul);
-        o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-      }
-      const int c = 4 * i + qq;                          // 8-dim chunk: block c / 8, unit c % 8
-      sts128(sQ + (uint32_t)(c >> 3) * (kHAtt * 128u) + sw128(qh, c & 7), o[0], o[1], o[2], o[3]);
-    }
+    if (qq == 0) s_qmax[warp * 8 + rr] = amax;
   }
+
   // ---------------------------------------------------------------- K tile: SWA rows (E4M3 -> f16, exact)
 #pragma unroll
-  for (int s4 = 0; s4 < 4; ++s4) {
-    const int jj = 4 * (4 * (warp & 1) + s4) + qq;       // dims 16 jj .. 16 jj + 15
+  for (int s4 = 0; s4 < 2; ++s4) {
+    const int jj = 4 * (2 * (warp & 3) + s4) + qq;       // dims 16 jj .. 16 jj + 15
     const uint32_t vw[4] = {sc[s4].x, sc[s4].y, sc[s4].z, sc[s4].w};
     uint32_t o[8];
 #pragma unroll
@@ -241,23 +227,21 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     sts128(blk + sw128(r, c0), o[0], o[1], o[2], o[3]);
     sts128(blk + sw128(r, c0 + 1), o[4], o[5], o[6], o[7]);
   }
-  if ((warp & 1) == 0 && qq == 0) s_valid[kTopRows + srow] = sval ? 1 : 0;
+  if ((warp & 3) == 0 && qq == 0) s_valid[kTopRows + srow] = sval ? 1 : 0;
 
   // ---------------------------------------------------------------- K tile: top-k rows (E2M1 x scale -> f16)
 #pragma unroll
-  for (int st = 0; st < 8; ++st) {
-    const int gsel = st >> 2;
-    const int r = 8 * (2 * warp + gsel) + rr;
-    const int j = 4 * (st & 3) + qq;
-    const uint32_t cw[4] = {kc[st].x, kc[st].y, kc[st].z, kc[st].w};
+  for (int s4 = 0; s4 < 4; ++s4) {
+    const int j = 4 * s4 + qq;
+    const uint32_t cw[4] = {kc[s4].x, kc[s4].y, kc[s4].z, kc[s4].w};
     uint32_t o[16];
 #pragma unroll
     for (int w = 0; w < 4; ++w) e2m1x8_to_f16x2x4(cw[w], o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
-      const uint32_t sb = (ks2[st] >> (8 * gi)) & 0xFFu;
+      const uint32_t sb = (ks2[s4] >> (8 * gi)) & 0xFFu;
       const float sf = (p.scale_fmt == HSA_SCALE_E8M0) ? e8m0_to_f32(sb) : e4m3_to_f32(sb);
-      const uint32_t s2 = kval[gsel] ? (uint32_t)__half_as_ushort(__float2half_rn(sf)) * 0x10001u : 0u;
+      const uint32_t s2 = kval ? (uint32_t)__half_as_ushort(__float2half_rn(sf)) * 0x10001u : 0u;
 #pragma unroll
       for (int u = 0; u < 8; ++u) o[8 * gi + u] = hmul2_u32(o[8 * gi + u], s2);
     }
@@ -265,8 +249,35 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     const uint32_t blk = sK + (uint32_t)(j >> 1) * kKbStride;
 #pragma unroll
     for (int w = 0; w < 4; ++w)
-      sts128(blk + sw128(r, 4 * (j & 1) + w), o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
-    if (qq == 0 && (st & 3) == 0) s_valid[r] = kval[gsel] ? 1 : 0;
+      sts128(blk + sw128(krow, 4 * (j & 1) + w), o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+  }
+  if (qq == 0) s_valid[krow] = kval ? 1 : 0;
+  __syncthreads();                    // s_qmax complete
+
+  // ---------------------------------------------------------------- q: bf16 -> f16 with a per-head shift
+  {
+    const float amax = fmaxf(s_qmax[(warp & ~1) * 8 + rr], s_qmax[(warp | 1) * 8 + rr]);
+    int sh = 0;
+    if (amax > 0.f) {
+      int e;
+      frexpf(amax, &e);
+      sh = max(-126, min(127, 15 - e));     // amax * 2^sh in [2^14, 2^15)
+    }
+    const float mul = __uint_as_float((uint32_t)(127 + sh) << 23);   // exact power of two
+    if ((warp & 1) == 0 && qq == 0) s_scale[qh] = p.sm_scale * __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16) * mul,
+                                            __uint_as_float(w[j] & 0xFFFF0000u) * mul);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      const int c = 4 * (8 * (warp & 1) + i) + qq;      // 8-dim chunk: block c / 8, unit c % 8
+      sts128(sQ + (uint32_t)(c >> 3) * (kHAtt * 128u) + sw128(qh, c & 7), o[0], o[1], o[2], o[3]);
+    }
   }
   fence_async_smem();
   tc_fence_before();
@@ -294,43 +305,48 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   tc_fence_after();
 
   // ---------------------------------------------------------------- logits -> staging [h][key] (Q region)
+  // Key group kg: 0..3 = pass-0 rows 32 kg + lane (TMEM lane quadrant kg), 4 = keys 128 + lane
+  // (pass-1 rows 96 + lane, quadrant 3). Warp w stages group w & 3, heads 16 (w >> 2) .. +15;
+  // the quadrant-3 warps also stage group 4.
   float* stg = reinterpret_cast<float*>(sm + kOffQ);
-  if (warp < 4 || warp == 7) {
-    // warps 0..3: keys 32w + lane from pass 0; warp 7: keys 128 + lane = pass-1 rows 96 + lane
-    const int qd = warp & 3;
-    const int key = (warp < 4) ? 32 * qd + lane : kTopRows + lane;
-    const uint32_t col = (warp < 4) ? kColS0 : kColS1;
-    const bool kv = s_valid[key] != 0;
-#pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      uint32_t r[32];
-      TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + col + 32u * hc, r);
+  {
+    auto stage = [&](int kg, int hq) {
+      const int qd = kg < 4 ? kg : 3;
+      const int key = kg < 4 ? 32 * kg + lane : kTopRows + lane;
+      const uint32_t col = (kg < 4 ? (uint32_t)kColS0 : (uint32_t)kColS1) + 16u * hq;
+      uint32_t r[16];
+      TMEM_LD16(tmem + ((uint32_t)(32 * qd) << 16) + col, r);
       tmem_wait_ld();
+      const bool kv = s_valid[key] != 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int h = 32 * hc + j;
+      for (int j = 0; j < 16; ++j) {
+        const int h = 16 * hq + j;
         stg[h * kSStride + key] = kv ? __uint_as_float(r[j]) * s_scale[h] : -INFINITY;
       }
-    }
+    };
+    stage(warp & 3, warp >> 2);
+    if ((warp & 3) == 3) stage(4, warp >> 2);
   }
   __syncthreads();
-  // per head: 4 threads, keys 4i + kq. The softmax is local to this CTA's 160 keys: its own
+  // per head: 8 threads, keys 8i + kq. The softmax is local to this CTA's 160 keys: its own
   // max m_c and sum l_c; the cluster combine below rescales the four partials.
-  const int hh = tid >> 2, kq = tid & 3;
-  float x[kRows / 4];
+  const int hh = tid >> 3, kq = tid & 7;
+  float x[kRows / 8];
   float mloc = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < kRows / 4; ++i) {
-    x[i] = stg[hh * kSStride + 4 * i + kq];
+  for (int i = 0; i < kRows / 8; ++i) {
+    x[i] = stg[hh * kSStride + 8 * i + kq];
     mloc = fmaxf(mloc, x[i]);
   }
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
+  __syncthreads();                    // P^T below overwrites the staging rows other warps read
   float lsum = 0.f;
   // P^T (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys
 #pragma unroll
-  for (int i = 0; i < kRows / 4; ++i) {
-    const int key = 4 * i + kq;
+  for (int i = 0; i < kRows / 8; ++i) {
+    const int key = 8 * i + kq;
     const float pr = (mloc == -INFINITY) ? 0.f : exp2f((x[i] - mloc) * 1.4426950408889634f);
     const __half ph = __float2half_rn(pr);
     lsum += __half2float(ph);                   // the value the tensor core will see
@@ -339,6 +355,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   }
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
   if (kq == 0) {
     s_m[hh] = mloc;
     s_l[hh] = lsum;
@@ -372,19 +389,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   float* part = p.partial + ((size_t)row * kCluster) * kPartFloats;
   {
     float* mine = part + (size_t)rank * kPartFloats;
-    const int qd = warp & 3, half = warp >> 2;
+    const int qd = warp & 3;
 #pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      const int mt = 2 * half + u;
+    for (int k = 0; k < 2; ++k) {
+      const int job = (warp >> 2) + 4 * k;           // (M-tile, 32-head half)
+      const int mt = job >> 1, hc = job & 1;
       const int d = 128 * mt + 32 * qd + lane;
+      uint32_t r[32];
+      TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mt + 32 * hc), r);
+      tmem_wait_ld();
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        uint32_t r[32];
-        TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mt + 32 * hc), r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) __stcg(mine + (size_t)(32 * hc + j) * kDLat + d, __uint_as_float(r[j]));
-      }
+      for (int j = 0; j < 32; ++j) __stcg(mine + (size_t)(32 * hc + j) * kDLat + d, __uint_as_float(r[j]));
     }
     if (tid < kHAtt) {
       __stcg(mine + kHAtt * kDLat + 2 * tid, s_m[tid]);
@@ -424,32 +439,29 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   // ---------------------------------------------------------------- out[h] = sum_c w_c[h] O_c[h], c in rank order
   {
     float* out = p.out + ((size_t)row * kHAtt + 16 * rank) * kDLat;
-    constexpr int kPer = 16 * (kDLat / 4) / kAttnThreads;   // 8 float4 per thread
+    constexpr int kPer = 16 * (kDLat / 4) / kAttnThreads;   // 4 float4 per thread
+    float4 v[kCluster][kPer];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float4 v[kCluster][kPer / 2];
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + kAttnThreads * u;                 // float4 index within the 16-head slice
 #pragma unroll
-      for (int u = 0; u < kPer / 2; ++u) {
-        const int i = tid + kAttnThreads * (half * (kPer / 2) + u);   // float4 index within the 16-head slice
+      for (int c = 0; c < kCluster; ++c)
+        v[c][u] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)c * kPartFloats + (size_t)16 * rank * kDLat) + i);
+    }
 #pragma unroll
-        for (int c = 0; c < kCluster; ++c)
-          v[c][u] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)c * kPartFloats + (size_t)16 * rank * kDLat) + i);
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + kAttnThreads * u;
+      const int hl = i / (kDLat / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < kCluster; ++c) {
+        const float w = s_w[c * 16 + hl];
+        acc.x = fmaf(w, v[c][u].x, acc.x);
+        acc.y = fmaf(w, v[c][u].y, acc.y);
+        acc.z = fmaf(w, v[c][u].z, acc.z);
+        acc.w = fmaf(w, v[c][u].w, acc.w);
       }
-#pragma unroll
-      for (int u = 0; u < kPer / 2; ++u) {
-        const int i = tid + kAttnThreads * (half * (kPer / 2) + u);
-        const int hl = i / (kDLat / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < kCluster; ++c) {
-          const float w = s_w[c * 16 + hl];
-          acc.x = fmaf(w, v[c][u].x, acc.x);
-          acc.y = fmaf(w, v[c][u].y, acc.y);
-          acc.z = fmaf(w, v[c][u].z, acc.z);
-          acc.w = fmaf(w, v[c][u].w, acc.w);
-        }
-        reinterpret_cast<float4*>(out)[i] = acc;
-      }
+      reinterpret_cast<float4*>(out)[i] = acc;
     }
   }
 }
