@@ -130,7 +130,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   float* s_w = misc + 192;            // [4][16] combine weights of this CTA's heads
   int* s_valid = reinterpret_cast<int*>(misc + 256);      // [160]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 416);
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(misc + 418);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(misc + 418);   // [0] QK, [1..4] PV M-tiles
   float* s_qmax = misc + 64;          // [16 warps][8 heads] partial |q| maxima (before s_m / s_l are used)
   const uint32_t bar = smem_u32(s_bar);
 
@@ -146,7 +146,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    mbar_init(bar, 1);
+#pragma unroll
+    for (int i = 0; i < 5; ++i) mbar_init(bar + 8 * i, 1);
     fence_mbar_init();
   }
   griddep_wait();
@@ -366,40 +367,46 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   tc_fence_after();
 
   // ---------------------------------------------------------------- O^T = V^T . P^T
+  // One M-tile (128 dims) at a time, each with its own completion barrier, so the warps drain
+  // finished tiles while the tensor core works on the next ones.
   if (tid == 0) {
     const uint32_t id = idesc_f16(128, 64, true, false);
     const uint64_t a0 = sdesc(sK, kKbStride, 1024u), b0 = sdesc(sP, 16u, 1024u);
 #pragma unroll
-    for (int ks = 0; ks < kRows / 16; ++ks) {
-      const uint32_t bo = ((uint32_t)(ks >> 2) * (kHAtt * 128u) + (uint32_t)(ks & 3) * 32u) >> 4;
+    for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int ks = 0; ks < kRows / 16; ++ks) {
+        const uint32_t bo = ((uint32_t)(ks >> 2) * (kHAtt * 128u) + (uint32_t)(ks & 3) * 32u) >> 4;
         const uint32_t ao = ((uint32_t)(2 * mt) * kKbStride + (uint32_t)(16 * ks) * 128u) >> 4;
         umma_f16(tmem + kColO + 64 * mt, a0 + ao, b0 + bo, id, ks > 0);
       }
+      umma_commit(bar + 8u * (1 + mt));
     }
-    umma_commit(bar);
   }
-  if (!mbar_wait(bar, 1) && tid == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
-  tc_fence_after();
 
   // ---------------------------------------------------------------- unnormalised partial O -> L2
-  // partial[row][rank]: 64 x 512 fp32 outputs [h][d], then (m_c, l_c) for the 64 heads. The
-  // cluster peers read it right after the barrier below, so it is served from L2.
+  // Warp (quadrant qd = w & 3, tile mt = w >> 2) owns output dimension d = 128 mt + 32 qd + lane
+  // for all 64 heads: it sends the 48 heads other CTAs combine to the workspace (L2) and keeps
+  // this CTA's own 16 heads in registers. partial[row][c] = 64 x 512 fp32 [h][d], then (m_c, l_c).
+  const int qd = warp & 3, mtile = warp >> 2;
+  const int dim = 128 * mtile + 32 * qd + lane;
   float* part = p.partial + ((size_t)row * kCluster) * kPartFloats;
+  float own[16];
   {
+    if (!mbar_wait(bar + 8u * (1 + mtile), 0) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    tc_fence_after();
     float* mine = part + (size_t)rank * kPartFloats;
-    const int qd = warp & 3;
-#pragma unroll 1
-    for (int k = 0; k < 2; ++k) {
-      const int job = (warp >> 2) + 4 * k;           // (M-tile, 32-head half)
-      const int mt = job >> 1, hc = job & 1;
-      const int d = 128 * mt + 32 * qd + lane;
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
       uint32_t r[32];
-      TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mt + 32 * hc), r);
+      TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mtile + 32 * hc), r);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) __stcg(mine + (size_t)(32 * hc + j) * kDLat + d, __uint_as_float(r[j]));
+      for (int j = 0; j < 32; ++j) {
+        const int h = 32 * hc + j;
+        if ((h >> 4) == (int)rank) own[h & 15] = __uint_as_float(r[j]);
+        else __stcg(mine + (size_t)h * kDLat + dim, __uint_as_float(r[j]));
+      }
     }
     if (tid < kHAtt) {
       __stcg(mine + kHAtt * kDLat + 2 * tid, s_m[tid]);
@@ -434,35 +441,30 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 #pragma unroll
     for (int c = 0; c < kCluster; ++c) s_w[c * 16 + tid] = e[c] * inv;
   }
-  __syncthreads();
 
-  // ---------------------------------------------------------------- out[h] = sum_c w_c[h] O_c[h], c in rank order
+  // ---------------------------------------------------------------- out[h][dim] = sum_c w_c[h] O_c[h][dim], c in rank order
   {
-    float* out = p.out + ((size_t)row * kHAtt + 16 * rank) * kDLat;
-    constexpr int kPer = 16 * (kDLat / 4) / kAttnThreads;   // 4 float4 per thread
-    float4 v[kCluster][kPer];
+    float acc[16];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = tid + kAttnThreads * u;                 // float4 index within the 16-head slice
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    float v[16];
+    __syncthreads();                                      // s_w
 #pragma unroll
-      for (int c = 0; c < kCluster; ++c)
-        v[c][u] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)c * kPartFloats + (size_t)16 * rank * kDLat) + i);
-    }
+    for (uint32_t c = 0; c < kCluster; ++c) {
+      if (c == rank) {
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = tid + kAttnThreads * u;
-      const int hl = i / (kDLat / 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 16; ++j) v[j] = own[j];
+      } else {
+        const float* src = part + (size_t)c * kPartFloats + (size_t)(16 * rank) * kDLat + dim;
 #pragma unroll
-      for (int c = 0; c < kCluster; ++c) {
-        const float w = s_w[c * 16 + hl];
-        acc.x = fmaf(w, v[c][u].x, acc.x);
-        acc.y = fmaf(w, v[c][u].y, acc.y);
-        acc.z = fmaf(w, v[c][u].z, acc.z);
-        acc.w = fmaf(w, v[c][u].w, acc.w);
+        for (int j = 0; j < 16; ++j) v[j] = __ldcg(src + (size_t)j * kDLat);
       }
-      reinterpret_cast<float4*>(out)[i] = acc;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = fmaf(s_w[c * 16 + j], v[j], acc[j]);
     }
+    float* out = p.out + ((size_t)row * kHAtt + 16 * rank) * kDLat + dim;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[(size_t)j * kDLat] = acc[j];
   }
 }
 
