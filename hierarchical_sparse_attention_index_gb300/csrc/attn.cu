@@ -4,21 +4,24 @@
 //
 // One thread-block cluster of 4 CTAs per (request, query). CTA j owns 160 keys: top-k slots
 // [128j, 128j+128) and SWA window rows [32j, 32j+32). Four CTAs per row fit a batch of 32
-// requests in one wave of 128 SMs. Each CTA:
-//  1. issues every global load at once: its 160 rows (gathered once and shared by all 64
-//     heads) and the 64x512 bf16 query. It dequantises the rows to f16 (E2M1 x scale, or E4M3
-//     for SWA) into a 128B-swizzled K-major shared tile. The query is converted to f16 after a
-//     per-head power-of-two shift (exact within f16), in the same layout;
-//  2. tcgen05: S^T = K . Q^T in two M=128 passes (rows 0..127, then rows 32..159, of which only
-//     keys 128..159 are used), accumulated in TMEM;
-//  3. runs a softmax local to its 160 keys (own max m_c and sum l_c per head) and writes
-//     P^T (f16) as the next B operand; no cluster exchange is needed before PV;
-//  4. tcgen05: O^T[512 dims][64 heads] = V^T . P^T, reading the same tile as an MN-major
-//     A operand (K = V = the 512-d latent), 4 M-tiles of 128 dims x 10 k-steps;
-//  5. writes its unnormalised partial O_c and (m_c, l_c) to the workspace (L2) straight from
-//     TMEM. After one cluster barrier each CTA forms its 16 heads as
-//     sum_c exp(m_c - M) O_c / sum_c exp(m_c - M) l_c over c in rank order (deterministic).
-//     L2 moves these 128 KB per CTA several times faster than distributed shared memory.
+// requests in one wave of 128 SMs. Each CTA runs 16 worker warps and one MMA warp:
+//  1. the workers issue every global load at once (the 160 rows, gathered once and shared by
+//     all 64 heads, and the 64x512 bf16 query) and dequantise: the query to f16 after a
+//     per-head power-of-two shift (exact within f16), the rows to f16 (E2M1 x scale, or E4M3
+//     for SWA), into 128B-swizzled K-major shared tiles. Rows are converted 128 dims at a time;
+//  2. the MMA warp runs S^T = K . Q^T on tcgen05 (TMEM accumulators) in two M=128 passes
+//     (rows 0..127, then rows 32..159, of which only keys 128..159 are used), each 128-dim step
+//     as soon as all workers have converted it;
+//  3. the workers run a softmax local to the 160 keys (own max m_c and sum l_c per head) and
+//     write P^T (f16) as the next B operand; no cluster exchange is needed before PV;
+//  4. the MMA warp runs O^T[512 dims][64 heads] = V^T . P^T, reading the same tile as an
+//     MN-major A operand (K = V = the 512-d latent), one 128-dim M-tile at a time;
+//  5. each worker drains one output dimension of a finished M-tile: the 48 heads the other
+//     CTAs combine go to the workspace (L2), this CTA's own 16 stay in registers. (m_c, l_c)
+//     are published before PV (cluster barrier phase A) and the partials after (phase B);
+//     each CTA then forms its 16 heads as sum_c exp(m_c - M) O_c / sum_c exp(m_c - M) l_c over
+//     c in rank order (deterministic). L2 moves these partials several times faster than
+//     distributed shared memory.
 // Setup (TMEM allocation, barrier init) runs before the programmatic-dependency wait, so it
 // overlaps the tail of the previous kernel in the stream. Every wait is bounded.
 #include "hsa_common.cuh"
@@ -27,7 +30,9 @@
 namespace hsa {
 namespace {
 
-constexpr int kAttnThreads = 512;
+constexpr int kWorkWarps = 16;                           // load, convert, softmax, drain, combine
+constexpr int kWorkThreads = kWorkWarps * 32;
+constexpr int kAttnThreads = kWorkThreads + 32;          // + one warp that issues the tcgen05 MMAs
 constexpr int kCluster = kAttnSplit;
 constexpr int kRows = 160;                               // keys per CTA
 constexpr int kTopRows = 128;
@@ -87,8 +92,11 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
       : "r"(taddr))
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -97,9 +105,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 // byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-swizzled block
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
@@ -125,19 +130,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const uint32_t sK = base + kOffK, sQ = base + kOffQ, sP = base + kOffQ;
   float* misc = reinterpret_cast<float*>(sm + kOffMisc);
   float* s_scale = misc;              // [64] logit scale per head
-  float* s_m = misc + 64;             // [64] local max
-  float* s_l = misc + 128;            // [64] local sum
+  float* s_qmax = misc + 64;          // [16 warps][8 heads] partial |q| maxima
   float* s_w = misc + 192;            // [4][16] combine weights of this CTA's heads
   int* s_valid = reinterpret_cast<int*>(misc + 256);      // [160]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 416);
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(misc + 418);   // [0] QK, [1..4] PV M-tiles
-  float* s_qmax = misc + 64;          // [16 warps][8 heads] partial |q| maxima (before s_m / s_l are used)
-  const uint32_t bar = smem_u32(s_bar);
+  // mbarriers: [0] QK done, [1..4] PV tile done, [5..8] K-tile step s converted (all 16 warps)
+  const uint32_t bar = smem_u32(misc + 418);
+  const uint32_t kb_bar = bar + 8u * 5;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
   const int row = blockIdx.x / kCluster;              // (b, q) flattened
   const int b = row / p.nq, qi = row % p.nq;
+  float* part = p.partial + ((size_t)row * kCluster) * kPartFloats;
 
   // ---------------------------------------------------------------- setup (overlaps the previous kernel)
   if (warp == 0) {
@@ -147,17 +152,78 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   }
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 5; ++i) mbar_init(bar + 8 * i, 1);
+    for (int i = 0; i < 5; ++i) mbar_init(bar + 8u * i, 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mbar_init(kb_bar + 8u * i, kWorkWarps);
     fence_mbar_init();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
   griddep_wait();
   griddep_launch_dependents();
+
+  if (warp == kWorkWarps) {
+    // ---------------------------------------------------------------- MMA warp
+    if (lane == 0) {
+      // S^T = K . Q^T in two M=128 passes (rows 0..127 -> columns 0..63, rows 32..159 -> 64..127),
+      // 64-dim block by block as the worker warps finish converting them. Descriptors are formed
+      // once; a k-step only moves the start-address field (address >> 4), which cannot carry out
+      // of its 14 bits because every operand lies below 256 KB.
+      const uint32_t id = idesc_f16(128, 64, false, false);
+      const uint64_t a0 = sdesc(sK, 16u, 1024u), a1 = sdesc(sK + 32u * 128u, 16u, 1024u);
+      const uint64_t b0 = sdesc(sQ, 16u, 1024u);
+      bool ok = true;
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        ok = mbar_wait(kb_bar + 8u * st, 0) && ok;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int k = 8 * st + kk;
+          const uint32_t ko = ((uint32_t)(k >> 2) * kKbStride + (uint32_t)(k & 3) * 32u) >> 4;
+          const uint32_t qo = ((uint32_t)(k >> 2) * (kHAtt * 128u) + (uint32_t)(k & 3) * 32u) >> 4;
+          umma_f16(tmem + kColS0, a0 + ko, b0 + qo, id, k > 0);
+          umma_f16(tmem + kColS1, a1 + ko, b0 + qo, id, k > 0);
+        }
+      }
+      umma_commit(bar);
+      if (!ok) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    }
+    __syncwarp();
+    named_bar_sync(2, kAttnThreads);  // P^T written by the worker warps
+    if (lane == 0) {
+      tc_fence_after();
+      // O^T = V^T . P^T one M-tile (128 dims) at a time, each with its own completion barrier,
+      // so the workers drain finished tiles while the tensor core works on the next ones
+      const uint32_t id = idesc_f16(128, 64, true, false);
+      const uint64_t a0 = sdesc(sK, kKbStride, 1024u), b0 = sdesc(sP, 16u, 1024u);
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int ks = 0; ks < kRows / 16; ++ks) {
+          const uint32_t bo = ((uint32_t)(ks >> 2) * (kHAtt * 128u) + (uint32_t)(ks & 3) * 32u) >> 4;
+          const uint32_t ao = ((uint32_t)(2 * mt) * kKbStride + (uint32_t)(16 * ks) * 128u) >> 4;
+          umma_f16(tmem + kColO + 64 * mt, a0 + ao, b0 + bo, id, ks > 0);
+        }
+        umma_commit(bar + 8u * (1 + mt));
+      }
+    }
+    __syncwarp();
+    cluster_arrive();                 // phase A: (m, l) published
+    cluster_wait();
+    cluster_arrive();                 // phase B: partials published
+    cluster_wait();
+    return;
+  }
+
+  // ---------------------------------------------------------------- worker warps (0..15)
   const int vis = __ldg(p.vis + row);
 
-  // ---------------------------------------------------------------- issue every global load up front
-  // Lane = 8 q + rr. One warp-wide load covers 8 rows (rr) x 64 contiguous bytes (4 lanes q x
-  // 16 B), so every sector fetched is used whole, and in the shared-memory stores that follow,
-  // the 8 lanes of each store phase write 8 different rows (distinct swizzled 16-byte units).
+  // issue every global load up front. Lane = 8 q + rr. One warp-wide load covers 8 rows (rr) x
+  // 64 contiguous bytes (4 lanes q x 16 B), so every sector fetched is used whole, and in the
+  // shared-memory stores that follow, the 8 lanes of each store phase write 8 different rows.
   const int rr = lane & 7, qq = lane >> 3;
   // top-k rows: warp w owns rows 8w + rr; step s takes code chunk j = 4 s + qq (dims 32j..32j+31).
   // The row index goes first: the row loads depend on it.
@@ -229,31 +295,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     sts128(blk + sw128(r, c0 + 1), o[4], o[5], o[6], o[7]);
   }
   if ((warp & 3) == 0 && qq == 0) s_valid[kTopRows + srow] = sval ? 1 : 0;
-
-  // ---------------------------------------------------------------- K tile: top-k rows (E2M1 x scale -> f16)
-#pragma unroll
-  for (int s4 = 0; s4 < 4; ++s4) {
-    const int j = 4 * s4 + qq;
-    const uint32_t cw[4] = {kc[s4].x, kc[s4].y, kc[s4].z, kc[s4].w};
-    uint32_t o[16];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) e2m1x8_to_f16x2x4(cw[w], o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      const uint32_t sb = (ks2[s4] >> (8 * gi)) & 0xFFu;
-      const float sf = (p.scale_fmt == HSA_SCALE_E8M0) ? e8m0_to_f32(sb) : e4m3_to_f32(sb);
-      const uint32_t s2 = kval ? (uint32_t)__half_as_ushort(__float2half_rn(sf)) * 0x10001u : 0u;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) o[8 * gi + u] = hmul2_u32(o[8 * gi + u], s2);
-    }
-    // dims 32j + 8w -> block kb = j / 2, 16-byte chunk 4 (j & 1) + w
-    const uint32_t blk = sK + (uint32_t)(j >> 1) * kKbStride;
-#pragma unroll
-    for (int w = 0; w < 4; ++w)
-      sts128(blk + sw128(krow, 4 * (j & 1) + w), o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
-  }
-  if (qq == 0) s_valid[krow] = kval ? 1 : 0;
-  __syncthreads();                    // s_qmax complete
+  named_bar_sync(1, kWorkThreads);    // s_qmax complete
 
   // ---------------------------------------------------------------- q: bf16 -> f16 with a per-head shift
   {
@@ -280,30 +322,39 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       sts128(sQ + (uint32_t)(c >> 3) * (kHAtt * 128u) + sw128(qh, c & 7), o[0], o[1], o[2], o[3]);
     }
   }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
 
-  // ---------------------------------------------------------------- S^T = K . Q^T (two M=128 passes)
-  if (tid == 0) {
-    // Descriptors are formed once; a k-step only moves the start-address field (address >> 4),
-    // which cannot carry out of its 14 bits because every operand lies below 256 KB.
-    const uint32_t id = idesc_f16(128, 64, false, false);
-    const uint64_t a0 = sdesc(sK, 16u, 1024u), a1 = sdesc(sK + 32u * 128u, 16u, 1024u);
-    const uint64_t b0 = sdesc(sQ, 16u, 1024u);
+  // ---------------------------------------------------------------- K tile: top-k rows (E2M1 x scale -> f16)
+  // Step s converts dims 128 s .. 128 s + 127 (blocks 2s, 2s+1) of this warp's 8 rows; after it
+  // the warp arrives on step s's barrier, and the MMA warp runs that step's QK k-steps.
 #pragma unroll
-    for (int k = 0; k < kDLat / 16; ++k) {
-      const uint32_t ko = ((uint32_t)(k >> 2) * kKbStride + (uint32_t)(k & 3) * 32u) >> 4;
-      const uint32_t qo = ((uint32_t)(k >> 2) * (kHAtt * 128u) + (uint32_t)(k & 3) * 32u) >> 4;
-      umma_f16(tmem + kColS0, a0 + ko, b0 + qo, id, k > 0);
-      umma_f16(tmem + kColS1, a1 + ko, b0 + qo, id, k > 0);
+  for (int s4 = 0; s4 < 4; ++s4) {
+    const int j = 4 * s4 + qq;
+    const uint32_t cw[4] = {kc[s4].x, kc[s4].y, kc[s4].z, kc[s4].w};
+    uint32_t o[16];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) e2m1x8_to_f16x2x4(cw[w], o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const uint32_t sb = (ks2[s4] >> (8 * gi)) & 0xFFu;
+      const float sf = (p.scale_fmt == HSA_SCALE_E8M0) ? e8m0_to_f32(sb) : e4m3_to_f32(sb);
+      const uint32_t s2 = kval ? (uint32_t)__half_as_ushort(__float2half_rn(sf)) * 0x10001u : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o[8 * gi + u] = hmul2_u32(o[8 * gi + u], s2);
     }
-    umma_commit(bar);
+    // dims 32j + 8w -> block kb = j / 2, 16-byte chunk 4 (j & 1) + w
+    const uint32_t blk = sK + (uint32_t)(j >> 1) * kKbStride;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      sts128(blk + sw128(krow, 4 * (j & 1) + w), o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(kb_bar + 8u * s4);
   }
+  if (qq == 0) s_valid[krow] = kval ? 1 : 0;
+
   if (!mbar_wait(bar, 0) && tid == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
   tc_fence_after();
+  named_bar_sync(1, kWorkThreads);    // s_valid, s_scale visible
 
   // ---------------------------------------------------------------- logits -> staging [h][key] (Q region)
   // Key group kg: 0..3 = pass-0 rows 32 kg + lane (TMEM lane quadrant kg), 4 = keys 128 + lane
@@ -328,61 +379,65 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     stage(warp & 3, warp >> 2);
     if ((warp & 3) == 3) stage(4, warp >> 2);
   }
-  __syncthreads();
-  // per head: 8 threads, keys 8i + kq. The softmax is local to this CTA's 160 keys: its own
-  // max m_c and sum l_c; the cluster combine below rescales the four partials.
+  named_bar_sync(1, kWorkThreads);
+  // per head: 8 threads; thread kq takes the 8-key runs kq, kq + 8 and (kq < 4) kq + 16. The
+  // softmax is local to this CTA's 160 keys: its own max m_c and sum l_c; the cluster combine
+  // below rescales the four partials.
   const int hh = tid >> 3, kq = tid & 7;
-  float x[kRows / 8];
+  float x[3][8];
   float mloc = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < kRows / 8; ++i) {
-    x[i] = stg[hh * kSStride + 8 * i + kq];
-    mloc = fmaxf(mloc, x[i]);
+  for (int u = 0; u < 3; ++u) {
+    const int ch = kq + 8 * u;
+    if (ch < kRows / 8) {
+      const float4 a = *reinterpret_cast<const float4*>(stg + hh * kSStride + 8 * ch);
+      const float4 c = *reinterpret_cast<const float4*>(stg + hh * kSStride + 8 * ch + 4);
+      x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
+      x[u][4] = c.x; x[u][5] = c.y; x[u][6] = c.z; x[u][7] = c.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mloc = fmaxf(mloc, x[u][e]);
   }
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-  __syncthreads();                    // P^T below overwrites the staging rows other warps read
+  named_bar_sync(1, kWorkThreads);    // P^T below overwrites the staging rows other warps read
   float lsum = 0.f;
-  // P^T (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys
+  // P^T (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys; one 8-key
+  // run is one 16-byte unit
 #pragma unroll
-  for (int i = 0; i < kRows / 8; ++i) {
-    const int key = 8 * i + kq;
-    const float pr = (mloc == -INFINITY) ? 0.f : exp2f((x[i] - mloc) * 1.4426950408889634f);
-    const __half ph = __float2half_rn(pr);
-    lsum += __half2float(ph);                   // the value the tensor core will see
-    sts16(sP + (uint32_t)(key >> 6) * (kHAtt * 128u) + sw128(hh, (key & 63) >> 3) + (uint32_t)(key & 7) * 2u,
-          __half_as_ushort(ph));
+  for (int u = 0; u < 3; ++u) {
+    const int ch = kq + 8 * u;
+    if (ch < kRows / 8) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = (mloc == -INFINITY) ? 0.f : exp2f((x[u][2 * e] - mloc) * 1.4426950408889634f);
+        const float p1 = (mloc == -INFINITY) ? 0.f : exp2f((x[u][2 * e + 1] - mloc) * 1.4426950408889634f);
+        const __half2 h = __floats2half2_rn(p0, p1);
+        const float2 back = __half22float2(h);       // the values the tensor core will see
+        lsum += back.x + back.y;
+        pk[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      const int key = 8 * ch;
+      sts128(sP + (uint32_t)(key >> 6) * (kHAtt * 128u) + sw128(hh, (key & 63) >> 3), pk[0], pk[1], pk[2], pk[3]);
+    }
   }
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
-  if (kq == 0) {
-    s_m[hh] = mloc;
-    s_l[hh] = lsum;
-  }
   fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  // ---------------------------------------------------------------- O^T = V^T . P^T
-  // One M-tile (128 dims) at a time, each with its own completion barrier, so the warps drain
-  // finished tiles while the tensor core works on the next ones.
-  if (tid == 0) {
-    const uint32_t id = idesc_f16(128, 64, true, false);
-    const uint64_t a0 = sdesc(sK, kKbStride, 1024u), b0 = sdesc(sP, 16u, 1024u);
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-      for (int ks = 0; ks < kRows / 16; ++ks) {
-        const uint32_t bo = ((uint32_t)(ks >> 2) * (kHAtt * 128u) + (uint32_t)(ks & 3) * 32u) >> 4;
-        const uint32_t ao = ((uint32_t)(2 * mt) * kKbStride + (uint32_t)(16 * ks) * 128u) >> 4;
-        umma_f16(tmem + kColO + 64 * mt, a0 + ao, b0 + bo, id, ks > 0);
-      }
-      umma_commit(bar + 8u * (1 + mt));
-    }
+  named_bar_arrive(2, kAttnThreads);  // P^T ready for the MMA warp
+  // (m_c, l_c) of the 64 heads go to the workspace now; the peers read them after phase A
+  float* mine = part + (size_t)rank * kPartFloats;
+  if (kq == 0) {
+    __stcg(mine + kHAtt * kDLat + 2 * hh, mloc);
+    __stcg(mine + kHAtt * kDLat + 2 * hh + 1, lsum);
   }
+  cluster_arrive();                   // phase A
 
   // ---------------------------------------------------------------- unnormalised partial O -> L2
   // Warp (quadrant qd = w & 3, tile mt = w >> 2) owns output dimension d = 128 mt + 32 qd + lane
@@ -390,12 +445,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   // this CTA's own 16 heads in registers. partial[row][c] = 64 x 512 fp32 [h][d], then (m_c, l_c).
   const int qd = warp & 3, mtile = warp >> 2;
   const int dim = 128 * mtile + 32 * qd + lane;
-  float* part = p.partial + ((size_t)row * kCluster) * kPartFloats;
   float own[16];
   {
     if (!mbar_wait(bar + 8u * (1 + mtile), 0) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
     tc_fence_after();
-    float* mine = part + (size_t)rank * kPartFloats;
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
       uint32_t r[32];
@@ -408,16 +461,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
         else __stcg(mine + (size_t)h * kDLat + dim, __uint_as_float(r[j]));
       }
     }
-    if (tid < kHAtt) {
-      __stcg(mine + kHAtt * kDLat + 2 * tid, s_m[tid]);
-      __stcg(mine + kHAtt * kDLat + 2 * tid + 1, s_l[tid]);
-    }
   }
   tc_fence_before();
-  cluster_sync();               // release/acquire at cluster scope: every partial of this row is visible
-  tc_fence_after();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
-
+  cluster_wait();                     // phase A: every CTA's (m, l) is visible
   // combine weights of this CTA's heads: w_c = exp(m_c - M) / sum_c' exp(m_c' - M) l_c'
   if (tid < 16) {
     const int h = 16 * (int)rank + tid;
@@ -441,6 +487,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 #pragma unroll
     for (int c = 0; c < kCluster; ++c) s_w[c * 16 + tid] = e[c] * inv;
   }
+  cluster_arrive();                   // phase B: this CTA's partial is published
+  cluster_wait();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 
   // ---------------------------------------------------------------- out[h][dim] = sum_c w_c[h] O_c[h][dim], c in rank order
   {
@@ -448,7 +498,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
     float v[16];
-    __syncthreads();                                      // s_w
 #pragma unroll
     for (uint32_t c = 0; c < kCluster; ++c) {
       if (c == rank) {
