@@ -250,10 +250,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   }
   uint4 kc[4];
   uint32_t ks2[4];
-  const bool kval = (kidx >= 0) && (kidx < vis) && (kidx < p.cap);
-  if (kidx >= 0 && !kval && qq == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
   {
-    const size_t e = (size_t)b * p.cap + (kval ? kidx : 0);
+    // the gather address depends on the index alone (clamped into the cache); whether the row
+    // counts (index in [0, vis)) is applied when it is converted
+    const size_t e = (size_t)b * p.cap + (size_t)min(max(kidx, 0), (int)imin64(p.cap, 0x7fffffff) - 1);
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) {
       const int j = 4 * s4 + qq;
@@ -261,6 +261,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       ks2[s4] = __ldg(reinterpret_cast<const uint16_t*>(p.kv_s + e * 32) + j);
     }
   }
+
+  const bool kval = (kidx >= 0) && (kidx < vis) && (kidx < p.cap);
+  if (kidx >= 0 && !kval && qq == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
 
   // ---------------------------------------------------------------- q: per-head |q| max (partial)
   {
