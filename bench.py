@@ -218,7 +218,7 @@ def per_kernel_times(H, torch, I, reps=10):
 # time of the capture: once the source changes, the figure no longer applies and is reported
 # as null.
 NCU_TRAFFIC = {
-    "sparse_attn_decode": ("attn.cu", "ca10f05583471101c92f1457ed0adaf18ac5ef4aa0abb80bd729cb394dc78a37", 10612736,
+    "sparse_attn_decode": ("attn.cu", "291044a3ab222a32bad92ce072ef29837370ca7bad555d98653430ee1321138b", 10602496,
                            "profiles/sparse_attn_b32_t128k.md"),
 }
 
