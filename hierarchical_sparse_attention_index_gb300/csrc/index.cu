@@ -45,7 +45,7 @@ constexpr int kWarpCodes = 32 * 64, kWarpScales = 32 * 4, kWarpSlots = 32 * 4;
 
 struct ScanSmemLayout {
   int nst, nlr;
-  size_t codes, scales, slotpos, bfrag, wsc, hist, bars, misc, total;
+  size_t codes, scales, slotpos, bfrag, wsc, hist, sfl, bars, misc, total;
 };
 
 __host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq) {
@@ -66,6 +66,7 @@ __host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq
   L.bfrag = o;   o += (size_t)nql * 2 * 8 * 32 * 2 * 4;
   L.wsc = o;     o += (size_t)nql * 16 * 4;
   L.hist = o;    o += (size_t)L.nlr * (kHistBins / 2) * 4;
+  L.sfl = o;     o += (size_t)kConsumerWarps * 32 * 16;   // per warp: its 32 rows' 4 group scales as floats
   L.bars = o;    o += 2 * kMaxStages * 8;
   L.misc = o;    o += 256;
   L.total = o;
@@ -487,7 +488,17 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     if (warp * 32 < nrows) {
       const bool two = warp * 32 + 16 < nrows;        // the warp's second 16-row tile holds data
       const uint32_t a_base = codes + (uint32_t)(row_off + g) * 64u + 16u * t;
-      const uint32_t s_base = scales + (uint32_t)(row_off + g) * 4u;
+      // the warp's 32 rows' E8M0 group scales as floats, once per stage: 2^(b-127) is byte b
+      // moved to the exponent field (b = 0 only occurs with all-zero codes, where 0 * 0 = 0)
+      const uint32_t sf_base = smem_u32(smem + L.sfl) + (uint32_t)warp * 512u;
+      {
+        const uint32_t S = lds32(scales + (uint32_t)(row_off + lane) * 4u);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sf_base + (uint32_t)lane * 16u),
+                     "r"((S << 23) & 0x7F800000u), "r"((S << 15) & 0x7F800000u), "r"((S << 7) & 0x7F800000u),
+                     "r"((S >> 1) & 0x7F800000u)
+                     : "memory");
+        __syncwarp();
+      }
       // this lane's row after the reduce-scatter below: rows 8t .. 8t+7 of the warp's 32 are
       // the 8-entry block t, one row per lane g
       const int r_mine = warp * 32 + 8 * t + g;
@@ -500,7 +511,12 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
           if (mt == 1 && !two) break;
           const uint4 A0 = lds128(a_base + (uint32_t)mt * 1024u);
           const uint4 A1 = lds128(a_base + (uint32_t)mt * 1024u + 512u);
-          const uint32_t S0 = lds32(s_base + (uint32_t)mt * 64u), S1 = lds32(s_base + (uint32_t)mt * 64u + 32u);
+          const uint4 SF0 = lds128(sf_base + (uint32_t)(16 * mt + g) * 16u);
+          const uint4 SF1 = lds128(sf_base + (uint32_t)(16 * mt + g + 8) * 16u);
+          const float sf0[4] = {__uint_as_float(SF0.x), __uint_as_float(SF0.y), __uint_as_float(SF0.z),
+                                __uint_as_float(SF0.w)};
+          const float sf1[4] = {__uint_as_float(SF1.x), __uint_as_float(SF1.y), __uint_as_float(SF1.z),
+                                __uint_as_float(SF1.w)};
           const uint32_t aw0[4] = {A0.x, A0.y, A0.z, A0.w}, aw1[4] = {A1.x, A1.y, A1.z, A1.w};
           float tot[2][4];
 #pragma unroll
@@ -509,11 +525,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
             uint32_t f0, f1, f2, f3, h0, h1, h2, h3;
             e2m1x8_to_f16x2x4(aw0[gi], f0, f1, f2, f3);
             e2m1x8_to_f16x2x4(aw1[gi], h0, h1, h2, h3);
-            // E8M0 scale as a float, 2^(b-127): byte gi moved to the exponent field. b = 0 only
-            // occurs with all-zero codes (amax = 0), where 0 * 0 = 0 either way
-            const int sh = 23 - 8 * gi;
-            const float sc0 = __uint_as_float((sh >= 0 ? (S0 << sh) : (S0 >> -sh)) & 0x7F800000u);
-            const float sc1 = __uint_as_float((sh >= 0 ? (S1 << sh) : (S1 >> -sh)) & 0x7F800000u);
+            const float sc0 = sf0[gi], sc1 = sf1[gi];
             float tmp[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
