@@ -314,6 +314,7 @@ def run_hsa(args):
     if not args.no_e2e:
         e2e = run_e2e(H, torch, I, args, world, barrier, st)
     line = make_line(args, world, value, tmax, clocks, e2e, roofline)
+    line["cache_write_m2"] = cache_write_m2(H, torch, hbm_peak, peak_src)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args, sample_requests=2, steps=20)
     if rank == 0:
@@ -321,6 +322,44 @@ def run_hsa(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def cache_write_m2(H, torch, hbm_peak, peak_src, reps=5):
+    """The encoder's m = 2 cache write (three KV-source layers x 65,536 tokens of bf16 wkv and
+    wgate, N(0,1) and N(0,2)): device time per layer with CUDA events, and its HBM roofline
+    (algorithmic bytes = the two bf16 projections read + 356 B written per entry)."""
+    n, layers = synth.CFG3_TOKENS, synth.CFG3_LAYERS
+    dev = []
+    for layer in layers:
+        wkv = torch.from_numpy(synth.latents_bf16(synth.CFG3_SEED, layer, 0, n).view(np.int16)).cuda()
+        wg = torch.from_numpy(synth.gates_bf16(synth.CFG3_SEED, layer, 0, n).view(np.int16)).cuda()
+        W = torch.from_numpy(synth.w_idx_bf16(synth.CFG3_SEED, layer).view(np.int16)).cuda()
+        dev.append((wkv.view(torch.bfloat16)[None], wg.view(torch.bfloat16)[None], W.view(torch.bfloat16),
+                    H.Cache(1, n // 2, 2)))
+    st = torch.cuda.current_stream()
+
+    def once():
+        for wkv, wg, W, cache in dev:
+            H.hsa_cache_write_compress(cache, wkv, wg, W, n, None)
+
+    once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        once()
+    e1.record(st)
+    torch.cuda.synchronize()
+    code, flags = H.hsa_get_device_status()
+    if code != 0 or flags != 0:
+        raise RuntimeError(f"device status after the cache write: code {code} flags {flags}")
+    t_layer = 1e-3 * e0.elapsed_time(e1) / (reps * len(layers))
+    bytes_layer = n * 2 * 512 * 2 + (n // 2) * 356
+    ach = bytes_layer / t_layer / 1e9
+    return {"workload": f"m2 write, {len(layers)} layers x {n} tokens", "us_per_layer": round(1e6 * t_layer, 2),
+            "tokens_per_s": round(n / t_layer, 1), "bytes_per_layer": bytes_layer,
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(ach / hbm_peak, 4), "peak_source": peak_src}}
 
 
 def run_e2e(H, torch, I, args, world, barrier, st):

@@ -1,0 +1,83 @@
+// Device helpers shared by the score kernels: a block exclusive scan and the histogram
+// threshold search behind the exact top-k selection.
+#pragma once
+
+#include "hsa_common.cuh"
+#include "hsa_internal.h"
+
+namespace hsa {
+
+// Exclusive prefix sum over the first `nthreads` threads (a multiple of 32); scratch holds 32 ints.
+// The caller's threads must all call it (named barrier `bar_id` over `nthreads`).
+__device__ __forceinline__ int excl_scan(int v, int* scratch, int bar_id, int nthreads, int* total, int tid = -1) {
+  if (tid < 0) tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  named_bar_sync(bar_id, nthreads);
+  const int nw = nthreads >> 5;
+  if (warp == 0) {
+    int t = (lane < nw) ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < nw) scratch[lane] = t;   // inclusive warp totals
+  }
+  named_bar_sync(bar_id, nthreads);
+  const int before = (warp > 0) ? scratch[warp - 1] : 0;
+  *total = scratch[nw - 1];
+  named_bar_sync(bar_id, nthreads);
+  return before + x - v;
+}
+
+// Threshold bin for a top-K over a 4096-bin histogram (the bin holding the K-th largest key) and
+// the counts above it, written to *st with ready = 1; NT threads, named barrier 1, thread
+// indices 0..NT-1 taken from `tid`.
+template <int NT>
+__device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, int* scratch, int tid = -1) {
+  if (tid < 0) tid = threadIdx.x;
+  constexpr int kPerT = kHistBins / NT;   // bins per thread
+  uint32_t cnt[kPerT];
+  int local = 0;
+  const int top = kHistBins - kPerT * (tid + 1);   // this thread owns bins [top, top+kPerT), high first
+#pragma unroll
+  for (int i = 0; i < kPerT; ++i) {
+    cnt[i] = __ldcg(ghist + top + kPerT - 1 - i);
+    local += (int)cnt[i];
+  }
+  int total;
+  const int excl = excl_scan(local, scratch, 1, NT, &total, tid);
+  if (total <= K) {
+    if (tid == 0) {
+      st->thr_bin = -1;
+      st->above = total;
+      st->nvalid = total;
+      __threadfence();
+      st->ready = 1;
+    }
+  } else if (excl < K && excl + local >= K) {
+    int run = excl;
+#pragma unroll
+    for (int i = 0; i < kPerT; ++i) {
+      if (run + (int)cnt[i] >= K) {
+        st->thr_bin = top + kPerT - 1 - i;
+        st->above = run;
+        st->nvalid = total;
+        __threadfence();
+        st->ready = 1;
+        break;
+      }
+      run += (int)cnt[i];
+    }
+  }
+  named_bar_sync(1, NT);
+}
+
+}  // namespace hsa

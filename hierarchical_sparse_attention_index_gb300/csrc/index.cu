@@ -25,6 +25,7 @@
 #include <algorithm>
 
 #include "hsa_common.cuh"
+#include "hsa_hist.cuh"
 #include "hsa_internal.h"
 
 namespace hsa {
@@ -91,75 +92,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Exclusive prefix sum over the first `nthreads` threads (a multiple of 32); scratch holds 32 ints.
-// The caller's threads must all call it (named barrier `bar_id` over `nthreads`).
-__device__ __forceinline__ int excl_scan(int v, int* scratch, int bar_id, int nthreads, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  named_bar_sync(bar_id, nthreads);
-  const int nw = nthreads >> 5;
-  if (warp == 0) {
-    int t = (lane < nw) ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    if (lane < nw) scratch[lane] = t;   // inclusive warp totals
-  }
-  named_bar_sync(bar_id, nthreads);
-  const int before = (warp > 0) ? scratch[warp - 1] : 0;
-  *total = scratch[nw - 1];
-  named_bar_sync(bar_id, nthreads);
-  return before + x - v;
-}
-
-// Threshold bin for a top-K over a 4096-bin histogram; 256 consumer threads (named barrier 1).
-__device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, int* scratch) {
-  const int tid = threadIdx.x;
-  constexpr int kPerT = kHistBins / kConsumers;   // bins per thread
-  uint32_t cnt[kPerT];
-  int local = 0;
-  const int top = kHistBins - kPerT * (tid + 1);   // this thread owns bins [top, top+kPerT), high first
-#pragma unroll
-  for (int i = 0; i < kPerT; ++i) {
-    cnt[i] = __ldcg(ghist + top + kPerT - 1 - i);
-    local += (int)cnt[i];
-  }
-  int total;
-  const int excl = excl_scan(local, scratch, 1, kConsumers, &total);
-  if (total <= K) {
-    if (tid == 0) {
-      st->thr_bin = -1;
-      st->above = total;
-      st->nvalid = total;
-      __threadfence();
-      st->ready = 1;
-    }
-  } else if (excl < K && excl + local >= K) {
-    int run = excl;
-#pragma unroll
-    for (int i = 0; i < kPerT; ++i) {
-      if (run + (int)cnt[i] >= K) {
-        st->thr_bin = top + kPerT - 1 - i;
-        st->above = run;
-        st->nvalid = total;
-        __threadfence();
-        st->ready = 1;
-        break;
-      }
-      run += (int)cnt[i];
-    }
-  }
-  named_bar_sync(1, kConsumers);
 }
 
 // kPoolMode: Reindex (segment = one (request, query) row, entries gathered through the pool);
@@ -287,12 +219,12 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     if (misc[1]) {
       __threadfence();
       if (kPoolMode) {
-        compute_threshold(p.hist + (size_t)seg * kHistBins, kTopK, p.state + seg, scratch);
+        compute_threshold<kConsumers>(p.hist + (size_t)seg * kHistBins, kTopK, p.state + seg, scratch);
       } else {
         for (int q = 0; q < p.nq; ++q) {
           const int row = seg * p.nq + q;
-          compute_threshold(p.hist + (size_t)(2 * row) * kHistBins, kTopK, p.state + 2 * row, scratch);
-          compute_threshold(p.hist + (size_t)(2 * row + 1) * kHistBins, kCandBlocks, p.state + 2 * row + 1,
+          compute_threshold<kConsumers>(p.hist + (size_t)(2 * row) * kHistBins, kTopK, p.state + 2 * row, scratch);
+          compute_threshold<kConsumers>(p.hist + (size_t)(2 * row + 1) * kHistBins, kCandBlocks, p.state + 2 * row + 1,
                             scratch);
         }
       }
