@@ -5,10 +5,12 @@
 // One thread-block cluster of 4 CTAs per (request, query). CTA j owns 160 keys: top-k slots
 // [128j, 128j+128) and SWA window rows [32j, 32j+32). Four CTAs per row fit a batch of 32
 // requests in one wave of 128 SMs. Each CTA runs 16 worker warps and one MMA warp:
-//  1. the workers issue every global load at once (the 160 rows, gathered once and shared by
-//     all 64 heads, and the 64x512 bf16 query) and dequantise: the query to f16 after a
-//     per-head power-of-two shift (exact within f16), the rows to f16 (E2M1 x scale, or E4M3
-//     for SWA), into 128B-swizzled K-major shared tiles. Rows are converted 128 dims at a time;
+//  1. the 64x512 bf16 query arrives by TMA: each CTA of the cluster loads 16 heads and
+//     multicasts them to all four, already in the 128B-swizzled K-major layout. The workers
+//     issue the row loads (the 160 rows, gathered once and shared by all 64 heads), convert
+//     the query in place to f16 after a per-head power-of-two shift (exact within f16; each
+//     warp owns 4 whole heads, so no block barrier), and dequantise the rows to f16
+//     (E2M1 x scale, or E4M3 for SWA) into a 128B-swizzled K-major tile, 128 dims at a time;
 //  2. the MMA warp runs S^T = K . Q^T on tcgen05 (TMEM accumulators) in two M=128 passes
 //     (rows 0..127, then rows 32..159, of which only keys 128..159 are used), each 128-dim step
 //     as soon as all workers have converted it;
@@ -22,8 +24,9 @@
 //     each CTA then forms its 16 heads as sum_c exp(m_c - M) O_c / sum_c exp(m_c - M) l_c over
 //     c in rank order (deterministic). L2 moves these partials several times faster than
 //     distributed shared memory.
-// Setup (TMEM allocation, barrier init) runs before the programmatic-dependency wait, so it
-// overlaps the tail of the previous kernel in the stream. Every wait is bounded.
+// Setup (TMEM allocation, barrier init, one cluster barrier so that peers may signal this
+// CTA's query barrier) runs before the programmatic-dependency wait, so it overlaps the tail
+// of the previous kernel in the stream. Every wait is bounded.
 #include "hsa_common.cuh"
 #include "hsa_internal.h"
 
@@ -116,13 +119,28 @@ __device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t m, uint32_t x) {
                                    __habs2(*reinterpret_cast<const __nv_bfloat162*>(&x)));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
+// 2-D tiled TMA load multicast to the CTAs in `mask`: the box lands at the same shared-memory
+// offset in each, and each destination's mbarrier at `bar` receives the byte count
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t s2) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&s2));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads, 1)
-    sparse_attn_kernel(const AttnParams p) {
+    sparse_attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;      // 1024-byte alignment for the swizzled tiles
@@ -130,13 +148,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const uint32_t sK = base + kOffK, sQ = base + kOffQ, sP = base + kOffQ;
   float* misc = reinterpret_cast<float*>(sm + kOffMisc);
   float* s_scale = misc;              // [64] logit scale per head
-  float* s_qmax = misc + 64;          // [16 warps][8 heads] partial |q| maxima
   float* s_w = misc + 192;            // [4][16] combine weights of this CTA's heads
   int* s_valid = reinterpret_cast<int*>(misc + 256);      // [160]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 416);
-  // mbarriers: [0] QK done, [1..4] PV tile done, [5..8] K-tile step s converted (all 16 warps)
+  // mbarriers: [0] QK done, [1..4] PV tile done, [5..8] K-tile step s converted (all 16 warps),
+  // [9] query landed (64 KB from the four CTAs' multicasts)
   const uint32_t bar = smem_u32(misc + 418);
   const uint32_t kb_bar = bar + 8u * 5;
+  const uint32_t q_bar = bar + 8u * 9;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -155,11 +174,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     for (int i = 0; i < 5; ++i) mbar_init(bar + 8u * i, 1);
 #pragma unroll
     for (int i = 0; i < 4; ++i) mbar_init(kb_bar + 8u * i, kWorkWarps);
+    mbar_init(q_bar, 1);
     fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive();                   // every CTA's query barrier is initialised before any multicast
+  cluster_wait();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
   griddep_wait();
   griddep_launch_dependents();
@@ -167,6 +189,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   if (warp == kWorkWarps) {
     // ---------------------------------------------------------------- MMA warp
     if (lane == 0) {
+      // query: this CTA's 16 heads, 8 boxes of 64 dims x 16 heads (2 KB each), to all 4 CTAs
+      mbar_arrive_expect_tx(q_bar, kQBytes);
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb)
+        tma_load_2d_mc(sQ + (uint32_t)kb * (kHAtt * 128u) + rank * (16u * 128u), &p.qmap, 64 * kb,
+                       row * kHAtt + 16 * (int)rank, q_bar, (uint16_t)((1u << kCluster) - 1u));
       // S^T = K . Q^T in two M=128 passes (rows 0..127 -> columns 0..63, rows 32..159 -> 64..127),
       // 64-dim block by block as the worker warps finish converting them. Descriptors are formed
       // once; a k-step only moves the start-address field (address >> 4), which cannot carry out
@@ -229,14 +257,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   // The row index goes first: the row loads depend on it.
   const int krow = 8 * warp + rr;
   const int kidx = __ldg(p.topk + (size_t)row * kTopK + rank * kTopRows + krow);
-  // q: warp w owns heads 8 (w >> 1) + rr; step s takes 8-dim chunk 4 (8 (w & 1) + s) + qq
-  uint4 qraw[8];
-  const int qh = 8 * (warp >> 1) + rr;
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHAtt + qh) * kDLat);
-#pragma unroll
-    for (int s4 = 0; s4 < 8; ++s4) qraw[s4] = __ldg(src + 4 * (8 * (warp & 1) + s4) + qq);
-  }
   // SWA: this CTA's 32 window rows (w = 32 rank + r, position vis - 128 + w) are one contiguous
   // 16 KB block; warp w takes rows 8 (w >> 2) + rr, FP8 chunks jj = 4 (2 (w & 3) + s) + qq
   uint4 sc[2];
@@ -265,19 +285,49 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const bool kval = (kidx >= 0) && (kidx < vis) && (kidx < p.cap);
   if (kidx >= 0 && !kval && qq == 0) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
 
-  // ---------------------------------------------------------------- q: per-head |q| max (partial)
+  // ---------------------------------------------------------------- q: bf16 -> f16 in place, per-head shift
+  // Warp w owns heads 4w .. 4w+3 whole: lane = 8 hq + c reads 16-byte chunk c of each of the 8
+  // 64-dim blocks of head 4w + hq (one phase of 8 lanes reads one 128-byte row: no conflicts),
+  // takes the head's |q| max over its 8 lanes and writes the f16 values back to the same place.
   {
+    const int qh = 4 * warp + (lane >> 3), c = lane & 7;
+    const uint32_t a0 = sQ + sw128((uint32_t)qh, (uint32_t)c);
+    if (!mbar_wait(q_bar, 0) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    uint4 qv[8];
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) qv[kb] = lds128(a0 + (uint32_t)kb * (kHAtt * 128u));
     uint32_t m2 = 0u;                 // bf16x2 running max of |q|
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) m2 = bf16x2_max_abs(m2, w[j]);
+    for (int kb = 0; kb < 8; ++kb) {
+      m2 = bf16x2_max_abs(m2, qv[kb].x);
+      m2 = bf16x2_max_abs(m2, qv[kb].y);
+      m2 = bf16x2_max_abs(m2, qv[kb].z);
+      m2 = bf16x2_max_abs(m2, qv[kb].w);
     }
     float amax = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-    if (qq == 0) s_qmax[warp * 8 + rr] = amax;
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    int sh = 0;
+    if (amax > 0.f) {
+      int e;
+      frexpf(amax, &e);
+      sh = max(-126, min(127, 15 - e));     // amax * 2^sh in [2^14, 2^15)
+    }
+    const float mul = __uint_as_float((uint32_t)(127 + sh) << 23);   // exact power of two
+    if (c == 0) s_scale[qh] = p.sm_scale * __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      const uint32_t w[4] = {qv[kb].x, qv[kb].y, qv[kb].z, qv[kb].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16) * mul,
+                                            __uint_as_float(w[j] & 0xFFFF0000u) * mul);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      sts128(a0 + (uint32_t)kb * (kHAtt * 128u), o[0], o[1], o[2], o[3]);
+    }
   }
 
   // ---------------------------------------------------------------- K tile: SWA rows (E4M3 -> f16, exact)
@@ -298,33 +348,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     sts128(blk + sw128(r, c0 + 1), o[4], o[5], o[6], o[7]);
   }
   if ((warp & 3) == 0 && qq == 0) s_valid[kTopRows + srow] = sval ? 1 : 0;
-  named_bar_sync(1, kWorkThreads);    // s_qmax complete
-
-  // ---------------------------------------------------------------- q: bf16 -> f16 with a per-head shift
-  {
-    const float amax = fmaxf(s_qmax[(warp & ~1) * 8 + rr], s_qmax[(warp | 1) * 8 + rr]);
-    int sh = 0;
-    if (amax > 0.f) {
-      int e;
-      frexpf(amax, &e);
-      sh = max(-126, min(127, 15 - e));     // amax * 2^sh in [2^14, 2^15)
-    }
-    const float mul = __uint_as_float((uint32_t)(127 + sh) << 23);   // exact power of two
-    if ((warp & 1) == 0 && qq == 0) s_scale[qh] = p.sm_scale * __uint_as_float((uint32_t)(127 - sh) << 23);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16) * mul,
-                                            __uint_as_float(w[j] & 0xFFFF0000u) * mul);
-        o[j] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      const int c = 4 * (8 * (warp & 1) + i) + qq;      // 8-dim chunk: block c / 8, unit c % 8
-      sts128(sQ + (uint32_t)(c >> 3) * (kHAtt * 128u) + sw128(qh, c & 7), o[0], o[1], o[2], o[3]);
-    }
-  }
 
   // ---------------------------------------------------------------- K tile: top-k rows (E2M1 x scale -> f16)
   // Step s converts dims 128 s .. 128 s + 127 (blocks 2s, 2s+1) of this warp's 8 rows; after it
@@ -522,6 +545,26 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 
 }  // namespace
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// the driver's tensor-map encoder, looked up once through the runtime (no libcuda link)
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+}  // namespace
+
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -531,7 +574,19 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s) {
     attr_set = true;
   }
   const int rows = p.batch * p.nq;
-  return launch_pdl(sparse_attn_kernel, dim3(rows * kCluster), dim3(kAttnThreads), kSmemBytes, s, p);
+  const EncodeTiledFn encode = encode_tiled();
+  if (!encode) return cudaErrorNotSupported;
+  AttnParams a = p;
+  // q viewed as [rows * 64 heads][512 dims] bf16: a box is 64 dims (128 B, the swizzle span) x 16 heads
+  const cuuint64_t dims[2] = {(cuuint64_t)kDLat, (cuuint64_t)rows * kHAtt};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDLat * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&a.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return launch_pdl(sparse_attn_kernel, dim3(rows * kCluster), dim3(kAttnThreads), kSmemBytes, s, a);
 }
 
 }  // namespace hsa

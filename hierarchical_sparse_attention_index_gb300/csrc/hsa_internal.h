@@ -2,6 +2,7 @@
 // parameter blocks and launchers. Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -91,6 +92,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention
 struct AttnParams {
+  CUtensorMap qmap;       // q as a 2-D bf16 tensor [B*nq*64][512], 64 x 16 boxes, 128-byte swizzle
   int32_t batch, nq;
   int64_t cap;
   int32_t scale_fmt;
