@@ -18,12 +18,14 @@
 //     write P^T (f16) as the next B operand; no cluster exchange is needed before PV;
 //  4. the MMA warp runs O^T[512 dims][64 heads] = V^T . P^T, reading the same tile as an
 //     MN-major A operand (K = V = the 512-d latent), one 128-dim M-tile at a time;
-//  5. each worker drains one output dimension of a finished M-tile: the 48 heads the other
-//     CTAs combine go to the workspace (L2), this CTA's own 16 stay in registers. (m_c, l_c)
-//     are published before PV (cluster barrier phase A) and the partials after (phase B);
-//     each CTA then forms its 16 heads as sum_c exp(m_c - M) O_c / sum_c exp(m_c - M) l_c over
-//     c in rank order (deterministic). L2 moves these partials several times faster than
-//     distributed shared memory.
+//  5. each worker drains one output dimension of a finished M-tile, normalised by l_c: the 48
+//     heads the other CTAs combine go to the workspace (L2) as f16 pairs, this CTA's own 16
+//     stay in registers in fp32. (m_c, l_c) of the 16 heads a peer owns go straight into the
+//     peer's shared memory before PV (cluster barrier phase A), the partials after (phase B);
+//     each CTA then forms its 16 heads as sum_c w_c (O_c / l_c), w_c = exp(m_c - M) l_c /
+//     sum_c' exp(m_c' - M) l_c', over c in rank order (deterministic). L2 moves the partials
+//     several times faster than distributed shared memory; the normalised partial is a convex
+//     combination of f16 tile values, so it cannot leave the f16 range.
 // Setup (TMEM allocation, barrier init, one cluster barrier so that peers may signal this
 // CTA's query barrier) runs before the programmatic-dependency wait, so it overlaps the tail
 // of the previous kernel in the stream. Every wait is bounded.
@@ -101,6 +103,14 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// store a float pair to the same shared-memory variable in CTA `peer` of the cluster
+__device__ __forceinline__ void st_cluster_f2(uint32_t local_addr, uint32_t peer, float a, float b) {
+  asm volatile(
+      "{ .reg .b32 ra; mapa.shared::cluster.u32 ra, %0, %1; st.shared::cluster.v2.f32 [ra], {%2, %3}; }" ::"r"(
+          local_addr),
+      "r"(peer), "f"(a), "f"(b)
+      : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -147,7 +157,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   uint8_t* sm = smem_raw + (base - raw_base);
   const uint32_t sK = base + kOffK, sQ = base + kOffQ, sP = base + kOffQ;
   float* misc = reinterpret_cast<float*>(sm + kOffMisc);
-  float* s_scale = misc;              // [64] logit scale per head
+  float* s_scale = misc;              // [64] logit scale per head (read while staging the logits)
+  float* s_invl = misc;               // [64] then 1 / l of this CTA's keys per head (read by the drain)
+  float2* s_ml = reinterpret_cast<float2*>(misc + 64);   // [4 CTAs][16 own heads] (m_c, l_c), written by peers
   float* s_w = misc + 192;            // [4][16] combine weights of this CTA's heads
   int* s_valid = reinterpret_cast<int*>(misc + 256);      // [160]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 416);
@@ -161,7 +173,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const uint32_t rank = cluster_rank();
   const int row = blockIdx.x / kCluster;              // (b, q) flattened
   const int b = row / p.nq, qi = row % p.nq;
-  float* part = p.partial + ((size_t)row * kCluster) * kPartFloats;
+  // workspace partial of CTA c: [32 head pairs][512 dims] f16x2 (the pairs it does not own)
+  uint32_t* part = reinterpret_cast<uint32_t*>(p.partial + ((size_t)row * kCluster) * kPartFloats);
 
   // ---------------------------------------------------------------- setup (overlaps the previous kernel)
   if (warp == 0) {
@@ -455,20 +468,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+  if (kq == 0) s_invl[hh] = (lsum > 0.f) ? 1.f / lsum : 0.f;
   fence_async_smem();
-  named_bar_arrive(2, kAttnThreads);  // P^T ready for the MMA warp
-  // (m_c, l_c) of the 64 heads go to the workspace now; the peers read them after phase A
-  float* mine = part + (size_t)rank * kPartFloats;
-  if (kq == 0) {
-    __stcg(mine + kHAtt * kDLat + 2 * hh, mloc);
-    __stcg(mine + kHAtt * kDLat + 2 * hh + 1, lsum);
-  }
+  named_bar_sync(2, kAttnThreads);    // P^T ready for the MMA warp; s_invl visible to every worker
+  // (m_c, l_c) of head hh go to the CTA that owns it (slot [rank][hh % 16]); read after phase A
+  if (kq == 0) st_cluster_f2(smem_u32(s_ml + rank * 16 + (hh & 15)), (uint32_t)(hh >> 4), mloc, lsum);
+  uint32_t* mine = part + (size_t)rank * kPartFloats;
   cluster_arrive();                   // phase A
 
-  // ---------------------------------------------------------------- unnormalised partial O -> L2
+  // ---------------------------------------------------------------- partial O / l -> L2
   // Warp (quadrant qd = w & 3, tile mt = w >> 2) owns output dimension d = 128 mt + 32 qd + lane
-  // for all 64 heads: it sends the 48 heads other CTAs combine to the workspace (L2) and keeps
-  // this CTA's own 16 heads in registers. partial[row][c] = 64 x 512 fp32 [h][d], then (m_c, l_c).
+  // for all 64 heads: it sends the 48 heads other CTAs combine to the workspace (L2) as f16
+  // pairs [h / 2][d] and keeps this CTA's own 16 heads in registers (fp32).
   const int qd = warp & 3, mtile = warp >> 2;
   const int dim = 128 * mtile + 32 * qd + lane;
   float own[16];
@@ -481,22 +492,27 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mtile + 32 * hc), r);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 32; j += 2) {
         const int h = 32 * hc + j;
-        if ((h >> 4) == (int)rank) own[h & 15] = __uint_as_float(r[j]);
-        else __stcg(mine + (size_t)h * kDLat + dim, __uint_as_float(r[j]));
+        const float o0 = __uint_as_float(r[j]) * s_invl[h], o1 = __uint_as_float(r[j + 1]) * s_invl[h + 1];
+        if ((h >> 4) == (int)rank) {
+          own[h & 15] = o0;
+          own[(h & 15) + 1] = o1;
+        } else {
+          const __half2 v = __floats2half2_rn(o0, o1);
+          __stcg(mine + (size_t)(h >> 1) * kDLat + dim, *reinterpret_cast<const uint32_t*>(&v));
+        }
       }
     }
   }
   tc_fence_before();
   cluster_wait();                     // phase A: every CTA's (m, l) is visible
-  // combine weights of this CTA's heads: w_c = exp(m_c - M) / sum_c' exp(m_c' - M) l_c'
+  // combine weights of this CTA's heads: w_c = exp(m_c - M) l_c / sum_c' exp(m_c' - M) l_c'
   if (tid < 16) {
-    const int h = 16 * (int)rank + tid;
     float mc[kCluster], lc[kCluster];
 #pragma unroll
     for (int c = 0; c < kCluster; ++c) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(part + (size_t)c * kPartFloats + kHAtt * kDLat) + h);
+      const float2 ml = s_ml[c * 16 + tid];
       mc[c] = ml.x;
       lc[c] = ml.y;
     }
@@ -511,7 +527,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     }
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
-    for (int c = 0; c < kCluster; ++c) s_w[c * 16 + tid] = e[c] * inv;
+    for (int c = 0; c < kCluster; ++c) s_w[c * 16 + tid] = e[c] * lc[c] * inv;
   }
   cluster_arrive();                   // phase B: this CTA's partial is published
   cluster_wait();
@@ -530,9 +546,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = own[j];
       } else {
-        const float* src = part + (size_t)c * kPartFloats + (size_t)(16 * rank) * kDLat + dim;
+        const uint32_t* src = part + (size_t)c * kPartFloats + (size_t)(8 * rank) * kDLat + dim;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __ldcg(src + (size_t)j * kDLat);
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t u = __ldcg(src + (size_t)j * kDLat);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
+          v[2 * j] = f.x;
+          v[2 * j + 1] = f.y;
+        }
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = fmaf(s_w[c * 16 + j], v[j], acc[j]);
