@@ -48,11 +48,13 @@ constexpr uint32_t kOffK = 0, kOffQ = kTileBytes, kOffMisc = kOffQ + kQBytes;
 constexpr uint32_t kMiscBytes = 1792;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;   // + alignment slack
 constexpr size_t kPartFloats = (size_t)kHAtt * kDLat + 2 * kHAtt;   // one CTA's partial in the workspace
-constexpr int kSStride = 168;                            // fp32 staging row stride (conflict-free)
+constexpr int kSStride = kRows;                          // fp32 logit staging [64 heads][160 keys]
+constexpr uint32_t kOffPinQ = 40960;                     // P^T after the staging rows, inside the Q region
 constexpr int kTmemCols = 512;
 constexpr int kColS0 = 0, kColS1 = 64, kColO = 256;
 static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kHAtt * kSStride * 4 <= (int)kQBytes, "logit staging");
+static_assert(kHAtt * kSStride * 4 <= (int)kOffPinQ && kOffPinQ % 1024 == 0, "logit staging");
+static_assert(kOffPinQ + 3 * kHAtt * 128 <= kQBytes, "P^T (160 keys in three 64-key blocks)");
 
 // ------------------------------------------------------------------ tcgen05 helpers
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -155,7 +157,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;      // 1024-byte alignment for the swizzled tiles
   uint8_t* sm = smem_raw + (base - raw_base);
-  const uint32_t sK = base + kOffK, sQ = base + kOffQ, sP = base + kOffQ;
+  const uint32_t sK = base + kOffK, sQ = base + kOffQ, sP = base + kOffQ + kOffPinQ;
   float* misc = reinterpret_cast<float*>(sm + kOffMisc);
   float* s_scale = misc;              // [64] logit scale per head (read while staging the logits)
   float* s_invl = misc;               // [64] then 1 / l of this CTA's keys per head (read by the drain)
@@ -443,10 +445,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-  named_bar_sync(1, kWorkThreads);    // P^T below overwrites the staging rows other warps read
   float lsum = 0.f;
   // P^T (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys; one 8-key
   // run is one 16-byte unit
+  // p = 2^(x log2 e - m log2 e); a head with no valid key has m = -inf and every x = -inf, so
+  // its offset is 0 and every p is 0
+  const float kLog2e = 1.4426950408889634f;
+  const float ml2 = (mloc == -INFINITY) ? 0.f : mloc * kLog2e;
 #pragma unroll
   for (int u = 0; u < 3; ++u) {
     const int ch = kq + 8 * u;
@@ -454,11 +459,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       uint32_t pk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = (mloc == -INFINITY) ? 0.f : exp2f((x[u][2 * e] - mloc) * 1.4426950408889634f);
-        const float p1 = (mloc == -INFINITY) ? 0.f : exp2f((x[u][2 * e + 1] - mloc) * 1.4426950408889634f);
+        const float p0 = exp2f(fmaf(x[u][2 * e], kLog2e, -ml2));
+        const float p1 = exp2f(fmaf(x[u][2 * e + 1], kLog2e, -ml2));
+        lsum += p0 + p1;
         const __half2 h = __floats2half2_rn(p0, p1);
-        const float2 back = __half22float2(h);       // the values the tensor core will see
-        lsum += back.x + back.y;
         pk[e] = *reinterpret_cast<const uint32_t*>(&h);
       }
       const int key = 8 * ch;
