@@ -3,27 +3,46 @@
 // [890B] §三: main KV E2M1 + scale per 16, indexer K E2M1 + E8M0 per 32; [CED] CSA2: indexer K
 // is projected from the main-KV entry).
 //
-// A persistent CTA handles 16 entries per iteration:
-//  1. pooling: one warp per entry; per channel a softmax over the m gate values and the
-//     weighted sum of the m wkv values (fp32). Then RMSNorm (eps 1e-6, unit gain), kept in
-//     shared memory;
-//  2. main-KV quantisation: per 16-channel group, scale = the smallest E8M0 (or E4M3) value
-//     s with 6 s >= amax (an exact integer/bit computation); codes are RNE E2M1 of x / s,
-//     from the hardware cvt. -0 is cleared to +0;
-//  3. indexer K = latent . W_idx (W_idx bf16 kept in shared memory, fp32 FMA), then group-32
-//     E8M0 quantisation, written in the fragment byte order of include/hsa.h.
+// A persistent CTA of 16 warps writes tiles of 32 entries:
+//  1. pooling, one warp per entry (2 per warp), lane l owning channels 16l .. 16l+15: per
+//     channel a softmax over the two gate values and the weighted sum of the two wkv values in
+//     fp32 (with e = exp(-|g0 - g1|), the larger gate weighs 1 / (1 + e) and the other
+//     e / (1 + e): one exponential and one reciprocal, within a few 1e-7 of the exact
+//     weights), then RMSNorm (eps 1e-6, unit gain) as one correctly rounded 1 / rms. The
+//     lane's 16 channels are one main-KV group, so its scale (the smallest E8M0 or E4M3 value s
+//     with 6 s >= amax, an exact bit computation) and its codes (RNE E2M1 of x / s from the
+//     hardware cvt, -0 cleared to +0) come straight from registers. The raw inputs of the warp's next entries are loaded while it works;
+//  2. the normalised latent is split into three bf16 terms, hi + mid + lo = x exactly (each
+//     term the bf16 rounding of what the previous ones left), stacked as the 96 rows (term t,
+//     entry r -> row 32 t + r) of one 128B-swizzled K-major tile;
+//  3. indexer K^T = W_idx^T . [hi | mid | lo]^T on tcgen05 (kind::f16, bf16 x bf16, fp32
+//     accumulate in tensor memory: 128 lanes = K dims, 96 columns), one M=128 N=96 MMA per
+//     16-dim k-step, so W_idx is read once per tile. W_idx stays in shared memory for the whole
+//     launch as the MN-major A operand; every product is exact and the only roundings are the
+//     fp32 accumulations and the final hi + mid + lo sum of the three columns of an entry;
+//  4. each warp reads one 32-dim group (its tensor-memory lane quadrant) of 8 entries: the
+//     group max is one warp reduction, the E8M0 scale and E2M1 codes follow as in step 1, and
+//     the bytes are written in the fragment order of include/hsa.h.
 #include "hsa_common.cuh"
 #include "hsa_internal.h"
+#include "hsa_tc.cuh"
 
 namespace hsa {
 namespace {
 
-constexpr int kWThreads = 256;
-constexpr int kEnt = 16;
-constexpr size_t kOffLat = 0;                                  // [16][512] f32
-constexpr size_t kOffW = kOffLat + kEnt * kDLat * 4;          // [512][128] bf16
-constexpr size_t kOffK = kOffW + (size_t)kDLat * kDIdx * 2;    // [16][128] f32
-constexpr size_t kWSmem = kOffK + kEnt * kDIdx * 4;
+constexpr int kWWarps = 16;
+constexpr int kWThreads = kWWarps * 32;
+constexpr int kTileE = 32;                                 // entries per tile (the MMA's N)
+constexpr int kEntPerWarp = kTileE / kWWarps;
+constexpr uint32_t kWBytes = (uint32_t)kDLat * kDIdx * 2;  // W_idx, bf16, MN-major A operand
+constexpr int kBRows = 3 * kTileE;                         // hi, mid, lo terms of the tile's entries
+constexpr uint32_t kBBlock = (uint32_t)kBRows * 128u;      // one 64-dim block of the B tile
+constexpr uint32_t kOffW = 0, kOffB = kWBytes, kOffMisc = kOffB + 8 * kBBlock;
+constexpr uint32_t kMiscBytes = 64;
+constexpr uint32_t kWSmem = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 128;                        // 96 used
+static_assert(kWSmem <= 232448, "shared memory");
+static_assert(kEntPerWarp * kWWarps == kTileE, "entries per warp");
 
 // smallest e with 6 * 2^e >= amax (amax > 0), clamped to [-127, 127]; returns the E8M0 byte
 __device__ __forceinline__ uint32_t e8m0_byte_for(float amax) {
@@ -62,230 +81,316 @@ __device__ __forceinline__ uint32_t e4m3_byte_for(float amax) {
   return byte;
 }
 
-// 16 floats (8 pairs) -> 8 bytes of E2M1 pairs (element 2j low nibble), no -0
-__device__ __forceinline__ uint2 pack16(const float* v, float inv_or_s, bool divide) {
-  uint32_t b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float lo = divide ? __fdiv_rn(v[2 * j], inv_or_s) : v[2 * j] * inv_or_s;
-    const float hi = divide ? __fdiv_rn(v[2 * j + 1], inv_or_s) : v[2 * j + 1] * inv_or_s;
-    uint32_t x = f32x2_to_e2m1x2(hi, lo) & 0xFFu;
-    if ((x & 0x07u) == 0u) x &= 0xF0u;
-    if ((x & 0x70u) == 0u) x &= 0x0Fu;
-    b[j] = x;
-  }
-  uint2 r;
-  r.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  r.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+// one E2M1 pair byte (lo -> low nibble), -0 cleared to +0
+__device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
+  uint32_t x = f32x2_to_e2m1x2(hi, lo) & 0xFFu;
+  if ((x & 0x07u) == 0u) x &= 0xF0u;
+  if ((x & 0x70u) == 0u) x &= 0x0Fu;
+  return x;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// bf16x2 of (a, b), round to nearest even; a in the low half
+__device__ __forceinline__ uint32_t bf16x2_rn(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
   return r;
 }
 
-__device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+// (request b, index i) of an entry; entries are numbered request-major
+struct Loc {
+  int64_t b, i;
+};
+__device__ __forceinline__ Loc locate(int64_t ge, int64_t n) { return Loc{ge / n, ge % n}; }
+// the entry `off` (< 32) places after `base`: one step per request boundary crossed, no division
+__device__ __forceinline__ Loc step(Loc base, int off, int64_t n) {
+  Loc l{base.b, base.i + off};
+  while (l.i >= n) {
+    l.i -= n;
+    ++l.b;
+  }
+  return l;
+}
 
+// raw inputs of one entry for one lane: per token, its 16 channels of wkv (and of wgate)
+template <int kRatio>
+struct EntryRaw {
+  uint4 kv[kRatio][2];
+  uint4 g[kRatio == 2 ? 2 : 1][2];
+};
+
+template <int kRatio>
+__device__ __forceinline__ void load_entry(const WriteParams& p, bool valid, Loc l, int lane, EntryRaw<kRatio>& r) {
+  if (valid) {
+    const int64_t tok0 = l.b * p.n_tokens + l.i * kRatio;
+#pragma unroll
+    for (int tk = 0; tk < kRatio; ++tk) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.wkv + (tok0 + tk) * kDLat + 16 * lane);
+      r.kv[tk][0] = __ldg(src);
+      r.kv[tk][1] = __ldg(src + 1);
+      if (kRatio == 2) {
+        const uint4* gs = reinterpret_cast<const uint4*>(p.wgate + (tok0 + tk) * kDLat + 16 * lane);
+        r.g[tk][0] = __ldg(gs);
+        r.g[tk][1] = __ldg(gs + 1);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int tk = 0; tk < kRatio; ++tk) {
+      r.kv[tk][0] = r.kv[tk][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (kRatio == 2) r.g[tk][0] = r.g[tk][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+template <int kRatio>
 __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WriteParams p) {
-  extern __shared__ __align__(16) uint8_t wsm[];
-  float* lat = reinterpret_cast<float*>(wsm + kOffLat);
-  uint16_t* W = reinterpret_cast<uint16_t*>(wsm + kOffW);
-  float* Ks = reinterpret_cast<float*>(wsm + kOffK);
+  extern __shared__ uint8_t wsm_raw[];
+  const uint32_t raw_base = smem_u32(wsm_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;     // 1024-byte alignment for the swizzled tiles
+  uint8_t* sm = wsm_raw + (base - raw_base);
+  const uint32_t sW = base + kOffW, sB = base + kOffB;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+  const uint32_t mma_bar = base + kOffMisc + 8u;          // MMAs of the current tile done
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == 0) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  if (tid == 0) {
+    mbar_init(mma_bar, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
   griddep_wait();
   griddep_launch_dependents();
 
-  for (int i = tid; i < kDLat * kDIdx / 8; i += kWThreads)
-    reinterpret_cast<uint4*>(W)[i] = __ldg(reinterpret_cast<const uint4*>(p.w_idx) + i);
-  __syncthreads();
+  const int64_t total = (int64_t)p.batch * p.n_entries;
+  const int64_t ntiles = (total + kTileE - 1) / kTileE;
+  int64_t tile = blockIdx.x;
 
-  const int64_t per_req = p.n_entries;
-  const int64_t total = (int64_t)p.batch * per_req;
-  const int64_t ntiles = (total + kEnt - 1) / kEnt;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    // ------------------------------------------------------------ 1. pooling + RMSNorm
-    for (int el = warp; el < kEnt; el += kWThreads / 32) {
-      const int64_t ge = tile * kEnt + el;
+  // the warp's first entries go in flight before W_idx is staged
+  EntryRaw<kRatio> raw[kEntPerWarp];
+  Loc cur = locate(tile * kTileE, p.n_entries);          // first entry of the current tile
+#pragma unroll
+  for (int j = 0; j < kEntPerWarp; ++j) {
+    const int r = kEntPerWarp * warp + j;
+    load_entry<kRatio>(p, tile * kTileE + r < total, step(cur, r, p.n_entries), lane, raw[j]);
+  }
+
+  // W_idx [512 k][128 d] bf16 -> MN-major 128B-swizzled A operand: 64-dim block mb at mb * 64 KB,
+  // row k at k * 128 B, 16-byte chunk (d % 64) / 8 swizzled by k
+  for (int i = tid; i < kDLat * kDIdx / 8; i += kWThreads) {
+    const int k = i >> 4, c16 = i & 15;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.w_idx) + i);
+    sts128(sW + (uint32_t)(c16 >> 3) * 65536u + sw128((uint32_t)k, (uint32_t)(c16 & 7)), v.x, v.y, v.z, v.w);
+  }
+
+  const uint32_t idesc = idesc_f16(128, kBRows, true, false, true);
+  uint32_t phase = 0;
+  for (; tile < ntiles; tile += gridDim.x) {
+    const Loc nxt = locate((tile + gridDim.x) * kTileE, p.n_entries);
+    // ------------------------------------------------------------ 1 + 2: pooling, RMSNorm, main KV, B tile
+#pragma unroll
+    for (int j = 0; j < kEntPerWarp; ++j) {
+      const int r = kEntPerWarp * warp + j;                 // entry row of the tile
+      const int64_t ge = tile * kTileE + r;
       float x[16];
-      if (ge < total) {
-        const int64_t b = ge / per_req, i = ge % per_req;
-        const int64_t tok0 = b * p.n_tokens + i * p.ratio;
-        // lane handles channels [8*lane, 8*lane+8) and [256 + 8*lane, ...)
+      if (kRatio == 1) {
+        const uint32_t w[8] = {raw[j].kv[0][0].x, raw[j].kv[0][0].y, raw[j].kv[0][0].z, raw[j].kv[0][0].w,
+                               raw[j].kv[0][1].x, raw[j].kv[0][1].y, raw[j].kv[0][1].z, raw[j].kv[0][1].w};
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int c0 = half * 256 + 8 * lane;
-          if (p.ratio == 1) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.wkv + tok0 * kDLat + c0));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              x[8 * half + 2 * j] = bf16_to_f32((uint16_t)(w[j] & 0xFFFFu));
-              x[8 * half + 2 * j + 1] = bf16_to_f32((uint16_t)(w[j] >> 16));
-            }
-          } else {
-            float g[2][8], xv[2][8];
-#pragma unroll
-            for (int tk = 0; tk < 2; ++tk) {
-              const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.wkv + (tok0 + tk) * kDLat + c0));
-              const uint4 gg = __ldg(reinterpret_cast<const uint4*>(p.wgate + (tok0 + tk) * kDLat + c0));
-              const uint32_t w[4] = {v.x, v.y, v.z, v.w}, wg[4] = {gg.x, gg.y, gg.z, gg.w};
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                xv[tk][2 * j] = bf16_to_f32((uint16_t)(w[j] & 0xFFFFu));
-                xv[tk][2 * j + 1] = bf16_to_f32((uint16_t)(w[j] >> 16));
-                g[tk][2 * j] = bf16_to_f32((uint16_t)(wg[j] & 0xFFFFu));
-                g[tk][2 * j + 1] = bf16_to_f32((uint16_t)(wg[j] >> 16));
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float mx = fmaxf(g[0][j], g[1][j]);
-              const float e0 = expf(g[0][j] - mx), e1 = expf(g[1][j] - mx);
-              const float s = e0 + e1;
-              x[8 * half + j] = (e0 / s) * xv[0][j] + (e1 / s) * xv[1][j];
-            }
-          }
+        for (int u = 0; u < 8; ++u) {
+          x[2 * u] = bf16_lo(w[u]);
+          x[2 * u + 1] = bf16_hi(w[u]);
         }
-        float ss = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) ss = fmaf(x[j], x[j], ss);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float rms = sqrtf(ss / (float)kDLat + 1e-6f);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = x[j] / rms;
       } else {
+        const uint32_t a0[8] = {raw[j].kv[0][0].x, raw[j].kv[0][0].y, raw[j].kv[0][0].z, raw[j].kv[0][0].w,
+                                raw[j].kv[0][1].x, raw[j].kv[0][1].y, raw[j].kv[0][1].z, raw[j].kv[0][1].w};
+        const uint32_t a1[8] = {raw[j].kv[1][0].x, raw[j].kv[1][0].y, raw[j].kv[1][0].z, raw[j].kv[1][0].w,
+                                raw[j].kv[1][1].x, raw[j].kv[1][1].y, raw[j].kv[1][1].z, raw[j].kv[1][1].w};
+        const uint32_t g0[8] = {raw[j].g[0][0].x, raw[j].g[0][0].y, raw[j].g[0][0].z, raw[j].g[0][0].w,
+                                raw[j].g[0][1].x, raw[j].g[0][1].y, raw[j].g[0][1].z, raw[j].g[0][1].w};
+        const uint32_t g1[8] = {raw[j].g[1][0].x, raw[j].g[1][0].y, raw[j].g[1][0].z, raw[j].g[1][0].w,
+                                raw[j].g[1][1].x, raw[j].g[1][1].y, raw[j].g[1][1].z, raw[j].g[1][1].w};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = 0.f;
+        for (int u = 0; u < 16; ++u) {
+          const float x0 = (u & 1) ? bf16_hi(a0[u >> 1]) : bf16_lo(a0[u >> 1]);
+          const float x1 = (u & 1) ? bf16_hi(a1[u >> 1]) : bf16_lo(a1[u >> 1]);
+          const float q0 = (u & 1) ? bf16_hi(g0[u >> 1]) : bf16_lo(g0[u >> 1]);
+          const float q1 = (u & 1) ? bf16_hi(g1[u >> 1]) : bf16_lo(g1[u >> 1]);
+          const float d = q1 - q0;
+          const float e = __expf(-fabsf(d));
+          const float wb = __fdividef(1.f, 1.f + e), ws = e * wb;
+          x[u] = (d > 0.f) ? fmaf(wb, x1, ws * x0) : fmaf(wb, x0, ws * x1);
+        }
       }
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float4* dst = reinterpret_cast<float4*>(lat + el * kDLat + half * 256 + 8 * lane);
-        dst[0] = make_float4(x[8 * half], x[8 * half + 1], x[8 * half + 2], x[8 * half + 3]);
-        dst[1] = make_float4(x[8 * half + 4], x[8 * half + 5], x[8 * half + 6], x[8 * half + 7]);
-      }
-    }
-    __syncthreads();
+      // the raw registers are free: the warp's entry of the next tile goes in flight
+      load_entry<kRatio>(p, (tile + gridDim.x) * kTileE + r < total, step(nxt, r, p.n_entries), lane, raw[j]);
 
-    // ------------------------------------------------------------ 2. main-KV quantisation
-    for (int gi = tid; gi < kEnt * 32; gi += kWThreads) {
-      const int el = gi >> 5, grp = gi & 31;
-      const int64_t ge = tile * kEnt + el;
-      if (ge >= total) continue;
-      const int64_t b = ge / per_req, i = ge % per_req;
-      const int64_t entry = (p.start_entry ? __ldg(p.start_entry + b) : 0) + i;
-      if (entry < 0 || entry >= p.cap) {
-        if (grp == 0) flag_status(p.status, HSA_FLAG_WRITE_RANGE);
-        continue;
-      }
-      const float* v = lat + el * kDLat + grp * 16;
-      float amax = 0.f;
+      float ss = 0.f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
-      uint32_t sb;
-      uint2 codes;
-      if (p.scale_fmt == HSA_SCALE_E8M0) {
-        sb = e8m0_byte_for(amax);
-        const float inv = __uint_as_float((uint32_t)(254 - (int)sb) << 23);   // 2^-(sb-127), exact
-        float vv[16];
+      for (int u = 0; u < 16; ++u) ss = fmaf(x[u], x[u], ss);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) vv[j] = v[j];
-        if (sb == 0u || sb == 254u) {
-          codes = pack16(vv, e8m0_to_f32(sb), true);
+      for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float inv_rms = 1.f / sqrtf(ss / (float)kDLat + 1e-6f);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) x[u] *= inv_rms;
+
+      if (ge < total) {
+        const Loc l = step(cur, r, p.n_entries);
+        const int64_t b = l.b, entry = (p.start_entry ? __ldg(p.start_entry + l.b) : 0) + l.i;
+        if (entry < 0 || entry >= p.cap) {
+          if (lane == 0) flag_status(p.status, HSA_FLAG_WRITE_RANGE);
         } else {
-          codes = pack16(vv, inv, false);
-        }
-      } else {
-        sb = e4m3_byte_for(amax);
-        float vv[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) vv[j] = v[j];
-        codes = pack16(vv, e4m3_to_f32(sb), true);
-      }
-      const size_t eo = (size_t)b * p.cap + entry;
-      *reinterpret_cast<uint2*>(p.kv_q + eo * 256 + grp * 8) = codes;
-      p.kv_s[eo * 32 + grp] = (uint8_t)sb;
-    }
-
-    // ------------------------------------------------------------ 3. indexer projection (fp32)
-    {
-      const int c = tid & 127, e0 = (tid >> 7) * 8;
-      float acc[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll 2
-      for (int d = 0; d < kDLat; d += 4) {
-        const float w0 = bf16_to_f32(W[(d + 0) * kDIdx + c]), w1 = bf16_to_f32(W[(d + 1) * kDIdx + c]);
-        const float w2 = bf16_to_f32(W[(d + 2) * kDIdx + c]), w3 = bf16_to_f32(W[(d + 3) * kDIdx + c]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 l = *reinterpret_cast<const float4*>(lat + (e0 + j) * kDLat + d);
-          float a = acc[j];
-          a = fmaf(l.x, w0, a);
-          a = fmaf(l.y, w1, a);
-          a = fmaf(l.z, w2, a);
-          a = fmaf(l.w, w3, a);
-          acc[j] = a;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) Ks[(e0 + j) * kDIdx + c] = acc[j];
-    }
-    __syncthreads();
-    if (tid < kEnt * 4) {
-      const int el = tid >> 2, grp = tid & 3;
-      const int64_t ge = tile * kEnt + el;
-      if (ge < total) {
-        const int64_t b = ge / per_req, i = ge % per_req;
-        const int64_t entry = (p.start_entry ? __ldg(p.start_entry + b) : 0) + i;
-        if (entry >= 0 && entry < p.cap) {
-          const float* v = Ks + el * kDIdx + grp * 32;
+          // main KV: this lane's 16 channels are group `lane`
           float amax = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-          const uint32_t sb = e8m0_byte_for(amax);
-          float vv[16];
-          uint32_t nb[16];
+          for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(x[u]));
+          uint32_t sb, c8[8];
+          if (p.scale_fmt == HSA_SCALE_E8M0) {
+            sb = e8m0_byte_for(amax);
+            if (sb == 0u || sb == 254u) {
+              const float s = e8m0_to_f32(sb);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(__fdiv_rn(x[2 * u], s), __fdiv_rn(x[2 * u + 1], s));
+            } else {
+              const float inv = __uint_as_float((uint32_t)(254 - (int)sb) << 23);   // 2^(127 - sb), exact
 #pragma unroll
-            for (int j = 0; j < 16; ++j) vv[j] = v[16 * hh + j];
-            uint2 c8 = (sb == 0u || sb == 254u) ? pack16(vv, e8m0_to_f32(sb), true)
-                                                : pack16(vv, __uint_as_float((uint32_t)(254 - (int)sb) << 23), false);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              nb[8 * hh + j] = (c8.x >> (8 * j)) & 0xFFu;
-              nb[8 * hh + 4 + j] = (c8.y >> (8 * j)) & 0xFFu;
+              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(x[2 * u] * inv, x[2 * u + 1] * inv);
             }
-          }
-          // fragment order: stored byte 16t + 4grp + {0,1,2,3} = logical 16grp + {2t, 2t+1, 8+2t, 9+2t}
-          const size_t eo = (size_t)b * p.cap + entry;
-          uint8_t* dst = p.ik_q + eo * 64;
+          } else {
+            sb = e4m3_byte_for(amax);
+            const float s = e4m3_to_f32(sb);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t w = nb[2 * t] | (nb[2 * t + 1] << 8) | (nb[8 + 2 * t] << 16) | (nb[9 + 2 * t] << 24);
-            *reinterpret_cast<uint32_t*>(dst + 16 * t + 4 * grp) = w;
+            for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(__fdiv_rn(x[2 * u], s), __fdiv_rn(x[2 * u + 1], s));
           }
-          p.ik_s[eo * 4 + grp] = (uint8_t)sb;
+          const size_t eo = (size_t)b * p.cap + entry;
+          uint2 codes;
+          codes.x = c8[0] | (c8[1] << 8) | (c8[2] << 16) | (c8[3] << 24);
+          codes.y = c8[4] | (c8[5] << 8) | (c8[6] << 16) | (c8[7] << 24);
+          *reinterpret_cast<uint2*>(p.kv_q + eo * 256 + 8 * lane) = codes;
+          p.kv_s[eo * 32 + lane] = (uint8_t)sb;
         }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) x[u] = 0.f;
+      }
+
+      // x = hi + mid + lo exactly, each a bf16; dims 16 lane .. 16 lane + 15 are block lane / 4,
+      // 16-byte chunks 2 (lane & 3) and 2 (lane & 3) + 1 of row r
+      uint32_t t[3][8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float a = x[2 * u], c = x[2 * u + 1];
+        t[0][u] = bf16x2_rn(a, c);
+        const float ra = a - bf16_lo(t[0][u]), rc = c - bf16_hi(t[0][u]);
+        t[1][u] = bf16x2_rn(ra, rc);
+        t[2][u] = bf16x2_rn(ra - bf16_lo(t[1][u]), rc - bf16_hi(t[1][u]));
+      }
+      // the previous tile's MMAs have finished reading the B tile (waited at its epilogue)
+      const uint32_t blk = sB + (uint32_t)(lane >> 2) * kBBlock;
+#pragma unroll
+      for (int tm = 0; tm < 3; ++tm) {
+        const uint32_t row = (uint32_t)(kTileE * tm + r);
+        sts128(blk + sw128(row, 2u * (lane & 3)), t[tm][0], t[tm][1], t[tm][2], t[tm][3]);
+        sts128(blk + sw128(row, 2u * (lane & 3) + 1u), t[tm][4], t[tm][5], t[tm][6], t[tm][7]);
       }
     }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
+
+    // ------------------------------------------------------------ 3: K^T = W^T . [hi | mid | lo]^T, 32 k-steps
+    if (tid == 0) {
+      tc_fence_after();
+      const uint64_t a0 = sdesc(sW, 65536u, 1024u), b0 = sdesc(sB, 16u, 1024u);
+#pragma unroll
+      for (int k = 0; k < kDLat / 16; ++k) {
+        const uint32_t ao = ((uint32_t)k * 16u * 128u) >> 4;
+        const uint32_t bo = ((uint32_t)(k >> 2) * kBBlock + (uint32_t)(k & 3) * 32u) >> 4;
+        umma_f16(tmem, a0 + ao, b0 + bo, idesc, k > 0);
+      }
+      umma_commit(mma_bar);
+    }
+    if (!mbar_wait(mma_bar, phase) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    phase ^= 1u;
+    tc_fence_after();
+
+    // ------------------------------------------------------------ 4: indexer K, group q = warp & 3, entries 8 (warp >> 2) ..
+    {
+      const int q = warp & 3, e0 = 8 * (warp >> 2);
+      uint32_t vh[8], vm[8], vl[8];
+      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)e0;
+      TMEM_LD8(ta, vh);
+      TMEM_LD8(ta + kTileE, vm);
+      TMEM_LD8(ta + 2 * kTileE, vl);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t ge = tile * kTileE + e0 + j;
+        if (ge >= total) continue;                          // uniform across the warp
+        const Loc l = step(cur, e0 + j, p.n_entries);
+        const int64_t b = l.b, entry = (p.start_entry ? __ldg(p.start_entry + l.b) : 0) + l.i;
+        if (entry < 0 || entry >= p.cap) continue;           // flagged in step 1
+        const float val = (__uint_as_float(vh[j]) + __uint_as_float(vm[j])) + __uint_as_float(vl[j]);
+        uint32_t mbits;
+        asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mbits) : "r"(__float_as_uint(val) & 0x7FFFFFFFu));
+        const uint32_t sb = e8m0_byte_for(__uint_as_float(mbits));
+        // lane 2i builds the byte of dims 2i, 2i+1 of the group
+        const float other = __shfl_xor_sync(0xffffffffu, val, 1);
+        // x / s: a multiply by the exact inverse 2^(127 - sb), or a true division where that
+        // inverse is not a normal float (sb = 0, 254); sb is the same across the warp
+        float lo, hi;
+        if (sb == 0u || sb == 254u) {
+          const float sc = e8m0_to_f32(sb);
+          lo = __fdiv_rn(val, sc);
+          hi = __fdiv_rn(other, sc);
+        } else {
+          const float inv = __uint_as_float((uint32_t)(254 - (int)sb) << 23);
+          lo = val * inv;
+          hi = other * inv;
+        }
+        const uint32_t byte = (lane & 1) ? 0u : e2m1_pair(lo, hi);
+        // fragment order: stored word t of group q (offset 16 t + 4 q) = logical bytes 2t, 2t+1,
+        // 8+2t, 9+2t of the group, i.e. the bytes of lanes 4t, 4t+2, 16+4t, 18+4t
+        const uint32_t y = byte | (__shfl_down_sync(0xffffffffu, byte, 2) << 8);
+        const uint32_t word = y | (__shfl_down_sync(0xffffffffu, y, 16) << 16);
+        const size_t eo = (size_t)b * p.cap + entry;
+        if (lane < 16 && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.ik_q + eo * 64 + 4 * lane + 4 * q) = word;
+        if (lane == 0) p.ik_s[eo * 4 + q] = (uint8_t)sb;
+      }
+    }
+    tc_fence_before();
+    __syncthreads();                  // tensor memory read before the next tile's MMAs overwrite it
+    cur = nxt;
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_free(tmem, kTmemCols);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_cache_write(const WriteParams& p, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(cache_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
+  auto kern = (p.ratio == 2) ? cache_write_kernel<2> : cache_write_kernel<1>;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[p.ratio - 1]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[p.ratio - 1] = true;
   }
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t ntiles = ((int64_t)p.batch * p.n_entries + kEnt - 1) / kEnt;
-  int grid = (int)imin64(ntiles, (int64_t)sms);
+  const int64_t ntiles = ((int64_t)p.batch * p.n_entries + kTileE - 1) / kTileE;
+  const int grid = (int)imin64(ntiles, (int64_t)sms);
   if (grid < 1) return cudaSuccess;
-  return launch_pdl(cache_write_kernel, dim3(grid), dim3(kWThreads), kWSmem, s, p);
+  return launch_pdl(kern, dim3(grid), dim3(kWThreads), kWSmem, s, p);
 }
 
 }  // namespace hsa
