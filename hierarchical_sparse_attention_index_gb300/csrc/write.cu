@@ -11,7 +11,8 @@
 //     weights), then RMSNorm (eps 1e-6, unit gain) as one correctly rounded 1 / rms. The
 //     lane's 16 channels are one main-KV group, so its scale (the smallest E8M0 or E4M3 value s
 //     with 6 s >= amax, an exact bit computation) and its codes (RNE E2M1 of x / s from the
-//     hardware cvt, -0 cleared to +0) come straight from registers. The raw inputs of the warp's next entries are loaded while it works;
+//     hardware cvt, -0 cleared to +0) come straight from registers. The raw inputs of the
+//     warp's next entries are loaded while it works;
 //  2. the normalised latent is split into three bf16 terms, hi + mid + lo = x exactly (each
 //     term the bf16 rounding of what the previous ones left), stacked as the 96 rows (term t,
 //     entry r -> row 32 t + r) of one 128B-swizzled K-major tile;
@@ -44,14 +45,21 @@ constexpr uint32_t kTmemCols = 128;                        // 96 used
 static_assert(kWSmem <= 232448, "shared memory");
 static_assert(kEntPerWarp * kWWarps == kTileE, "entries per warp");
 
-// smallest e with 6 * 2^e >= amax (amax > 0), clamped to [-127, 127]; returns the E8M0 byte
+// E8M0 byte of the smallest e with 6 * 2^e >= amax (amax >= 0), e clamped to [-127, 127]. With
+// amax = f 2^E, f in [1, 2): 6 * 2^(E-2) = 1.5 * 2^E covers f <= 1.5, else 6 * 2^(E-1) does, so
+// the byte is the exponent field - 2, + 1 when the mantissa field exceeds half. Zero and
+// subnormal amax (< 2^-126 <= 6 * 2^-127) take byte 0.
 __device__ __forceinline__ uint32_t e8m0_byte_for(float amax) {
-  if (!(amax > 0.f)) return 0u;
-  int E;
-  const float m = frexpf(amax, &E);     // amax = m 2^E, m in [0.5, 1)
-  int e = (m <= 0.75f) ? E - 3 : E - 2;  // 6 * 2^(E-3) = 0.75 * 2^E
-  e = max(-127, min(127, e));
-  return (uint32_t)(e + 127);
+  const uint32_t u = __float_as_uint(amax);
+  const int b = (int)(u >> 23) - 2 + ((u & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+  return (u >> 23) == 0u ? 0u : (uint32_t)max(0, min(254, b));
+}
+// 1 / 2^(sb - 127) as two exact power-of-two factors: 2^(127 - sb) and 1 for sb <= 253; for
+// sb = 254 (whose inverse is below the normal range) 2^-64 and 2^-63, so (x f1) f2 rounds
+// once, exactly like x / s
+__device__ __forceinline__ void e8m0_inv(uint32_t sb, float& f1, float& f2) {
+  f1 = (sb >= 254u) ? __uint_as_float(63u << 23) : __uint_as_float((254u - sb) << 23);
+  f2 = (sb >= 254u) ? __uint_as_float(64u << 23) : 1.f;
 }
 
 // smallest positive E4M3 value s with 6 s >= amax (saturating at 448); returns the byte
@@ -81,12 +89,13 @@ __device__ __forceinline__ uint32_t e4m3_byte_for(float amax) {
   return byte;
 }
 
-// one E2M1 pair byte (lo -> low nibble), -0 cleared to +0
-__device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
-  uint32_t x = f32x2_to_e2m1x2(hi, lo) & 0xFFu;
-  if ((x & 0x07u) == 0u) x &= 0xF0u;
-  if ((x & 0x70u) == 0u) x &= 0x0Fu;
-  return x;
+// one E2M1 pair byte (lo -> low nibble), RNE, saturating
+__device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) { return f32x2_to_e2m1x2(hi, lo) & 0xFFu; }
+// -0 -> +0 in eight packed E2M1 codes: a nibble keeps its sign bit only if its magnitude bits
+// are nonzero (magnitude + 7 carries into bit 3 exactly then; no carry leaves the nibble)
+__device__ __forceinline__ uint32_t e2m1_clear_neg_zero(uint32_t w) {
+  const uint32_t m = w & 0x77777777u;
+  return w & (0x77777777u | ((m + 0x77777777u) & 0x88888888u));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -253,15 +262,10 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
           uint32_t sb, c8[8];
           if (p.scale_fmt == HSA_SCALE_E8M0) {
             sb = e8m0_byte_for(amax);
-            if (sb == 0u || sb == 254u) {
-              const float s = e8m0_to_f32(sb);
+            float f1, f2;
+            e8m0_inv(sb, f1, f2);
 #pragma unroll
-              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(__fdiv_rn(x[2 * u], s), __fdiv_rn(x[2 * u + 1], s));
-            } else {
-              const float inv = __uint_as_float((uint32_t)(254 - (int)sb) << 23);   // 2^(127 - sb), exact
-#pragma unroll
-              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(x[2 * u] * inv, x[2 * u + 1] * inv);
-            }
+            for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair((x[2 * u] * f1) * f2, (x[2 * u + 1] * f1) * f2);
           } else {
             sb = e4m3_byte_for(amax);
             const float s = e4m3_to_f32(sb);
@@ -270,8 +274,8 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
           }
           const size_t eo = (size_t)b * p.cap + entry;
           uint2 codes;
-          codes.x = c8[0] | (c8[1] << 8) | (c8[2] << 16) | (c8[3] << 24);
-          codes.y = c8[4] | (c8[5] << 8) | (c8[6] << 16) | (c8[7] << 24);
+          codes.x = e2m1_clear_neg_zero(c8[0] | (c8[1] << 8) | (c8[2] << 16) | (c8[3] << 24));
+          codes.y = e2m1_clear_neg_zero(c8[4] | (c8[5] << 8) | (c8[6] << 16) | (c8[7] << 24));
           *reinterpret_cast<uint2*>(p.kv_q + eo * 256 + 8 * lane) = codes;
           p.kv_s[eo * 32 + lane] = (uint8_t)sb;
         }
@@ -329,39 +333,40 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
       TMEM_LD8(ta + kTileE, vm);
       TMEM_LD8(ta + 2 * kTileE, vl);
       tmem_wait_ld();
+      // the 8 entries as independent chains: value, group max, scale, codes, fragment-order word
+      uint32_t word[8], sbs[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int64_t ge = tile * kTileE + e0 + j;
-        if (ge >= total) continue;                          // uniform across the warp
-        const Loc l = step(cur, e0 + j, p.n_entries);
-        const int64_t b = l.b, entry = (p.start_entry ? __ldg(p.start_entry + l.b) : 0) + l.i;
-        if (entry < 0 || entry >= p.cap) continue;           // flagged in step 1
         const float val = (__uint_as_float(vh[j]) + __uint_as_float(vm[j])) + __uint_as_float(vl[j]);
         uint32_t mbits;
         asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mbits) : "r"(__float_as_uint(val) & 0x7FFFFFFFu));
         const uint32_t sb = e8m0_byte_for(__uint_as_float(mbits));
+        float f1, f2;
+        e8m0_inv(sb, f1, f2);
         // lane 2i builds the byte of dims 2i, 2i+1 of the group
         const float other = __shfl_xor_sync(0xffffffffu, val, 1);
-        // x / s: a multiply by the exact inverse 2^(127 - sb), or a true division where that
-        // inverse is not a normal float (sb = 0, 254); sb is the same across the warp
-        float lo, hi;
-        if (sb == 0u || sb == 254u) {
-          const float sc = e8m0_to_f32(sb);
-          lo = __fdiv_rn(val, sc);
-          hi = __fdiv_rn(other, sc);
-        } else {
-          const float inv = __uint_as_float((uint32_t)(254 - (int)sb) << 23);
-          lo = val * inv;
-          hi = other * inv;
-        }
-        const uint32_t byte = (lane & 1) ? 0u : e2m1_pair(lo, hi);
+        const uint32_t byte = (lane & 1) ? 0u : e2m1_pair((val * f1) * f2, (other * f1) * f2);
         // fragment order: stored word t of group q (offset 16 t + 4 q) = logical bytes 2t, 2t+1,
         // 8+2t, 9+2t of the group, i.e. the bytes of lanes 4t, 4t+2, 16+4t, 18+4t
         const uint32_t y = byte | (__shfl_down_sync(0xffffffffu, byte, 2) << 8);
-        const uint32_t word = y | (__shfl_down_sync(0xffffffffu, y, 16) << 16);
-        const size_t eo = (size_t)b * p.cap + entry;
-        if (lane < 16 && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.ik_q + eo * 64 + 4 * lane + 4 * q) = word;
-        if (lane == 0) p.ik_s[eo * 4 + q] = (uint8_t)sb;
+        word[j] = e2m1_clear_neg_zero(y | (__shfl_down_sync(0xffffffffu, y, 16) << 16));
+        sbs[j] = sb;
+      }
+      Loc l = step(cur, e0, p.n_entries);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (tile * kTileE + e0 + j < total) {
+          const int64_t entry = (p.start_entry ? __ldg(p.start_entry + l.b) : 0) + l.i;
+          if (entry >= 0 && entry < p.cap) {                 // out-of-range entries were flagged in step 1
+            const size_t eo = (size_t)l.b * p.cap + entry;
+            if (lane < 16 && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.ik_q + eo * 64 + 4 * lane + 4 * q) = word[j];
+            if (lane == 0) p.ik_s[eo * 4 + q] = (uint8_t)sbs[j];
+          }
+        }
+        if (++l.i == p.n_entries) {
+          l.i = 0;
+          ++l.b;
+        }
       }
     }
     tc_fence_before();
