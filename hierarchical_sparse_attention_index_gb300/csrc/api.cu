@@ -192,6 +192,30 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
   uint8_t* W = static_cast<uint8_t*>(ws);
   const cudaStream_t s = (cudaStream_t)stream;
 
+  if (pool_mode) {
+    // one fused launch: rescoring over the pool and the exact top-512, one cluster per row; the
+    // keys, slots and counts its CTAs exchange live in the Reindex score, candidate and sure
+    // regions of the workspace
+    ReindexParams rp;
+    memset(&rp, 0, sizeof(rp));
+    rp.batch = cache->batch;
+    rp.nq = nq;
+    rp.cap = cache->capacity;
+    rp.ik_q = cache->ik_q;
+    rp.ik_s = cache->ik_s;
+    rp.q = static_cast<const uint16_t*>(q);
+    rp.w = w;
+    rp.vis = vis;
+    rp.pool = pool;
+    rp.xkey = reinterpret_cast<uint32_t*>(W + L.off_pscores);
+    rp.xslot = reinterpret_cast<uint32_t*>(W + L.off_cand_pool);
+    rp.xcount = reinterpret_cast<int32_t*>(W + L.off_sure_pool);
+    rp.ld_xcount = kTopK;
+    rp.topk_out = topk_out;
+    rp.status = status;
+    return cuda_fail(launch_reindex(rp, s), "reindex launch");
+  }
+
   ScanParams sp;
   memset(&sp, 0, sizeof(sp));
   sp.pool_mode = pool_mode ? 1 : 0;

@@ -90,6 +90,25 @@ struct SelectParams {
 cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, cudaStream_t s);
 
+// ------------------------------------------------------------------ fused Reindex (one cluster per row)
+struct ReindexParams {
+  int32_t batch, nq;
+  int64_t cap;
+  const uint8_t* ik_q;
+  const uint8_t* ik_s;
+  const uint16_t* q;     // bf16 [B][nq][16][128]
+  const float* w;        // [B][nq][16]
+  const int32_t* vis;    // [B][nq]
+  const int32_t* pool;   // [B][nq][16384]
+  uint32_t* xkey;        // workspace [rows][4 CTAs][4096]: order keys of the elements each CTA publishes
+  uint32_t* xslot;       // workspace [rows][4 CTAs][4096]: their CTA-local slots
+  int32_t* xcount;       // workspace: CTA c of row r publishes (count, valid elements) at xcount[r * ld_xcount + 2c]
+  int64_t ld_xcount;
+  int32_t* topk_out;     // [B][nq][512]
+  uint32_t* status;
+};
+cudaError_t launch_reindex(const ReindexParams& p, cudaStream_t s);
+
 // ------------------------------------------------------------------ attention
 struct AttnParams {
   CUtensorMap qmap;       // q as a 2-D bf16 tensor [B*nq*64][512], 64 x 16 boxes, 128-byte swizzle

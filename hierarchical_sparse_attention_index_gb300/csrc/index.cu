@@ -27,6 +27,7 @@
 #include "hsa_common.cuh"
 #include "hsa_hist.cuh"
 #include "hsa_internal.h"
+#include "hsa_score.cuh"
 
 namespace hsa {
 namespace {
@@ -72,26 +73,6 @@ __host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq
   L.misc = o;    o += 256;
   L.total = o;
   return L;
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // kPoolMode: Reindex (segment = one (request, query) row, entries gathered through the pool);
@@ -237,64 +218,15 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     named_bar_sync(1, kConsumers);
     for (int ql = 0; ql < nql && tid < 256; ++ql) {
       const int row = kPoolMode ? seg : seg * p.nq + ql;
-      const int h = tid >> 4, d0 = (tid & 15) * 8;
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)row * kHIdx + h) * kDIdx + d0));
-      float x[8];
-      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(rw[i] << 16);
-        x[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      int sh = 0;
-      if (amax > 0.f) {
-        int e;
-        frexpf(amax, &e);          // amax = m * 2^e, m in [0.5, 1)
-        sh = 15 - e;               // amax * 2^sh in [2^14, 2^15)
-      }
-      uint32_t pk[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half lo = __float2half_rn(ldexpf(x[2 * i], sh));
-        const __half hi = __float2half_rn(ldexpf(x[2 * i + 1], sh));
-        pk[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-      }
-      // dims d0..d0+7 -> k-step s = d0/16, t' = (d0%16)/4 and t'+1
-      const int ks = d0 >> 4, tp = (d0 & 15) >> 2;
-      const int nt = h >> 3, gp = h & 7;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int ln = 4 * gp + tp + u;
-        uint32_t* dst = bfrag + ((((size_t)ql * 2 + nt) * 8 + ks) * 32 + ln) * 2;
-        dst[0] = pk[2 * u];
-        dst[1] = pk[2 * u + 1];
-      }
-      if ((tid & 15) == 0) wsc[ql * 16 + h] = ldexpf(__ldg(p.w + (size_t)row * kHIdx + h), -sh);
+      stage_query(p.q + (size_t)row * kHIdx * kDIdx, p.w + (size_t)row * kHIdx, bfrag + ql * kQFragWords,
+                  wsc + ql * kQWeights, tid);
       if (tid < 8 && !kPoolMode && tid == ql) svis[ql] = (int)imin64(__ldg(p.vis + row), p.cap);
     }
     if (kPoolMode && tid == 0) svis[0] = __ldg(p.vis + seg);
     named_bar_sync(1, kConsumers);
   };
 
-  auto load_query_regs = [&](int ql) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint2 v = *reinterpret_cast<const uint2*>(bfrag + ((((size_t)ql * 2 + nt) * 8 + s) * 32 + lane) * 2);
-        B[nt][s][0] = v.x;
-        B[nt][s][1] = v.y;
-      }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) wr[nt][j] = wsc[ql * 16 + nt * 8 + 2 * t + j];
-  };
+  auto load_query_regs = [&](int ql) { load_query_frags(bfrag + ql * kQFragWords, wsc + ql * kQWeights, lane, B, wr); };
 
   // Stage index, ring parity and (segment, chunk) advance incrementally. Segment changes and
   // histogram flushes are the same for every consumer warp, so the named barriers inside them
@@ -324,33 +256,9 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     }
   };
   auto gather = [&](int sg, int slot, int pv) {
-    // run u (slots 8u .. 8u+7 of the warp) starts at the pool value of lane 8u; a run is fetched
-    // only if that start is an 8-aligned in-range entry, and a slot is scored only if it holds
-    // start + its offset and is visible; anything else is flagged
-    const int vis = __ldg(p.vis + sg);
-    const int64_t ebase = (int64_t)(sg / p.nq) * p.cap;
-    const int j = lane & 7;
-    const int base = __shfl_sync(0xffffffffu, pv, lane & ~7);
-    const bool bok = (base >= 0) && ((base & 7) == 0) && (base < p.cap);
-    int outv = -1;
-    if (bok && pv >= 0) {
-      if (pv == base + j && pv < vis) outv = pv;
-      else if (pv != base + j || pv >= p.cap) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-    } else if (j == 0 && base >= 0 && !bok) {
-      flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-    }
-    ring_slots[slot * 32 + lane] = outv;
-    const uint32_t dc = ring_codes + (uint32_t)(slot * kWarpCodes), ds = ring_scales + (uint32_t)(slot * kWarpScales);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int bb = __shfl_sync(0xffffffffu, base, 8 * u);
-      if (bb >= 0 && (bb & 7) == 0 && bb < p.cap) cp_async16(dc + u * 512 + lane * 16, p.ik_q + (ebase + bb) * 64 + lane * 16);
-    }
-    const int us = (lane >> 1) & 3;
-    const int bs = __shfl_sync(0xffffffffu, base, 8 * us);
-    if (lane < 8 && bs >= 0 && (bs & 7) == 0 && bs < p.cap)
-      cp_async16(ds + us * 32 + (lane & 1) * 16, p.ik_s + (ebase + bs) * 4 + (lane & 1) * 16);
-    cp_async_commit();
+    gather_runs(p.ik_q, p.ik_s, (int64_t)(sg / p.nq) * p.cap, p.cap, __ldg(p.vis + sg), pv, lane,
+                ring_codes + (uint32_t)(slot * kWarpCodes), ring_scales + (uint32_t)(slot * kWarpScales),
+                ring_slots + slot * 32, p.status);
   };
   if (kPoolMode) {
     int pv0[kRing - 1], sg0[kRing - 1];
@@ -419,73 +327,14 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
 
     if (warp * 32 < nrows) {
       const bool two = warp * 32 + 16 < nrows;        // the warp's second 16-row tile holds data
-      const uint32_t a_base = codes + (uint32_t)(row_off + g) * 64u + 16u * t;
-      // the warp's 32 rows' E8M0 group scales as floats, once per stage: 2^(b-127) is byte b
-      // moved to the exponent field (b = 0 only occurs with all-zero codes, where 0 * 0 = 0)
       const uint32_t sf_base = smem_u32(smem + L.sfl) + (uint32_t)warp * 512u;
-      {
-        const uint32_t S = lds32(scales + (uint32_t)(row_off + lane) * 4u);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sf_base + (uint32_t)lane * 16u),
-                     "r"((S << 23) & 0x7F800000u), "r"((S << 15) & 0x7F800000u), "r"((S << 7) & 0x7F800000u),
-                     "r"((S >> 1) & 0x7F800000u)
-                     : "memory");
-        __syncwarp();
-      }
-      // this lane's row after the reduce-scatter below: rows 8t .. 8t+7 of the warp's 32 are
-      // the 8-entry block t, one row per lane g
+      stage_group_scales(scales, row_off, sf_base, lane);
+      // this lane's row after the reduce-scatter: rows 8t .. 8t+7 of the warp's 32 are the
+      // 8-entry block t, one row per lane g
       const int r_mine = warp * 32 + 8 * t + g;
       for (int ql = 0; ql < nql; ++ql) {
         if (nql > 1) load_query_regs(ql);
-        // vp[mt][0/1]: ReLU-weighted sum over this lane's 4 heads for rows g / g+8 of tile mt
-        float vp[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          if (mt == 1 && !two) break;
-          const uint4 A0 = lds128(a_base + (uint32_t)mt * 1024u);
-          const uint4 A1 = lds128(a_base + (uint32_t)mt * 1024u + 512u);
-          const uint4 SF0 = lds128(sf_base + (uint32_t)(16 * mt + g) * 16u);
-          const uint4 SF1 = lds128(sf_base + (uint32_t)(16 * mt + g + 8) * 16u);
-          const float sf0[4] = {__uint_as_float(SF0.x), __uint_as_float(SF0.y), __uint_as_float(SF0.z),
-                                __uint_as_float(SF0.w)};
-          const float sf1[4] = {__uint_as_float(SF1.x), __uint_as_float(SF1.y), __uint_as_float(SF1.z),
-                                __uint_as_float(SF1.w)};
-          const uint32_t aw0[4] = {A0.x, A0.y, A0.z, A0.w}, aw1[4] = {A1.x, A1.y, A1.z, A1.w};
-          float tot[2][4];
-#pragma unroll
-          for (int gi = 0; gi < 4; ++gi) {
-            // group gi = word gi of each row's chunk = k-steps 2gi (bytes 0,1) and 2gi+1 (bytes 2,3)
-            uint32_t f0, f1, f2, f3, h0, h1, h2, h3;
-            e2m1x8_to_f16x2x4(aw0[gi], f0, f1, f2, f3);
-            e2m1x8_to_f16x2x4(aw1[gi], h0, h1, h2, h3);
-            const float sc0 = sf0[gi], sc1 = sf1[gi];
-            float tmp[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              mma_f16_16816_zc(tmp[nt], f0, h0, f1, h1, B[nt][2 * gi][0], B[nt][2 * gi][1]);
-              mma_f16_16816(tmp[nt], f2, h2, f3, h3, B[nt][2 * gi + 1][0], B[nt][2 * gi + 1][1]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              tot[nt][0] = gi ? fmaf(sc0, tmp[nt][0], tot[nt][0]) : sc0 * tmp[nt][0];
-              tot[nt][1] = gi ? fmaf(sc0, tmp[nt][1], tot[nt][1]) : sc0 * tmp[nt][1];
-              tot[nt][2] = gi ? fmaf(sc1, tmp[nt][2], tot[nt][2]) : sc1 * tmp[nt][2];
-              tot[nt][3] = gi ? fmaf(sc1, tmp[nt][3], tot[nt][3]) : sc1 * tmp[nt][3];
-            }
-          }
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              vp[mt][0] = fmaf(wr[nt][j], fmaxf(tot[nt][j], 0.f), vp[mt][0]);
-              vp[mt][1] = fmaf(wr[nt][j], fmaxf(tot[nt][2 + j], 0.f), vp[mt][1]);
-            }
-        }
-        // Reduce-scatter over the 4 head lanes t of a row group: after it, lane (g, t) holds
-        // the full 16-head score of row 8t + g of the warp (tile t >> 1, row g + 8 (t & 1)).
-        const bool hi2 = (t & 2) != 0, hi1 = (t & 1) != 0;
-        const float k0 = (hi2 ? vp[1][0] : vp[0][0]) + __shfl_xor_sync(0xffffffffu, hi2 ? vp[0][0] : vp[1][0], 2);
-        const float k1 = (hi2 ? vp[1][1] : vp[0][1]) + __shfl_xor_sync(0xffffffffu, hi2 ? vp[0][1] : vp[1][1], 2);
-        float v = (hi1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, hi1 ? k0 : k1, 1);
+        float v = score_rows32(codes, row_off, sf_base, two, B, wr, lane);
         bool ok;
         if (!kPoolMode) {
           ok = c * kChunk + r_mine < svis[ql];

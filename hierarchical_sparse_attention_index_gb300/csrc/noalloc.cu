@@ -21,20 +21,16 @@ namespace hsa {
 namespace {
 
 constexpr int kNoAllocMaxRows = 32;   // batch * nq
-// per (request, query) row: slot scores, candidates, sure list, histogram, select state, done flag
-constexpr size_t kRowHist = (size_t)kHistBins * 4;
-constexpr size_t kRowScores = (size_t)kPool * 4;
-constexpr size_t kRowCand = (size_t)kPool * 4;
-constexpr size_t kRowSure = (size_t)kTopK * 4;
+// per (request, query) row: the fused Reindex kernel's exchange areas - 4 CTAs' published
+// order keys and slots (4096 words each) and their (count, valid elements) pairs
+constexpr int kRxCounts = 4;
+constexpr size_t kRowKey = (size_t)kPool * 4;
+constexpr size_t kRowSlot = (size_t)kPool * 4;
 constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-constexpr size_t kOffHist = 0;
-constexpr size_t kOffState = kOffHist + align256(kNoAllocMaxRows * kRowHist);
-constexpr size_t kOffDone = kOffState + align256(kNoAllocMaxRows * sizeof(SelState));
-constexpr size_t kZeroEnd = kOffDone + align256(kNoAllocMaxRows * 4);
-constexpr size_t kOffScores = kZeroEnd;
-constexpr size_t kOffCand = kOffScores + align256(kNoAllocMaxRows * kRowScores);
-constexpr size_t kOffSure = kOffCand + align256(kNoAllocMaxRows * kRowCand);
-constexpr size_t kScratchBytes = kOffSure + align256(kNoAllocMaxRows * kRowSure);   // about 4.7 MB
+constexpr size_t kOffKey = 0;
+constexpr size_t kOffSlot = kOffKey + align256(kNoAllocMaxRows * kRowKey);
+constexpr size_t kOffCount = kOffSlot + align256(kNoAllocMaxRows * kRowSlot);
+constexpr size_t kScratchBytes = kOffCount + align256(kNoAllocMaxRows * 2 * kRxCounts * 4);   // about 4.2 MB
 
 static __device__ __align__(256) uint8_t g_reindex_scratch[kScratchBytes];
 
@@ -82,51 +78,23 @@ extern "C" HSA_API hsa_status hsa_index_reindex_noalloc(const hsa_cache* cache, 
   hsa_status st = scratch_for_current_device(&W, &status, &sms);
   if (st != HSA_OK) return st;
   const cudaStream_t s = (cudaStream_t)stream;
-  const int32_t rows = cache->batch * nq;
-  // the histogram / select-state / done-flag region must start at zero
-  if (cudaMemsetAsync(W, 0, kZeroEnd, s) != cudaSuccess) return HSA_ERR_CUDA;
-
-  ScanParams sp;
-  memset(&sp, 0, sizeof(sp));
-  sp.pool_mode = 1;
-  sp.batch = cache->batch;
-  sp.nq = nq;
-  sp.cap = cache->capacity;
-  sp.ik_q = cache->ik_q;
-  sp.ik_s = cache->ik_s;
-  sp.q = static_cast<const uint16_t*>(q);
-  sp.w = w;
-  sp.vis = vis;
-  sp.pool = pool;
-  sp.n_seg = rows;
-  sp.chunks_per_seg = kPool / kScanChunk;
-  sp.total_items = sp.n_seg * sp.chunks_per_seg;
-  sp.scores = reinterpret_cast<float*>(W + kOffScores);
-  sp.ld_s = kPool;
-  sp.hist = reinterpret_cast<uint32_t*>(W + kOffHist);
-  sp.state = reinterpret_cast<SelState*>(W + kOffState);
-  sp.seg_done = reinterpret_cast<uint32_t*>(W + kOffDone);
-  sp.status = status;
-
-  SelectParams se;
-  memset(&se, 0, sizeof(se));
-  se.pool_mode = 1;
-  se.batch = cache->batch;
-  se.nq = nq;
-  se.max_vis = max_vis;
-  se.vis = vis;
-  se.pool = pool;
-  se.scores = sp.scores;
-  se.ld_s = kPool;
-  se.hist = sp.hist;
-  se.state = sp.state;
-  se.cand = reinterpret_cast<int32_t*>(W + kOffCand);
-  se.ld_cand = kPool;
-  se.sure = reinterpret_cast<int32_t*>(W + kOffSure);
-  se.ld_sure = kTopK;
-  se.topk_out = topk_out;
-  se.status = status;
-  if (launch_index_scan(sp, sms, s) != cudaSuccess) return HSA_ERR_CUDA;
-  if (launch_select(se, s) != cudaSuccess) return HSA_ERR_CUDA;
+  ReindexParams rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.batch = cache->batch;
+  rp.nq = nq;
+  rp.cap = cache->capacity;
+  rp.ik_q = cache->ik_q;
+  rp.ik_s = cache->ik_s;
+  rp.q = static_cast<const uint16_t*>(q);
+  rp.w = w;
+  rp.vis = vis;
+  rp.pool = pool;
+  rp.xkey = reinterpret_cast<uint32_t*>(W + kOffKey);
+  rp.xslot = reinterpret_cast<uint32_t*>(W + kOffSlot);
+  rp.xcount = reinterpret_cast<int32_t*>(W + kOffCount);
+  rp.ld_xcount = 2 * kRxCounts;
+  rp.topk_out = topk_out;
+  rp.status = status;
+  if (launch_reindex(rp, s) != cudaSuccess) return HSA_ERR_CUDA;
   return HSA_OK;
 }

@@ -1,0 +1,350 @@
+// Fused Reindex indexer ([CED] Figure 5 right: the Reindex pass rescored over the candidate pool;
+// [ARCH] §3.3 候选池 重排; [10100] 层次化稀疏索引器): per (request, query) row, score the
+// 16,384 pool slots s = sum_h w_h ReLU(q_h . k) and emit the exact top-512 (ties to the lower
+// slot), ascending, in one launch.
+//
+// One thread-block cluster of 4 CTAs per row; CTA r owns slots [4096 r, 4096 r + 4096):
+//  1. 16 warps score 256 slots each: 8 groups of 32 slots (four 8-entry runs) gathered with
+//     cp.async into a per-warp ring 4 groups ahead, scored with warp MMAs (shared with the scan
+//     kernel); scores stay in shared memory with a 4096-bin histogram of their top 12 key bits;
+//  2. the CTA finds its own threshold bin b_r (the bin of its 512-th largest key) and publishes,
+//     through the workspace, every valid element in a bin >= b_r (order key and slot), their
+//     count and its number of valid elements. The row's top-512 lies inside the union of the
+//     four lists: an element of CTA r in the row's top-512 is in CTA r's own top-512;
+//  3. after one cluster barrier every CTA loads the union and selects the same top-K,
+//     K = min(512, valid elements of the row): a histogram of the union's top key bits gives the
+//     threshold bin, and the elements in it are ranked by (key desc, slot asc) - by counting
+//     when there are few, by an exact radix select otherwise;
+//  4. each CTA writes its selected slots' positions in ascending slot order at the offset given
+//     by the counts of the CTAs before it; CTA 0 pads the tail with -1.
+#include "hsa_common.cuh"
+#include "hsa_hist.cuh"
+#include "hsa_internal.h"
+#include "hsa_score.cuh"
+
+namespace hsa {
+namespace {
+
+constexpr int kRxWarps = 16;
+constexpr int kRxThreads = kRxWarps * 32;
+constexpr int kRxCluster = 4;
+constexpr int kSlotsPerCta = kPool / kRxCluster;          // 4096
+constexpr int kSlotsPerWarp = kSlotsPerCta / kRxWarps;    // 256
+constexpr int kGroups = kSlotsPerWarp / 32;               // 8 groups of 32 slots per warp
+constexpr int kRxRing = 5;                                // gathers run 4 groups ahead
+constexpr uint32_t kGrpCodes = 32 * 64, kGrpScales = 32 * 4;
+constexpr int kRankMax = 512;                             // threshold-bin elements ranked by counting up to this many
+constexpr int kPerT = kHistBins / kRxThreads;             // 8 bins (or slots) per thread
+
+// shared-memory layout (bytes)
+constexpr uint32_t kOffRing = 0;                                                  // [16 warps][5][codes|scales]
+constexpr uint32_t kRingBytes = (uint32_t)kRxWarps * kRxRing * (kGrpCodes + kGrpScales);
+constexpr uint32_t kOffSlots = kOffRing + kRingBytes;                             // [16][5][32] int
+constexpr uint32_t kOffBfrag = kOffSlots + kRxWarps * kRxRing * 32 * 4;
+constexpr uint32_t kOffWsc = kOffBfrag + kQFragWords * 4;
+constexpr uint32_t kOffSfl = kOffWsc + kQWeights * 4;                              // [16 warps][512 B]
+constexpr uint32_t kOffSc = kOffSfl + kRxWarps * 512;                              // [4096] scores
+constexpr uint32_t kOffHist = kOffSc + kSlotsPerCta * 4;                           // [4096] counts
+constexpr uint32_t kOffSel = kOffHist + kHistBins * 4;                             // [4096 bits] taken slots
+constexpr uint32_t kOffScr = kOffSel + kSlotsPerCta / 8;                           // scratch ints
+constexpr uint32_t kScrInts = 128;
+constexpr uint32_t kRxSmem = kOffScr + kScrInts * 4;
+static_assert(kRxSmem <= 232448, "shared memory");
+// after scoring, the rings hold the union (64-bit composites) and the score array the ranked
+// threshold-bin elements
+static_assert((uint32_t)kPool * 8 <= kRingBytes, "union staging fits the rings");
+static_assert(kRankMax * 8 <= kSlotsPerCta * 4, "ranked elements fit the score array");
+
+__device__ __forceinline__ uint32_t rx_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void rx_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// (order key, inverted row slot): larger = better, ties to the lower slot
+__device__ __forceinline__ uint64_t comp_of(uint32_t key, uint32_t row_slot) {
+  return ((uint64_t)key << 32) | (uint64_t)(~row_slot);
+}
+__device__ __forceinline__ uint32_t slot_of(uint64_t comp) { return ~(uint32_t)comp; }
+__device__ __forceinline__ int bin_of(uint64_t comp) { return (int)(comp >> (32 + kHistShift)); }
+
+// Threshold bin of a top-K over `hist` (4096 bins, thread 0 holding the 8 highest): the bin
+// holding the K-th largest key and the count above it into scr[64], scr[65]; -1 and the total
+// when the histogram holds K or fewer. Returns the total. All kRxThreads threads call it.
+__device__ __forceinline__ int find_threshold(const uint32_t* hist, int K, int* scr, int tid) {
+  const int top = kHistBins - kPerT * (tid + 1);
+  int hc[kPerT], local = 0;
+#pragma unroll
+  for (int i = 0; i < kPerT; ++i) {
+    hc[i] = (int)hist[top + i];
+    local += hc[i];
+  }
+  int total;
+  const int excl = excl_scan(local, scr, 1, kRxThreads, &total, tid);
+  if (total <= K) {
+    if (tid == 0) {
+      scr[64] = -1;
+      scr[65] = total;
+    }
+  } else if (excl < K && excl + local >= K) {
+    int run = excl;
+#pragma unroll
+    for (int i = kPerT - 1; i >= 0; --i) {
+      if (run + hc[i] >= K) {
+        scr[64] = top + i;
+        scr[65] = run;
+        break;
+      }
+      run += hc[i];
+    }
+  }
+  named_bar_sync(1, kRxThreads);
+  return total;
+}
+
+__global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads, 1)
+    reindex_kernel(const ReindexParams p) {
+  extern __shared__ __align__(1024) uint8_t rsm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)rx_cluster_rank();
+  const int row = blockIdx.x / kRxCluster;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(rsm + kOffHist);
+  float* sc = reinterpret_cast<float*>(rsm + kOffSc);
+  uint32_t* sel = reinterpret_cast<uint32_t*>(rsm + kOffSel);
+  int* scr = reinterpret_cast<int*>(rsm + kOffScr);
+  uint32_t* bfrag = reinterpret_cast<uint32_t*>(rsm + kOffBfrag);
+  float* wsc = reinterpret_cast<float*>(rsm + kOffWsc);
+
+  for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;
+  for (int i = tid; i < kSlotsPerCta / 32; i += kRxThreads) sel[i] = 0u;
+  if (tid < kScrInts) scr[tid] = 0;
+  griddep_wait();
+  griddep_launch_dependents();
+
+  const int vis = __ldg(p.vis + row);
+  const int32_t* pool_row = p.pool + (size_t)row * kPool;
+  if (tid < 256) stage_query(p.q + (size_t)row * kHIdx * kDIdx, p.w + (size_t)row * kHIdx, bfrag, wsc, tid);
+
+  // ---------------------------------------------------------------- 1. score this warp's 256 slots
+  const int slot0 = kSlotsPerCta * rank + kSlotsPerWarp * warp;   // first slot (row-relative) of the warp
+  const int64_t ebase = (int64_t)(row / p.nq) * p.cap;
+  const uint32_t ring = smem_u32(rsm + kOffRing) + (uint32_t)(warp * kRxRing) * (kGrpCodes + kGrpScales);
+  int* slots = reinterpret_cast<int*>(rsm + kOffSlots) + warp * kRxRing * 32;
+  // a group's pool values are loaded one gather ahead, so a gather never waits for them
+  auto pool_val = [&](int grp) { return (grp < kGroups) ? __ldg(pool_row + slot0 + 32 * grp + lane) : -1; };
+  auto gather = [&](int grp, int pv) {
+    const int rs = grp % kRxRing;
+    const uint32_t dc = ring + (uint32_t)rs * (kGrpCodes + kGrpScales);
+    gather_runs(p.ik_q, p.ik_s, ebase, p.cap, vis, pv, lane, dc, dc + kGrpCodes, slots + rs * 32, p.status);
+  };
+  {
+    int pv0[kRxRing - 1];
+#pragma unroll
+    for (int k = 0; k < kRxRing - 1; ++k) pv0[k] = pool_val(k);
+#pragma unroll
+    for (int k = 0; k < kRxRing - 1; ++k) gather(k, pv0[k]);
+  }
+  int pv_next = pool_val(kRxRing - 1);
+  __syncthreads();                    // staged query visible
+  uint32_t B[2][8][2];
+  float wr[2][2];
+  load_query_frags(bfrag, wsc, lane, B, wr);
+  const uint32_t sf_base = smem_u32(rsm + kOffSfl) + (uint32_t)warp * 512u;
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll 1
+  for (int k = 0; k < kGroups; ++k) {
+    if (k + kRxRing - 1 < kGroups) {
+      gather(k + kRxRing - 1, pv_next);
+      pv_next = pool_val(k + kRxRing);
+    } else {
+      cp_async_commit();
+    }
+    cp_async_wait<kRxRing - 1>();     // group k's runs have landed
+    __syncwarp();
+    const int rs = k % kRxRing;
+    const uint32_t codes = ring + (uint32_t)rs * (kGrpCodes + kGrpScales);
+    stage_group_scales(codes + kGrpCodes, 0, sf_base, lane);
+    float v = score_rows32(codes, 0, sf_base, true, B, wr, lane);
+    const bool ok = slots[rs * 32 + 8 * t + g] >= 0;
+    v = ok ? v : -INFINITY;
+    const int ls = kSlotsPerWarp * warp + 32 * k + 8 * t + g;   // CTA-local slot
+    sc[ls] = v;
+    if (ok) atomicAdd(hist + (order_key(v) >> kHistShift), 1u);
+    __syncwarp();                     // ring buffer rs is free for the gather 4 groups ahead
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- 2. publish this CTA's own top region
+  // scr: [0, 32) scan scratch; 64, 65 threshold bin and count above it; 72 published count;
+  // 73 ranked count; 76 + c slots CTA c keeps; 80..82 radix digit, count above it, count in it;
+  // 84..85 the cut composite of the rank count
+  const int nval_local = find_threshold(hist, kTopK, scr, tid);
+  const int lthr = scr[64];
+  {
+    const size_t xo = ((size_t)row * kRxCluster + rank) * kSlotsPerCta;
+#pragma unroll
+    for (int i = 0; i < kPerT; ++i) {
+      const int ls = kPerT * tid + i;
+      const float v = sc[ls];
+      if (v == -INFINITY) continue;
+      const uint32_t key = order_key(v);
+      if ((int)(key >> kHistShift) >= lthr) {
+        const int j = atomicAdd(scr + 72, 1);
+        __stcg(p.xkey + xo + j, key);
+        __stcg(p.xslot + xo + j, (uint32_t)ls);
+      }
+    }
+  }
+  named_bar_sync(1, kRxThreads);
+  if (tid == 0) {
+    __stcg(p.xcount + (size_t)row * p.ld_xcount + 2 * rank, scr[72]);
+    __stcg(p.xcount + (size_t)row * p.ld_xcount + 2 * rank + 1, nval_local);
+  }
+  rx_cluster_sync();                  // the four lists are in L2
+
+  // ---------------------------------------------------------------- 3. the row's top-K over the union
+  int ubase[kRxCluster], U = 0, nvalid = 0;
+#pragma unroll
+  for (int c = 0; c < kRxCluster; ++c) {
+    ubase[c] = U;
+    U += __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c);
+    nvalid += __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c + 1);
+  }
+  const int K = min(kTopK, nvalid);
+  auto cta_of = [&](int i) {
+    int c = 0;
+#pragma unroll
+    for (int d = 1; d < kRxCluster; ++d) c += (i >= ubase[d]) ? 1 : 0;
+    return c;
+  };
+  uint64_t* ust = reinterpret_cast<uint64_t*>(rsm + kOffRing);   // the rings are free now
+  for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;
+  for (int i = tid; i < U; i += kRxThreads) {
+    const int c = cta_of(i);
+    const size_t xo = ((size_t)row * kRxCluster + c) * kSlotsPerCta + (size_t)(i - ubase[c]);
+    ust[i] = comp_of(__ldcg(p.xkey + xo), (uint32_t)(kSlotsPerCta * c) + __ldcg(p.xslot + xo));
+  }
+  named_bar_sync(1, kRxThreads);
+  for (int i = tid; i < U; i += kRxThreads) atomicAdd(hist + bin_of(ust[i]), 1u);
+  named_bar_sync(1, kRxThreads);
+  find_threshold(hist, K, scr, tid);
+  const int thr = scr[64], need = K - scr[65];
+  // the cut: element taken iff (comp & mask) >= prefix
+  uint64_t prefix = 0, mask = 0;
+  if (thr >= 0) {
+    const int Cn = (int)hist[thr];
+    prefix = (uint64_t)thr << (32 + kHistShift);
+    mask = (uint64_t)(kHistBins - 1) << (32 + kHistShift);
+    if (need < Cn && Cn <= kRankMax) {
+      // few elements in the threshold bin: the need-th largest of them by counting
+      uint64_t* rk = reinterpret_cast<uint64_t*>(sc);             // the scores are published
+      for (int i = tid; i < U; i += kRxThreads)
+        if (bin_of(ust[i]) == thr) rk[atomicAdd(scr + 73, 1)] = ust[i];
+      named_bar_sync(1, kRxThreads);
+      for (int i = tid; i < Cn; i += kRxThreads) {
+        const uint64_t ci = rk[i];
+        int better = 0;
+        for (int j = 0; j < Cn; ++j) better += (rk[j] > ci) ? 1 : 0;
+        if (better == need - 1) *reinterpret_cast<uint64_t*>(scr + 84) = ci;
+      }
+      named_bar_sync(1, kRxThreads);
+      prefix = *reinterpret_cast<const uint64_t*>(scr + 84);
+      mask = ~0ull;
+    } else if (need < Cn) {
+      // many: exact radix select below the bin, 11-bit digits over composite bits 51..0
+      int remaining = need;
+      const int shifts[5] = {41, 30, 19, 8, 0};
+      const int widths[5] = {11, 11, 11, 11, 8};
+      constexpr int kDigitBins = 2048, kPerD = kDigitBins / kRxThreads;   // 4 bins per thread, high first
+      for (int d = 0; d < 5; ++d) {
+        const int sh = shifts[d];
+        const uint32_t wm = (1u << widths[d]) - 1u;
+        for (int i = tid; i < kDigitBins; i += kRxThreads) hist[i] = 0u;
+        named_bar_sync(1, kRxThreads);
+        for (int i = tid; i < U; i += kRxThreads) {
+          const uint64_t comp = ust[i];
+          if ((comp & mask) == prefix) atomicAdd(hist + ((comp >> sh) & wm), 1u);
+        }
+        named_bar_sync(1, kRxThreads);
+        const int dtop = kDigitBins - kPerD * (tid + 1);
+        int dc[kPerD], dl = 0;
+#pragma unroll
+        for (int i = 0; i < kPerD; ++i) {
+          dc[i] = (int)hist[dtop + kPerD - 1 - i];
+          dl += dc[i];
+        }
+        int dtot;
+        const int dex = excl_scan(dl, scr, 1, kRxThreads, &dtot, tid);
+        if (dex < remaining && dex + dl >= remaining) {
+          int run = dex;
+#pragma unroll
+          for (int i = 0; i < kPerD; ++i) {
+            if (run + dc[i] >= remaining) {
+              scr[80] = dtop + kPerD - 1 - i;
+              scr[81] = run;
+              scr[82] = dc[i];
+              break;
+            }
+            run += dc[i];
+          }
+        }
+        named_bar_sync(1, kRxThreads);
+        remaining -= scr[81];
+        prefix |= (uint64_t)scr[80] << sh;
+        mask |= (uint64_t)wm << sh;
+        const bool all_in = (scr[82] == remaining);
+        named_bar_sync(1, kRxThreads);
+        if (all_in) break;
+      }
+    }
+  }
+  for (int i = tid; i < U; i += kRxThreads) {
+    const uint64_t comp = ust[i];
+    if ((comp & mask) >= prefix) {
+      const int c = cta_of(i);
+      atomicAdd(scr + 76 + c, 1);
+      if (c == rank) {
+        const int ls = (int)slot_of(comp) - kSlotsPerCta * rank;
+        atomicOr(sel + (ls >> 5), 1u << (ls & 31));
+      }
+    }
+  }
+  named_bar_sync(1, kRxThreads);
+
+  // ---------------------------------------------------------------- 4. emit this CTA's slots, ascending
+  int off = 0;
+#pragma unroll
+  for (int c = 0; c < kRxCluster; ++c) off += (c < rank) ? scr[76 + c] : 0;
+  uint32_t mine = (sel[tid >> 2] >> (kPerT * (tid & 3))) & 0xFFu;   // local slots 8 tid .. 8 tid + 7
+  int total;
+  int at = off + excl_scan(__popc(mine), scr, 1, kRxThreads, &total, tid);
+  int32_t* out = p.topk_out + (size_t)row * kTopK;
+  const int32_t* pl = pool_row + kSlotsPerCta * rank + kPerT * tid;
+  while (mine) {
+    const int i = __ffs(mine) - 1;
+    mine &= mine - 1u;
+    if (at < kTopK) out[at] = __ldg(pl + i);
+    ++at;
+  }
+  if (rank == 0)
+    for (int j = K + tid; j < kTopK; j += kRxThreads) out[j] = -1;
+}
+
+}  // namespace
+
+cudaError_t launch_reindex(const ReindexParams& p, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(reindex_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRxSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int rows = p.batch * p.nq;
+  return launch_pdl(reindex_kernel, dim3(rows * kRxCluster), dim3(kRxThreads), kRxSmem, s, p);
+}
+
+}  // namespace hsa
