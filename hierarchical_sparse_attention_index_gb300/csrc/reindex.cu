@@ -72,6 +72,17 @@ __device__ __forceinline__ uint64_t comp_of(uint32_t key, uint32_t row_slot) {
 __device__ __forceinline__ uint32_t slot_of(uint64_t comp) { return ~(uint32_t)comp; }
 __device__ __forceinline__ int bin_of(uint64_t comp) { return (int)(comp >> (32 + kHistShift)); }
 
+// Slot in a shared list for each lane with `pred`, from one atomic per warp; every lane calls it.
+__device__ __forceinline__ int warp_append(bool pred, int* counter, int lane) {
+  const uint32_t m = __ballot_sync(0xffffffffu, pred);
+  if (!m) return 0;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(m & ((1u << lane) - 1u));
+}
+
 // Threshold bin of a top-K over `hist` (4096 bins, thread 0 holding the 8 highest): the bin
 // holding the K-th largest key and the count above it into scr[64], scr[65]; -1 and the total
 // when the histogram holds K or fewer. Returns the total. All kRxThreads threads call it.
@@ -190,10 +201,10 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     for (int i = 0; i < kPerT; ++i) {
       const int ls = kPerT * tid + i;
       const float v = sc[ls];
-      if (v == -INFINITY) continue;
       const uint32_t key = order_key(v);
-      if ((int)(key >> kHistShift) >= lthr) {
-        const int j = atomicAdd(scr + 72, 1);
+      const bool pub = (v != -INFINITY) && (int)(key >> kHistShift) >= lthr;
+      const int j = warp_append(pub, scr + 72, lane);
+      if (pub) {
         __stcg(p.xkey + xo + j, key);
         __stcg(p.xslot + xo + j, (uint32_t)ls);
       }
@@ -233,36 +244,59 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   named_bar_sync(1, kRxThreads);
   find_threshold(hist, K, scr, tid);
   const int thr = scr[64], need = K - scr[65];
-  // the cut: element taken iff (comp & mask) >= prefix
+  // The cut: an element is taken iff (comp & mask) >= prefix. Inside the threshold bin, a second
+  // 4096-bin histogram over the next 12 key bits narrows the elements still to be ranked to those
+  // sharing 24 key bits; they are ranked by counting when there are few, by an exact radix
+  // select over the remaining composite bits (key bits 7..0, then the inverted slot) otherwise.
   uint64_t prefix = 0, mask = 0;
-  if (thr >= 0) {
-    const int Cn = (int)hist[thr];
-    prefix = (uint64_t)thr << (32 + kHistShift);
-    mask = (uint64_t)(kHistBins - 1) << (32 + kHistShift);
-    if (need < Cn && Cn <= kRankMax) {
-      // few elements in the threshold bin: the need-th largest of them by counting
+  if (thr >= 0 && need < (int)hist[thr]) {
+    int need_r = need;
+    prefix = (uint64_t)thr << 52;
+    mask = 0xFFFull << 52;
+    named_bar_sync(1, kRxThreads);    // hist[thr] read everywhere
+    for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;
+    named_bar_sync(1, kRxThreads);
+    for (int i = tid; i < U; i += kRxThreads) {
+      const uint64_t comp = ust[i];
+      if ((comp & mask) == prefix) atomicAdd(hist + ((comp >> 40) & 0xFFFu), 1u);
+    }
+    named_bar_sync(1, kRxThreads);
+    find_threshold(hist, need_r, scr, tid);
+    const int thr2 = scr[64];
+    need_r -= scr[65];
+    prefix |= (uint64_t)thr2 << 40;
+    mask |= 0xFFFull << 40;
+    const int Cn2 = (int)hist[thr2];
+    if (need_r < Cn2 && Cn2 <= kRankMax) {
+      // few left: the need_r-th largest of them by counting
       uint64_t* rk = reinterpret_cast<uint64_t*>(sc);             // the scores are published
-      for (int i = tid; i < U; i += kRxThreads)
-        if (bin_of(ust[i]) == thr) rk[atomicAdd(scr + 73, 1)] = ust[i];
+      for (int i0 = warp * 32; i0 < U; i0 += kRxThreads) {
+        const int i = i0 + lane;
+        const uint64_t comp = (i < U) ? ust[i] : 0ull;
+        const bool in = (i < U) && (comp & mask) == prefix;
+        const int j = warp_append(in, scr + 73, lane);
+        if (in) rk[j] = comp;
+      }
       named_bar_sync(1, kRxThreads);
-      for (int i = tid; i < Cn; i += kRxThreads) {
+      for (int i = tid; i < Cn2; i += kRxThreads) {
         const uint64_t ci = rk[i];
         int better = 0;
-        for (int j = 0; j < Cn; ++j) better += (rk[j] > ci) ? 1 : 0;
-        if (better == need - 1) *reinterpret_cast<uint64_t*>(scr + 84) = ci;
+        for (int j = 0; j < Cn2; ++j) better += (rk[j] > ci) ? 1 : 0;
+        if (better == need_r - 1) *reinterpret_cast<uint64_t*>(scr + 84) = ci;
       }
       named_bar_sync(1, kRxThreads);
       prefix = *reinterpret_cast<const uint64_t*>(scr + 84);
       mask = ~0ull;
-    } else if (need < Cn) {
-      // many: exact radix select below the bin, 11-bit digits over composite bits 51..0
-      int remaining = need;
-      const int shifts[5] = {41, 30, 19, 8, 0};
-      const int widths[5] = {11, 11, 11, 11, 8};
+    } else if (need_r < Cn2) {
+      // many left (ties in 24 key bits): exact radix select, 11-bit digits over composite bits 39..0
+      int remaining = need_r;
+      const int shifts[4] = {29, 18, 7, 0};
+      const int widths[4] = {11, 11, 11, 7};
       constexpr int kDigitBins = 2048, kPerD = kDigitBins / kRxThreads;   // 4 bins per thread, high first
-      for (int d = 0; d < 5; ++d) {
+      for (int d = 0; d < 4; ++d) {
         const int sh = shifts[d];
         const uint32_t wm = (1u << widths[d]) - 1u;
+        named_bar_sync(1, kRxThreads);
         for (int i = tid; i < kDigitBins; i += kRxThreads) hist[i] = 0u;
         named_bar_sync(1, kRxThreads);
         for (int i = tid; i < U; i += kRxThreads) {
@@ -301,6 +335,9 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
         if (all_in) break;
       }
     }
+  } else if (thr >= 0) {
+    prefix = (uint64_t)thr << 52;     // every element of the threshold bin is taken
+    mask = 0xFFFull << 52;
   }
   for (int i = tid; i < U; i += kRxThreads) {
     const uint64_t comp = ust[i];
