@@ -207,8 +207,8 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
     rp.w = w;
     rp.vis = vis;
     rp.pool = pool;
-    rp.xkey = reinterpret_cast<uint32_t*>(W + L.off_pscores);
-    rp.xslot = reinterpret_cast<uint32_t*>(W + L.off_cand_pool);
+    rp.xlist_lo = reinterpret_cast<uint64_t*>(W + L.off_pscores);
+    rp.xlist_hi = reinterpret_cast<uint64_t*>(W + L.off_cand_pool);
     rp.xcount = reinterpret_cast<int32_t*>(W + L.off_sure_pool);
     rp.ld_xcount = kTopK;
     rp.topk_out = topk_out;

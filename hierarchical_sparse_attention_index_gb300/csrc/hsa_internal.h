@@ -100,8 +100,8 @@ struct ReindexParams {
   const float* w;        // [B][nq][16]
   const int32_t* vis;    // [B][nq]
   const int32_t* pool;   // [B][nq][16384]
-  uint32_t* xkey;        // workspace [rows][4 CTAs][4096]: order keys of the elements each CTA publishes
-  uint32_t* xslot;       // workspace [rows][4 CTAs][4096]: their CTA-local slots
+  uint64_t* xlist_lo;    // workspace [rows][4 CTAs][2048]: entries 0..2047 of the (key, slot) lists the CTAs publish
+  uint64_t* xlist_hi;    // workspace [rows][4 CTAs][2048]: entries 2048..4095 of the same lists
   int32_t* xcount;       // workspace: CTA c of row r publishes (count, valid elements) at xcount[r * ld_xcount + 2c]
   int64_t ld_xcount;
   int32_t* topk_out;     // [B][nq][512]

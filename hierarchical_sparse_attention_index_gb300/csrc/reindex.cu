@@ -138,7 +138,6 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
 
   const int vis = __ldg(p.vis + row);
   const int32_t* pool_row = p.pool + (size_t)row * kPool;
-  if (tid < 256) stage_query(p.q + (size_t)row * kHIdx * kDIdx, p.w + (size_t)row * kHIdx, bfrag, wsc, tid);
 
   // ---------------------------------------------------------------- 1. score this warp's 256 slots
   const int slot0 = kSlotsPerCta * rank + kSlotsPerWarp * warp;   // first slot (row-relative) of the warp
@@ -153,9 +152,11 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     gather_runs(p.ik_q, p.ik_s, ebase, p.cap, vis, pv, lane, dc, dc + kGrpCodes, slots + rs * 32, p.status);
   };
   {
+    // the prologue's pool values go in flight before the query is staged
     int pv0[kRxRing - 1];
 #pragma unroll
     for (int k = 0; k < kRxRing - 1; ++k) pv0[k] = pool_val(k);
+    if (tid < 256) stage_query(p.q + (size_t)row * kHIdx * kDIdx, p.w + (size_t)row * kHIdx, bfrag, wsc, tid);
 #pragma unroll
     for (int k = 0; k < kRxRing - 1; ++k) gather(k, pv0[k]);
   }
@@ -195,21 +196,36 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   // 84..85 the cut composite of the rank count
   const int nval_local = find_threshold(hist, kTopK, scr, tid);
   const int lthr = scr[64];
+  // list entry j of CTA c: its composite, at entry j of [row][c][2048] in the first region for
+  // j < 2048, else at entry j - 2048 of the second
+  auto list_at = [&](int c, int j) -> uint64_t* {
+    uint64_t* base = (j < kSlotsPerCta / 2) ? p.xlist_lo : p.xlist_hi;
+    return base + ((size_t)row * kRxCluster + c) * (kSlotsPerCta / 2) + (j & (kSlotsPerCta / 2 - 1));
+  };
   {
-    const size_t xo = ((size_t)row * kRxCluster + rank) * kSlotsPerCta;
+    // the warp's 8 rounds of appends take one atomic: round i's lanes follow rounds 0..i-1
+    uint32_t keys[kPerT], bal[kPerT];
+    int n = 0;
 #pragma unroll
     for (int i = 0; i < kPerT; ++i) {
-      const int ls = kPerT * tid + i;
-      const float v = sc[ls];
-      const uint32_t key = order_key(v);
-      const bool pub = (v != -INFINITY) && (int)(key >> kHistShift) >= lthr;
-      const int j = warp_append(pub, scr + 72, lane);
-      if (pub) {
-        __stcg(p.xkey + xo + j, key);
-        __stcg(p.xslot + xo + j, (uint32_t)ls);
-      }
+      const float v = sc[kPerT * tid + i];
+      keys[i] = order_key(v);
+      bal[i] = __ballot_sync(0xffffffffu, (v != -INFINITY) && (int)(keys[i] >> kHistShift) >= lthr);
+      n += __popc(bal[i]);
+    }
+    int base = 0;
+    if (lane == 0 && n) base = atomicAdd(scr + 72, n);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < kPerT; ++i) {
+      if ((bal[i] >> lane) & 1u)
+        __stcg(list_at(rank, base + __popc(bal[i] & lt)),
+               comp_of(keys[i], (uint32_t)(kSlotsPerCta * rank + kPerT * tid + i)));
+      base += __popc(bal[i]);
     }
   }
+  for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;   // read by find_threshold above
   named_bar_sync(1, kRxThreads);
   if (tid == 0) {
     __stcg(p.xcount + (size_t)row * p.ld_xcount + 2 * rank, scr[72]);
@@ -218,12 +234,24 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   rx_cluster_sync();                  // the four lists are in L2
 
   // ---------------------------------------------------------------- 3. the row's top-K over the union
+  // the first kSpec entries a thread may need of each list are loaded with the counts, before
+  // the counts are known (entries past a count are ignored)
+  constexpr int kSpec = 2;
+  int cnt[kRxCluster], nv[kRxCluster];
+  uint64_t spec[kRxCluster][kSpec];
+#pragma unroll
+  for (int c = 0; c < kRxCluster; ++c) {
+    cnt[c] = __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c);
+    nv[c] = __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c + 1);
+#pragma unroll
+    for (int sp = 0; sp < kSpec; ++sp) spec[c][sp] = __ldcg(list_at(c, tid + kRxThreads * sp));
+  }
   int ubase[kRxCluster], U = 0, nvalid = 0;
 #pragma unroll
   for (int c = 0; c < kRxCluster; ++c) {
     ubase[c] = U;
-    U += __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c);
-    nvalid += __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c + 1);
+    U += cnt[c];
+    nvalid += nv[c];
   }
   const int K = min(kTopK, nvalid);
   auto cta_of = [&](int i) {
@@ -233,14 +261,22 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     return c;
   };
   uint64_t* ust = reinterpret_cast<uint64_t*>(rsm + kOffRing);   // the rings are free now
-  for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;
-  for (int i = tid; i < U; i += kRxThreads) {
-    const int c = cta_of(i);
-    const size_t xo = ((size_t)row * kRxCluster + c) * kSlotsPerCta + (size_t)(i - ubase[c]);
-    ust[i] = comp_of(__ldcg(p.xkey + xo), (uint32_t)(kSlotsPerCta * c) + __ldcg(p.xslot + xo));
+#pragma unroll
+  for (int c = 0; c < kRxCluster; ++c) {
+#pragma unroll
+    for (int sp = 0; sp < kSpec; ++sp) {
+      const int j = tid + kRxThreads * sp;
+      if (j < cnt[c]) {
+        ust[ubase[c] + j] = spec[c][sp];
+        atomicAdd(hist + bin_of(spec[c][sp]), 1u);
+      }
+    }
+    for (int j = tid + kRxThreads * kSpec; j < cnt[c]; j += kRxThreads) {
+      const uint64_t comp = __ldcg(list_at(c, j));
+      ust[ubase[c] + j] = comp;
+      atomicAdd(hist + bin_of(comp), 1u);
+    }
   }
-  named_bar_sync(1, kRxThreads);
-  for (int i = tid; i < U; i += kRxThreads) atomicAdd(hist + bin_of(ust[i]), 1u);
   named_bar_sync(1, kRxThreads);
   find_threshold(hist, K, scr, tid);
   const int thr = scr[64], need = K - scr[65];
@@ -339,15 +375,23 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     prefix = (uint64_t)thr << 52;     // every element of the threshold bin is taken
     mask = 0xFFFull << 52;
   }
-  for (int i = tid; i < U; i += kRxThreads) {
-    const uint64_t comp = ust[i];
-    if ((comp & mask) >= prefix) {
+  {
+    int taken_c[kRxCluster] = {0, 0, 0, 0};   // per CTA, taken elements seen by this warp
+    for (int i0 = warp * 32; i0 < U; i0 += kRxThreads) {
+      const int i = i0 + lane;
+      const uint64_t comp = (i < U) ? ust[i] : 0ull;
+      const bool taken = (i < U) && (comp & mask) >= prefix;
       const int c = cta_of(i);
-      atomicAdd(scr + 76 + c, 1);
-      if (c == rank) {
+#pragma unroll
+      for (int d = 0; d < kRxCluster; ++d) taken_c[d] += __popc(__ballot_sync(0xffffffffu, taken && c == d));
+      if (taken && c == rank) {
         const int ls = (int)slot_of(comp) - kSlotsPerCta * rank;
         atomicOr(sel + (ls >> 5), 1u << (ls & 31));
       }
+    }
+    if (lane < kRxCluster) {
+      const int v = (lane == 0) ? taken_c[0] : (lane == 1) ? taken_c[1] : (lane == 2) ? taken_c[2] : taken_c[3];
+      if (v) atomicAdd(scr + 76 + lane, v);
     }
   }
   named_bar_sync(1, kRxThreads);
