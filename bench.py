@@ -218,8 +218,14 @@ def per_kernel_times(H, torch, I, reps=10):
 # time of the capture: once the source changes, the figure no longer applies and is reported
 # as null.
 NCU_TRAFFIC = {
-    "sparse_attn_decode": ("attn.cu", "291044a3ab222a32bad92ce072ef29837370ca7bad555d98653430ee1321138b", 10602496,
+    # kernel: (sources it is built from, sha256 over them in order, dram read + write bytes of one
+    # launch from one ncu capture, the profile summary); the figure is dropped once a source changes
+    "sparse_attn_decode": (('attn.cu', 'hsa_tc.cuh'), "939b1e82415d13e473ac1c4977eae49fbd72a547845da29a15c16d59b4921021", 10603008,
                            "profiles/sparse_attn_b32_t128k.md"),
+    "index_reindex": (('reindex.cu', 'hsa_score.cuh'), "9d79813cfe991d3419f74057afc75224e988ce812d09cbb3578fb2d8583adf97", 43334400,
+                      "profiles/reindex_kernel_b32_t128k.md"),
+    "cache_write_m2": (('write.cu', 'hsa_tc.cuh'), "899e2950b450a5084d68505b66c5ff4957b27303871e98a48d5925231560e876", 140035584,
+                       "profiles/cache_write_m2_3x65536.md"),
 }
 
 
@@ -228,14 +234,15 @@ def ncu_traffic(kernel):
     rec = NCU_TRAFFIC.get(kernel)
     if rec is None:
         return None, None
-    fname, digest, traffic, src = rec
-    path = os.path.join(ROOT, "hierarchical_sparse_attention_index_gb300", "csrc", fname)
+    files, digest, traffic, src = rec
+    d = hashlib.sha256()
     try:
-        with open(path, "rb") as f:
-            now = hashlib.sha256(f.read()).hexdigest()
+        for fname in files:
+            with open(os.path.join(ROOT, "hierarchical_sparse_attention_index_gb300", "csrc", fname), "rb") as f:
+                d.update(f.read())
     except OSError:
         return None, None
-    return (traffic, src) if now == digest else (None, None)
+    return (traffic, src) if d.hexdigest() == digest else (None, None)
 
 
 def run_hsa(args):
@@ -356,10 +363,12 @@ def cache_write_m2(H, torch, hbm_peak, peak_src, reps=5):
     t_layer = 1e-3 * e0.elapsed_time(e1) / (reps * len(layers))
     bytes_layer = n * 2 * 512 * 2 + (n // 2) * 356
     ach = bytes_layer / t_layer / 1e9
+    traffic, traffic_src = ncu_traffic("cache_write_m2")
     return {"workload": f"m2 write, {len(layers)} layers x {n} tokens", "us_per_layer": round(1e6 * t_layer, 2),
             "tokens_per_s": round(n / t_layer, 1), "bytes_per_layer": bytes_layer,
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(ach / hbm_peak, 4), "peak_source": peak_src}}
+                         "frac": round(ach / hbm_peak, 4), "traffic": traffic, "traffic_source": traffic_src,
+                         "peak_source": peak_src}}
 
 
 def run_e2e(H, torch, I, args, world, barrier, st):

@@ -88,17 +88,16 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   L->off_hist_full = take((size_t)rows * 2 * kHistBins * 4);
   L->off_state_full = take((size_t)rows * 2 * sizeof(SelState));
   L->off_done_full = take((size_t)batch * 4);
-  L->off_hist_pool = take((size_t)rows * kHistBins * 4);
-  L->off_state_pool = take((size_t)rows * sizeof(SelState));
-  L->off_done_pool = take((size_t)rows * 4);
   L->zero_end = o;
   L->off_scores = take((size_t)rows * L->ld_s * 4);
   L->off_blkmax = take((size_t)rows * L->ld_b * 4);
   L->off_cand_full = take((size_t)rows * (L->ld_s + L->ld_b) * 4);
   L->off_sure_full = take((size_t)rows * (kTopK + kCandBlocks) * 4);
-  L->off_pscores = take((size_t)rows * kPool * 4);
-  L->off_cand_pool = take((size_t)rows * kPool * 4);
-  L->off_sure_pool = take((size_t)rows * kTopK * 4);
+  // fused Reindex: per row, the 4 CTAs' lists of 64-bit (key, slot) composites (entries 0..2047
+  // and 2048..4095 of each) and their (count, valid elements) pairs
+  L->off_rx_lo = take((size_t)rows * kPool / 2 * 8);
+  L->off_rx_hi = take((size_t)rows * kPool / 2 * 8);
+  L->off_rx_count = take((size_t)rows * 2 * kRxSplit * 4);
   // attention partials: per row, 4 CTAs x (64 x 512 unnormalised outputs + 64 (max, sum) pairs)
   L->attn_bytes = (size_t)rows * kAttnSplit * (kHAtt * kDLat + 2 * kHAtt) * 4;
   L->off_attn = take(L->attn_bytes);
@@ -194,8 +193,7 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
 
   if (pool_mode) {
     // one fused launch: rescoring over the pool and the exact top-512, one cluster per row; the
-    // keys, slots and counts its CTAs exchange live in the Reindex score, candidate and sure
-    // regions of the workspace
+    // lists and counts its CTAs exchange live in the workspace's Reindex regions
     ReindexParams rp;
     memset(&rp, 0, sizeof(rp));
     rp.batch = cache->batch;
@@ -207,10 +205,10 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
     rp.w = w;
     rp.vis = vis;
     rp.pool = pool;
-    rp.xlist_lo = reinterpret_cast<uint64_t*>(W + L.off_pscores);
-    rp.xlist_hi = reinterpret_cast<uint64_t*>(W + L.off_cand_pool);
-    rp.xcount = reinterpret_cast<int32_t*>(W + L.off_sure_pool);
-    rp.ld_xcount = kTopK;
+    rp.xlist_lo = reinterpret_cast<uint64_t*>(W + L.off_rx_lo);
+    rp.xlist_hi = reinterpret_cast<uint64_t*>(W + L.off_rx_hi);
+    rp.xcount = reinterpret_cast<int32_t*>(W + L.off_rx_count);
+    rp.ld_xcount = 2 * kRxSplit;
     rp.topk_out = topk_out;
     rp.status = status;
     return cuda_fail(launch_reindex(rp, s), "reindex launch");
@@ -218,7 +216,6 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
 
   ScanParams sp;
   memset(&sp, 0, sizeof(sp));
-  sp.pool_mode = pool_mode ? 1 : 0;
   sp.batch = cache->batch;
   sp.nq = nq;
   sp.cap = cache->capacity;
@@ -227,53 +224,36 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
   sp.q = static_cast<const uint16_t*>(q);
   sp.w = w;
   sp.vis = vis;
-  sp.pool = pool;
   sp.status = status;
+  sp.n_seg = cache->batch;
+  sp.chunks_per_seg = (int32_t)((std::max(max_vis, (int64_t)1) + kScanChunk - 1) / kScanChunk);
+  sp.total_items = sp.n_seg * sp.chunks_per_seg;
+  sp.scores = reinterpret_cast<float*>(W + L.off_scores);
+  sp.ld_s = L.ld_s;
+  sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
+  sp.ld_b = L.ld_b;
+  sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_full);
+  sp.state = reinterpret_cast<SelState*>(W + L.off_state_full);
+  sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_full);
   SelectParams se;
   memset(&se, 0, sizeof(se));
-  se.pool_mode = sp.pool_mode;
   se.batch = cache->batch;
   se.nq = nq;
   se.max_vis = max_vis;
   se.vis = vis;
-  se.pool = pool;
   se.topk_out = topk_out;
   se.pool_out = pool_out;
   se.status = status;
-  if (!pool_mode) {
-    sp.n_seg = cache->batch;
-    sp.chunks_per_seg = (int32_t)((std::max(max_vis, (int64_t)1) + kScanChunk - 1) / kScanChunk);
-    sp.scores = reinterpret_cast<float*>(W + L.off_scores);
-    sp.ld_s = L.ld_s;
-    sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
-    sp.ld_b = L.ld_b;
-    sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_full);
-    sp.state = reinterpret_cast<SelState*>(W + L.off_state_full);
-    sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_full);
-    se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_full);
-    se.ld_cand = L.ld_s + L.ld_b;
-    se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_full);
-    se.ld_sure = kTopK + kCandBlocks;
-  } else {
-    sp.n_seg = L.rows;
-    sp.chunks_per_seg = kPool / kScanChunk;
-    sp.scores = reinterpret_cast<float*>(W + L.off_pscores);
-    sp.ld_s = kPool;
-    sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_pool);
-    sp.state = reinterpret_cast<SelState*>(W + L.off_state_pool);
-    sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_pool);
-    se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_pool);
-    se.ld_cand = kPool;
-    se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_pool);
-    se.ld_sure = kTopK;
-  }
-  sp.total_items = sp.n_seg * sp.chunks_per_seg;
   se.scores = sp.scores;
   se.ld_s = sp.ld_s;
   se.blkmax = sp.blkmax;
   se.ld_b = sp.ld_b;
   se.hist = sp.hist;
   se.state = sp.state;
+  se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_full);
+  se.ld_cand = L.ld_s + L.ld_b;
+  se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_full);
+  se.ld_sure = kTopK + kCandBlocks;
   hsa_status r = cuda_fail(launch_index_scan(sp, sms, s), "index scan launch");
   if (r != HSA_OK) return r;
   return cuda_fail(launch_select(se, s), "select launch");

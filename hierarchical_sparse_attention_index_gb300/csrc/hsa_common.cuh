@@ -26,6 +26,7 @@ constexpr int kHistBins = 4096;        // top 12 bits of the order key
 constexpr int kScanChunk = 512;        // entries per pipeline stage of the scoring kernel
 constexpr int kHistShift = 20;
 constexpr int kAttnSplit = 4;          // attention CTAs (one cluster) per (request, query)
+constexpr int kRxSplit = 4;            // fused Reindex CTAs (one cluster) per (request, query)
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

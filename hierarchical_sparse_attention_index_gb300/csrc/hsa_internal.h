@@ -29,7 +29,7 @@ struct WsLayout {
   int64_t ld_s;        // score row stride (positions), a multiple of kScanChunk
   int64_t ld_b;        // block-max row stride (blocks) = ld_s / 8
   size_t off_scores, off_blkmax, off_hist_full, off_cand_full, off_sure_full, off_state_full, off_done_full;
-  size_t off_pscores, off_hist_pool, off_cand_pool, off_sure_pool, off_state_pool, off_done_pool;
+  size_t off_rx_lo, off_rx_hi, off_rx_count;   // fused Reindex exchange lists and counts
   size_t off_attn;     // attention partials
   size_t attn_bytes;
   size_t zero_begin, zero_end;   // region that must be zero between calls (hist + state + counters)
@@ -43,8 +43,7 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L);
 bool device_status_ptr(uint32_t** status, int* sms);
 
 // ------------------------------------------------------------------ index scoring
-struct ScanParams {
-  int32_t pool_mode;     // 0: Full (segment = request, nq queries share K); 1: Reindex (segment = (b,q))
+struct ScanParams {         // Full mode: a segment is one request, its nq queries share K
   int32_t batch, nq;
   int64_t cap;
   const uint8_t* ik_q;
@@ -52,38 +51,35 @@ struct ScanParams {
   const uint16_t* q;     // bf16 [B][nq][16][128]
   const float* w;        // [B][nq][16]
   const int32_t* vis;    // [B][nq]
-  const int32_t* pool;   // Reindex: [B][nq][16384]
   int32_t n_seg;
   int32_t chunks_per_seg;
   int32_t total_items;
-  float* scores;         // Full: [rows][ld_s]; Reindex: [rows][16384]
+  float* scores;         // [rows][ld_s]
   int64_t ld_s;
-  float* blkmax;         // Full: [rows][ld_b]
+  float* blkmax;         // [rows][ld_b]
   int64_t ld_b;
-  uint32_t* hist;        // Full: [rows][2][4096]; Reindex: [rows][4096]
-  SelState* state;       // Full: [rows][2]; Reindex: [rows]
+  uint32_t* hist;        // [rows][2][4096]
+  SelState* state;       // [rows][2]
   uint32_t* seg_done;    // [n_seg]
   uint32_t* status;
 };
 
-struct SelectParams {
-  int32_t pool_mode;
+struct SelectParams {       // the Full step's position top-512 and block top-2048
   int32_t batch, nq;
   int64_t max_vis;
   const int32_t* vis;
-  const int32_t* pool;   // Reindex: slot -> position
   const float* scores;
   int64_t ld_s;
   const float* blkmax;
   int64_t ld_b;
   uint32_t* hist;
   SelState* state;
-  int32_t* cand;         // Full: [rows][ld_s + ld_b]; Reindex: [rows][16384]
+  int32_t* cand;         // [rows][ld_s + ld_b]
   int64_t ld_cand;
-  int32_t* sure;         // Full: [rows][512 + 2048]; Reindex: [rows][512]
+  int32_t* sure;         // [rows][512 + 2048]
   int64_t ld_sure;
   int32_t* topk_out;     // [rows][512]
-  int32_t* pool_out;     // Full: [rows][16384]
+  int32_t* pool_out;     // [rows][16384]
   uint32_t* status;
 };
 

@@ -1,10 +1,10 @@
-// Indexer kernels: FP4 indexer-K scoring (Full scan and Reindex pool rescoring) and the exact
-// top-k selection behind both ([CED] Figure 5; [ARCH] §3.3; [COST] §3.2; [10100] 层次化稀疏索引器).
+// Full-mode indexer kernels: FP4 indexer-K scoring over every visible position and the exact
+// top-k selections behind it ([CED] Figure 5; [ARCH] §3.3; [COST] §3.2; [10100] 层次化稀疏索引器).
+// The Reindex pass has its own fused kernel (reindex.cu).
 //
 // Scoring, s_t = sum_h w_h ReLU(q_h . k_t):
-//  - One producer warp streams 256-entry stages of indexer K into a 4-deep shared-memory ring
-//    with bulk async copies (contiguous rows for Full; 8-entry runs gathered through the pool
-//    for Reindex). Eight consumer warps score them.
+//  - One producer warp streams 512-entry stages of indexer K into a 3-deep shared-memory ring
+//    with bulk async copies. Sixteen consumer warps score them.
 //  - Each consumer thread reads its 16-byte chunk of an entry with one shared load. That chunk
 //    holds the entry's bytes in "fragment order" (include/hsa.h). The thread converts E2M1 pairs
 //    to f16x2 with the hardware cvt and feeds them straight into m16n8k16 tensor-core MMAs as
@@ -40,31 +40,20 @@ constexpr int kScanThreads = kConsumers + 32;
 constexpr int kCodesBytes = kChunk * 64;
 constexpr int kScaleBytes = kChunk * 4;
 constexpr int kFlushItems = 120;   // packed 16-bit histogram counters: flush before 65536 entries
-// Reindex: each consumer warp gathers its own 32 pool slots (four 8-entry runs) of the stages
-// ahead into a private ring of kRing buffers with cp.async (16 bytes per lane, 512-byte runs).
-constexpr int kRing = 4;
-constexpr int kWarpCodes = 32 * 64, kWarpScales = 32 * 4, kWarpSlots = 32 * 4;
 
 struct ScanSmemLayout {
   int nst, nlr;
-  size_t codes, scales, slotpos, bfrag, wsc, hist, sfl, bars, misc, total;
+  size_t codes, scales, bfrag, wsc, hist, sfl, bars, misc, total;
 };
 
-__host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq) {
+__host__ __device__ inline ScanSmemLayout scan_smem_layout(int nq) {
   ScanSmemLayout L;
-  const int nql = pool_mode ? 1 : nq;
-  L.nst = pool_mode ? 1 : ((nql <= 2) ? 3 : (nql <= 5 ? 2 : 1));
-  L.nlr = pool_mode ? 1 : 2 * nq;
+  const int nql = nq;
+  L.nst = (nql <= 2) ? 3 : (nql <= 5 ? 2 : 1);
+  L.nlr = 2 * nq;
   size_t o = 0;
-  if (pool_mode) {     // per-warp rings [warp][kRing][...]
-    L.codes = o;   o += (size_t)kConsumerWarps * kRing * kWarpCodes;
-    L.scales = o;  o += (size_t)kConsumerWarps * kRing * kWarpScales;
-    L.slotpos = o; o += (size_t)kConsumerWarps * kRing * kWarpSlots;
-  } else {
-    L.codes = o;   o += (size_t)L.nst * kCodesBytes;
-    L.scales = o;  o += (size_t)L.nst * kScaleBytes;
-    L.slotpos = o;
-  }
+  L.codes = o;   o += (size_t)L.nst * kCodesBytes;
+  L.scales = o;  o += (size_t)L.nst * kScaleBytes;
   L.bfrag = o;   o += (size_t)nql * 2 * 8 * 32 * 2 * 4;
   L.wsc = o;     o += (size_t)nql * 16 * 4;
   L.hist = o;    o += (size_t)L.nlr * (kHistBins / 2) * 4;
@@ -75,14 +64,13 @@ __host__ __device__ inline ScanSmemLayout scan_smem_layout(int pool_mode, int nq
   return L;
 }
 
-// kPoolMode: Reindex (segment = one (request, query) row, entries gathered through the pool);
-// kOneQuery: one query per segment (always in Reindex; nq == 1 in Full).
-template <bool kPoolMode, bool kOneQuery>
+// A segment is one request (its nq queries share the request's indexer K); kOneQuery: nq == 1.
+template <bool kOneQuery>
 __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const ScanSmemLayout L = scan_smem_layout(kPoolMode, p.nq);
+  const ScanSmemLayout L = scan_smem_layout(p.nq);
   const int nql = kOneQuery ? 1 : p.nq;
-  const int nst = kPoolMode ? 1 : (kOneQuery ? 3 : L.nst);   // compile-time where it can be (scan_smem_layout)
+  const int nst = kOneQuery ? 3 : L.nst;   // compile-time where it can be (scan_smem_layout)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last flag, [2..9] vis, [16..48) scratch
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
@@ -113,8 +101,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   const int cps = p.chunks_per_seg;
 
   if (warp == kConsumerWarps) {
-    // ---------------------------------------------------------------- producer warp (Full only)
-    if (kPoolMode) return;
+    // ---------------------------------------------------------------- producer warp
     int s = 0, round = 0, seg = i0 / cps, c = i0 % cps;
     for (int it = i0; it < i1; ++it) {
       if (round > 0) {
@@ -172,9 +159,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   auto flush_hist = [&](int seg) {
     named_bar_sync(1, kConsumers);
     for (int lr = 0; lr < L.nlr; ++lr) {
-      int grow;
-      if (kPoolMode) grow = seg;
-      else grow = (seg * p.nq + (lr >> 1)) * 2 + (lr & 1);
+      const int grow = (seg * p.nq + (lr >> 1)) * 2 + (lr & 1);
       uint32_t* gh = p.hist + (size_t)grow * kHistBins;
       uint32_t* sh = hist_sm + lr * (kHistBins / 2);
       for (int i = tid; i < kHistBins / 2; i += kConsumers) {
@@ -199,15 +184,11 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     named_bar_sync(1, kConsumers);
     if (misc[1]) {
       __threadfence();
-      if (kPoolMode) {
-        compute_threshold<kConsumers>(p.hist + (size_t)seg * kHistBins, kTopK, p.state + seg, scratch);
-      } else {
-        for (int q = 0; q < p.nq; ++q) {
-          const int row = seg * p.nq + q;
-          compute_threshold<kConsumers>(p.hist + (size_t)(2 * row) * kHistBins, kTopK, p.state + 2 * row, scratch);
-          compute_threshold<kConsumers>(p.hist + (size_t)(2 * row + 1) * kHistBins, kCandBlocks, p.state + 2 * row + 1,
-                            scratch);
-        }
+      for (int q = 0; q < p.nq; ++q) {
+        const int row = seg * p.nq + q;
+        compute_threshold<kConsumers>(p.hist + (size_t)(2 * row) * kHistBins, kTopK, p.state + 2 * row, scratch);
+        compute_threshold<kConsumers>(p.hist + (size_t)(2 * row + 1) * kHistBins, kCandBlocks, p.state + 2 * row + 1,
+                                      scratch);
       }
       if (tid == 0) p.seg_done[seg] = 0;
     }
@@ -217,12 +198,11 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   auto load_segment = [&](int seg) {
     named_bar_sync(1, kConsumers);
     for (int ql = 0; ql < nql && tid < 256; ++ql) {
-      const int row = kPoolMode ? seg : seg * p.nq + ql;
+      const int row = seg * p.nq + ql;
       stage_query(p.q + (size_t)row * kHIdx * kDIdx, p.w + (size_t)row * kHIdx, bfrag + ql * kQFragWords,
                   wsc + ql * kQWeights, tid);
-      if (tid < 8 && !kPoolMode && tid == ql) svis[ql] = (int)imin64(__ldg(p.vis + row), p.cap);
+      if (tid < 8 && tid == ql) svis[ql] = (int)imin64(__ldg(p.vis + row), p.cap);
     }
-    if (kPoolMode && tid == 0) svis[0] = __ldg(p.vis + seg);
     named_bar_sync(1, kConsumers);
   };
 
@@ -237,47 +217,6 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   bool dead = false;
   int vmax_seg = 0;                // Full: visible rows of the current request (max over its queries)
 
-  // Reindex: this warp's slots of item k are pool[seg][c * kChunk + warp * 32 + lane]; the
-  // warp gathers their four 8-entry runs itself, kRing - 1 items ahead of the one it scores.
-  int rs = 0;                      // ring buffer of the current item
-  int iseg = seg, ic = c;          // next item whose runs are gathered
-  int lseg = seg, lc = c;          // next item whose pool values are loaded
-  int pv_next = -1;                // pool value (this lane's slot) of the next item to gather
-  const uint32_t ring_codes = smem_u32(smem + L.codes) + (uint32_t)(warp * kRing * kWarpCodes);
-  const uint32_t ring_scales = smem_u32(smem + L.scales) + (uint32_t)(warp * kRing * kWarpScales);
-  int* const ring_slots = reinterpret_cast<int*>(smem + L.slotpos) + warp * kRing * 32;
-  auto pool_val = [&](int sg, int ch) -> int {
-    return __ldg(p.pool + (int64_t)sg * kPool + ch * kChunk + warp * 32 + lane);
-  };
-  auto advance = [&](int& sg, int& ch) {
-    if (++ch == cps) {
-      ch = 0;
-      ++sg;
-    }
-  };
-  auto gather = [&](int sg, int slot, int pv) {
-    gather_runs(p.ik_q, p.ik_s, (int64_t)(sg / p.nq) * p.cap, p.cap, __ldg(p.vis + sg), pv, lane,
-                ring_codes + (uint32_t)(slot * kWarpCodes), ring_scales + (uint32_t)(slot * kWarpScales),
-                ring_slots + slot * 32, p.status);
-  };
-  if (kPoolMode) {
-    int pv0[kRing - 1], sg0[kRing - 1];
-#pragma unroll
-    for (int j = 0; j < kRing - 1; ++j) {
-      pv0[j] = (i0 + j < i1) ? pool_val(lseg, lc) : -1;
-      sg0[j] = lseg;
-      advance(lseg, lc);
-    }
-#pragma unroll
-    for (int j = 0; j < kRing - 1; ++j) {
-      if (i0 + j < i1) gather(sg0[j], j, pv0[j]);
-      else cp_async_commit();
-      advance(iseg, ic);
-    }
-    pv_next = (i0 + kRing - 1 < i1) ? pool_val(lseg, lc) : -1;
-    advance(lseg, lc);
-  }
-
   for (int it = i0; it < i1; ++it) {
     if (seg != cur_seg) {
       if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
@@ -286,44 +225,25 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       since_flush = 0;
       load_segment(seg);
       if (nql == 1) load_query_regs(0);
-      if (!kPoolMode) {
-        int vmax = 0;
-        for (int q = 0; q < nql; ++q) vmax = max(vmax, svis[q]);
-        vmax_seg = vmax;           // svis is already capped at the capacity
-      }
+      int vmax = 0;
+      for (int q = 0; q < nql; ++q) vmax = max(vmax, svis[q]);
+      vmax_seg = vmax;             // svis is already capped at the capacity
     } else if (since_flush >= kFlushItems) {
       flush_hist(seg);
       since_flush = 0;
     }
     ++seg_items;
     ++since_flush;
-    uint32_t codes, scales;
-    const int* slotpos = nullptr;
-    int row_off;                   // first row of this warp inside the buffer it reads
-    if (kPoolMode) {
-      if (it + kRing - 1 < i1) gather(iseg, rs == 0 ? kRing - 1 : rs - 1, pv_next);
-      else cp_async_commit();
-      advance(iseg, ic);
-      pv_next = (it + kRing < i1) ? pool_val(lseg, lc) : -1;
-      advance(lseg, lc);
-      cp_async_wait<kRing - 1>();  // this item's runs have landed
-      __syncwarp();
-      codes = ring_codes + (uint32_t)(rs * kWarpCodes);
-      scales = ring_scales + (uint32_t)(rs * kWarpScales);
-      slotpos = ring_slots + rs * 32;
-      row_off = 0;
-    } else {
-      if (!dead && *reinterpret_cast<volatile int*>(misc) != 0) dead = true;
-      if (!dead && !mbar_wait(full0 + 8 * s, ph)) {
-        flag_status(p.status, HSA_FLAG_TIMEOUT);
-        *reinterpret_cast<volatile int*>(misc) = 1;
-        dead = true;
-      }
-      codes = smem_u32(smem + L.codes) + (uint32_t)s * kCodesBytes;
-      scales = smem_u32(smem + L.scales) + (uint32_t)s * kScaleBytes;
-      row_off = warp * 32;
+    if (!dead && *reinterpret_cast<volatile int*>(misc) != 0) dead = true;
+    if (!dead && !mbar_wait(full0 + 8 * s, ph)) {
+      flag_status(p.status, HSA_FLAG_TIMEOUT);
+      *reinterpret_cast<volatile int*>(misc) = 1;
+      dead = true;
     }
-    const int nrows = dead ? 0 : (kPoolMode ? kChunk : max(0, min(kChunk, vmax_seg - c * kChunk)));
+    const uint32_t codes = smem_u32(smem + L.codes) + (uint32_t)s * kCodesBytes;
+    const uint32_t scales = smem_u32(smem + L.scales) + (uint32_t)s * kScaleBytes;
+    const int row_off = warp * 32;   // first row of this warp inside the stage
+    const int nrows = dead ? 0 : max(0, min(kChunk, vmax_seg - c * kChunk));
 
     if (warp * 32 < nrows) {
       const bool two = warp * 32 + 16 < nrows;        // the warp's second 16-row tile holds data
@@ -335,15 +255,10 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       for (int ql = 0; ql < nql; ++ql) {
         if (nql > 1) load_query_regs(ql);
         float v = score_rows32(codes, row_off, sf_base, two, B, wr, lane);
-        bool ok;
-        if (!kPoolMode) {
-          ok = c * kChunk + r_mine < svis[ql];
-        } else {
-          ok = slotpos[8 * t + g] >= 0;
-        }
+        const bool ok = c * kChunk + r_mine < svis[ql];
         v = ok ? v : -INFINITY;
         const uint32_t bin = order_key(v) >> kHistShift;
-        if (!kPoolMode) {
+        {
           const int row = cur_seg * p.nq + ql;
           p.scores[(size_t)row * p.ld_s + c * kChunk + r_mine] = v;
           if (ok) atomicAdd(hist_sm + (2 * ql) * (kHistBins / 2) + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
@@ -358,21 +273,14 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
             const uint32_t bb = order_key(bm) >> kHistShift;
             atomicAdd(hist_sm + (2 * ql + 1) * (kHistBins / 2) + (bb >> 1), (bb & 1) ? 0x10000u : 1u);
           }
-        } else {
-          p.scores[(size_t)cur_seg * kPool + c * kChunk + r_mine] = v;
-          if (ok) atomicAdd(hist_sm + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
         }
       }
     }
     __syncwarp();
-    if (!kPoolMode) {
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      if (++s == nst) {
-        s = 0;
-        ph ^= 1u;
-      }
-    } else if (++rs == kRing) {
-      rs = 0;
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (++s == nst) {
+      s = 0;
+      ph ^= 1u;
     }
     if (++c == cps) {
       c = 0;
@@ -430,11 +338,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   const float* data;
   int n, K;
   int64_t cand_off = 0;
-  if (p.pool_mode) {
-    data = p.scores + (size_t)row * kPool;
-    n = kPool;
-    K = kTopK;
-  } else if (which == 0) {
+  if (which == 0) {
     data = p.scores + (size_t)row * p.ld_s;
     n = vis;
     K = kTopK;
@@ -444,7 +348,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
     K = kCandBlocks;
     cand_off = p.ld_s;
   }
-  SelState* st = p.state + (p.pool_mode ? row : 2 * row + which);
+  SelState* st = p.state + 2 * row + which;
   const int nwords = (max(n, 1) + 31) >> 5;
   uint32_t* bitmap = fsm;                       // [nwords]
   uint32_t* shist = fsm + ((nwords + 3) & ~3);  // [2048]
@@ -452,7 +356,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   int* s_cidx = scratch + 64;                   // [kFinStage]
   uint32_t* s_ckey = reinterpret_cast<uint32_t*>(s_cidx + kFinStage);   // [kFinStage]
   int* gcand = p.cand + (size_t)row * p.ld_cand + cand_off;              // overflow candidates
-  const int gcap = (int)(p.pool_mode ? kPool : (which == 0 ? p.ld_s : p.ld_b));
+  const int gcap = (int)(which == 0 ? p.ld_s : p.ld_b);
 
   __shared__ int s_thr, s_nvalid, s_ready, s_ncand, s_nsure;
   __shared__ int s_digit, s_above, s_cnt;
@@ -579,20 +483,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   for (int i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
   int total;
   int o = block_excl_scan_1024(cnt, scratch, &total);
-  if (p.pool_mode) {
-    int32_t* out = p.topk_out + (size_t)row * kTopK;
-    const int32_t* pl = p.pool + (size_t)row * kPool;
-    for (int i = w0; i < w1; ++i) {
-      uint32_t m = bitmap[i];
-      while (m) {
-        const int b = __ffs(m) - 1;
-        m &= m - 1;
-        if (o < kTopK) out[o] = __ldg(pl + i * 32 + b);
-        ++o;
-      }
-    }
-    for (int j = total + tid; j < kTopK; j += kSelThreads) out[j] = -1;
-  } else if (which == 0) {
+  if (which == 0) {
     int32_t* out = p.topk_out + (size_t)row * kTopK;
     for (int i = w0; i < w1; ++i) {
       uint32_t m = bitmap[i];
@@ -632,7 +523,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
     for (int j = 8 * min(total, kCandBlocks) + tid; j < kPool; j += kSelThreads) out[j] = -1;
   }
   // clear this row's histogram and state for the next call
-  uint32_t* gh = p.hist + (size_t)(p.pool_mode ? row : 2 * row + which) * kHistBins;
+  uint32_t* gh = p.hist + (size_t)(2 * row + which) * kHistBins;
   for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0;
   if (tid == 0) {
     st->thr_bin = 0;
@@ -646,10 +537,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
 
 }  // namespace
 
-template <bool kPoolMode, bool kOneQuery>
+template <bool kOneQuery>
 cudaError_t launch_scan_variant(const ScanParams& p, int num_sms, cudaStream_t s) {
-  const ScanSmemLayout L = scan_smem_layout(kPoolMode, p.nq);
-  auto kern = index_scan_kernel<kPoolMode, kOneQuery>;
+  const ScanSmemLayout L = scan_smem_layout(p.nq);
+  auto kern = index_scan_kernel<kOneQuery>;
   static int set_bytes = 0;        // the attribute is per function, set to the largest size seen
   if ((int)L.total > set_bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
@@ -667,16 +558,14 @@ cudaError_t launch_scan_variant(const ScanParams& p, int num_sms, cudaStream_t s
 }
 
 cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s) {
-  if (p.pool_mode) return launch_scan_variant<true, true>(p, num_sms, s);
-  if (p.nq == 1) return launch_scan_variant<false, true>(p, num_sms, s);
-  return launch_scan_variant<false, false>(p, num_sms, s);
+  if (p.nq == 1) return launch_scan_variant<true>(p, num_sms, s);
+  return launch_scan_variant<false>(p, num_sms, s);
 }
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
   const int rows = p.batch * p.nq;
-  const int nsel = p.pool_mode ? 1 : 2;
-  const int64_t nmax = p.pool_mode ? kPool : p.max_vis;
-  const int64_t nwords = (std::max<int64_t>(nmax, 1) + 31) / 32;
+  const int nsel = 2;               // position top-512 and block top-2048
+  const int64_t nwords = (std::max<int64_t>(p.max_vis, 1) + 31) / 32;
   const size_t smem = (size_t)((nwords + 3) & ~3) * 4 + 2048 * 4 + 64 * 4 + (size_t)kFinStage * 8;
   static size_t set_bytes = 0;
   if (smem > set_bytes) {

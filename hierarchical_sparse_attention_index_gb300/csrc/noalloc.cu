@@ -24,13 +24,12 @@ constexpr int kNoAllocMaxRows = 32;   // batch * nq
 // per (request, query) row: the fused Reindex kernel's exchange areas - the lists of 64-bit
 // (key, slot) composites its 4 CTAs publish (entries 0..2047 and 2048..4095 of each, in two
 // regions) and their (count, valid elements) pairs
-constexpr int kRxCounts = 4;
 constexpr size_t kRowList = (size_t)kPool / 2 * 8;   // 4 CTAs x 2048 composites
 constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 constexpr size_t kOffListLo = 0;
 constexpr size_t kOffListHi = kOffListLo + align256(kNoAllocMaxRows * kRowList);
 constexpr size_t kOffCount = kOffListHi + align256(kNoAllocMaxRows * kRowList);
-constexpr size_t kScratchBytes = kOffCount + align256(kNoAllocMaxRows * 2 * kRxCounts * 4);   // about 4.2 MB
+constexpr size_t kScratchBytes = kOffCount + align256(kNoAllocMaxRows * 2 * kRxSplit * 4);   // about 4.2 MB
 
 static __device__ __align__(256) uint8_t g_reindex_scratch[kScratchBytes];
 
@@ -92,7 +91,7 @@ extern "C" HSA_API hsa_status hsa_index_reindex_noalloc(const hsa_cache* cache, 
   rp.xlist_lo = reinterpret_cast<uint64_t*>(W + kOffListLo);
   rp.xlist_hi = reinterpret_cast<uint64_t*>(W + kOffListHi);
   rp.xcount = reinterpret_cast<int32_t*>(W + kOffCount);
-  rp.ld_xcount = 2 * kRxCounts;
+  rp.ld_xcount = 2 * kRxSplit;
   rp.topk_out = topk_out;
   rp.status = status;
   if (launch_reindex(rp, s) != cudaSuccess) return HSA_ERR_CUDA;

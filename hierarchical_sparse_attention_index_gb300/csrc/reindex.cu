@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kRxWarps = 16;
 constexpr int kRxThreads = kRxWarps * 32;
-constexpr int kRxCluster = 4;
+constexpr int kRxCluster = kRxSplit;
 constexpr int kSlotsPerCta = kPool / kRxCluster;          // 4096
 constexpr int kSlotsPerWarp = kSlotsPerCta / kRxWarps;    // 256
 constexpr int kGroups = kSlotsPerWarp / 32;               // 8 groups of 32 slots per warp
