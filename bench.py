@@ -407,6 +407,14 @@ def run_e2e(H, torch, I, args, world, barrier, st):
             "d2h_bytes_per_step": d2h, "steps": e2e_steps, "wall_s": round(time.perf_counter() - t0, 4)}
 
 
+def kernels_per_step():
+    """Kernels one hsa_schedule_step launches: a Full layer runs the scan and its selection kernel,
+    a Reindex layer the fused Reindex kernel, a Reuse layer nothing of its own, and every layer
+    one attention kernel."""
+    per_mode = {0: 2, 1: 1, 2: 0}
+    return sum(per_mode[MODES_BY_LAYER.get(l, 2)] + 1 for l in LAYERS)
+
+
 def make_line(args, world, value, tmax, clocks, e2e, roofline):
     B, T = CFG.batch, CFG.T
     return {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
@@ -418,7 +426,7 @@ def make_line(args, world, value, tmax, clocks, e2e, roofline):
                        "parallelism": f"replicas x{world} (requests sharded, no collective)",
                        "l2": "inputs larger than L2 (1.49 GB FP4 cache per step)",
                        "step": "hsa_schedule_step captured in one CUDA graph"},
-            "clocks": clocks, "gpu_launches": args.steps * 35, "e2e": e2e, "roofline": roofline}
+            "clocks": clocks, "gpu_launches": args.steps * kernels_per_step(), "e2e": e2e, "roofline": roofline}
 
 
 def _threads_used():
