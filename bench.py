@@ -8,8 +8,8 @@ Prints one JSON line (rank 0). `value` is decode steps/s summed over ranks (weak
 rank runs its own batch of 32 requests; no collective on the data path). The step runs through
 hsa_schedule_step, captured once in a CUDA graph and replayed. Inputs are resident in HBM and
 larger than L2 (the 1.49 GB cache). `e2e` repeats the measurement through the same public call,
-with the step's per-layer inputs copied from pinned host memory and the outputs copied back
-inside the timed region. `--impl reference` times the fp64 CPU oracle on a bounded sample of the
+with every step's inputs copied from pinned host memory and its outputs copied back inside the
+timed region, two steps in flight (upload, compute and download on three streams). `--impl reference` times the fp64 CPU oracle on a bounded sample of the
 same workload.
 """
 from __future__ import annotations
@@ -214,9 +214,9 @@ def per_kernel_times(H, torch, I, reps=10):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each kernel, from the
-# ncu captures summarised in profiles/, keyed by the SHA-256 of the kernel's source file at the
-# time of the capture: once the source changes, the figure no longer applies and is reported
-# as null.
+# ncu captures summarised in profiles/, keyed by the SHA-256 of the kernel's source files at the
+# time of the capture: once a source changes, the figure no longer applies and is reported as
+# null.
 NCU_TRAFFIC = {
     # kernel: (sources it is built from, sha256 over them in order, dram read + write bytes of one
     # launch from one ncu capture, the profile summary); the figure is dropped once a source changes
@@ -372,39 +372,101 @@ def cache_write_m2(H, torch, hbm_peak, peak_src, reps=5):
 
 
 def run_e2e(H, torch, I, args, world, barrier, st):
-    # end to end through the same public call with host buffers (pinned), copies in the timed region
-    hin = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
-           for k, v in I["host"].items()}
-    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in I["outs"]]
-    htopk = [torch.empty(t_.shape, dtype=t_.dtype).pin_memory() if t_ is not None else None for t_ in I["topk"]]
-    h2d = sum(v.numel() * v.element_size() for v in hin.values())
-    d2h = sum(o.numel() * o.element_size() for o in hout) + sum(x.numel() * 4 for x in htopk if x is not None)
-    e2e_steps = max(3, min(args.steps, 50))
-
-    def e2e_step():
-        for k, v in hin.items():
-            dst = I["dev"][k]
-            (dst.view(torch.int16) if dst.dtype == torch.bfloat16 else dst).copy_(v, non_blocking=True)
-        H.hsa_schedule_step(I["cache"], I["step"], I["ws"])
-        for o, h in zip(I["outs"], hout):
-            h.copy_(o, non_blocking=True)
-        for x, h in zip(I["topk"], htopk):
-            if x is not None:
-                h.copy_(x, non_blocking=True)
-
+    """End to end through the same public call (hsa_schedule_step) with the step's inputs in pinned
+    host memory and its results read back to pinned host memory, every step's copies inside the
+    timed region. Run the way a server keeps two batches in flight: each step's inputs are packed
+    in one host buffer and one device slot (one H2D copy), its results in one device slot (one D2H
+    copy), and three streams - copy-in, compute, copy-out - ordered by per-slot events overlap
+    step i's compute with the upload of step i + 1 and the download of step i - 1."""
+    B, nq = CFG.batch, CFG.nq
+    align = 256
+    keys = list(I["host"].keys())
+    lay, off = {}, 0
+    for k in keys:
+        v = I["host"][k]
+        lay[k] = (off, v.nbytes)
+        off += (v.nbytes + align - 1) // align * align
+    in_bytes = off
+    hin = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    hin_np = hin.numpy()
+    for k in keys:
+        o, n = lay[k]
+        hin_np[o:o + n] = np.ascontiguousarray(I["host"][k]).view(np.uint8).reshape(-1)
+    idx_j = [j for j, t_ in enumerate(I["topk"]) if t_ is not None]
+    out_n = sum(o.numel() for o in I["outs"])
+    topk_n = sum(I["topk"][j].numel() for j in idx_j)
+    h2d = sum(n for _, n in lay.values())
+    d2h = out_n * 4 + topk_n * 4
+    modes = [MODES_BY_LAYER.get(l, 2) for l in LAYERS]
+    slots = []
     for _ in range(2):
-        e2e_step()
+        din = torch.empty(in_bytes, dtype=torch.uint8, device="cuda")
+        dev = {}
+        for k in keys:
+            o, n = lay[k]
+            v = I["host"][k]
+            t = din[o:o + n]
+            t = t.view(torch.int16).view(torch.bfloat16) if v.dtype == np.uint16 else t.view(torch.from_numpy(v[:0]).dtype)
+            dev[k] = t.view(v.shape)
+        dres = torch.empty(out_n + topk_n, dtype=torch.float32, device="cuda")
+        outs, at = [], 0
+        for o in I["outs"]:
+            outs.append(dres[at:at + o.numel()].view(o.shape))
+            at += o.numel()
+        topk = [None] * len(I["topk"])
+        for j in idx_j:
+            n = I["topk"][j].numel()
+            topk[j] = dres[at:at + n].view(torch.int32).view(I["topk"][j].shape)
+            at += n
+        step = H.StepArgs(modes, [dev.get(("qi", l)) for l in LAYERS], [dev.get(("wi", l)) for l in LAYERS],
+                          [dev[("qa", l)] for l in LAYERS], [dev[("sw", l)] for l in LAYERS], outs, topk,
+                          I["pool"], I["vis"], nq, CFG.T, 1.0)
+        hres = torch.empty(out_n + topk_n, dtype=torch.float32).pin_memory()
+        slots.append(dict(din=din, dres=dres, step=step, hres=hres, ev_in=torch.cuda.Event(),
+                          ev_comp=torch.cuda.Event(), ev_out=torch.cuda.Event()))
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step(i):
+        sl = slots[i % 2]
+        s_in.wait_event(sl["ev_comp"])          # step i - 2 has finished reading this slot's inputs
+        with torch.cuda.stream(s_in):
+            sl["din"].copy_(hin, non_blocking=True)
+            sl["ev_in"].record(s_in)
+        st.wait_event(sl["ev_in"])
+        st.wait_event(sl["ev_out"])             # step i - 2's results have left this slot
+        H.hsa_schedule_step(I["cache"], sl["step"], I["ws"], stream=st)
+        sl["ev_comp"].record(st)
+        s_out.wait_event(sl["ev_comp"])
+        with torch.cuda.stream(s_out):
+            sl["hres"].copy_(sl["dres"], non_blocking=True)
+            sl["ev_out"].record(s_out)
+
+    for i in range(4):
+        e2e_step(i)
+    torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(st)
-    for _ in range(e2e_steps):
-        e2e_step()
-    f1.record(st)
+    f0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    f1.record(s_out)
+    torch.cuda.synchronize()
     barrier()
     te = max(f0.elapsed_time(f1) * 1e-3, 1e-9)
+    code, flags = H.hsa_get_device_status()
+    if code != 0 or flags != 0:
+        raise RuntimeError(f"device status after the end-to-end steps: code {code} flags {flags}")
+    # the results that came back must be those of the device-resident step on the same inputs
+    H.hsa_schedule_step(I["cache"], I["step"], I["ws"], stream=st)
+    torch.cuda.synchronize()
+    ref = torch.cat([o.reshape(-1) for o in I["outs"]] + [I["topk"][j].reshape(-1).view(torch.float32) for j in idx_j])
+    if not torch.equal(slots[(e2e_steps - 1) % 2]["hres"], ref.cpu()):
+        raise RuntimeError("end-to-end results differ from the device-resident step")
     return {"value": round(world * e2e_steps / te, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": e2e_steps, "wall_s": round(time.perf_counter() - t0, 4)}
+            "d2h_bytes_per_step": d2h, "steps": e2e_steps, "wall_s": round(time.perf_counter() - t0, 4),
+            "copies_per_step": {"h2d": 1, "d2h": 1}, "in_flight": 2}
 
 
 def kernels_per_step():
