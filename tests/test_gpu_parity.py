@@ -157,7 +157,8 @@ def test_index_full_ties(hsa):
 
 
 # ------------------------------------------------------------------ Reindex
-@pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 3000, 1), (1, 200000, 1)])
+@pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 3000, 1), (1, 200000, 1), (1, 300, 1),
+                                    (1, 50, 2)])
 def test_index_reindex(hsa, B, T, nq):
     H = hsa
     oc, q, w, vis, cache, ws, topk, pool = _full_case(H, B, T, nq)
@@ -181,6 +182,57 @@ def test_index_reindex(hsa, B, T, nq):
             P.check_set_band(g[:kk], ref[ref >= 0], s, f"reindex b{b} q{i}")
             if -(-v // 8) <= 2048:    # the pool is the whole context: reindex == full top-k
                 P.check_topk(g, s, v, name="reindex-as-full")
+
+
+def _reindex_direct(H, cache, q, w, T, pool_np):
+    vis = torch.tensor([[T]], dtype=torch.int32, device="cuda")
+    out = torch.full((1, 1, 512), -7, dtype=torch.int32, device="cuda")
+    ws = H.new_workspace(1, 1, T)
+    H.hsa_index_reindex(cache, q, w, vis, 1, T, dev(pool_np), out, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0, (code, flags)
+    return out.cpu().numpy()[0, 0]
+
+
+def test_index_reindex_all_tied(hsa):
+    """Every score equal (a zero query) over a pool of 2000 scattered blocks and 384 empty slots:
+    each cluster CTA publishes its whole quarter (past the first half of its list) and the
+    selection falls to the slot order, so the result is the pool's first 512 positions."""
+    H = hsa
+    T = 40000
+    oc = P.oracle_cache(6, 20, 1, T, T)
+    cache = gpu_cache(H, oc, T)
+    blocks = np.sort(np.random.default_rng(6).choice(T // 8, 2000, replace=False))
+    pool = np.full((1, 1, 16384), -1, np.int32)
+    pool[0, 0, :16000] = (8 * blocks[:, None] + np.arange(8)[None, :]).reshape(-1)
+    q = torch.zeros(1, 1, 16, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(1, 1, 16, device="cuda")
+    got = _reindex_direct(H, cache, q, w, T, pool)
+    assert got.tolist() == pool[0, 0, :512].tolist()
+
+
+def test_index_reindex_three_score_classes(hsa):
+    """Entry e's indexer K is one of three code patterns (e % 3), so the pool's scores take three
+    values and the best class is one large tie: the top-512 are that class's lowest positions,
+    exactly (no tolerance band)."""
+    H = hsa
+    T = 20000
+    rng = np.random.default_rng(7)
+    pat_q = rng.integers(0, 256, (3, 64), dtype=np.uint8)
+    pat_s = np.full((3, 4), 127, np.uint8)
+    cls = np.arange(T) % 3
+    ik_q, ik_s = pat_q[cls][None], pat_s[cls][None]
+    z = np.zeros((1, T, 256), np.uint8)
+    cache = H.Cache(1, T, 1, tensors=(dev(z), dev(np.zeros((1, T, 32), np.uint8)), dev(ik_q), dev(ik_s)))
+    qb = synth.index_q_bf16(7, 24, 1, 1)
+    wv = synth.index_w(7, 24, 1, 1)
+    s3 = O.index_scores(P.f32(qb[0, 0]), wv[0, 0], O.index_k_dequant(pat_q, pat_s), 3)
+    assert len(set(np.round(s3, 6).tolist())) == 3, s3
+    best = int(np.argmax(s3))
+    pool = np.arange(16384, dtype=np.int32)[None, None]
+    got = _reindex_direct(H, cache, dev_bf16(qb), dev(wv), T, pool)
+    want = np.nonzero(cls[:16384] == best)[0][:512]
+    assert got.tolist() == want.tolist()
 
 
 # ------------------------------------------------------------------ attention
