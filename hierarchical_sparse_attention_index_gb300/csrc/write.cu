@@ -24,6 +24,8 @@
 //  4. each warp reads one 32-dim group (its tensor-memory lane quadrant) of 8 entries: the
 //     group max is one warp reduction, the E8M0 scale and E2M1 codes follow as in step 1, and
 //     the bytes are written in the fragment order of include/hsa.h.
+// The accumulators are double-buffered in tensor memory: step 4 of a tile runs while the next
+// tile's MMAs (issued as soon as its B tile is written) run into the other buffer.
 #include "hsa_common.cuh"
 #include "hsa_internal.h"
 #include "hsa_tc.cuh"
@@ -41,7 +43,8 @@ constexpr uint32_t kBBlock = (uint32_t)kBRows * 128u;      // one 64-dim block o
 constexpr uint32_t kOffW = 0, kOffB = kWBytes, kOffMisc = kOffB + 8 * kBBlock;
 constexpr uint32_t kMiscBytes = 64;
 constexpr uint32_t kWSmem = kOffMisc + kMiscBytes + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 128;                        // 96 used
+constexpr uint32_t kDCols = 128;                           // columns of one accumulator buffer (96 used)
+constexpr uint32_t kTmemCols = 2 * kDCols;                 // two buffers: one computed, one read back
 static_assert(kWSmem <= 232448, "shared memory");
 static_assert(kEntPerWarp * kWWarps == kTileE, "entries per warp");
 
@@ -200,6 +203,56 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
 
   const uint32_t idesc = idesc_f16(128, kBRows, true, false, true);
   uint32_t phase = 0;
+  // step 4 for tile `etile` (first entry ecur) from the accumulators at column ecol: group
+  // q = warp & 3, entries 8 (warp >> 2) .. + 7
+  auto epilogue = [&](int64_t etile, Loc ecur, uint32_t ecol) {
+    const int q = warp & 3, e0 = 8 * (warp >> 2);
+    uint32_t vh[8], vm[8], vl[8];
+    const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + ecol + (uint32_t)e0;
+    TMEM_LD8(ta, vh);
+    TMEM_LD8(ta + kTileE, vm);
+    TMEM_LD8(ta + 2 * kTileE, vl);
+    tmem_wait_ld();
+    // the 8 entries as independent chains: value, group max, scale, codes, fragment-order word
+    uint32_t word[8], sbs[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float val = (__uint_as_float(vh[j]) + __uint_as_float(vm[j])) + __uint_as_float(vl[j]);
+      uint32_t mbits;
+      asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mbits) : "r"(__float_as_uint(val) & 0x7FFFFFFFu));
+      const uint32_t sb = e8m0_byte_for(__uint_as_float(mbits));
+      float f1, f2;
+      e8m0_inv(sb, f1, f2);
+      // lane 2i builds the byte of dims 2i, 2i+1 of the group
+      const float other = __shfl_xor_sync(0xffffffffu, val, 1);
+      const uint32_t byte = (lane & 1) ? 0u : e2m1_pair((val * f1) * f2, (other * f1) * f2);
+      // fragment order: stored word t of group q (offset 16 t + 4 q) = logical bytes 2t, 2t+1,
+      // 8+2t, 9+2t of the group, i.e. the bytes of lanes 4t, 4t+2, 16+4t, 18+4t
+      const uint32_t y = byte | (__shfl_down_sync(0xffffffffu, byte, 2) << 8);
+      word[j] = e2m1_clear_neg_zero(y | (__shfl_down_sync(0xffffffffu, y, 16) << 16));
+      sbs[j] = sb;
+    }
+    Loc l = step(ecur, e0, p.n_entries);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (etile * kTileE + e0 + j < total) {
+        const int64_t entry = (p.start_entry ? __ldg(p.start_entry + l.b) : 0) + l.i;
+        if (entry >= 0 && entry < p.cap) {                 // out-of-range entries were flagged in step 1
+          const size_t eo = (size_t)l.b * p.cap + entry;
+          if (lane < 16 && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.ik_q + eo * 64 + 4 * lane + 4 * q) = word[j];
+          if (lane == 0) p.ik_s[eo * 4 + q] = (uint8_t)sbs[j];
+        }
+      }
+      if (++l.i == p.n_entries) {
+        l.i = 0;
+        ++l.b;
+      }
+    }
+  };
+  int db = 0;                         // accumulator buffer of the tile being computed
+  bool have_prev = false;
+  int64_t prev_tile = 0;
+  Loc prev_cur = cur;
   for (; tile < ntiles; tile += gridDim.x) {
     const Loc nxt = locate((tile + gridDim.x) * kTileE, p.n_entries);
     // ------------------------------------------------------------ 1 + 2: pooling, RMSNorm, main KV, B tile
@@ -309,6 +362,8 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
     __syncthreads();
 
     // ------------------------------------------------------------ 3: K^T = W^T . [hi | mid | lo]^T, 32 k-steps
+    // into accumulator buffer db; the previous tile's buffer is read back while these run
+    const uint32_t dcol = (uint32_t)db * kDCols;
     if (tid == 0) {
       tc_fence_after();
       const uint64_t a0 = sdesc(sW, 65536u, 1024u), b0 = sdesc(sB, 16u, 1024u);
@@ -316,63 +371,24 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
       for (int k = 0; k < kDLat / 16; ++k) {
         const uint32_t ao = ((uint32_t)k * 16u * 128u) >> 4;
         const uint32_t bo = ((uint32_t)(k >> 2) * kBBlock + (uint32_t)(k & 3) * 32u) >> 4;
-        umma_f16(tmem, a0 + ao, b0 + bo, idesc, k > 0);
+        umma_f16(tmem + dcol, a0 + ao, b0 + bo, idesc, k > 0);
       }
       umma_commit(mma_bar);
     }
+    // ------------------------------------------------------------ 4: the previous tile's indexer K
+    if (have_prev) epilogue(prev_tile, prev_cur, dcol ^ kDCols);
     if (!mbar_wait(mma_bar, phase) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
     phase ^= 1u;
-    tc_fence_after();
-
-    // ------------------------------------------------------------ 4: indexer K, group q = warp & 3, entries 8 (warp >> 2) ..
-    {
-      const int q = warp & 3, e0 = 8 * (warp >> 2);
-      uint32_t vh[8], vm[8], vl[8];
-      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)e0;
-      TMEM_LD8(ta, vh);
-      TMEM_LD8(ta + kTileE, vm);
-      TMEM_LD8(ta + 2 * kTileE, vl);
-      tmem_wait_ld();
-      // the 8 entries as independent chains: value, group max, scale, codes, fragment-order word
-      uint32_t word[8], sbs[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float val = (__uint_as_float(vh[j]) + __uint_as_float(vm[j])) + __uint_as_float(vl[j]);
-        uint32_t mbits;
-        asm("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mbits) : "r"(__float_as_uint(val) & 0x7FFFFFFFu));
-        const uint32_t sb = e8m0_byte_for(__uint_as_float(mbits));
-        float f1, f2;
-        e8m0_inv(sb, f1, f2);
-        // lane 2i builds the byte of dims 2i, 2i+1 of the group
-        const float other = __shfl_xor_sync(0xffffffffu, val, 1);
-        const uint32_t byte = (lane & 1) ? 0u : e2m1_pair((val * f1) * f2, (other * f1) * f2);
-        // fragment order: stored word t of group q (offset 16 t + 4 q) = logical bytes 2t, 2t+1,
-        // 8+2t, 9+2t of the group, i.e. the bytes of lanes 4t, 4t+2, 16+4t, 18+4t
-        const uint32_t y = byte | (__shfl_down_sync(0xffffffffu, byte, 2) << 8);
-        word[j] = e2m1_clear_neg_zero(y | (__shfl_down_sync(0xffffffffu, y, 16) << 16));
-        sbs[j] = sb;
-      }
-      Loc l = step(cur, e0, p.n_entries);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (tile * kTileE + e0 + j < total) {
-          const int64_t entry = (p.start_entry ? __ldg(p.start_entry + l.b) : 0) + l.i;
-          if (entry >= 0 && entry < p.cap) {                 // out-of-range entries were flagged in step 1
-            const size_t eo = (size_t)l.b * p.cap + entry;
-            if (lane < 16 && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.ik_q + eo * 64 + 4 * lane + 4 * q) = word[j];
-            if (lane == 0) p.ik_s[eo * 4 + q] = (uint8_t)sbs[j];
-          }
-        }
-        if (++l.i == p.n_entries) {
-          l.i = 0;
-          ++l.b;
-        }
-      }
-    }
-    tc_fence_before();
-    __syncthreads();                  // tensor memory read before the next tile's MMAs overwrite it
+    tc_fence_after();                 // this tile's accumulators (read next iteration) and B tile are done
+    prev_tile = tile;
+    prev_cur = cur;
+    have_prev = true;
+    db ^= 1;
     cur = nxt;
   }
+  if (have_prev) epilogue(prev_tile, prev_cur, (uint32_t)(db ^ 1) * kDCols);
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_free(tmem, kTmemCols);
