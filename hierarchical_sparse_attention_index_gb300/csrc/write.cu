@@ -6,9 +6,9 @@
 // A persistent CTA of 16 warps writes tiles of 32 entries:
 //  1. pooling, one warp per entry (2 per warp), lane l owning channels 16l .. 16l+15: per
 //     channel a softmax over the two gate values and the weighted sum of the two wkv values in
-//     fp32 (with e = exp(-|g0 - g1|), the larger gate weighs 1 / (1 + e) and the other
-//     e / (1 + e): one exponential and one reciprocal, within a few 1e-7 of the exact
-//     weights), then RMSNorm (eps 1e-6, unit gain) as one correctly rounded 1 / rms. The
+//     fp32 (p0 = 1 / (1 + e^(g1 - g0)), x = x1 + p0 (x0 - x1): one exponential and one
+//     reciprocal, within a few ulp of x1 of the exact pooled value), then RMSNorm (eps 1e-6,
+//     unit gain) as one correctly rounded 1 / rms. The
 //     lane's 16 channels are one main-KV group, so its scale (the smallest E8M0 or E4M3 value s
 //     with 6 s >= amax, an exact bit computation) and its codes (RNE E2M1 of x / s from the
 //     hardware cvt, -0 cleared to +0) come straight from registers. The raw inputs of the
@@ -90,6 +90,13 @@ __device__ __forceinline__ uint32_t e4m3_byte_for(float amax) {
   for (int i = 0; i < 2; ++i)
     if (byte < 0x7Eu && 6.f * e4m3_to_f32(byte) < amax) ++byte;
   return byte;
+}
+
+// 1 / y to within one ulp (rcp.approx; 1 / inf = 0)
+__device__ __forceinline__ float rcp_approx(float y) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return r;
 }
 
 // one E2M1 pair byte (lo -> low nibble), RNE, saturating
@@ -284,10 +291,8 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
           const float x1 = (u & 1) ? bf16_hi(a1[u >> 1]) : bf16_lo(a1[u >> 1]);
           const float q0 = (u & 1) ? bf16_hi(g0[u >> 1]) : bf16_lo(g0[u >> 1]);
           const float q1 = (u & 1) ? bf16_hi(g1[u >> 1]) : bf16_lo(g1[u >> 1]);
-          const float d = q1 - q0;
-          const float e = __expf(-fabsf(d));
-          const float wb = __fdividef(1.f, 1.f + e), ws = e * wb;
-          x[u] = (d > 0.f) ? fmaf(wb, x1, ws * x0) : fmaf(wb, x0, ws * x1);
+          // p0 = 1 / (1 + e^(g1 - g0)) (an infinite power gives p0 = 0), x = x1 + p0 (x0 - x1)
+          x[u] = fmaf(rcp_approx(1.f + __expf(q1 - q0)), x0 - x1, x1);
         }
       }
       // the raw registers are free: the warp's entry of the next tile goes in flight
@@ -317,8 +322,13 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
             sb = e8m0_byte_for(amax);
             float f1, f2;
             e8m0_inv(sb, f1, f2);
+            if (sb < 254u) {                // f2 = 1
 #pragma unroll
-            for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair((x[2 * u] * f1) * f2, (x[2 * u + 1] * f1) * f2);
+              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(x[2 * u] * f1, x[2 * u + 1] * f1);
+            } else {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair((x[2 * u] * f1) * f2, (x[2 * u + 1] * f1) * f2);
+            }
           } else {
             sb = e4m3_byte_for(amax);
             const float s = e4m3_to_f32(sb);
