@@ -224,7 +224,7 @@ NCU_TRAFFIC = {
                            "profiles/sparse_attn_b32_t128k.md"),
     "index_reindex": (('reindex.cu', 'hsa_score.cuh'), "9d79813cfe991d3419f74057afc75224e988ce812d09cbb3578fb2d8583adf97", 43334400,
                       "profiles/reindex_kernel_b32_t128k.md"),
-    "cache_write_m2": (('write.cu', 'hsa_tc.cuh'), "899e2950b450a5084d68505b66c5ff4957b27303871e98a48d5925231560e876", 140035584,
+    "cache_write_m2": (('write.cu', 'hsa_tc.cuh'), "32144ab50c059910f8f58379198c31e77eb4f6fae039a577566dd5c649352e92", 140277248,
                        "profiles/cache_write_m2_3x65536.md"),
 }
 
