@@ -294,6 +294,11 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
 constexpr int kSelThreads = 1024;
 constexpr int kFinStage = 8192;   // threshold-bin candidates kept in shared memory; more spill to the workspace
 
+// the smallest float whose order key is `key` (inverse of order_key)
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 __device__ __forceinline__ int block_excl_scan_1024(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -373,7 +378,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   const int thr = s_ready ? s_thr : -1;
   const int Keff = min(K, s_ready ? s_nvalid : 0);
 
-  // 1. one pass over the row: 8 float4 loads in flight per thread
+  // 1. one pass over the row: 8 float4 loads in flight per thread; one float compare against the
+  //    lowest value of the threshold bin rejects most elements before any key arithmetic (it is
+  //    conservative: the bin test below is exact)
+  const float f_lo = (thr < 0) ? -INFINITY : key_to_float((uint32_t)thr << kHistShift);
   const int n4 = (n + 3) >> 2;
   for (int base = 0; base < n4; base += 8 * kSelThreads) {
     float4 v[8];
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int e = e0 + j;
-        if (e >= n || f[j] == -INFINITY) continue;
+        if (!(f[j] >= f_lo) || f[j] == -INFINITY || e >= n) continue;
         const uint32_t key = order_key(f[j]);
         const int bin = (int)(key >> kHistShift);
         if (thr < 0 || bin > thr) {
