@@ -58,12 +58,6 @@ static_assert(kHAtt * kSStride * 4 <= (int)kOffPinQ && kOffPinQ % 1024 == 0, "lo
 static_assert(kOffPinQ + 3 * kHAtt * 128 <= kQBytes, "P^T (160 keys in three 64-key blocks)");
 
 
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // store a float pair to the same shared-memory variable in CTA `peer` of the cluster
 __device__ __forceinline__ void st_cluster_f2(uint32_t local_addr, uint32_t peer, float a, float b) {
   asm volatile(
@@ -71,11 +65,6 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t local_addr, uint32_t peer
           local_addr),
       "r"(peer), "f"(a), "f"(b)
       : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
 }
 // elementwise max(m, |x|) on bf16 pairs
 __device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t m, uint32_t x) {

@@ -180,6 +180,36 @@ inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Slot in a shared list for each lane with `pred`, from one atomic per warp; every lane calls it.
+__device__ __forceinline__ int warp_append(bool pred, int* counter, int lane) {
+  const uint32_t m = __ballot_sync(0xffffffffu, pred);
+  if (!m) return 0;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(m & ((1u << lane) - 1u));
+}
+
+// ------------------------------------------------------------------ thread-block clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// every thread of every CTA of the cluster; orders the memory accesses before it (global ones
+// included) before those after it, cluster-wide
+__device__ __forceinline__ void cluster_sync_all() {
+  cluster_arrive();
+  cluster_wait();
+}
+
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
 }

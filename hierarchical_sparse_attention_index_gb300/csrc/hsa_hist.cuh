@@ -80,4 +80,41 @@ __device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, in
   named_bar_sync(1, NT);
 }
 
+// Threshold bin of a top-K over a 4096-bin histogram in shared memory held by NT threads (thread 0
+// holding the highest bins): the bin holding the K-th largest key and the count above it go to
+// out[0], out[1]; -1 and the total when the histogram holds K or fewer. Returns the total. All
+// NT threads call it (named barrier 1).
+template <int NT>
+__device__ __forceinline__ int smem_threshold(const uint32_t* hist, int K, int* scratch, int* out, int tid) {
+  constexpr int kPer = kHistBins / NT;
+  const int top = kHistBins - kPer * (tid + 1);
+  int hc[kPer], local = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    hc[i] = (int)hist[top + i];
+    local += hc[i];
+  }
+  int total;
+  const int excl = excl_scan(local, scratch, 1, NT, &total, tid);
+  if (total <= K) {
+    if (tid == 0) {
+      out[0] = -1;
+      out[1] = total;
+    }
+  } else if (excl < K && excl + local >= K) {
+    int run = excl;
+#pragma unroll
+    for (int i = kPer - 1; i >= 0; --i) {
+      if (run + hc[i] >= K) {
+        out[0] = top + i;
+        out[1] = run;
+        break;
+      }
+      run += hc[i];
+    }
+  }
+  named_bar_sync(1, NT);
+  return total;
+}
+
 }  // namespace hsa

@@ -17,11 +17,12 @@
 //    ([ARCH] §3.3 块 max 是上界) and a 4096-bin histogram of the top 12 bits of each score's
 //    order key. The last CTA to finish a request turns the histograms into the threshold bins
 //    of the position top-512 and the block top-2048.
-// Selection (exact; ties to the lower index), one CTA per (row, selection): elements above the
-// threshold bin are taken, elements in it become candidates, and an 11-bit-digit radix select
-// over (low key bits, inverted index) composites picks the remaining ones. A bitmap over the
-// index space then emits the result in ascending order, expands blocks into the candidate
-// pool, and clears the workspace state.
+// Selection (exact; ties to the lower index), one 4-CTA cluster per (row, selection), each CTA
+// streaming a quarter of the array: elements above the threshold bin are taken, elements in it
+// become candidates, and after one cluster barrier a count or an 11-bit-digit radix select over
+// (low key bits, inverted index) composites picks the remaining ones. Each quarter's bitmap is
+// emitted in ascending order at its offset (blocks expanded into the candidate pool), and the
+// workspace state is cleared.
 #include <algorithm>
 
 #include "hsa_common.cuh"
@@ -291,58 +292,40 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
 }
 
 // ------------------------------------------------------------------ select
-constexpr int kSelThreads = 1024;
-constexpr int kFinStage = 8192;   // threshold-bin candidates kept in shared memory; more spill to the workspace
+constexpr int kSelThreads = 512;
+constexpr int kSelSplit = 4;        // CTAs (one cluster) per (row, selection)
+constexpr int kSelStage = 4096;     // candidates ranked from shared memory; more are ranked from L2
+constexpr int kSelRankMax = 512;    // candidates ranked by counting up to this many
 
 // the smallest float whose order key is `key` (inverse of order_key)
 __device__ __forceinline__ float key_to_float(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-__device__ __forceinline__ int block_excl_scan_1024(int v, int* scratch, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int tt = scratch[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, tt, o);
-      if (lane >= o) tt += y;
-    }
-    scratch[lane] = tt;
-  }
-  __syncthreads();
-  const int before = warp ? scratch[warp - 1] : 0;
-  *total = scratch[31];
-  __syncthreads();
-  return before + x - v;
-}
-
-// One CTA per (row, selection): the exact top-K of one score array, emitted ascending.
-//  1. stream the row once: an element whose 12-bit key bin lies above the threshold bin the
-//     score pass found is taken at once (a bit in the index bitmap); an element in the
-//     threshold bin becomes a candidate (index + low 20 key bits, in shared memory);
-//  2. an 11-bit-digit radix select over the candidates' (low key bits, inverted index)
-//     composites takes the remaining K - above, ties to the lower index;
-//  3. the bitmap is emitted in ascending order (Reindex: through the pool; Full blocks: expanded
-//     into 8 positions each), and the row's histogram and state are cleared for the next call.
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
+// The exact top-K of one score array (positions, or 8-position block maxima), emitted ascending,
+// by one cluster of 4 CTAs, CTA r owning the quarter [r Q, (r + 1) Q) of the array:
+//  1. stream the quarter once: an element whose 12-bit key bin lies above the threshold bin the
+//     score pass found is taken at once (a bit in the quarter's bitmap); an element in the
+//     threshold bin becomes a candidate (its index, written to the workspace). A float compare
+//     against the bin's lowest value rejects most elements before any key arithmetic;
+//  2. each CTA publishes (taken, candidates) counts; after one cluster barrier every CTA makes
+//     the same cut among all candidates by (low key bits desc, index asc): a histogram of their
+//     next 12 key bits, then a count over those left in its threshold bin (an 11-bit-digit radix
+//     select when many tie in 24 key bits) - and marks its own;
+//  3. each CTA emits its quarter's bitmap in ascending order at the offset the counts give
+//     (blocks expanded into 8 pool positions); CTA 0 pads the tail and clears the row's histogram
+//     and selection state for the next call.
+__global__ void __cluster_dims__(kSelSplit, 1, 1) __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
   extern __shared__ __align__(16) uint32_t fsm[];
-  const int row = blockIdx.x, which = blockIdx.y;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = (int)cluster_rank();
+  const int unit = blockIdx.x / kSelSplit;            // (row, selection)
+  const int row = unit >> 1, which = unit & 1;
   griddep_wait();
   griddep_launch_dependents();
   const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
   const float* data;
   int n, K;
-  int64_t cand_off = 0;
   if (which == 0) {
     data = p.scores + (size_t)row * p.ld_s;
     n = vis;
@@ -351,20 +334,25 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
     data = p.blkmax + (size_t)row * p.ld_b;
     n = (vis + kBlk - 1) / kBlk;
     K = kCandBlocks;
-    cand_off = p.ld_s;
   }
   SelState* st = p.state + 2 * row + which;
-  const int nwords = (max(n, 1) + 31) >> 5;
-  uint32_t* bitmap = fsm;                       // [nwords]
-  uint32_t* shist = fsm + ((nwords + 3) & ~3);  // [2048]
-  int* scratch = reinterpret_cast<int*>(shist + 2048);   // [64]
-  int* s_cidx = scratch + 64;                   // [kFinStage]
-  uint32_t* s_ckey = reinterpret_cast<uint32_t*>(s_cidx + kFinStage);   // [kFinStage]
-  int* gcand = p.cand + (size_t)row * p.ld_cand + cand_off;              // overflow candidates
-  const int gcap = (int)(which == 0 ? p.ld_s : p.ld_b);
+  const int Q = ((n + kSelSplit - 1) / kSelSplit + 31) & ~31;   // quarter length, a multiple of 32
+  const int lo = min(n, rank * Q), hi = min(n, lo + Q);
+  const int nwq = Q >> 5;                              // bitmap words of a quarter
+  uint32_t* bitmap = fsm;                              // [nwq]
+  uint32_t* shist = fsm + ((nwq + 3) & ~3);           // [4096] second-level bins, then radix digits
+  int* scratch = reinterpret_cast<int*>(shist + kHistBins);   // [64]
+  uint64_t* cst = reinterpret_cast<uint64_t*>(scratch + 64);   // [kSelStage] candidate composites
+  // candidate indices of CTA c: the workspace's candidate row, split in quarters
+  int* cand_row = p.cand + (size_t)row * p.ld_cand + (which ? p.ld_s : 0);
+  int* xcnt = p.sure + (size_t)row * p.ld_sure + 8 * which;   // [4 CTAs][taken, candidates]
 
   __shared__ int s_thr, s_nvalid, s_ready, s_ncand, s_nsure;
   __shared__ int s_digit, s_above, s_cnt;
+  __shared__ int s_taken[kSelSplit];
+  __shared__ __align__(8) uint64_t s_cut;
+  __shared__ __align__(8) uint64_t s_rk[kSelRankMax];   // candidates ranked by counting
+  __shared__ int s_out[2], s_nrk;
   if (tid == 0) {
     volatile SelState* vs = st;
     s_ready = vs->ready;
@@ -373,124 +361,193 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
     s_ncand = 0;
     s_nsure = 0;
   }
-  for (int i = tid; i < nwords; i += kSelThreads) bitmap[i] = 0;
+  if (tid < kSelSplit) s_taken[tid] = 0;
+  if (tid == 0) s_nrk = 0;
+  for (int i = tid; i < nwq; i += kSelThreads) bitmap[i] = 0;
   __syncthreads();
   const int thr = s_ready ? s_thr : -1;
   const int Keff = min(K, s_ready ? s_nvalid : 0);
 
-  // 1. one pass over the row: 8 float4 loads in flight per thread; one float compare against the
-  //    lowest value of the threshold bin rejects most elements before any key arithmetic (it is
-  //    conservative: the bin test below is exact)
+  // 1. one pass over the quarter: 8 float4 loads in flight per thread
   const float f_lo = (thr < 0) ? -INFINITY : key_to_float((uint32_t)thr << kHistShift);
-  const int n4 = (n + 3) >> 2;
-  for (int base = 0; base < n4; base += 8 * kSelThreads) {
+  int* my_cand = cand_row + (size_t)rank * Q;
+  for (int base = lo; base < hi; base += 32 * kSelThreads) {
     float4 v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int i4 = base + u * kSelThreads + tid;
-      v[u] = (i4 < n4) ? __ldcg(reinterpret_cast<const float4*>(data) + i4)
+      const int e0 = base + 4 * (u * kSelThreads + tid);
+      v[u] = (e0 < hi) ? __ldcg(reinterpret_cast<const float4*>(data + e0))
                        : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int e0 = 4 * (base + u * kSelThreads + tid);
+      const int e0 = base + 4 * (u * kSelThreads + tid);
       const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int e = e0 + j;
-        if (!(f[j] >= f_lo) || f[j] == -INFINITY || e >= n) continue;
+        if (!(f[j] >= f_lo) || f[j] == -INFINITY || e >= hi) continue;
         const uint32_t key = order_key(f[j]);
         const int bin = (int)(key >> kHistShift);
         if (thr < 0 || bin > thr) {
-          atomicOr(bitmap + (e >> 5), 1u << (e & 31));
+          atomicOr(bitmap + ((e - lo) >> 5), 1u << ((e - lo) & 31));
           atomicAdd(&s_nsure, 1);
         } else if (bin == thr) {
-          const int slot = atomicAdd(&s_ncand, 1);
-          if (slot < kFinStage) {
-            s_cidx[slot] = e;
-            s_ckey[slot] = key & 0xFFFFFu;
-          } else if (slot - kFinStage < gcap) {
-            gcand[slot - kFinStage] = e;
-          } else {
-            flag_status(p.status, HSA_FLAG_INDEX_RANGE);
-          }
+          my_cand[atomicAdd(&s_ncand, 1)] = e;          // at most Q per quarter
         }
       }
     }
   }
   __syncthreads();
-  const int ncand = min(s_ncand, kFinStage + gcap);
-  const int need = Keff - s_nsure;
+  if (tid == 0) {
+    __stcg(xcnt + 2 * rank, s_nsure);
+    __stcg(xcnt + 2 * rank + 1, s_ncand);
+  }
+  cluster_sync_all();                 // every quarter's counts and candidates are in L2
 
-  // 2. exact selection of the remaining `need` among the candidates
-  if (thr >= 0 && need > 0 && ncand > 0) {
-    auto comp_of = [&](int i) -> uint64_t {
-      int e;
-      uint32_t k20;
-      if (i < kFinStage) {
-        e = s_cidx[i];
-        k20 = s_ckey[i];
-      } else {
-        e = __ldcg(gcand + (i - kFinStage));
-        k20 = order_key(__ldcg(data + e)) & 0xFFFFFu;
-      }
-      return ((uint64_t)k20 << 32) | (uint64_t)(~(uint32_t)e);
-    };
-    uint64_t prefix = 0, mask = 0;
-    int remaining = need;
-    const int shifts[5] = {41, 30, 19, 8, 0};
-    const int widths[5] = {11, 11, 11, 11, 8};
-    for (int d = 0; d < 5; ++d) {
-      const int sh = shifts[d];
-      const uint32_t wm = (1u << widths[d]) - 1u;
-      for (int i = tid; i < 2048; i += kSelThreads) shist[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < ncand; i += kSelThreads) {
-        const uint64_t comp = comp_of(i);
-        if ((comp & mask) == prefix) atomicAdd(shist + ((comp >> sh) & wm), 1u);
-      }
-      __syncthreads();
-      // 2048 bins, 2 per thread, highest first
-      const int hi_bin = 2047 - 2 * tid;
-      const int c_hi = (int)shist[hi_bin], c_lo = (int)shist[hi_bin - 1];
-      int tot;
-      const int excl = block_excl_scan_1024(c_hi + c_lo, scratch, &tot);
-      if (excl < remaining && excl + c_hi + c_lo >= remaining) {
-        if (excl + c_hi >= remaining) {
-          s_digit = hi_bin;
-          s_above = excl;
-          s_cnt = c_hi;
-        } else {
-          s_digit = hi_bin - 1;
-          s_above = excl + c_hi;
-          s_cnt = c_lo;
-        }
-      }
-      __syncthreads();
-      remaining -= s_above;
-      prefix |= (uint64_t)s_digit << sh;
-      mask |= (uint64_t)wm << sh;
-      const bool all_in = (s_cnt == remaining);
-      __syncthreads();
-      if (all_in) break;
+  // 2. the cut among the candidates: candidate i is taken iff (comp & mask) >= prefix
+  int sure_c[kSelSplit], cbase[kSelSplit], S = 0, C = 0;
+#pragma unroll
+  for (int c = 0; c < kSelSplit; ++c) {
+    sure_c[c] = __ldcg(xcnt + 2 * c);
+    cbase[c] = C;
+    C += __ldcg(xcnt + 2 * c + 1);
+    S += sure_c[c];
+  }
+  const int need = Keff - S;
+  auto cta_of = [&](int i) {
+    int c = 0;
+#pragma unroll
+    for (int d = 1; d < kSelSplit; ++d) c += (i >= cbase[d]) ? 1 : 0;
+    return c;
+  };
+  // composite of candidate i (global index over the four lists): low key bits, inverted index
+  auto comp_at = [&](int i) -> uint64_t {
+    const int c = cta_of(i);
+    const int e = __ldcg(cand_row + (size_t)c * Q + (i - cbase[c]));
+    return ((uint64_t)(order_key(__ldcg(data + e)) & 0xFFFFFu) << 32) | (uint64_t)(~(uint32_t)e);
+  };
+  const bool none = (thr < 0) || (need <= 0);
+  uint64_t prefix = none ? ~0ull : 0ull, mask = none ? ~0ull : 0ull;   // none: no composite reaches ~0
+  if (!none && need < C) {
+    const bool staged = C <= kSelStage;
+    if (staged) {
+      for (int i = tid; i < C; i += kSelThreads) cst[i] = comp_at(i);
+      named_bar_sync(1, kSelThreads);
     }
-    for (int i = tid; i < ncand; i += kSelThreads) {
-      const uint64_t comp = comp_of(i);
-      if ((comp & mask) >= prefix) {
-        const int e = (int)(~(uint32_t)(comp & 0xFFFFFFFFull));
+    auto comp = [&](int i) -> uint64_t { return staged ? cst[i] : comp_at(i); };
+    // level 2: a 4096-bin histogram of the next 12 key bits (composite bits 51..40) narrows the
+    // candidates still to be ranked to those sharing 24 key bits
+    for (int i = tid; i < kHistBins; i += kSelThreads) shist[i] = 0u;
+    named_bar_sync(1, kSelThreads);
+    for (int i = tid; i < C; i += kSelThreads) atomicAdd(shist + ((comp(i) >> 40) & 0xFFFu), 1u);
+    named_bar_sync(1, kSelThreads);
+    smem_threshold<kSelThreads>(shist, need, scratch, s_out, tid);
+    const int thr2 = s_out[0];
+    const int need_r = need - s_out[1];
+    prefix = (uint64_t)thr2 << 40;
+    mask = 0xFFFull << 40;
+    const int C2 = (int)shist[thr2];
+    if (need_r < C2 && C2 <= kSelRankMax) {
+      // few left: the need_r-th largest of them by counting (composites are distinct)
+      for (int i0 = warp * 32; i0 < C; i0 += kSelThreads) {
+        const int i = i0 + lane;
+        const uint64_t c64 = (i < C) ? comp(i) : 0ull;
+        const bool in = (i < C) && (c64 & mask) == prefix;
+        const int j = warp_append(in, &s_nrk, lane);
+        if (in) s_rk[j] = c64;
+      }
+      named_bar_sync(1, kSelThreads);
+      for (int i = tid; i < C2; i += kSelThreads) {
+        const uint64_t ci = s_rk[i];
+        int better = 0;
+        for (int j = 0; j < C2; ++j) better += (s_rk[j] > ci) ? 1 : 0;
+        if (better == need_r - 1) s_cut = ci;
+      }
+      named_bar_sync(1, kSelThreads);
+      prefix = s_cut;
+      mask = ~0ull;
+    } else if (need_r < C2) {
+      // many left (ties in 24 key bits): radix select, 11-bit digits over composite bits 39..0
+      int remaining = need_r;
+      const int shifts[4] = {29, 18, 7, 0};
+      const int widths[4] = {11, 11, 11, 7};
+      constexpr int kPerD = 2048 / kSelThreads;        // 4 digit bins per thread, high first
+      for (int d = 0; d < 4; ++d) {
+        const int sh = shifts[d];
+        const uint32_t wm = (1u << widths[d]) - 1u;
+        named_bar_sync(1, kSelThreads);
+        for (int i = tid; i < 2048; i += kSelThreads) shist[i] = 0u;
+        named_bar_sync(1, kSelThreads);
+        for (int i = tid; i < C; i += kSelThreads) {
+          const uint64_t c64 = comp(i);
+          if ((c64 & mask) == prefix) atomicAdd(shist + ((c64 >> sh) & wm), 1u);
+        }
+        named_bar_sync(1, kSelThreads);
+        const int dtop = 2048 - kPerD * (tid + 1);
+        int dc[kPerD], dl = 0;
+#pragma unroll
+        for (int i = 0; i < kPerD; ++i) {
+          dc[i] = (int)shist[dtop + kPerD - 1 - i];
+          dl += dc[i];
+        }
+        int dtot;
+        const int dex = excl_scan(dl, scratch, 1, kSelThreads, &dtot, tid);
+        if (dex < remaining && dex + dl >= remaining) {
+          int run = dex;
+#pragma unroll
+          for (int i = 0; i < kPerD; ++i) {
+            if (run + dc[i] >= remaining) {
+              s_digit = dtop + kPerD - 1 - i;
+              s_above = run;
+              s_cnt = dc[i];
+              break;
+            }
+            run += dc[i];
+          }
+        }
+        named_bar_sync(1, kSelThreads);
+        remaining -= s_above;
+        prefix |= (uint64_t)s_digit << sh;
+        mask |= (uint64_t)wm << sh;
+        const bool all_in = (s_cnt == remaining);
+        named_bar_sync(1, kSelThreads);
+        if (all_in) break;
+      }
+    }
+  }
+  if (!none) {
+    // mark this quarter's taken candidates; count every CTA's
+    int taken_c[kSelSplit] = {0, 0, 0, 0};
+    for (int i0 = warp * 32; i0 < C; i0 += kSelThreads) {
+      const int i = i0 + lane;
+      const uint64_t c64 = (i < C) ? (C <= kSelStage && need < C ? cst[i] : comp_at(i)) : 0ull;
+      const bool taken = (i < C) && (c64 & mask) >= prefix;
+      const int c = cta_of(i);
+#pragma unroll
+      for (int d = 0; d < kSelSplit; ++d) taken_c[d] += __popc(__ballot_sync(0xffffffffu, taken && c == d));
+      if (taken && c == rank) {
+        const int e = (int)(~(uint32_t)c64) - lo;
         atomicOr(bitmap + (e >> 5), 1u << (e & 31));
       }
     }
+    if (lane < kSelSplit) {
+      const int v = (lane == 0) ? taken_c[0] : (lane == 1) ? taken_c[1] : (lane == 2) ? taken_c[2] : taken_c[3];
+      if (v) atomicAdd(s_taken + lane, v);
+    }
   }
   __syncthreads();
 
-  // 3. ascending emission
-  const int per = (nwords + kSelThreads - 1) / kSelThreads;
-  const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
+  // 3. ascending emission at this quarter's offset
+  int off = 0;
+#pragma unroll
+  for (int c = 0; c < kSelSplit; ++c) off += (c < rank) ? sure_c[c] + s_taken[c] : 0;
+  const int per = (nwq + kSelThreads - 1) / kSelThreads;
+  const int w0 = min(nwq, tid * per), w1 = min(nwq, w0 + per);
   int cnt = 0;
   for (int i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
   int total;
-  int o = block_excl_scan_1024(cnt, scratch, &total);
+  int o = off + excl_scan(cnt, scratch, 1, kSelThreads, &total, tid);
   if (which == 0) {
     int32_t* out = p.topk_out + (size_t)row * kTopK;
     for (int i = w0; i < w1; ++i) {
@@ -498,11 +555,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
       while (m) {
         const int b = __ffs(m) - 1;
         m &= m - 1;
-        if (o < kTopK) out[o] = i * 32 + b;
+        if (o < kTopK) out[o] = lo + i * 32 + b;
         ++o;
       }
     }
-    for (int j = total + tid; j < kTopK; j += kSelThreads) out[j] = -1;
+    if (rank == 0)
+      for (int j = Keff + tid; j < kTopK; j += kSelThreads) out[j] = -1;
   } else {
     int32_t* out = p.pool_out + (size_t)row * kPool;
     for (int i = w0; i < w1; ++i) {
@@ -510,39 +568,42 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
       while (m) {
         const int b = __ffs(m) - 1;
         m &= m - 1;
-        const int blk = i * 32 + b;
+        const int blk = lo + i * 32 + b;
         if (o < kCandBlocks) {
-          int4 lo, hi;
+          int4 lo4, hi4;
           const int q0 = blk * 8;
-          lo.x = (q0 + 0 < vis) ? q0 + 0 : -1;
-          lo.y = (q0 + 1 < vis) ? q0 + 1 : -1;
-          lo.z = (q0 + 2 < vis) ? q0 + 2 : -1;
-          lo.w = (q0 + 3 < vis) ? q0 + 3 : -1;
-          hi.x = (q0 + 4 < vis) ? q0 + 4 : -1;
-          hi.y = (q0 + 5 < vis) ? q0 + 5 : -1;
-          hi.z = (q0 + 6 < vis) ? q0 + 6 : -1;
-          hi.w = (q0 + 7 < vis) ? q0 + 7 : -1;
-          reinterpret_cast<int4*>(out + 8 * o)[0] = lo;
-          reinterpret_cast<int4*>(out + 8 * o)[1] = hi;
+          lo4.x = (q0 + 0 < vis) ? q0 + 0 : -1;
+          lo4.y = (q0 + 1 < vis) ? q0 + 1 : -1;
+          lo4.z = (q0 + 2 < vis) ? q0 + 2 : -1;
+          lo4.w = (q0 + 3 < vis) ? q0 + 3 : -1;
+          hi4.x = (q0 + 4 < vis) ? q0 + 4 : -1;
+          hi4.y = (q0 + 5 < vis) ? q0 + 5 : -1;
+          hi4.z = (q0 + 6 < vis) ? q0 + 6 : -1;
+          hi4.w = (q0 + 7 < vis) ? q0 + 7 : -1;
+          reinterpret_cast<int4*>(out + 8 * o)[0] = lo4;
+          reinterpret_cast<int4*>(out + 8 * o)[1] = hi4;
         }
         ++o;
       }
     }
-    for (int j = 8 * min(total, kCandBlocks) + tid; j < kPool; j += kSelThreads) out[j] = -1;
+    if (rank == 0)
+      for (int j = 8 * min(Keff, kCandBlocks) + tid; j < kPool; j += kSelThreads) out[j] = -1;
   }
-  // clear this row's histogram and state for the next call
-  uint32_t* gh = p.hist + (size_t)(2 * row + which) * kHistBins;
-  for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0;
-  if (tid == 0) {
-    st->thr_bin = 0;
-    st->above = 0;
-    st->nvalid = 0;
-    st->nsure = 0;
-    st->ncand = 0;
-    st->ready = 0;
+  // clear this row's histogram and state for the next call (every CTA read the state before the
+  // cluster barrier above)
+  if (rank == 0) {
+    uint32_t* gh = p.hist + (size_t)(2 * row + which) * kHistBins;
+    for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0;
+    if (tid == 0) {
+      st->thr_bin = 0;
+      st->above = 0;
+      st->nvalid = 0;
+      st->nsure = 0;
+      st->ncand = 0;
+      st->ready = 0;
+    }
   }
 }
-
 }  // namespace
 
 template <bool kOneQuery>
@@ -572,16 +633,16 @@ cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s) 
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
   const int rows = p.batch * p.nq;
-  const int nsel = 2;               // position top-512 and block top-2048
-  const int64_t nwords = (std::max<int64_t>(p.max_vis, 1) + 31) / 32;
-  const size_t smem = (size_t)((nwords + 3) & ~3) * 4 + 2048 * 4 + 64 * 4 + (size_t)kFinStage * 8;
+  const int64_t q = ((std::max<int64_t>(p.max_vis, 1) + kSelSplit - 1) / kSelSplit + 31) / 32;   // bitmap words of a quarter
+  const size_t smem = (size_t)((q + 3) & ~3) * 4 + kHistBins * 4 + 64 * 4 + (size_t)kSelStage * 8;
   static size_t set_bytes = 0;
   if (smem > set_bytes) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     set_bytes = smem;
   }
-  return launch_pdl(select_kernel, dim3((unsigned)rows, (unsigned)nsel), dim3(kSelThreads), smem, s, p);
+  // one cluster of 4 CTAs per (row, selection): the position top-512, then the block top-2048
+  return launch_pdl(select_kernel, dim3((unsigned)(rows * 2 * kSelSplit)), dim3(kSelThreads), smem, s, p);
 }
 
 }  // namespace hsa

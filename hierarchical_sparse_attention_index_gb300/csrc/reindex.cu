@@ -55,16 +55,6 @@ static_assert(kRxSmem <= 232448, "shared memory");
 static_assert((uint32_t)kPool * 8 <= kRingBytes, "union staging fits the rings");
 static_assert(kRankMax * 8 <= kSlotsPerCta * 4, "ranked elements fit the score array");
 
-__device__ __forceinline__ uint32_t rx_cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void rx_cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // (order key, inverted row slot): larger = better, ties to the lower slot
 __device__ __forceinline__ uint64_t comp_of(uint32_t key, uint32_t row_slot) {
   return ((uint64_t)key << 32) | (uint64_t)(~row_slot);
@@ -72,56 +62,16 @@ __device__ __forceinline__ uint64_t comp_of(uint32_t key, uint32_t row_slot) {
 __device__ __forceinline__ uint32_t slot_of(uint64_t comp) { return ~(uint32_t)comp; }
 __device__ __forceinline__ int bin_of(uint64_t comp) { return (int)(comp >> (32 + kHistShift)); }
 
-// Slot in a shared list for each lane with `pred`, from one atomic per warp; every lane calls it.
-__device__ __forceinline__ int warp_append(bool pred, int* counter, int lane) {
-  const uint32_t m = __ballot_sync(0xffffffffu, pred);
-  if (!m) return 0;
-  const int leader = __ffs(m) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(m));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return base + __popc(m & ((1u << lane) - 1u));
-}
-
-// Threshold bin of a top-K over `hist` (4096 bins, thread 0 holding the 8 highest): the bin
-// holding the K-th largest key and the count above it into scr[64], scr[65]; -1 and the total
-// when the histogram holds K or fewer. Returns the total. All kRxThreads threads call it.
+// Threshold bin of a top-K over `hist` into scr[64], scr[65] (smem_threshold over this CTA's threads)
 __device__ __forceinline__ int find_threshold(const uint32_t* hist, int K, int* scr, int tid) {
-  const int top = kHistBins - kPerT * (tid + 1);
-  int hc[kPerT], local = 0;
-#pragma unroll
-  for (int i = 0; i < kPerT; ++i) {
-    hc[i] = (int)hist[top + i];
-    local += hc[i];
-  }
-  int total;
-  const int excl = excl_scan(local, scr, 1, kRxThreads, &total, tid);
-  if (total <= K) {
-    if (tid == 0) {
-      scr[64] = -1;
-      scr[65] = total;
-    }
-  } else if (excl < K && excl + local >= K) {
-    int run = excl;
-#pragma unroll
-    for (int i = kPerT - 1; i >= 0; --i) {
-      if (run + hc[i] >= K) {
-        scr[64] = top + i;
-        scr[65] = run;
-        break;
-      }
-      run += hc[i];
-    }
-  }
-  named_bar_sync(1, kRxThreads);
-  return total;
+  return smem_threshold<kRxThreads>(hist, K, scr, scr + 64, tid);
 }
 
 __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads, 1)
     reindex_kernel(const ReindexParams p) {
   extern __shared__ __align__(1024) uint8_t rsm[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rank = (int)rx_cluster_rank();
+  const int rank = (int)cluster_rank();
   const int row = blockIdx.x / kRxCluster;
   uint32_t* hist = reinterpret_cast<uint32_t*>(rsm + kOffHist);
   float* sc = reinterpret_cast<float*>(rsm + kOffSc);
@@ -231,7 +181,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     __stcg(p.xcount + (size_t)row * p.ld_xcount + 2 * rank, scr[72]);
     __stcg(p.xcount + (size_t)row * p.ld_xcount + 2 * rank + 1, nval_local);
   }
-  rx_cluster_sync();                  // the four lists are in L2
+  cluster_sync_all();                  // the four lists are in L2
 
   // ---------------------------------------------------------------- 3. the row's top-K over the union
   // the first kSpec entries a thread may need of each list are loaded with the counts, before
