@@ -220,9 +220,9 @@ def per_kernel_times(H, torch, I, reps=10):
 NCU_TRAFFIC = {
     # kernel: (sources it is built from, sha256 over them in order, dram read + write bytes of one
     # launch from one ncu capture, the profile summary); the figure is dropped once a source changes
-    "sparse_attn_decode": (('attn.cu', 'hsa_tc.cuh'), "939b1e82415d13e473ac1c4977eae49fbd72a547845da29a15c16d59b4921021", 10603008,
+    "sparse_attn_decode": (('attn.cu', 'hsa_tc.cuh'), "bc3556a43eceb8f2ec76816302bf12d82e4601fa4fbeb42ce15398cb38a6643f", 10603776,
                            "profiles/sparse_attn_b32_t128k.md"),
-    "index_reindex": (('reindex.cu', 'hsa_score.cuh'), "9d79813cfe991d3419f74057afc75224e988ce812d09cbb3578fb2d8583adf97", 43334400,
+    "index_reindex": (('reindex.cu', 'hsa_score.cuh'), "feace6e1cb617558a3770a3bd6b3056711193a1fcffe7580944ca62d6d33ee3d", 43313664,
                       "profiles/reindex_kernel_b32_t128k.md"),
     "cache_write_m2": (('write.cu', 'hsa_tc.cuh'), "32144ab50c059910f8f58379198c31e77eb4f6fae039a577566dd5c649352e92", 140277248,
                        "profiles/cache_write_m2_3x65536.md"),
