@@ -304,18 +304,19 @@ def run_hsa(args):
     shares = {"sparse_attn_decode": attn_calls * kt["sparse_attn_decode"], "index_full": kt["index_full"],
               "index_reindex": 4 * kt["index_reindex"]}
     dominant = max(shares, key=shares.get)
-    if dominant == "sparse_attn_decode":
-        ach = attn_bytes / kt["sparse_attn_decode"] / 1e9
-    elif dominant == "index_full":
-        ach = scan_bytes / kt["index_full"] / 1e9
-    else:
-        ach = B * 16384 * SCAN_B / kt["index_reindex"] / 1e9
+    # algorithmic bytes per call: attention 409,600 B per request; the Full call's 68 B per position
+    # plus the 4 B score it writes; the Reindex call's 68 B per pool slot
+    call_bytes = {"sparse_attn_decode": attn_bytes, "index_full": scan_bytes, "index_reindex": B * 16384 * SCAN_B}
+    ach = call_bytes[dominant] / kt[dominant] / 1e9
     traffic, traffic_src = ncu_traffic(dominant)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": traffic,
                 "traffic_source": traffic_src, "peak_source": peak_src,
                 "per_call_us": {k: round(v * 1e6, 2) for k, v in kt.items()},
-                "step_share": {k: round(v / sum(shares.values()), 3) for k, v in shares.items()}}
+                "step_share": {k: round(v / sum(shares.values()), 3) for k, v in shares.items()},
+                "per_call": {k: {"bytes": call_bytes[k], "achieved_gbs": round(call_bytes[k] / kt[k] / 1e9, 1),
+                                 "frac": round(call_bytes[k] / kt[k] / 1e9 / hbm_peak, 4),
+                                 "traffic": ncu_traffic(k)[0]} for k in kt}}
 
     e2e = None
     if not args.no_e2e:
