@@ -33,6 +33,32 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Packed fp32 pairs (sm_100 f32x2 arithmetic): each instruction performs two independent IEEE
+// round-to-nearest operations, so the results equal the scalar fmaf / multiply bit for bit.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_relu(uint64_t v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  return f2_pack(fmaxf(lo, 0.f), fmaxf(hi, 0.f));
+}
+
 // Shared-memory sizes of one staged query: B fragments [2 n-tiles][8 k-steps][32 lanes][2] and
 // the 16 shifted head weights.
 constexpr int kQFragWords = 2 * 8 * 32 * 2;
@@ -134,14 +160,16 @@ __device__ __forceinline__ float score_rows32(uint32_t codes, int row_off, uint3
     const float sf1[4] = {__uint_as_float(SF1.x), __uint_as_float(SF1.y), __uint_as_float(SF1.z),
                           __uint_as_float(SF1.w)};
     const uint32_t aw0[4] = {A0.x, A0.y, A0.z, A0.w}, aw1[4] = {A1.x, A1.y, A1.z, A1.w};
-    float tot[2][4];
+    // tot[nt][r]: the scaled sums of heads (8 nt + 2 t, +1) for row g (r = 0) or g + 8 (r = 1),
+    // packed in pairs
+    uint64_t tot[2][2];
 #pragma unroll
     for (int gi = 0; gi < 4; ++gi) {
       // group gi = word gi of each row's chunk = k-steps 2gi (bytes 0,1) and 2gi+1 (bytes 2,3)
       uint32_t f0, f1, f2, f3, h0, h1, h2, h3;
       e2m1x8_to_f16x2x4(aw0[gi], f0, f1, f2, f3);
       e2m1x8_to_f16x2x4(aw1[gi], h0, h1, h2, h3);
-      const float sc0 = sf0[gi], sc1 = sf1[gi];
+      const uint64_t sc0 = f2_pack(sf0[gi], sf0[gi]), sc1 = f2_pack(sf1[gi], sf1[gi]);
       float tmp[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -150,19 +178,24 @@ __device__ __forceinline__ float score_rows32(uint32_t codes, int row_off, uint3
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        tot[nt][0] = gi ? fmaf(sc0, tmp[nt][0], tot[nt][0]) : sc0 * tmp[nt][0];
-        tot[nt][1] = gi ? fmaf(sc0, tmp[nt][1], tot[nt][1]) : sc0 * tmp[nt][1];
-        tot[nt][2] = gi ? fmaf(sc1, tmp[nt][2], tot[nt][2]) : sc1 * tmp[nt][2];
-        tot[nt][3] = gi ? fmaf(sc1, tmp[nt][3], tot[nt][3]) : sc1 * tmp[nt][3];
+        const uint64_t a = f2_pack(tmp[nt][0], tmp[nt][1]), c = f2_pack(tmp[nt][2], tmp[nt][3]);
+        tot[nt][0] = gi ? f2_fma(sc0, a, tot[nt][0]) : f2_mul(sc0, a);
+        tot[nt][1] = gi ? f2_fma(sc1, c, tot[nt][1]) : f2_mul(sc1, c);
       }
     }
+    // ReLU-weighted head sums, the head pair (2t, 2t+1) of each n-tile accumulated as a pair
+    uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        vp[mt][0] = fmaf(wr[nt][j], fmaxf(tot[nt][j], 0.f), vp[mt][0]);
-        vp[mt][1] = fmaf(wr[nt][j], fmaxf(tot[nt][2 + j], 0.f), vp[mt][1]);
-      }
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint64_t w2 = f2_pack(wr[nt][0], wr[nt][1]);
+      acc0 = f2_fma(w2, f2_relu(tot[nt][0]), acc0);
+      acc1 = f2_fma(w2, f2_relu(tot[nt][1]), acc1);
+    }
+    float lo, hi;
+    f2_unpack(acc0, lo, hi);
+    vp[mt][0] = lo + hi;
+    f2_unpack(acc1, lo, hi);
+    vp[mt][1] = lo + hi;
   }
   // Reduce-scatter over the 4 head lanes t of a row group: after it, lane (g, t) holds the full
   // 16-head score of row 8t + g of the warp (tile t >> 1, row g + 8 (t & 1)).
