@@ -384,13 +384,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
   mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-  float lsum = 0.f;
   // P^T (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys; one 8-key
   // run is one 16-byte unit
   // p = 2^(x log2 e - m log2 e); a head with no valid key has m = -inf and every x = -inf, so
-  // its offset is 0 and every p is 0
+  // its offset is 0 and every p is 0. Values below 2^-126 flush to zero (f16 P rounds everything
+  // below 2^-25 to zero anyway). Key pairs run as packed fp32 pairs.
   const float kLog2e = 1.4426950408889634f;
   const float ml2 = (mloc == -INFINITY) ? 0.f : mloc * kLog2e;
+  const uint64_t l2e2 = f2_pack(kLog2e, kLog2e), nml2 = f2_pack(-ml2, -ml2);
+  uint64_t ls2 = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int u = 0; u < 3; ++u) {
     const int ch = kq + 8 * u;
@@ -398,15 +400,22 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       uint32_t pk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = exp2f(fmaf(x[u][2 * e], kLog2e, -ml2));
-        const float p1 = exp2f(fmaf(x[u][2 * e + 1], kLog2e, -ml2));
-        lsum += p0 + p1;
+        float z0, z1;
+        f2_unpack(f2_fma(f2_pack(x[u][2 * e], x[u][2 * e + 1]), l2e2, nml2), z0, z1);
+        const float p0 = ex2_ftz(z0), p1 = ex2_ftz(z1);
+        ls2 = f2_add(ls2, f2_pack(p0, p1));
         const __half2 h = __floats2half2_rn(p0, p1);
         pk[e] = *reinterpret_cast<const uint32_t*>(&h);
       }
       const int key = 8 * ch;
       sts128(sP + (uint32_t)(key >> 6) * (kHAtt * 128u) + sw128(hh, (key & 63) >> 3), pk[0], pk[1], pk[2], pk[3]);
     }
+  }
+  float lsum;
+  {
+    float a, c;
+    f2_unpack(ls2, a, c);
+    lsum = a + c;
   }
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
   lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
@@ -437,7 +446,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int h = 32 * hc + j;
-        const float o0 = __uint_as_float(r[j]) * s_invl[h], o1 = __uint_as_float(r[j + 1]) * s_invl[h + 1];
+        const float2 il = *reinterpret_cast<const float2*>(s_invl + h);
+        float o0, o1;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), f2_pack(il.x, il.y)), o0, o1);
         if ((h >> 4) == (int)rank) {
           own[h & 15] = o0;
           own[(h & 15) + 1] = o1;
@@ -479,9 +490,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 
   // ---------------------------------------------------------------- out[h][dim] = sum_c w_c[h] O_c[h][dim], c in rank order
   {
-    float acc[16];
+    uint64_t acc2[8];                 // head pairs (j, j + 1) of this CTA's 16
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc2[j] = f2_pack(0.f, 0.f);
     float v[16];
 #pragma unroll
     for (uint32_t c = 0; c < kCluster; ++c) {
@@ -499,11 +510,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
         }
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = fmaf(s_w[c * 16 + j], v[j], acc[j]);
+      for (int j = 0; j < 16; j += 2) {
+        const float2 wc = *reinterpret_cast<const float2*>(s_w + c * 16 + j);
+        acc2[j >> 1] = f2_fma(f2_pack(wc.x, wc.y), f2_pack(v[j], v[j + 1]), acc2[j >> 1]);
+      }
     }
     float* out = p.out + ((size_t)row * kHAtt + 16 * rank) * kDLat + dim;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) out[(size_t)j * kDLat] = acc[j];
+    for (int j = 0; j < 16; j += 2) {
+      float a, c;
+      f2_unpack(acc2[j >> 1], a, c);
+      out[(size_t)j * kDLat] = a;
+      out[(size_t)(j + 1) * kDLat] = c;
+    }
   }
 }
 

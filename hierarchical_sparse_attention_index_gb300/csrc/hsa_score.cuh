@@ -33,32 +33,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Packed fp32 pairs (sm_100 f32x2 arithmetic): each instruction performs two independent IEEE
-// round-to-nearest operations, so the results equal the scalar fmaf / multiply bit for bit.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_relu(uint64_t v) {
-  float lo, hi;
-  f2_unpack(v, lo, hi);
-  return f2_pack(fmaxf(lo, 0.f), fmaxf(hi, 0.f));
-}
-
 // Shared-memory sizes of one staged query: B fragments [2 n-tiles][8 k-steps][32 lanes][2] and
 // the 16 shifted head weights.
 constexpr int kQFragWords = 2 * 8 * 32 * 2;
