@@ -105,6 +105,43 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   return true;
 }
 
+// inputs_ready: q and swa are complete when the kernel is launched (no kernel of the same
+// schedule_step writes them), so the kernel may fetch them before its programmatic-dependency wait
+hsa_status attn_common(const hsa_cache* cache, const void* q, const int32_t* topk, const uint8_t* swa,
+                       const int32_t* vis, int32_t nq, int64_t max_vis, float sm_scale, float* out, void* ws,
+                       size_t ws_bytes, hsa_stream_t stream, bool inputs_ready) {
+  hsa_status st = check_cache(cache);
+  if (st != HSA_OK) return st;
+  st = check_query(cache, nq, max_vis);
+  if (st != HSA_OK) return st;
+  if (!q || !topk || !swa || !vis || !out) return HSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(swa) || !aligned16(out)) return HSA_ERR_ALIGN;
+  WsLayout L;
+  if (!make_ws_layout(cache->batch, nq, max_vis, &L)) return HSA_ERR_SHAPE;
+  if (!ws || ws_bytes < L.total) return HSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return HSA_ERR_ALIGN;
+  uint32_t* status;
+  int sms;
+  if (!device_info(&status, &sms)) return HSA_ERR_UNSUPPORTED;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.batch = cache->batch;
+  p.nq = nq;
+  p.cap = cache->capacity;
+  p.scale_fmt = cache->kv_scale_fmt;
+  p.kv_q = cache->kv_q;
+  p.kv_s = cache->kv_s;
+  p.q = static_cast<const uint16_t*>(q);
+  p.topk = topk;
+  p.swa = swa;
+  p.vis = vis;
+  p.sm_scale = sm_scale;
+  p.inputs_ready = inputs_ready ? 1 : 0;
+  p.out = out;
+  p.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.off_attn);
+  p.status = status;
+  return cuda_fail(launch_attention(p, (cudaStream_t)stream), "attention launch");
+}
 }  // namespace hsa
 
 using namespace hsa;
@@ -271,39 +308,11 @@ hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, const float*
   return index_common(true, cache, q, w, vis, nq, max_vis, pool, topk_out, nullptr, ws, ws_bytes, stream);
 }
 
+
 hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const int32_t* topk, const uint8_t* swa,
                                   const int32_t* vis, int32_t nq, int64_t max_vis, float sm_scale, float* out,
                                   void* ws, size_t ws_bytes, hsa_stream_t stream) {
-  hsa_status st = check_cache(cache);
-  if (st != HSA_OK) return st;
-  st = check_query(cache, nq, max_vis);
-  if (st != HSA_OK) return st;
-  if (!q || !topk || !swa || !vis || !out) return HSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(swa) || !aligned16(out)) return HSA_ERR_ALIGN;
-  WsLayout L;
-  if (!make_ws_layout(cache->batch, nq, max_vis, &L)) return HSA_ERR_SHAPE;
-  if (!ws || ws_bytes < L.total) return HSA_ERR_WORKSPACE;
-  if (!aligned16(ws)) return HSA_ERR_ALIGN;
-  uint32_t* status;
-  int sms;
-  if (!device_info(&status, &sms)) return HSA_ERR_UNSUPPORTED;
-  AttnParams p;
-  memset(&p, 0, sizeof(p));
-  p.batch = cache->batch;
-  p.nq = nq;
-  p.cap = cache->capacity;
-  p.scale_fmt = cache->kv_scale_fmt;
-  p.kv_q = cache->kv_q;
-  p.kv_s = cache->kv_s;
-  p.q = static_cast<const uint16_t*>(q);
-  p.topk = topk;
-  p.swa = swa;
-  p.vis = vis;
-  p.sm_scale = sm_scale;
-  p.out = out;
-  p.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.off_attn);
-  p.status = status;
-  return cuda_fail(launch_attention(p, (cudaStream_t)stream), "attention launch");
+  return attn_common(cache, q, topk, swa, vis, nq, max_vis, sm_scale, out, ws, ws_bytes, stream, false);
 }
 
 hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, void* ws, size_t ws_bytes,
@@ -334,8 +343,8 @@ hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, voi
       latest = a->topk[l];
     }
     if (st != HSA_OK) return st;
-    st = hsa_sparse_attn_decode(cache, a->q_attn[l], latest, a->swa[l], a->vis, a->nq, a->max_vis, a->sm_scale,
-                                a->out[l], ws, ws_bytes, stream);
+    st = attn_common(cache, a->q_attn[l], latest, a->swa[l], a->vis, a->nq, a->max_vis, a->sm_scale,
+                                a->out[l], ws, ws_bytes, stream, true);
     if (st != HSA_OK) return st;
   }
   return HSA_OK;

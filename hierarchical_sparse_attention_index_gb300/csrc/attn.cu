@@ -137,18 +137,46 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   cluster_arrive();                   // every CTA's query barrier is initialised before any multicast
   cluster_wait();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
-  griddep_wait();
-  griddep_launch_dependents();
-
-  if (warp == kWorkWarps) {
-    // ---------------------------------------------------------------- MMA warp
-    if (lane == 0) {
-      // query: this CTA's 16 heads, 8 boxes of 64 dims x 16 heads (2 KB each), to all 4 CTAs
+  // query: this CTA's 16 heads, 8 boxes of 64 dims x 16 heads (2 KB each), to all 4 CTAs
+  auto issue_query = [&]() {
+    if (warp == kWorkWarps && lane == 0) {
       mbar_arrive_expect_tx(q_bar, kQBytes);
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb)
         tma_load_2d_mc(sQ + (uint32_t)kb * (kHAtt * 128u) + rank * (16u * 128u), &p.qmap, 64 * kb,
                        row * kHAtt + 16 * (int)rank, q_bar, (uint16_t)((1u << kCluster) - 1u));
+    }
+  };
+  // SWA: this CTA's 32 window rows (w = 32 rank + r, position vis - 128 + w) are one contiguous
+  // 16 KB block; worker warp w takes rows 8 (w >> 2) + rr, FP8 chunks jj = 4 (2 (w & 3) + s) + qq
+  // (lane = 8 qq + rr)
+  const int rr = lane & 7, qq = lane >> 3;
+  const int srow = 8 * (warp >> 2) + rr;
+  uint4 sc[2];
+  auto load_swa = [&]() {
+    if (warp < kWorkWarps) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.swa + ((size_t)b * (kSwa + p.nq - 1) + qi + 32 * (int)rank + srow) * kDLat);
+#pragma unroll
+      for (int s4 = 0; s4 < 2; ++s4) sc[s4] = __ldg(src + 4 * (2 * (warp & 3) + s4) + qq);
+    }
+  };
+  // Inputs that no kernel of the same step writes (schedule_step) are fetched while the previous
+  // kernel drains; otherwise only after the programmatic-dependency wait.
+  if (p.inputs_ready) {
+    issue_query();
+    load_swa();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  if (!p.inputs_ready) {
+    issue_query();
+    load_swa();
+  }
+
+  if (warp == kWorkWarps) {
+    // ---------------------------------------------------------------- MMA warp
+    if (lane == 0) {
       // S^T = K . Q^T in two M=128 passes (rows 0..127 -> columns 0..63, rows 32..159 -> 64..127),
       // 64-dim block by block as the worker warps finish converting them. Descriptors are formed
       // once; a k-step only moves the start-address field (address >> 4), which cannot carry out
@@ -206,22 +234,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   // issue every global load up front. Lane = 8 q + rr. One warp-wide load covers 8 rows (rr) x
   // 64 contiguous bytes (4 lanes q x 16 B), so every sector fetched is used whole, and in the
   // shared-memory stores that follow, the 8 lanes of each store phase write 8 different rows.
-  const int rr = lane & 7, qq = lane >> 3;
   // top-k rows: warp w owns rows 8w + rr; step s takes code chunk j = 4 s + qq (dims 32j..32j+31).
   // The row index goes first: the row loads depend on it.
   const int krow = 8 * warp + rr;
   const int kidx = __ldg(p.topk + (size_t)row * kTopK + rank * kTopRows + krow);
-  // SWA: this CTA's 32 window rows (w = 32 rank + r, position vis - 128 + w) are one contiguous
-  // 16 KB block; warp w takes rows 8 (w >> 2) + rr, FP8 chunks jj = 4 (2 (w & 3) + s) + qq
-  uint4 sc[2];
-  const int srow = 8 * (warp >> 2) + rr;
   const bool sval = (vis - kSwa + 32 * (int)rank + srow) >= 0;
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.swa + ((size_t)b * (kSwa + p.nq - 1) + qi + 32 * (int)rank + srow) * kDLat);
-#pragma unroll
-    for (int s4 = 0; s4 < 2; ++s4) sc[s4] = __ldg(src + 4 * (2 * (warp & 3) + s4) + qq);
-  }
   uint4 kc[4];
   uint32_t ks2[4];
   {

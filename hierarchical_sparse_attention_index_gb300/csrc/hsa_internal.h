@@ -118,6 +118,7 @@ struct AttnParams {
   const uint8_t* swa;     // [B][W+nq-1][512]
   const int32_t* vis;     // [B][nq]
   float sm_scale;
+  int32_t inputs_ready;   // 1: q and swa are complete at launch (schedule_step), read before the dependency wait
   float* out;             // [B][nq][64][512]
   float* partial;         // workspace: [B*nq][4][64*512 outputs, then 64 (max, sum) pairs]
   uint32_t* status;

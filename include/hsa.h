@@ -222,7 +222,10 @@ HSA_API hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q,
 /* One decode step over consecutive layer slots ([ARCH] §3.3: 1 full score + 4 pool rescores +
  * 15 inherits; [COST] §3.1; [CED] Figure 4). Slot l runs its indexer if FULL (which also
  * writes the pool) or REINDEX, then attention with the latest indices. Everything is
- * stream-ordered, with no host synchronisation. */
+ * stream-ordered, with no host synchronisation. The step's inputs (q_attn, swa, q_idx, w_idx,
+ * vis, pool when the first slot is not FULL) must be complete before the call's work starts on
+ * `stream` and must not alias anything the step writes (out, topk, pool, ws): the attention
+ * kernels fetch their queries and SWA rows while the previous kernel of the step drains. */
 HSA_API hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* args, void* ws,
                              size_t ws_bytes, hsa_stream_t stream);
 
