@@ -126,8 +126,11 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
             const int nc = (int)imin64((n + 7) & ~7, p.cap - p0);
             mbar_arrive_expect_tx(full, (uint32_t)nc * 68u);
             const int64_t e0 = (int64_t)seg * p.cap + p0;
-            bulk_g2s(dcodes, p.ik_q + e0 * 64, (uint32_t)nc * 64u, full);
-            bulk_g2s(dscales, p.ik_s + e0 * 4, (uint32_t)nc * 4u, full);
+            // indexer K is read once per Full call: evict it first, so that the scores the
+            // selection reads next stay in L2
+            const uint64_t pol = l2_policy_evict_first();
+            bulk_g2s_hint(dcodes, p.ik_q + e0 * 64, (uint32_t)nc * 64u, full, pol);
+            bulk_g2s_hint(dscales, p.ik_s + e0 * 4, (uint32_t)nc * 4u, full, pol);
           } else {
             mbar_arrive(full);
           }
