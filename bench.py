@@ -218,13 +218,20 @@ def per_kernel_times(H, torch, I, reps=10):
 # time of the capture: once a source changes, the figure no longer applies and is reported as
 # null.
 NCU_TRAFFIC = {
-    # kernel: (sources it is built from, sha256 over them in order, dram read + write bytes of one
-    # launch from one ncu capture, the profile summary); the figure is dropped once a source changes
-    "sparse_attn_decode": (('attn.cu', 'hsa_tc.cuh'), "bc3556a43eceb8f2ec76816302bf12d82e4601fa4fbeb42ce15398cb38a6643f", 10603776,
+    # call: (sources its kernels are built from, sha256 over them in order, dram read + write bytes
+    # of one call from one ncu capture (each kernel starts with a flushed L2), the profile summary);
+    # the figure is dropped once a source changes
+    "sparse_attn_decode": (('attn.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
+                           "e75deaa6c9158ed29f1db51782baa5780a3a8eaa08fd445a3339676e855a820b", 10603008,
                            "profiles/sparse_attn_b32_t128k.md"),
-    "index_reindex": (('reindex.cu', 'hsa_score.cuh'), "feace6e1cb617558a3770a3bd6b3056711193a1fcffe7580944ca62d6d33ee3d", 43313664,
+    "index_full": (('index.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
+                   "ae1c36e4c0845a5afb9b985f28948d3ed8c689f18f0d3473c39f7b9cbd39d34a", 311961088,
+                   "profiles/index_scan_b8_t128k.md"),
+    "index_reindex": (('reindex.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
+                      "cb7da590386dee4a0bda56d21a70cc043e150d2249d5c0aa7e195cca534393d4", 43337216,
                       "profiles/reindex_kernel_b32_t128k.md"),
-    "cache_write_m2": (('write.cu', 'hsa_tc.cuh'), "32144ab50c059910f8f58379198c31e77eb4f6fae039a577566dd5c649352e92", 140277248,
+    "cache_write_m2": (('write.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
+                       "61419994a52aa3822717e32526037c5e04fc985f85f40238101c387fc2c8696d", 139837440,
                        "profiles/cache_write_m2_3x65536.md"),
 }
 
