@@ -210,7 +210,7 @@ hsa_status hsa_cache_write_compress(const hsa_cache* cache, const void* wkv, con
 static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const void* q, const float* w,
                                const int32_t* vis, int32_t nq, int64_t max_vis, const int32_t* pool,
                                int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
-                               hsa_stream_t stream) {
+                               hsa_stream_t stream, bool inputs_ready = false) {
   hsa_status st = check_cache(cache);
   if (st != HSA_OK) return st;
   st = check_query(cache, nq, max_vis);
@@ -248,6 +248,7 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
     rp.ld_xcount = 2 * kRxSplit;
     rp.topk_out = topk_out;
     rp.status = status;
+    rp.inputs_ready = inputs_ready ? 1 : 0;
     return cuda_fail(launch_reindex(rp, s), "reindex launch");
   }
 
@@ -338,8 +339,10 @@ hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, voi
                           ws_bytes, stream);
       latest = a->topk[l];
     } else if (m == HSA_MODE_REINDEX) {
-      st = hsa_index_reindex(cache, a->q_idx[l], a->w_idx[l], a->vis, a->nq, a->max_vis, a->pool, a->topk[l], ws,
-                             ws_bytes, stream);
+      // the pool was written at least two kernels earlier and q_idx, w_idx are step inputs: the
+      // kernel may read them before its programmatic-dependency wait
+      st = index_common(true, cache, a->q_idx[l], a->w_idx[l], a->vis, a->nq, a->max_vis, a->pool, a->topk[l],
+                        nullptr, ws, ws_bytes, stream, true);
       latest = a->topk[l];
     }
     if (st != HSA_OK) return st;

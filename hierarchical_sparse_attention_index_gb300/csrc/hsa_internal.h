@@ -102,6 +102,8 @@ struct ReindexParams {
   int64_t ld_xcount;
   int32_t* topk_out;     // [B][nq][512]
   uint32_t* status;
+  int32_t inputs_ready;  // 1: q, w, vis and pool are complete at launch (schedule_step); the kernel then waits
+                         // on the previous kernel only before its first global write
 };
 cudaError_t launch_reindex(const ReindexParams& p, cudaStream_t s);
 

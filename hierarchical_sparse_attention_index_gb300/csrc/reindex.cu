@@ -83,7 +83,10 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;
   for (int i = tid; i < kSlotsPerCta / 32; i += kRxThreads) sel[i] = 0u;
   if (tid < kScrInts) scr[tid] = 0;
-  griddep_wait();
+  // Inside schedule_step everything this kernel reads was complete before it was launched (the
+  // pool two or more kernels earlier, q, w and vis before the step), so it scores while the
+  // previous kernel drains and waits for it only before its first global write.
+  if (!p.inputs_ready) griddep_wait();
   griddep_launch_dependents();
 
   const int vis = __ldg(p.vis + row);
@@ -140,6 +143,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   }
   __syncthreads();
 
+  if (p.inputs_ready) griddep_wait();
   // ---------------------------------------------------------------- 2. publish this CTA's own top region
   // scr: [0, 32) scan scratch; 64, 65 threshold bin and count above it; 72 published count;
   // 73 ranked count; 76 + c slots CTA c keeps; 80..82 radix digit, count above it, count in it;
