@@ -106,10 +106,12 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
 }
 
 // inputs_ready: q and swa are complete when the kernel is launched (no kernel of the same
-// schedule_step writes them), so the kernel may fetch them before its programmatic-dependency wait
+// schedule_step writes them), so the kernel may fetch them before its programmatic-dependency
+// wait; topk_ready: topk was written two or more kernels earlier (a Reuse slot), so the kernel
+// waits only before its first global write.
 hsa_status attn_common(const hsa_cache* cache, const void* q, const int32_t* topk, const uint8_t* swa,
                        const int32_t* vis, int32_t nq, int64_t max_vis, float sm_scale, float* out, void* ws,
-                       size_t ws_bytes, hsa_stream_t stream, bool inputs_ready) {
+                       size_t ws_bytes, hsa_stream_t stream, bool inputs_ready, bool topk_ready) {
   hsa_status st = check_cache(cache);
   if (st != HSA_OK) return st;
   st = check_query(cache, nq, max_vis);
@@ -137,6 +139,7 @@ hsa_status attn_common(const hsa_cache* cache, const void* q, const int32_t* top
   p.vis = vis;
   p.sm_scale = sm_scale;
   p.inputs_ready = inputs_ready ? 1 : 0;
+  p.topk_ready = (inputs_ready && topk_ready) ? 1 : 0;
   p.out = out;
   p.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.off_attn);
   p.status = status;
@@ -313,7 +316,7 @@ hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, const float*
 hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const int32_t* topk, const uint8_t* swa,
                                   const int32_t* vis, int32_t nq, int64_t max_vis, float sm_scale, float* out,
                                   void* ws, size_t ws_bytes, hsa_stream_t stream) {
-  return attn_common(cache, q, topk, swa, vis, nq, max_vis, sm_scale, out, ws, ws_bytes, stream, false);
+  return attn_common(cache, q, topk, swa, vis, nq, max_vis, sm_scale, out, ws, ws_bytes, stream, false, false);
 }
 
 hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, void* ws, size_t ws_bytes,
@@ -347,7 +350,7 @@ hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, voi
     }
     if (st != HSA_OK) return st;
     st = attn_common(cache, a->q_attn[l], latest, a->swa[l], a->vis, a->nq, a->max_vis, a->sm_scale,
-                                a->out[l], ws, ws_bytes, stream, true);
+                                a->out[l], ws, ws_bytes, stream, true, m == HSA_MODE_REUSE);
     if (st != HSA_OK) return st;
   }
   return HSA_OK;

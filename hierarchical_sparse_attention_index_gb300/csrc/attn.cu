@@ -162,12 +162,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     }
   };
   // Inputs that no kernel of the same step writes (schedule_step) are fetched while the previous
-  // kernel drains; otherwise only after the programmatic-dependency wait.
+  // kernel drains; otherwise only after the programmatic-dependency wait. Nothing is written to
+  // global memory before that wait.
   if (p.inputs_ready) {
     issue_query();
     load_swa();
   }
-  griddep_wait();
+  // A Reuse slot of schedule_step reads nothing the previous kernel wrote (its top-k is two or
+  // more kernels old): it waits only before its first global write, the partials drain.
+  if (!p.topk_ready) griddep_wait();
   griddep_launch_dependents();
   if (!p.inputs_ready) {
     issue_query();
@@ -449,6 +452,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   // Warp (quadrant qd = w & 3, tile mt = w >> 2) owns output dimension d = 128 mt + 32 qd + lane
   // for all 64 heads: it sends the 48 heads other CTAs combine to the workspace (L2) as f16
   // pairs [h / 2][d] and keeps this CTA's own 16 heads in registers (fp32).
+  if (p.topk_ready) griddep_wait();   // the previous kernel may still read the partials workspace
   const int qd = warp & 3, mtile = warp >> 2;
   const int dim = 128 * mtile + 32 * qd + lane;
   float own[16];

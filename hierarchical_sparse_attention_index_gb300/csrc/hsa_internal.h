@@ -121,6 +121,8 @@ struct AttnParams {
   const int32_t* vis;     // [B][nq]
   float sm_scale;
   int32_t inputs_ready;   // 1: q and swa are complete at launch (schedule_step), read before the dependency wait
+  int32_t topk_ready;     // 1 (with inputs_ready): topk is two or more kernels old (a Reuse slot); the kernel
+                          // waits for the previous one only before its first global write
   float* out;             // [B][nq][64][512]
   float* partial;         // workspace: [B*nq][4][64*512 outputs, then 64 (max, sum) pairs]
   uint32_t* status;
