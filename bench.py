@@ -222,16 +222,16 @@ NCU_TRAFFIC = {
     # of one call from one ncu capture (each kernel starts with a flushed L2), the profile summary);
     # the figure is dropped once a source changes
     "sparse_attn_decode": (('attn.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
-                           "e75deaa6c9158ed29f1db51782baa5780a3a8eaa08fd445a3339676e855a820b", 10603008,
+                           "e15c867df819ea0b62370d88a2383bcd1a0cd9c92915cfe02b91f6b23b9dd07d", 10605568,
                            "profiles/sparse_attn_b32_t128k.md"),
     "index_full": (('index.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
-                   "ae1c36e4c0845a5afb9b985f28948d3ed8c689f18f0d3473c39f7b9cbd39d34a", 311961088,
+                   "46f4405115f3dbe45f8cfdc93ec384f00ed92e3a215b7196a5e58aa704d1f0b2", 312457728,
                    "profiles/index_scan_b8_t128k.md"),
     "index_reindex": (('reindex.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
-                      "cb7da590386dee4a0bda56d21a70cc043e150d2249d5c0aa7e195cca534393d4", 43337216,
+                      "1ac35e69806f19cda19c1bae361cb8ada72dd3d7801ddb00c069809ecbe9c1d0", 43331840,
                       "profiles/reindex_kernel_b32_t128k.md"),
     "cache_write_m2": (('write.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
-                       "61419994a52aa3822717e32526037c5e04fc985f85f40238101c387fc2c8696d", 139837440,
+                       "f0a6da1c7f17b9fecf283d0ea6ed024188a04f949fb5425fb950500597266911", 139971072,
                        "profiles/cache_write_m2_3x65536.md"),
 }
 
