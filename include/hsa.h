@@ -225,7 +225,8 @@ HSA_API hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q,
  * stream-ordered, with no host synchronisation. The step's inputs (q_attn, swa, q_idx, w_idx,
  * vis, pool when the first slot is not FULL) must be complete before the call's work starts on
  * `stream` and must not alias anything the step writes (out, topk, pool, ws): the attention
- * kernels fetch their queries and SWA rows while the previous kernel of the step drains. */
+ * kernels fetch their queries and SWA rows, and the Reindex kernels their queries, weights and
+ * pool rows, while the previous kernel of the step drains. */
 HSA_API hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* args, void* ws,
                              size_t ws_bytes, hsa_stream_t stream);
 
