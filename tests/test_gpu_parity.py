@@ -336,3 +336,47 @@ def test_schedule_step(hsa):
             idx = t20 if l < 24 else t24
             ref = _attn_ref(oc, b, 0, T, idx[b, 0], sw[l][b], qa[l][b, 0], T, 1.0)
             P.check_attention(outs[j].cpu().numpy()[b, 0], ref, f"step attn L{l}")
+
+
+def test_schedule_step_matches_standalone_calls(hsa):
+    """Inside hsa_schedule_step the kernels read step inputs before their dependency wait and a
+    Reindex or Reuse-slot attention kernel waits only before its first global write; the
+    arithmetic is that of the standalone calls, so the step's indices and outputs equal theirs
+    bit for bit (two requests, a ragged length, slots Full, Reuse, Reindex, Reuse, Reuse)."""
+    H = hsa
+    B, T, nq, seed = 2, 12345, 1, 3
+    layers = [20, 21, 24, 25, 26]
+    modes = [H.HSA_MODE_FULL, H.HSA_MODE_REUSE, H.HSA_MODE_REINDEX, H.HSA_MODE_REUSE, H.HSA_MODE_REUSE]
+    cap = round8(T)
+    oc = P.oracle_cache(seed, 20, B, T, cap)
+    cache = gpu_cache(H, oc, cap)
+    d_vis = dev(synth.visibility(B, nq, T))
+    d_qi = {l: dev_bf16(synth.index_q_bf16(seed, l, B, nq)) for l in (20, 24)}
+    d_wi = {l: dev(synth.index_w(seed, l, B, nq)) for l in (20, 24)}
+    d_qa = {l: dev_bf16(synth.attn_q_bf16(seed, l, B, nq)) for l in layers}
+    d_sw = {l: dev(synth.swa_e4m3(seed, l, B, nq)) for l in layers}
+    ws = H.new_workspace(B, nq, T)
+    new_idx = lambda: torch.empty(B, nq, 512, dtype=torch.int32, device="cuda")  # noqa: E731
+    new_out = lambda: torch.empty(B, nq, 64, 512, device="cuda")  # noqa: E731
+
+    # standalone calls, one after the other
+    t20, pool, t24 = new_idx(), torch.empty(B, nq, 16384, dtype=torch.int32, device="cuda"), new_idx()
+    H.hsa_index_full(cache, d_qi[20], d_wi[20], d_vis, nq, T, t20, pool, ws)
+    H.hsa_index_reindex(cache, d_qi[24], d_wi[24], d_vis, nq, T, pool, t24, ws)
+    ref = {}
+    for l in layers:
+        ref[l] = new_out()
+        H.hsa_sparse_attn_decode(cache, d_qa[l], t20 if l < 24 else t24, d_sw[l], d_vis, nq, T, 1.0, ref[l], ws)
+
+    # the same work as one step
+    outs = [new_out() for _ in layers]
+    tk = [new_idx() if l in d_qi else None for l in layers]
+    s_pool = torch.empty_like(pool)
+    step = H.StepArgs(modes, [d_qi.get(l) for l in layers], [d_wi.get(l) for l in layers],
+                      [d_qa[l] for l in layers], [d_sw[l] for l in layers], outs, tk, s_pool, d_vis, nq, T, 1.0)
+    H.hsa_schedule_step(cache, step, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    assert torch.equal(tk[0], t20) and torch.equal(s_pool, pool) and torch.equal(tk[2], t24)
+    for j, l in enumerate(layers):
+        assert torch.equal(outs[j], ref[l]), f"slot {j} (layer {l})"
