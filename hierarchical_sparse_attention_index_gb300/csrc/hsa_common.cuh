@@ -258,6 +258,22 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// the address of the same shared-memory variable in CTA `peer` of the cluster
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_addr, uint32_t peer) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(peer));
+  return r;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t cluster_addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_cluster_u64(uint32_t cluster_addr) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
 // every thread of every CTA of the cluster; orders the memory accesses before it (global ones
 // included) before those after it, cluster-wide
 __device__ __forceinline__ void cluster_sync_all() {

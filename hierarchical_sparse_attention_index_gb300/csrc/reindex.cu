@@ -52,7 +52,7 @@ constexpr uint32_t kRxSmem = kOffScr + kScrInts * 4;
 static_assert(kRxSmem <= 232448, "shared memory");
 // after scoring, the rings hold the union (64-bit composites) and the score array the ranked
 // threshold-bin elements
-static_assert((uint32_t)kPool * 8 <= kRingBytes, "union staging fits the rings");
+static_assert((uint32_t)kPool * 8 + kSlotsPerCta * 8 <= kRingBytes, "union staging and own list fit the rings");
 static_assert(kRankMax * 8 <= kSlotsPerCta * 4, "ranked elements fit the score array");
 
 // (order key, inverted row slot): larger = better, ties to the lower slot
@@ -150,12 +150,11 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   // 84..85 the cut composite of the rank count
   const int nval_local = find_threshold(hist, kTopK, scr, tid);
   const int lthr = scr[64];
-  // list entry j of CTA c: its composite, at entry j of [row][c][2048] in the first region for
-  // j < 2048, else at entry j - 2048 of the second
-  auto list_at = [&](int c, int j) -> uint64_t* {
-    uint64_t* base = (j < kSlotsPerCta / 2) ? p.xlist_lo : p.xlist_hi;
-    return base + ((size_t)row * kRxCluster + c) * (kSlotsPerCta / 2) + (j & (kSlotsPerCta / 2 - 1));
-  };
+  // This CTA's list stays in its own shared memory (the rings are free now): entries at lst,
+  // the count and the number of valid elements at scr[90], scr[91]; the peers read them over
+  // distributed shared memory after the cluster barrier. The union is staged at ust.
+  uint64_t* ust = reinterpret_cast<uint64_t*>(rsm + kOffRing);
+  uint64_t* lst = reinterpret_cast<uint64_t*>(rsm + kOffRing + kPool * 8);
   {
     // the warp's 8 rounds of appends take one atomic: round i's lanes follow rounds 0..i-1
     uint32_t keys[kPerT], bal[kPerT];
@@ -174,31 +173,27 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
 #pragma unroll
     for (int i = 0; i < kPerT; ++i) {
       if ((bal[i] >> lane) & 1u)
-        __stcg(list_at(rank, base + __popc(bal[i] & lt)),
-               comp_of(keys[i], (uint32_t)(kSlotsPerCta * rank + kPerT * tid + i)));
+        lst[base + __popc(bal[i] & lt)] = comp_of(keys[i], (uint32_t)(kSlotsPerCta * rank + kPerT * tid + i));
       base += __popc(bal[i]);
     }
   }
   for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;   // read by find_threshold above
   named_bar_sync(1, kRxThreads);
   if (tid == 0) {
-    __stcg(p.xcount + (size_t)row * p.ld_xcount + 2 * rank, scr[72]);
-    __stcg(p.xcount + (size_t)row * p.ld_xcount + 2 * rank + 1, nval_local);
+    scr[90] = scr[72];
+    scr[91] = nval_local;
   }
-  cluster_sync_all();                  // the four lists are in L2
+  cluster_sync_all();                  // the four lists are published
 
   // ---------------------------------------------------------------- 3. the row's top-K over the union
-  // the first kSpec entries a thread may need of each list are loaded with the counts, before
-  // the counts are known (entries past a count are ignored)
-  constexpr int kSpec = 2;
   int cnt[kRxCluster], nv[kRxCluster];
-  uint64_t spec[kRxCluster][kSpec];
+  uint32_t lst_c[kRxCluster];
 #pragma unroll
   for (int c = 0; c < kRxCluster; ++c) {
-    cnt[c] = __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c);
-    nv[c] = __ldcg(p.xcount + (size_t)row * p.ld_xcount + 2 * c + 1);
-#pragma unroll
-    for (int sp = 0; sp < kSpec; ++sp) spec[c][sp] = __ldcg(list_at(c, tid + kRxThreads * sp));
+    const uint32_t scr_c = cluster_map(smem_u32(scr + 90), (uint32_t)c);
+    cnt[c] = ld_cluster_s32(scr_c);
+    nv[c] = ld_cluster_s32(scr_c + 4u);
+    lst_c[c] = cluster_map(smem_u32(lst), (uint32_t)c);
   }
   int ubase[kRxCluster], U = 0, nvalid = 0;
 #pragma unroll
@@ -214,23 +209,15 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     for (int d = 1; d < kRxCluster; ++d) c += (i >= ubase[d]) ? 1 : 0;
     return c;
   };
-  uint64_t* ust = reinterpret_cast<uint64_t*>(rsm + kOffRing);   // the rings are free now
 #pragma unroll
   for (int c = 0; c < kRxCluster; ++c) {
-#pragma unroll
-    for (int sp = 0; sp < kSpec; ++sp) {
-      const int j = tid + kRxThreads * sp;
-      if (j < cnt[c]) {
-        ust[ubase[c] + j] = spec[c][sp];
-        atomicAdd(hist + bin_of(spec[c][sp]), 1u);
-      }
-    }
-    for (int j = tid + kRxThreads * kSpec; j < cnt[c]; j += kRxThreads) {
-      const uint64_t comp = __ldcg(list_at(c, j));
+    for (int j = tid; j < cnt[c]; j += kRxThreads) {
+      const uint64_t comp = ld_cluster_u64(lst_c[c] + 8u * (uint32_t)j);
       ust[ubase[c] + j] = comp;
       atomicAdd(hist + bin_of(comp), 1u);
     }
   }
+  cluster_arrive();                   // done with the peers' lists (waited for before exit)
   named_bar_sync(1, kRxThreads);
   find_threshold(hist, K, scr, tid);
   const int thr = scr[64], need = K - scr[65];
@@ -367,6 +354,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   }
   if (rank == 0)
     for (int j = K + tid; j < kTopK; j += kRxThreads) out[j] = -1;
+  cluster_wait();                     // no peer still reads this CTA's list
 }
 
 }  // namespace
