@@ -95,9 +95,6 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   L->off_sure_full = take((size_t)rows * (kTopK + kCandBlocks) * 4);
   // fused Reindex: per row, the 4 CTAs' lists of 64-bit (key, slot) composites (entries 0..2047
   // and 2048..4095 of each) and their (count, valid elements) pairs
-  L->off_rx_lo = take((size_t)rows * kPool / 2 * 8);
-  L->off_rx_hi = take((size_t)rows * kPool / 2 * 8);
-  L->off_rx_count = take((size_t)rows * 2 * kRxSplit * 4);
   // attention partials: per row, 4 CTAs x (64 x 512 unnormalised outputs + 64 (max, sum) pairs)
   L->attn_bytes = (size_t)rows * kAttnSplit * (kHAtt * kDLat + 2 * kHAtt) * 4;
   L->off_attn = take(L->attn_bytes);
@@ -232,8 +229,9 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
   const cudaStream_t s = (cudaStream_t)stream;
 
   if (pool_mode) {
-    // one fused launch: rescoring over the pool and the exact top-512, one cluster per row; the
-    // lists and counts its CTAs exchange live in the workspace's Reindex regions
+    // one fused launch: rescoring over the pool and the exact top-512, one cluster per row; its
+    // CTAs exchange their candidate lists through distributed shared memory, so the workspace
+    // is not touched
     ReindexParams rp;
     memset(&rp, 0, sizeof(rp));
     rp.batch = cache->batch;
@@ -245,10 +243,6 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
     rp.w = w;
     rp.vis = vis;
     rp.pool = pool;
-    rp.xlist_lo = reinterpret_cast<uint64_t*>(W + L.off_rx_lo);
-    rp.xlist_hi = reinterpret_cast<uint64_t*>(W + L.off_rx_hi);
-    rp.xcount = reinterpret_cast<int32_t*>(W + L.off_rx_count);
-    rp.ld_xcount = 2 * kRxSplit;
     rp.topk_out = topk_out;
     rp.status = status;
     rp.inputs_ready = inputs_ready ? 1 : 0;

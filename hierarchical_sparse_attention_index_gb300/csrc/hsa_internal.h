@@ -29,7 +29,6 @@ struct WsLayout {
   int64_t ld_s;        // score row stride (positions), a multiple of kScanChunk
   int64_t ld_b;        // block-max row stride (blocks) = ld_s / 8
   size_t off_scores, off_blkmax, off_hist_full, off_cand_full, off_sure_full, off_state_full, off_done_full;
-  size_t off_rx_lo, off_rx_hi, off_rx_count;   // fused Reindex exchange lists and counts
   size_t off_attn;     // attention partials
   size_t attn_bytes;
   size_t zero_begin, zero_end;   // region that must be zero between calls (hist + state + counters)
@@ -96,10 +95,6 @@ struct ReindexParams {
   const float* w;        // [B][nq][16]
   const int32_t* vis;    // [B][nq]
   const int32_t* pool;   // [B][nq][16384]
-  uint64_t* xlist_lo;    // workspace [rows][4 CTAs][2048]: entries 0..2047 of the (key, slot) lists the CTAs publish
-  uint64_t* xlist_hi;    // workspace [rows][4 CTAs][2048]: entries 2048..4095 of the same lists
-  int32_t* xcount;       // workspace: CTA c of row r publishes (count, valid elements) at xcount[r * ld_xcount + 2c]
-  int64_t ld_xcount;
   int32_t* topk_out;     // [B][nq][512]
   uint32_t* status;
   int32_t inputs_ready;  // 1: q, w, vis and pool are complete at launch (schedule_step); the kernel then waits

@@ -179,7 +179,10 @@ HSA_API hsa_status hsa_index_full(const hsa_cache* cache, const void* q, const f
 /* Reindex-mode indexer ([CED] Figure 5 right; [ARCH] §3.3 池内过滤; [COST] §3.2).
  * Scores only the pool slots (pool[b][i][j] in [0, vis), others skipped) with this layer's
  * q and w, and writes the positions of the min(512, #valid) best, ascending, -1 padded.
- *   pool   i32 [B][nq][16384] as written by hsa_index_full */
+ *   pool   i32 [B][nq][16384] as written by hsa_index_full
+ *   ws     workspace of at least hsa_workspace_bytes(B, nq, max_vis) bytes, checked like the
+ *          other calls' so that one workspace serves every call; this call does not touch it
+ *          (its CTAs exchange their candidates through distributed shared memory) */
 HSA_API hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis,
                              int32_t nq, int64_t max_vis, const int32_t* pool, int32_t* topk_out,
                              void* ws, size_t ws_bytes, hsa_stream_t stream);
@@ -189,16 +192,9 @@ HSA_API hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, cons
  * that may only touch the buffers it is handed, code running inside an arena planned by an
  * inference server, or a latency-critical loop that must never wait on an allocator. They call
  * this instead of hsa_index_reindex. Arguments, outputs and errors are those of
- * hsa_index_reindex, without ws/ws_bytes. The scratch it needs (about 4.7 MB) is a fixed array
- * in the library's own device memory, which every GPU that loads the library holds until the
- * process exits.
- *  - batch * nq must be at most 32; larger requests return HSA_ERR_SHAPE and launch nothing.
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *    make that first call before capturing a stream into a CUDA graph.
- *  - Every call shares the one array and clears the part that must start at zero
- *    (cudaMemsetAsync on `stream`). Calls that overlap on the GPU (different streams, or
- *    different host threads without ordering) race on it and give undefined results.
- *  - It calls no cudaMalloc/cudaFree and no allocating library routine. */
+ * hsa_index_reindex, without ws/ws_bytes. The fused Reindex kernel keeps everything its CTAs
+ * exchange in shared memory, so no scratch memory is used; calls on different streams are
+ * independent. It calls no cudaMalloc/cudaFree and no allocating library routine. */
 HSA_API hsa_status hsa_index_reindex_noalloc(const hsa_cache* cache, const void* q, const float* w,
                                              const int32_t* vis, int32_t nq, int64_t max_vis, const int32_t* pool,
                                              int32_t* topk_out, hsa_stream_t stream);

@@ -1,11 +1,11 @@
 """The no-allocation Reindex entry point (hsa_index_reindex_noalloc), called through the C ABI.
 
 It serves callers that cannot allocate device memory, such as plugins limited to the buffers
-they are handed, or code inside an allocator-managed arena. It keeps its scratch in a fixed
-array inside the library. The test checks that two calls in a row give exactly the output of
-the workspace-based hsa_index_reindex, within the oracle's top-k band. It also checks that a
-request over the fixed maximum is rejected. This file is collected last and passes both on
-its own in a fresh process and after the other tests."""
+they are handed, or code inside an allocator-managed arena. The fused Reindex kernel keeps its
+exchange in shared memory, so the call uses no scratch memory at all. The tests check that two
+calls in a row give exactly the output of the workspace-based hsa_index_reindex, within the
+oracle's top-k band, and that a many-row request (36 rows) matches it too. This file is
+collected last and passes both on its own in a fresh process and after the other tests."""
 import numpy as np
 import pytest
 
@@ -69,15 +69,22 @@ def test_reindex_noalloc_matches_workspace_reindex(hsa):
                 P.check_set_band(g[g >= 0], o[o >= 0], s, f"noalloc call {call} b{b} q{i}")
 
 
-def test_reindex_noalloc_rejects_oversize(hsa):
+def test_reindex_noalloc_many_rows(hsa):
     H = hsa
-    B, nq, T = 9, 4, 64            # 36 rows > 32
-    cache = H.Cache(B, T, 1)
-    q = torch.zeros(B, nq, 16, 128, dtype=torch.bfloat16, device="cuda")
-    w = torch.ones(B, nq, 16, device="cuda")
-    vis = torch.full((B, nq), T, dtype=torch.int32, device="cuda")
-    pool = torch.full((B, nq, 16384), -1, dtype=torch.int32, device="cuda")
-    out = torch.empty(B, nq, 512, dtype=torch.int32, device="cuda")
-    with pytest.raises(H.HsaError) as e:
-        H.hsa_index_reindex_noalloc(cache, q, w, vis, nq, T, pool, out)
-    assert e.value.code == 2
+    B, nq, T, seed = 9, 4, 3000, 5            # 36 rows
+    oc = P.oracle_cache(seed, 20, B, T, T)
+    cache = H.Cache(B, T, 1, tensors=tuple(_dev(oc[k]) for k in ("kv_q", "kv_s", "ik_q", "ik_s")))
+    vis = _dev(synth.visibility(B, nq, T))
+    q20, w20 = synth.index_q_bf16(seed, 20, B, nq), synth.index_w(seed, 20, B, nq)
+    q24, w24 = synth.index_q_bf16(seed, 24, B, nq), synth.index_w(seed, 24, B, nq)
+    ws = H.new_workspace(B, nq, T)
+    top20 = torch.empty(B, nq, 512, dtype=torch.int32, device="cuda")
+    pool = torch.empty(B, nq, 16384, dtype=torch.int32, device="cuda")
+    H.hsa_index_full(cache, _dev_bf16(q20), _dev(w20), vis, nq, T, top20, pool, ws)
+    ref = torch.full((B, nq, 512), -7, dtype=torch.int32, device="cuda")
+    H.hsa_index_reindex(cache, _dev_bf16(q24), _dev(w24), vis, nq, T, pool, ref, ws)
+    out = torch.full((B, nq, 512), -7, dtype=torch.int32, device="cuda")
+    H.hsa_index_reindex_noalloc(cache, _dev_bf16(q24), _dev(w24), vis, nq, T, pool, out)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0, (code, flags)
+    assert torch.equal(out, ref)
