@@ -222,16 +222,16 @@ NCU_TRAFFIC = {
     # of one call from one ncu capture (each kernel starts with a flushed L2), the profile summary);
     # the figure is dropped once a source changes
     "sparse_attn_decode": (('attn.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
-                           "e15c867df819ea0b62370d88a2383bcd1a0cd9c92915cfe02b91f6b23b9dd07d", 10605568,
+                           "200b48ce7efd56723e34a84ba25d375de0f097e18d524bd77befea338894d7f2", 10604288,
                            "profiles/sparse_attn_b32_t128k.md"),
     "index_full": (('index.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
-                   "46f4405115f3dbe45f8cfdc93ec384f00ed92e3a215b7196a5e58aa704d1f0b2", 312457728,
+                   "81e9738821858d4314e8ef612f2387fa594dd2c46e5de6f5ae460eb3af9e83ff", 312347904,
                    "profiles/index_scan_b8_t128k.md"),
     "index_reindex": (('reindex.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
-                      "1ac35e69806f19cda19c1bae361cb8ada72dd3d7801ddb00c069809ecbe9c1d0", 43331840,
+                      "e057f39e990931a6397a6ca7715ffba91811e937dc45fc8e1ce7efec861b88ef", 42859776,
                       "profiles/reindex_kernel_b32_t128k.md"),
     "cache_write_m2": (('write.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
-                       "f0a6da1c7f17b9fecf283d0ea6ed024188a04f949fb5425fb950500597266911", 139971072,
+                       "c977b0c9fcffc4cf9d2e62324c5d04890211e311a130bb8d0f40459ee565e76c", 139664384,
                        "profiles/cache_write_m2_3x65536.md"),
 }
 
