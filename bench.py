@@ -228,7 +228,7 @@ NCU_TRAFFIC = {
                    "81e9738821858d4314e8ef612f2387fa594dd2c46e5de6f5ae460eb3af9e83ff", 312347904,
                    "profiles/index_scan_b8_t128k.md"),
     "index_reindex": (('reindex.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
-                      "e057f39e990931a6397a6ca7715ffba91811e937dc45fc8e1ce7efec861b88ef", 42859776,
+                      "46c4a308b46f4210c8881d390d6ec7d13a1371e119f913e7838f99b364316265", 42859776,
                       "profiles/reindex_kernel_b32_t128k.md"),
     "cache_write_m2": (('write.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
                        "c977b0c9fcffc4cf9d2e62324c5d04890211e311a130bb8d0f40459ee565e76c", 139664384,

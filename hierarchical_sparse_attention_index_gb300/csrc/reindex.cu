@@ -7,11 +7,13 @@
 //  1. 16 warps score 256 slots each: 8 groups of 32 slots (four 8-entry runs) gathered with
 //     cp.async into a per-warp ring 4 groups ahead, scored with warp MMAs (shared with the scan
 //     kernel); scores stay in shared memory with a 4096-bin histogram of their top 12 key bits;
-//  2. the CTA finds its own threshold bin b_r (the bin of its 512-th largest key) and publishes,
-//     through the workspace, every valid element in a bin >= b_r (order key and slot), their
-//     count and its number of valid elements. The row's top-512 lies inside the union of the
-//     four lists: an element of CTA r in the row's top-512 is in CTA r's own top-512;
-//  3. after one cluster barrier every CTA loads the union and selects the same top-K,
+//  2. the CTA finds its own threshold bin b_r (the bin of its 512-th largest key) and lists, in
+//     its own shared memory, every valid element in a bin >= b_r (order key and slot), with the
+//     list's count and its number of valid elements. The row's top-512 lies inside the union of
+//     the four lists: an element of CTA r in the row's top-512 is in CTA r's own top-512;
+//  3. after one cluster barrier every CTA reads the four lists over distributed shared memory
+//     (a split cluster arrive/wait keeps each CTA alive until its peers are done) and selects
+//     the same top-K,
 //     K = min(512, valid elements of the row): a histogram of the union's top key bits gives the
 //     threshold bin, and the elements in it are ranked by (key desc, slot asc) - by counting
 //     when there are few, by an exact radix select otherwise;
