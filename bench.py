@@ -213,26 +213,12 @@ def per_kernel_times(H, torch, I, reps=10):
     return out
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each kernel, from the
-# ncu captures summarised in profiles/, keyed by the SHA-256 of the kernel's source files at the
-# time of the capture: once a source changes, the figure no longer applies and is reported as
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one call, from one ncu capture of
+# the call's kernels, keyed by the SHA-256 of the kernels' source files at the time of the
+# capture. Once a source changes the figure no longer describes the kernel and is reported as
 # null.
 NCU_TRAFFIC = {
-    # call: (sources its kernels are built from, sha256 over them in order, dram read + write bytes
-    # of one call from one ncu capture (each kernel starts with a flushed L2), the profile summary);
-    # the figure is dropped once a source changes
-    "sparse_attn_decode": (('attn.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
-                           "200b48ce7efd56723e34a84ba25d375de0f097e18d524bd77befea338894d7f2", 10604288,
-                           "profiles/sparse_attn_b32_t128k.md"),
-    "index_full": (('index.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
-                   "81e9738821858d4314e8ef612f2387fa594dd2c46e5de6f5ae460eb3af9e83ff", 312347904,
-                   "profiles/index_scan_b8_t128k.md"),
-    "index_reindex": (('reindex.cu', 'hsa_common.cuh', 'hsa_hist.cuh', 'hsa_score.cuh', 'hsa_internal.h'),
-                      "46c4a308b46f4210c8881d390d6ec7d13a1371e119f913e7838f99b364316265", 42859776,
-                      "profiles/reindex_kernel_b32_t128k.md"),
-    "cache_write_m2": (('write.cu', 'hsa_common.cuh', 'hsa_tc.cuh', 'hsa_internal.h'),
-                       "c977b0c9fcffc4cf9d2e62324c5d04890211e311a130bb8d0f40459ee565e76c", 139664384,
-                       "profiles/cache_write_m2_3x65536.md"),
+    # call: (sources its kernels are built from, sha256 over them in order, dram read + write bytes)
 }
 
 
@@ -240,16 +226,16 @@ def ncu_traffic(kernel):
     import hashlib
     rec = NCU_TRAFFIC.get(kernel)
     if rec is None:
-        return None, None
-    files, digest, traffic, src = rec
+        return None
+    files, digest, traffic = rec
     d = hashlib.sha256()
     try:
         for fname in files:
             with open(os.path.join(ROOT, "hierarchical_sparse_attention_index_gb300", "csrc", fname), "rb") as f:
                 d.update(f.read())
     except OSError:
-        return None, None
-    return (traffic, src) if d.hexdigest() == digest else (None, None)
+        return None
+    return traffic if d.hexdigest() == digest else None
 
 
 def run_hsa(args):
@@ -307,23 +293,22 @@ def run_hsa(args):
     B, T = CFG.batch, CFG.T
     attn_bytes = B * ATTN_B_PER_REQ
     attn_calls = len(LAYERS)
-    scan_bytes = B * T * SCAN_B + B * T * 4
+    scan_bytes = B * T * SCAN_B
     shares = {"sparse_attn_decode": attn_calls * kt["sparse_attn_decode"], "index_full": kt["index_full"],
               "index_reindex": 4 * kt["index_reindex"]}
     dominant = max(shares, key=shares.get)
-    # algorithmic bytes per call: attention 409,600 B per request; the Full call's 68 B per position
-    # plus the 4 B score it writes; the Reindex call's 68 B per pool slot
+    # algorithmic bytes per call: attention 409,600 B per request; the Full call's 68 B per
+    # position; the Reindex call's 68 B per pool slot
     call_bytes = {"sparse_attn_decode": attn_bytes, "index_full": scan_bytes, "index_reindex": B * 16384 * SCAN_B}
     ach = call_bytes[dominant] / kt[dominant] / 1e9
-    traffic, traffic_src = ncu_traffic(dominant)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": traffic,
-                "traffic_source": traffic_src, "peak_source": peak_src,
+                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": ncu_traffic(dominant),
+                "peak_source": peak_src,
                 "per_call_us": {k: round(v * 1e6, 2) for k, v in kt.items()},
                 "step_share": {k: round(v / sum(shares.values()), 3) for k, v in shares.items()},
                 "per_call": {k: {"bytes": call_bytes[k], "achieved_gbs": round(call_bytes[k] / kt[k] / 1e9, 1),
                                  "frac": round(call_bytes[k] / kt[k] / 1e9 / hbm_peak, 4),
-                                 "traffic": ncu_traffic(k)[0]} for k in kt}}
+                                 "traffic": ncu_traffic(k)} for k in kt}}
 
     e2e = None
     if not args.no_e2e:
@@ -371,11 +356,10 @@ def cache_write_m2(H, torch, hbm_peak, peak_src, reps=5):
     t_layer = 1e-3 * e0.elapsed_time(e1) / (reps * len(layers))
     bytes_layer = n * 2 * 512 * 2 + (n // 2) * 356
     ach = bytes_layer / t_layer / 1e9
-    traffic, traffic_src = ncu_traffic("cache_write_m2")
     return {"workload": f"m2 write, {len(layers)} layers x {n} tokens", "us_per_layer": round(1e6 * t_layer, 2),
             "tokens_per_s": round(n / t_layer, 1), "bytes_per_layer": bytes_layer,
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(ach / hbm_peak, 4), "traffic": traffic, "traffic_source": traffic_src,
+                         "frac": round(ach / hbm_peak, 4), "traffic": ncu_traffic("cache_write_m2"),
                          "peak_source": peak_src}}
 
 
@@ -572,29 +556,40 @@ def run_reference(args):
     rank, world, _ = env_rank()
     if rank != 0:
         return
-    # Each timed step is one layer slot of one request (the oracle as it stands), cycling
-    # through the 20-slot schedule; 20 steps make one request-step, scaled to batch 32.
+    # Each timed step is one request's whole decode step (the 20-slot schedule, the oracle as it
+    # stands), cycling through the batch's requests; the value is scaled to a batch-32 step.
     B = CFG.batch
-    st = OracleStepper(0)
-    for _ in range(len(LAYERS)):          # one untimed request-step
-        st.slot()
-    st.i = 0
+    steppers = {}
+
+    def request_step(i):
+        r = i % 2                     # a bounded sample: requests 0 and 1 of the batch
+        if r not in steppers:
+            steppers[r] = OracleStepper(r)
+        st = steppers[r]
+        st.i = 0
+        for _ in range(len(LAYERS)):
+            st.slot()
+
+    for i in range(min(args.warmup, 1)):
+        request_step(i)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        st.slot()
+    for i in range(args.steps):
+        request_step(i)
     t = time.perf_counter() - t0
-    req_steps = args.steps / len(LAYERS)
-    value = req_steps / t / B
+    t_req = t / args.steps
+    value = 1.0 / (B * t_req)
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "steps/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / value, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_req, 3),
+            "step_unit": f"one request's decode step (1/{B} of a batch-{B} step); value is batch-{B} steps/s",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same seeded workload)",
             "config": {"workload": CFG.name, "batch_per_gpu": B, "ctx": CFG.T, "nq": CFG.nq,
                        "layers": "20..39 (1 Full, 4 Reindex, 15 Reuse, 20 attention)"},
             "cpu_baseline": {"value": round(value, 4), "unit": "steps/s", "cores": _threads_used(),
                              "kind": "oracle",
-                             "sample": f"request 0 of {B}, one layer slot per step over {args.steps} steps "
-                                       f"({req_steps:.2f} request-steps), scaled to a batch-{B} step"},
+                             "sample": f"requests 0 and 1 of {B}, one whole 20-slot decode step of one request "
+                                       f"per timed step ({args.steps} steps, {t:.2f} s), scaled to a batch-{B} "
+                                       f"step; cores = the BLAS threads numpy's matrix products ran on"},
             "e2e": {"value": round(value, 4), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

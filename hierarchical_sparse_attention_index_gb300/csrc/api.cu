@@ -41,15 +41,16 @@ bool device_info(uint32_t** status, int* sms) {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// Map a CUDA error to HSA_ERR_CUDA; with HSA_DEBUG set in the environment, name it on stderr.
+}  // namespace
+
 hsa_status cuda_fail(cudaError_t e, const char* where) {
   if (e == cudaSuccess) return HSA_OK;
   static const bool dbg = getenv("HSA_DEBUG") != nullptr;
   if (dbg) fprintf(stderr, "hsa: %s: %s\n", where, cudaGetErrorString(e));
   return HSA_ERR_CUDA;
 }
-inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 hsa_status check_cache(const hsa_cache* c) {
   if (!c || !c->kv_q || !c->kv_s || !c->ik_q || !c->ik_s) return HSA_ERR_INVALID_ARG;
@@ -67,9 +68,39 @@ hsa_status check_query(const hsa_cache* c, int32_t nq, int64_t max_vis) {
   return HSA_OK;
 }
 
+bool device_status_ptr(uint32_t** status, int* sms) { return device_info(status, sms); }
+
+namespace {
+struct SmemLimit {
+  int dev;
+  const void* func;
+  size_t bytes;
+};
+constexpr int kMaxSmemLimits = 256;
+SmemLimit g_smem_limits[kMaxSmemLimits];
+int g_n_smem_limits = 0;
 }  // namespace
 
-bool device_status_ptr(uint32_t** status, int* sms) { return device_info(status, sms); }
+cudaError_t ensure_smem_limit(const void* func, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int slot = -1;
+  for (int i = 0; i < g_n_smem_limits; ++i)
+    if (g_smem_limits[i].dev == dev && g_smem_limits[i].func == func) slot = i;
+  if (slot >= 0 && g_smem_limits[slot].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  if (slot < 0) {
+    if (g_n_smem_limits == kMaxSmemLimits) return cudaSuccess;   // set on every call from here on
+    slot = g_n_smem_limits++;
+    g_smem_limits[slot].dev = dev;
+    g_smem_limits[slot].func = func;
+  }
+  g_smem_limits[slot].bytes = bytes;
+  return cudaSuccess;
+}
 
 bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   if (batch < 1 || nq < 1 || nq > HSA_MAX_NQ || max_vis < 0 || max_vis > HSA_MAX_VIS) return false;
@@ -93,6 +124,7 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   L->off_blkmax = take((size_t)rows * L->ld_b * 4);
   L->off_cand_full = take((size_t)rows * (L->ld_s + L->ld_b) * 4);
   L->off_sure_full = take((size_t)rows * (kTopK + kCandBlocks) * 4);
+  L->full_end = o;
   // fused Reindex: per row, the 4 CTAs' lists of 64-bit (key, slot) composites (entries 0..2047
   // and 2048..4095 of each) and their (count, valid elements) pairs
   // attention partials: per row, 4 CTAs x (64 x 512 unnormalised outputs + 64 (max, sum) pairs)
@@ -100,6 +132,57 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
   L->off_attn = take(L->attn_bytes);
   L->total = o;
   return true;
+}
+
+hsa_status launch_index_full(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,
+                             int64_t max_vis, int32_t* topk_out, int32_t* pool_out, uint8_t* W,
+                             const WsLayout& L, cudaStream_t s) {
+  uint32_t* status;
+  int sms;
+  if (!device_info(&status, &sms)) return HSA_ERR_UNSUPPORTED;
+  ScanParams sp;
+  memset(&sp, 0, sizeof(sp));
+  sp.batch = cache->batch;
+  sp.nq = nq;
+  sp.cap = cache->capacity;
+  sp.ik_q = cache->ik_q;
+  sp.ik_s = cache->ik_s;
+  sp.q = static_cast<const uint16_t*>(q);
+  sp.w = w;
+  sp.vis = vis;
+  sp.status = status;
+  sp.n_seg = cache->batch;
+  sp.chunks_per_seg = (int32_t)((std::max(max_vis, (int64_t)1) + kScanChunk - 1) / kScanChunk);
+  sp.total_items = sp.n_seg * sp.chunks_per_seg;
+  sp.scores = reinterpret_cast<float*>(W + L.off_scores);
+  sp.ld_s = L.ld_s;
+  sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
+  sp.ld_b = L.ld_b;
+  sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_full);
+  sp.state = reinterpret_cast<SelState*>(W + L.off_state_full);
+  sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_full);
+  SelectParams se;
+  memset(&se, 0, sizeof(se));
+  se.batch = cache->batch;
+  se.nq = nq;
+  se.max_vis = max_vis;
+  se.vis = vis;
+  se.topk_out = topk_out;
+  se.pool_out = pool_out;
+  se.status = status;
+  se.scores = sp.scores;
+  se.ld_s = sp.ld_s;
+  se.blkmax = sp.blkmax;
+  se.ld_b = sp.ld_b;
+  se.hist = sp.hist;
+  se.state = sp.state;
+  se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_full);
+  se.ld_cand = L.ld_s + L.ld_b;
+  se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_full);
+  se.ld_sure = kTopK + kCandBlocks;
+  hsa_status r = cuda_fail(launch_index_scan(sp, sms, s), "index scan launch");
+  if (r != HSA_OK) return r;
+  return cuda_fail(launch_select(se, s), "select launch");
 }
 
 // inputs_ready: q and swa are complete when the kernel is launched (no kernel of the same
@@ -249,49 +332,7 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
     return cuda_fail(launch_reindex(rp, s), "reindex launch");
   }
 
-  ScanParams sp;
-  memset(&sp, 0, sizeof(sp));
-  sp.batch = cache->batch;
-  sp.nq = nq;
-  sp.cap = cache->capacity;
-  sp.ik_q = cache->ik_q;
-  sp.ik_s = cache->ik_s;
-  sp.q = static_cast<const uint16_t*>(q);
-  sp.w = w;
-  sp.vis = vis;
-  sp.status = status;
-  sp.n_seg = cache->batch;
-  sp.chunks_per_seg = (int32_t)((std::max(max_vis, (int64_t)1) + kScanChunk - 1) / kScanChunk);
-  sp.total_items = sp.n_seg * sp.chunks_per_seg;
-  sp.scores = reinterpret_cast<float*>(W + L.off_scores);
-  sp.ld_s = L.ld_s;
-  sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
-  sp.ld_b = L.ld_b;
-  sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_full);
-  sp.state = reinterpret_cast<SelState*>(W + L.off_state_full);
-  sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_full);
-  SelectParams se;
-  memset(&se, 0, sizeof(se));
-  se.batch = cache->batch;
-  se.nq = nq;
-  se.max_vis = max_vis;
-  se.vis = vis;
-  se.topk_out = topk_out;
-  se.pool_out = pool_out;
-  se.status = status;
-  se.scores = sp.scores;
-  se.ld_s = sp.ld_s;
-  se.blkmax = sp.blkmax;
-  se.ld_b = sp.ld_b;
-  se.hist = sp.hist;
-  se.state = sp.state;
-  se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_full);
-  se.ld_cand = L.ld_s + L.ld_b;
-  se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_full);
-  se.ld_sure = kTopK + kCandBlocks;
-  hsa_status r = cuda_fail(launch_index_scan(sp, sms, s), "index scan launch");
-  if (r != HSA_OK) return r;
-  return cuda_fail(launch_select(se, s), "select launch");
+  return launch_index_full(cache, q, w, vis, nq, max_vis, topk_out, pool_out, W, L, s);
 }
 
 hsa_status hsa_index_full(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,

@@ -5,8 +5,8 @@
 // One thread-block cluster of 4 CTAs per (request, query). CTA j owns 160 keys: top-k slots
 // [128j, 128j+128) and SWA window rows [32j, 32j+32). Four CTAs per row fit a batch of 32
 // requests in one wave of 128 SMs. Each CTA runs 16 worker warps and one MMA warp:
-//  1. the 64x512 bf16 query arrives by TMA: each CTA of the cluster loads 16 heads and
-//     multicasts them to all four, already in the 128B-swizzled K-major layout. The workers
+//  1. the 64x512 bf16 query arrives by TMA (each CTA loads all of it into its own shared
+//     memory), already in the 128B-swizzled K-major layout. The workers
 //     issue the row loads (the 160 rows, gathered once and shared by all 64 heads), convert
 //     the query in place to f16 after a per-head power-of-two shift (exact within f16; each
 //     warp owns 4 whole heads, so no block barrier), and dequantise the rows to f16
@@ -26,9 +26,9 @@
 //     sum_c' exp(m_c' - M) l_c', over c in rank order (deterministic). L2 moves the partials
 //     several times faster than distributed shared memory; the normalised partial is a convex
 //     combination of f16 tile values, so it cannot leave the f16 range.
-// Setup (TMEM allocation, barrier init, one cluster barrier so that peers may signal this
-// CTA's query barrier) runs before the programmatic-dependency wait, so it overlaps the tail
-// of the previous kernel in the stream. Every wait is bounded.
+// Setup (TMEM allocation, barrier init, the arrive half of a cluster barrier whose wait comes
+// before the first store into a peer's shared memory) runs before the programmatic-dependency
+// wait, so it overlaps the tail of the previous kernel in the stream. Every wait is bounded.
 #include "hsa_common.cuh"
 #include "hsa_internal.h"
 #include "hsa_tc.cuh"
@@ -72,14 +72,13 @@ __device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t m, uint32_t x) {
                                    __habs2(*reinterpret_cast<const __nv_bfloat162*>(&x)));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
-// 2-D tiled TMA load multicast to the CTAs in `mask`: the box lands at the same shared-memory
-// offset in each, and each destination's mbarrier at `bar` receives the byte count
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                               uint16_t mask) {
+// 2-D tiled TMA load of one box into this CTA's shared memory; the mbarrier at `bar` receives
+// the byte count
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -107,7 +106,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   int* s_valid = reinterpret_cast<int*>(misc + 256);      // [160]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(misc + 416);
   // mbarriers: [0] QK done, [1..4] PV tile done, [5..8] K-tile step s converted (all 16 warps),
-  // [9] query landed (64 KB from the four CTAs' multicasts)
+  // [9] query landed (64 KB)
   const uint32_t bar = smem_u32(misc + 418);
   const uint32_t kb_bar = bar + 8u * 5;
   const uint32_t q_bar = bar + 8u * 9;
@@ -134,17 +133,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_arrive();                   // every CTA's query barrier is initialised before any multicast
-  cluster_wait();
+  // Peers store into this CTA's (m, l) slots only once it runs: the matching wait comes right
+  // before each thread's first store into a peer (or, for the MMA warp, before phase A).
+  cluster_arrive();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
-  // query: this CTA's 16 heads, 8 boxes of 64 dims x 16 heads (2 KB each), to all 4 CTAs
+  // query: all 64 heads, 8 boxes of 64 dims x 64 heads (8 KB each), into this CTA's own shared
+  // memory
   auto issue_query = [&]() {
     if (warp == kWorkWarps && lane == 0) {
       mbar_arrive_expect_tx(q_bar, kQBytes);
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb)
-        tma_load_2d_mc(sQ + (uint32_t)kb * (kHAtt * 128u) + rank * (16u * 128u), &p.qmap, 64 * kb,
-                       row * kHAtt + 16 * (int)rank, q_bar, (uint16_t)((1u << kCluster) - 1u));
+        tma_load_2d(sQ + (uint32_t)kb * (kHAtt * 128u), &p.qmap, 64 * kb, row * kHAtt, q_bar);
     }
   };
   // SWA: this CTA's 32 window rows (w = 32 rank + r, position vis - 128 + w) are one contiguous
@@ -224,6 +224,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       }
     }
     __syncwarp();
+    cluster_wait();                   // setup barrier (arrived at the top)
     cluster_arrive();                 // phase A: (m, l) published
     cluster_wait();
     cluster_arrive();                 // phase B: partials published
@@ -443,7 +444,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   if (kq == 0) s_invl[hh] = (lsum > 0.f) ? 1.f / lsum : 0.f;
   fence_async_smem();
   named_bar_sync(2, kAttnThreads);    // P^T ready for the MMA warp; s_invl visible to every worker
-  // (m_c, l_c) of head hh go to the CTA that owns it (slot [rank][hh % 16]); read after phase A
+  // (m_c, l_c) of head hh go to the CTA that owns it (slot [rank][hh % 16]); read after phase A.
+  // Every peer has started (setup barrier).
+  cluster_wait();
   if (kq == 0) st_cluster_f2(smem_u32(s_ml + rank * 16 + (hh & 15)), (uint32_t)(hh >> 4), mloc, lsum);
   uint32_t* mine = part + (size_t)rank * kPartFloats;
   cluster_arrive();                   // phase A
@@ -570,21 +573,16 @@ EncodeTiledFn encode_tiled() {
 }  // namespace
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(sparse_attn_kernel), kSmemBytes);
+  if (e != cudaSuccess) return e;
   const int rows = p.batch * p.nq;
   const EncodeTiledFn encode = encode_tiled();
   if (!encode) return cudaErrorNotSupported;
   AttnParams a = p;
-  // q viewed as [rows * 64 heads][512 dims] bf16: a box is 64 dims (128 B, the swizzle span) x 16 heads
+  // q viewed as [rows * 64 heads][512 dims] bf16: a box is 64 dims (128 B, the swizzle span) x 64 heads
   const cuuint64_t dims[2] = {(cuuint64_t)kDLat, (cuuint64_t)rows * kHAtt};
   const cuuint64_t strides[1] = {(cuuint64_t)kDLat * 2};
-  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t box[2] = {64, 64};
   const cuuint32_t estr[2] = {1, 1};
   if (encode(&a.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.q), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

@@ -32,14 +32,33 @@ struct WsLayout {
   size_t off_attn;     // attention partials
   size_t attn_bytes;
   size_t zero_begin, zero_end;   // region that must be zero between calls (hist + state + counters)
+  size_t full_end;               // the Full call uses [0, full_end)
   size_t total;
 };
 
 bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L);
 
+// Host-side argument checks shared by the entry points (HSA_OK or the status to return).
+hsa_status check_cache(const hsa_cache* c);
+hsa_status check_query(const hsa_cache* c, int32_t nq, int64_t max_vis);
+// Map a CUDA error to HSA_ERR_CUDA; with HSA_DEBUG set in the environment, name it on stderr.
+hsa_status cuda_fail(cudaError_t e, const char* where);
+
+// The Full-mode indexer (scan, then selection) over checked arguments, with its scratch regions
+// at `ws` laid out by L. The region [L.zero_begin, L.zero_end) must be zero on entry; the
+// kernels leave it zero.
+hsa_status launch_index_full(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,
+                             int64_t max_vis, int32_t* topk_out, int32_t* pool_out, uint8_t* ws,
+                             const WsLayout& L, cudaStream_t s);
+
 // Device address of the per-device status word and the SM count of the current device;
 // false on a non-sm_100-family device.
 bool device_status_ptr(uint32_t** status, int* sms);
+
+// Raise the dynamic shared-memory limit of kernel `func` to `bytes` on the current device. The
+// attribute belongs to the device's context, so it is set once per (device, kernel) and again
+// whenever a larger size is asked for; thread-safe.
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
 
 // ------------------------------------------------------------------ index scoring
 struct ScanParams {         // Full mode: a segment is one request, its nq queries share K

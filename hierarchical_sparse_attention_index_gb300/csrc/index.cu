@@ -613,12 +613,8 @@ template <bool kOneQuery>
 cudaError_t launch_scan_variant(const ScanParams& p, int num_sms, cudaStream_t s) {
   const ScanSmemLayout L = scan_smem_layout(p.nq);
   auto kern = index_scan_kernel<kOneQuery>;
-  static int set_bytes = 0;        // the attribute is per function, set to the largest size seen
-  if ((int)L.total > set_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
-    if (e != cudaSuccess) return e;
-    set_bytes = (int)L.total;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), L.total);
+  if (e != cudaSuccess) return e;
   int per_sm = 1;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kScanThreads, L.total) != cudaSuccess ||
       per_sm < 1)
@@ -638,12 +634,8 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
   const int rows = p.batch * p.nq;
   const int64_t q = ((std::max<int64_t>(p.max_vis, 1) + kSelSplit - 1) / kSelSplit + 31) / 32;   // bitmap words of a quarter
   const size_t smem = (size_t)((q + 3) & ~3) * 4 + kHistBins * 4 + 64 * 4 + (size_t)kSelStage * 8;
-  static size_t set_bytes = 0;
-  if (smem > set_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    set_bytes = smem;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), smem);
+  if (e != cudaSuccess) return e;
   // one cluster of 4 CTAs per (row, selection): the position top-512, then the block top-2048
   return launch_pdl(select_kernel, dim3((unsigned)(rows * 2 * kSelSplit)), dim3(kSelThreads), smem, s, p);
 }

@@ -362,12 +362,8 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
 }  // namespace
 
 cudaError_t launch_reindex(const ReindexParams& p, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(reindex_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRxSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(reindex_kernel), kRxSmem);
+  if (e != cudaSuccess) return e;
   const int rows = p.batch * p.nq;
   return launch_pdl(reindex_kernel, dim3(rows * kRxCluster), dim3(kRxThreads), kRxSmem, s, p);
 }

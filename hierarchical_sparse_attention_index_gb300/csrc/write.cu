@@ -409,12 +409,8 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
 
 cudaError_t launch_cache_write(const WriteParams& p, cudaStream_t s) {
   auto kern = (p.ratio == 2) ? cache_write_kernel<2> : cache_write_kernel<1>;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[p.ratio - 1]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
-    if (e != cudaSuccess) return e;
-    attr_set[p.ratio - 1] = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), kWSmem);
+  if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
