@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libhsa.so")
 HSA_D_LATENT, HSA_D_INDEX, HSA_H_INDEX, HSA_H_ATTN = 512, 128, 16, 64
 HSA_TOPK, HSA_CAND_BLOCKS, HSA_BLOCK, HSA_POOL_SLOTS, HSA_SWA_W = 512, 2048, 8, 16384, 128
 HSA_MAX_NQ, HSA_MAX_VIS = 8, 1 << 20
+HSA_NOALLOC_SCRATCH_BYTES = 64 << 20
 HSA_SCALE_E8M0, HSA_SCALE_E4M3 = 0, 1
 HSA_MODE_FULL, HSA_MODE_REINDEX, HSA_MODE_REUSE = 0, 1, 2
 HSA_FLAG_INDEX_RANGE, HSA_FLAG_WRITE_RANGE, HSA_FLAG_TIMEOUT = 1, 2, 4
@@ -26,7 +27,7 @@ STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_SHAPE", 3: "HSA_ERR
 
 EXPORTS = ("hsa_abi_version", "hsa_status_string", "hsa_workspace_bytes", "hsa_workspace_init",
            "hsa_cache_write_compress", "hsa_index_full", "hsa_index_reindex", "hsa_sparse_attn_decode",
-           "hsa_schedule_step", "hsa_get_device_status", "hsa_index_reindex_noalloc")
+           "hsa_schedule_step", "hsa_get_device_status", "hsa_index_full_noalloc")
 
 
 class HsaError(RuntimeError):
@@ -76,7 +77,7 @@ def load_library(path: str = LIB_PATH):
         "hsa_sparse_attn_decode": (I32, [C, P, P, P, P, I32, I64, F, P, P, SZ, P]),
         "hsa_schedule_step": (I32, [C, ctypes.POINTER(hsa_step_args), P, SZ, P]),
         "hsa_get_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32)]),
-        "hsa_index_reindex_noalloc": (I32, [C, P, P, P, I32, I64, P, P, P]),
+        "hsa_index_full_noalloc": (I32, [C, P, P, P, I32, I64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -175,11 +176,13 @@ def hsa_index_reindex(cache: Cache, q, w, vis, nq, max_vis, pool, topk_out, ws, 
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def hsa_index_reindex_noalloc(cache: Cache, q, w, vis, nq, max_vis, pool, topk_out, stream=None):
-    """Reindex without a caller workspace: the scratch is a fixed array inside the library
-    (batch * nq <= 32). For callers that cannot allocate device memory."""
-    _check("hsa_index_reindex_noalloc", load_library().hsa_index_reindex_noalloc(
-        cache.ref, _ptr(q), _ptr(w), _ptr(vis), nq, max_vis, _ptr(pool), _ptr(topk_out), _stream(stream)))
+def hsa_index_full_noalloc(cache: Cache, q, w, vis, nq, max_vis, topk_out, pool_out, stream=None):
+    """hsa_index_full for callers that cannot allocate device memory: its scratch is a fixed
+    array inside the library (HSA_NOALLOC_SCRATCH_BYTES), shared by every call, so calls that
+    overlap on the GPU race. The first call on a device looks up the array's address there and
+    should come before any stream capture."""
+    _check("hsa_index_full_noalloc", load_library().hsa_index_full_noalloc(
+        cache.ref, _ptr(q), _ptr(w), _ptr(vis), nq, max_vis, _ptr(topk_out), _ptr(pool_out), _stream(stream)))
 
 
 def hsa_sparse_attn_decode(cache: Cache, q, topk, swa, vis, nq, max_vis, sm_scale, out, ws, stream=None):

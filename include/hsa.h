@@ -187,17 +187,29 @@ HSA_API hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, cons
                              int32_t nq, int64_t max_vis, const int32_t* pool, int32_t* topk_out,
                              void* ws, size_t ws_bytes, hsa_stream_t stream);
 
-/* Reindex without a workspace. The pages have no counterpart for this entry point; it is a
- * convenience of this library. Some callers cannot allocate device memory at all: a plugin
- * that may only touch the buffers it is handed, code running inside an arena planned by an
- * inference server, or a latency-critical loop that must never wait on an allocator. They call
- * this instead of hsa_index_reindex. Arguments, outputs and errors are those of
- * hsa_index_reindex, without ws/ws_bytes. The fused Reindex kernel keeps everything its CTAs
- * exchange in shared memory, so no scratch memory is used; calls on different streams are
- * independent. It calls no cudaMalloc/cudaFree and no allocating library routine. */
-HSA_API hsa_status hsa_index_reindex_noalloc(const hsa_cache* cache, const void* q, const float* w,
-                                             const int32_t* vis, int32_t nq, int64_t max_vis, const int32_t* pool,
-                                             int32_t* topk_out, hsa_stream_t stream);
+/* Size of the fixed device array behind hsa_index_full_noalloc: 64 MiB on every device that
+ * loads the library, held until the process exits. */
+#define HSA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+
+/* The Full-mode indexer without a caller workspace. The pages have no counterpart for this
+ * entry point; it is a convenience of this library for callers that cannot allocate device
+ * memory: a plugin that may only touch the buffers it is handed, code running inside a memory
+ * arena an inference server planned in advance, or a latency-critical loop that must never wait
+ * on an allocator. Arguments, outputs and results are those of hsa_index_full without ws and
+ * ws_bytes. The scratch the two Full kernels need lives in a fixed array of
+ * HSA_NOALLOC_SCRATCH_BYTES inside the library. Limits and behaviour:
+ *  - sizes whose Full scratch exceeds the array (about 41 B per row and visible position, e.g.
+ *    batch 32 x 1 query x 131,072 positions fits) return HSA_ERR_WORKSPACE; nothing is launched;
+ *  - the first call on a device looks up the array's address on that device; make that first
+ *    call before any stream capture;
+ *  - every call shares the array: each one clears the part that must start at zero with a
+ *    cudaMemsetAsync on `stream` before its kernels, and two calls that overlap on the GPU (other
+ *    streams, other threads) race on it;
+ *  - it calls no cudaMalloc / cudaFree and no allocating library routine.
+ * Other errors are those of hsa_index_full. */
+HSA_API hsa_status hsa_index_full_noalloc(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis,
+                                          int32_t nq, int64_t max_vis, int32_t* topk_out, int32_t* pool_out,
+                                          hsa_stream_t stream);
 
 /* Sparse attention ([CED] Figure 4: Selected Main KV ⊕ SWA KV -> Core Attention;
  * [890B] 注意力实际有多稀: 512 + 128 = 640 positions; [ARCH] §7: dequantise before attention).
