@@ -114,19 +114,14 @@ bool make_ws_layout(int32_t batch, int32_t nq, int64_t max_vis, WsLayout* L) {
     o += (bytes + 255) & ~(size_t)255;
     return at;
   };
-  // zero-between-calls region first
+  // zero-between-calls region first: the block-max histograms of the Full scan
   L->zero_begin = 0;
-  L->off_hist_full = take((size_t)rows * 2 * kHistBins * 4);
-  L->off_state_full = take((size_t)rows * 2 * sizeof(SelState));
-  L->off_done_full = take((size_t)batch * 4);
+  L->off_hist_full = take((size_t)rows * kHistBins * 4);
   L->zero_end = o;
   L->off_scores = take((size_t)rows * L->ld_s * 4);
   L->off_blkmax = take((size_t)rows * L->ld_b * 4);
-  L->off_cand_full = take((size_t)rows * (L->ld_s + L->ld_b) * 4);
-  L->off_sure_full = take((size_t)rows * (kTopK + kCandBlocks) * 4);
+  L->off_cand_full = take((size_t)rows * 2 * L->ld_b * 4);
   L->full_end = o;
-  // fused Reindex: per row, the 4 CTAs' lists of 64-bit (key, slot) composites (entries 0..2047
-  // and 2048..4095 of each) and their (count, valid elements) pairs
   // attention partials: per row, 4 CTAs x (64 x 512 unnormalised outputs + 64 (max, sum) pairs)
   L->attn_bytes = (size_t)rows * kAttnSplit * (kHAtt * kDLat + 2 * kHAtt) * 4;
   L->off_attn = take(L->attn_bytes);
@@ -159,8 +154,6 @@ hsa_status launch_index_full(const hsa_cache* cache, const void* q, const float*
   sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
   sp.ld_b = L.ld_b;
   sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_full);
-  sp.state = reinterpret_cast<SelState*>(W + L.off_state_full);
-  sp.seg_done = reinterpret_cast<uint32_t*>(W + L.off_done_full);
   SelectParams se;
   memset(&se, 0, sizeof(se));
   se.batch = cache->batch;
@@ -175,11 +168,8 @@ hsa_status launch_index_full(const hsa_cache* cache, const void* q, const float*
   se.blkmax = sp.blkmax;
   se.ld_b = sp.ld_b;
   se.hist = sp.hist;
-  se.state = sp.state;
   se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_full);
-  se.ld_cand = L.ld_s + L.ld_b;
-  se.sure = reinterpret_cast<int32_t*>(W + L.off_sure_full);
-  se.ld_sure = kTopK + kCandBlocks;
+  se.ld_cand = 2 * L.ld_b;
   hsa_status r = cuda_fail(launch_index_scan(sp, sms, s), "index scan launch");
   if (r != HSA_OK) return r;
   return cuda_fail(launch_select(se, s), "select launch");

@@ -37,49 +37,6 @@ __device__ __forceinline__ int excl_scan(int v, int* scratch, int bar_id, int nt
   return before + x - v;
 }
 
-// Threshold bin for a top-K over a 4096-bin histogram (the bin holding the K-th largest key) and
-// the counts above it, written to *st with ready = 1; NT threads, named barrier 1, thread
-// indices 0..NT-1 taken from `tid`.
-template <int NT>
-__device__ void compute_threshold(const uint32_t* ghist, int K, SelState* st, int* scratch, int tid = -1) {
-  if (tid < 0) tid = threadIdx.x;
-  constexpr int kPerT = kHistBins / NT;   // bins per thread
-  uint32_t cnt[kPerT];
-  int local = 0;
-  const int top = kHistBins - kPerT * (tid + 1);   // this thread owns bins [top, top+kPerT), high first
-#pragma unroll
-  for (int i = 0; i < kPerT; ++i) {
-    cnt[i] = __ldcg(ghist + top + kPerT - 1 - i);
-    local += (int)cnt[i];
-  }
-  int total;
-  const int excl = excl_scan(local, scratch, 1, NT, &total, tid);
-  if (total <= K) {
-    if (tid == 0) {
-      st->thr_bin = -1;
-      st->above = total;
-      st->nvalid = total;
-      __threadfence();
-      st->ready = 1;
-    }
-  } else if (excl < K && excl + local >= K) {
-    int run = excl;
-#pragma unroll
-    for (int i = 0; i < kPerT; ++i) {
-      if (run + (int)cnt[i] >= K) {
-        st->thr_bin = top + kPerT - 1 - i;
-        st->above = run;
-        st->nvalid = total;
-        __threadfence();
-        st->ready = 1;
-        break;
-      }
-      run += (int)cnt[i];
-    }
-  }
-  named_bar_sync(1, NT);
-}
-
 // Threshold bin of a top-K over a 4096-bin histogram in shared memory held by NT threads (thread 0
 // holding the highest bins): the bin holding the K-th largest key and the count above it go to
 // out[0], out[1]; -1 and the total when the histogram holds K or fewer. Returns the total. All

@@ -11,27 +11,15 @@
 
 namespace hsa {
 
-// Per selection row (one top-k over one array) state kept in the workspace. All counters are
-// zero between calls.
-struct SelState {
-  int32_t thr_bin;   // threshold histogram bin; -1 = every valid element is taken
-  int32_t above;     // elements in bins above thr_bin
-  int32_t nvalid;    // valid elements of the row
-  int32_t nsure;     // unused (kept zero)
-  int32_t ncand;     // unused (kept zero)
-  int32_t ready;     // 1 once thr_bin/above/nvalid are written for this call
-  int32_t pad[2];
-};
-
 // Workspace carve-up for hsa_index_full / hsa_index_reindex / hsa_sparse_attn_decode.
 struct WsLayout {
   int32_t rows;        // batch * nq
   int64_t ld_s;        // score row stride (positions), a multiple of kScanChunk
   int64_t ld_b;        // block-max row stride (blocks) = ld_s / 8
-  size_t off_scores, off_blkmax, off_hist_full, off_cand_full, off_sure_full, off_state_full, off_done_full;
+  size_t off_scores, off_blkmax, off_hist_full, off_cand_full;
   size_t off_attn;     // attention partials
   size_t attn_bytes;
-  size_t zero_begin, zero_end;   // region that must be zero between calls (hist + state + counters)
+  size_t zero_begin, zero_end;   // region that must be zero between calls (the block-max histograms)
   size_t full_end;               // the Full call uses [0, full_end)
   size_t total;
 };
@@ -76,13 +64,11 @@ struct ScanParams {         // Full mode: a segment is one request, its nq queri
   int64_t ld_s;
   float* blkmax;         // [rows][ld_b]
   int64_t ld_b;
-  uint32_t* hist;        // [rows][2][4096]
-  SelState* state;       // [rows][2]
-  uint32_t* seg_done;    // [n_seg]
+  uint32_t* hist;        // [rows][4096] counts of the block maxima's top 12 key bits
   uint32_t* status;
 };
 
-struct SelectParams {       // the Full step's position top-512 and block top-2048
+struct SelectParams {       // the Full step's block top-2048 (pool) and position top-512
   int32_t batch, nq;
   int64_t max_vis;
   const int32_t* vis;
@@ -90,12 +76,9 @@ struct SelectParams {       // the Full step's position top-512 and block top-20
   int64_t ld_s;
   const float* blkmax;
   int64_t ld_b;
-  uint32_t* hist;
-  SelState* state;
-  int32_t* cand;         // [rows][ld_s + ld_b]
+  uint32_t* hist;        // [rows][4096], cleared by the selection
+  int32_t* cand;         // [rows][2 * ld_b] threshold-bin candidates past the shared-memory stage
   int64_t ld_cand;
-  int32_t* sure;         // [rows][512 + 2048]
-  int64_t ld_sure;
   int32_t* topk_out;     // [rows][512]
   int32_t* pool_out;     // [rows][16384]
   uint32_t* status;

@@ -13,16 +13,22 @@
 //    fp32 to the per-group accumulator. The query is converted once per segment to f16, after a
 //    per-head power-of-two shift that keeps its largest element in [2^14, 2^15). The shift is
 //    folded back into the head weight.
-//  - The epilogue fuses the ReLU-weighted head sum, the visibility mask, the 8-entry block max
-//    ([ARCH] §3.3 块 max 是上界) and a 4096-bin histogram of the top 12 bits of each score's
-//    order key. The last CTA to finish a request turns the histograms into the threshold bins
-//    of the position top-512 and the block top-2048.
-// Selection (exact; ties to the lower index), one 4-CTA cluster per (row, selection), each CTA
-// streaming a quarter of the array: elements above the threshold bin are taken, elements in it
-// become candidates, and after one cluster barrier a count or an 11-bit-digit radix select over
-// (low key bits, inverted index) composites picks the remaining ones. Each quarter's bitmap is
-// emitted in ascending order at its offset (blocks expanded into the candidate pool), and the
-// workspace state is cleared.
+//  - The epilogue fuses the ReLU-weighted head sum, the visibility mask and the 8-entry block
+//    max ([ARCH] §3.3 块 max 是上界). It stores each score and each block max, and counts the
+//    block maxima in a 4096-bin histogram of the top 12 bits of their order keys (one count per
+//    block; positions are not histogrammed).
+// Selection (exact; ties to the lower index), one CTA per (request, query) row, from the block
+// maxima alone plus 4,096 scores ([ARCH] §3.3 时序澄清: both top-k's come from the one score
+// pass):
+//  - the histogram gives the threshold bins of the block top-2048 (the pool) and of the block
+//    top-512; one pass over the row's block maxima takes the blocks above each threshold bin
+//    and lists those inside it, and an exact cut among the listed ones completes both sets;
+//  - the position top-512 lies inside the positions of the top-512 blocks: a block ranked
+//    below them has at least 512 positions ranked above all of its own (each better block's
+//    maximum), so none of its positions can be in the top 512. The kernel reads the 4,096
+//    scores of those blocks and cuts the exact top-512 among them;
+//  - the pool (blocks expanded to 8 slots) and the top-512 are written in ascending order, and
+//    the row's histogram is cleared for the next call.
 #include <algorithm>
 
 #include "hsa_common.cuh"
@@ -40,7 +46,7 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kScanThreads = kConsumers + 32;
 constexpr int kCodesBytes = kChunk * 64;
 constexpr int kScaleBytes = kChunk * 4;
-constexpr int kFlushItems = 120;   // packed 16-bit histogram counters: flush before 65536 entries
+constexpr int kFlushItems = 960;   // packed 16-bit histogram counters (64 blocks per item): flush before 65536
 
 struct ScanSmemLayout {
   int nst, nlr;
@@ -51,7 +57,7 @@ __host__ __device__ inline ScanSmemLayout scan_smem_layout(int nq) {
   ScanSmemLayout L;
   const int nql = nq;
   L.nst = (nql <= 2) ? 3 : (nql <= 5 ? 2 : 1);
-  L.nlr = 2 * nq;
+  L.nlr = nq;                          // one block-max histogram per query
   size_t o = 0;
   L.codes = o;   o += (size_t)L.nst * kCodesBytes;
   L.scales = o;  o += (size_t)L.nst * kScaleBytes;
@@ -73,7 +79,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   const int nql = kOneQuery ? 1 : p.nq;
   const int nst = kOneQuery ? 3 : L.nst;   // compile-time where it can be (scan_smem_layout)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [1] last flag, [2..9] vis, [16..48) scratch
+  int* misc = reinterpret_cast<int*>(smem + L.misc);   // [0] abort, [2..9] vis
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -154,17 +160,15 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
   uint32_t* bfrag = reinterpret_cast<uint32_t*>(smem + L.bfrag);
   float* wsc = reinterpret_cast<float*>(smem + L.wsc);
   int* svis = misc + 2;
-  int* scratch = misc + 16;
 
   uint32_t B[2][8][2];   // query fragments of the current query (registers)
   float wr[2][2];
-  int cur_seg = -1, seg_items = 0, since_flush = 0;
+  int cur_seg = -1, since_flush = 0;
 
   auto flush_hist = [&](int seg) {
     named_bar_sync(1, kConsumers);
     for (int lr = 0; lr < L.nlr; ++lr) {
-      const int grow = (seg * p.nq + (lr >> 1)) * 2 + (lr & 1);
-      uint32_t* gh = p.hist + (size_t)grow * kHistBins;
+      uint32_t* gh = p.hist + (size_t)(seg * p.nq + lr) * kHistBins;
       uint32_t* sh = hist_sm + lr * (kHistBins / 2);
       for (int i = tid; i < kHistBins / 2; i += kConsumers) {
         const uint32_t v = sh[i];
@@ -174,27 +178,6 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
           sh[i] = 0;
         }
       }
-    }
-    __threadfence();
-    named_bar_sync(1, kConsumers);
-  };
-
-  auto finish_segment = [&](int seg, int nitems) {
-    flush_hist(seg);
-    if (tid == 0) {
-      const unsigned old = atomicAdd(p.seg_done + seg, (unsigned)nitems);
-      misc[1] = (old + (unsigned)nitems == (unsigned)cps) ? 1 : 0;
-    }
-    named_bar_sync(1, kConsumers);
-    if (misc[1]) {
-      __threadfence();
-      for (int q = 0; q < p.nq; ++q) {
-        const int row = seg * p.nq + q;
-        compute_threshold<kConsumers>(p.hist + (size_t)(2 * row) * kHistBins, kTopK, p.state + 2 * row, scratch);
-        compute_threshold<kConsumers>(p.hist + (size_t)(2 * row + 1) * kHistBins, kCandBlocks, p.state + 2 * row + 1,
-                                      scratch);
-      }
-      if (tid == 0) p.seg_done[seg] = 0;
     }
     named_bar_sync(1, kConsumers);
   };
@@ -223,9 +206,8 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
 
   for (int it = i0; it < i1; ++it) {
     if (seg != cur_seg) {
-      if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
+      if (cur_seg >= 0) flush_hist(cur_seg);
       cur_seg = seg;
-      seg_items = 0;
       since_flush = 0;
       load_segment(seg);
       if (nql == 1) load_query_regs(0);
@@ -236,7 +218,6 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       flush_hist(seg);
       since_flush = 0;
     }
-    ++seg_items;
     ++since_flush;
     if (!dead && *reinterpret_cast<volatile int*>(misc) != 0) dead = true;
     if (!dead && !mbar_wait(full0 + 8 * s, ph)) {
@@ -261,11 +242,9 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
         float v = score_rows32(codes, row_off, sf_base, two, B, wr, lane);
         const bool ok = c * kChunk + r_mine < svis[ql];
         v = ok ? v : -INFINITY;
-        const uint32_t bin = order_key(v) >> kHistShift;
         {
           const int row = cur_seg * p.nq + ql;
           p.scores[(size_t)row * p.ld_s + c * kChunk + r_mine] = v;
-          if (ok) atomicAdd(hist_sm + (2 * ql) * (kHistBins / 2) + (bin >> 1), (bin & 1) ? 0x10000u : 1u);
           // 8-entry block max: block t of the warp is held by lanes g = 0..7 of column t
           float bm = v;
           bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
@@ -275,7 +254,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
           if (g == 0 && jb * 8 < svis[ql]) {
             p.blkmax[(size_t)row * p.ld_b + jb] = bm;
             const uint32_t bb = order_key(bm) >> kHistShift;
-            atomicAdd(hist_sm + (2 * ql + 1) * (kHistBins / 2) + (bb >> 1), (bb & 1) ? 0x10000u : 1u);
+            atomicAdd(hist_sm + ql * (kHistBins / 2) + (bb >> 1), (bb & 1) ? 0x10000u : 1u);
           }
         }
       }
@@ -291,290 +270,297 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       ++seg;
     }
   }
-  if (cur_seg >= 0) finish_segment(cur_seg, seg_items);
+  if (cur_seg >= 0) flush_hist(cur_seg);
 }
 
 // ------------------------------------------------------------------ select
 constexpr int kSelThreads = 512;
-constexpr int kSelSplit = 4;        // CTAs (one cluster) per (row, selection)
-constexpr int kSelStage = 4096;     // candidates ranked from shared memory; more are ranked from L2
-constexpr int kSelRankMax = 512;    // candidates ranked by counting up to this many
+constexpr int kSelStage = 4096;     // threshold-bin candidates ranked from shared memory; more from L2
+constexpr int kSelRankMax = 512;    // elements ranked by counting up to this many
+constexpr int kTopBlocks = kTopK;   // the position top-512 lies inside the top-512 blocks
+constexpr int kPosCand = kTopBlocks * kBlk;   // 4096 position candidates
 
-// the smallest float whose order key is `key` (inverse of order_key)
-__device__ __forceinline__ float key_to_float(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+// (order key, inverted index): larger = better, ties to the lower index
+__device__ __forceinline__ uint64_t sel_comp(float v, uint32_t idx) {
+  return ((uint64_t)order_key(v) << 32) | (uint64_t)(~idx);
 }
 
-// The exact top-K of one score array (positions, or 8-position block maxima), emitted ascending,
-// by one cluster of 4 CTAs, CTA r owning the quarter [r Q, (r + 1) Q) of the array:
-//  1. stream the quarter once: an element whose 12-bit key bin lies above the threshold bin the
-//     score pass found is taken at once (a bit in the quarter's bitmap); an element in the
-//     threshold bin becomes a candidate (its index, written to the workspace). A float compare
-//     against the bin's lowest value rejects most elements before any key arithmetic;
-//  2. each CTA publishes (taken, candidates) counts; after one cluster barrier every CTA makes
-//     the same cut among all candidates by (low key bits desc, index asc): a histogram of their
-//     next 12 key bits, then a count over those left in its threshold bin (an 11-bit-digit radix
-//     select when many tie in 24 key bits) - and marks its own;
-//  3. each CTA emits its quarter's bitmap in ascending order at the offset the counts give
-//     (blocks expanded into 8 pool positions); CTA 0 pads the tail and clears the row's histogram
-//     and selection state for the next call.
-__global__ void __cluster_dims__(kSelSplit, 1, 1) __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
-  extern __shared__ __align__(16) uint32_t fsm[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rank = (int)cluster_rank();
-  const int unit = blockIdx.x / kSelSplit;            // (row, selection)
-  const int row = unit >> 1, which = unit & 1;
-  griddep_wait();
-  griddep_launch_dependents();
-  const int vis = (int)imin64(__ldg(p.vis + row), p.max_vis);
-  const float* data;
-  int n, K;
-  if (which == 0) {
-    data = p.scores + (size_t)row * p.ld_s;
-    n = vis;
-    K = kTopK;
-  } else {
-    data = p.blkmax + (size_t)row * p.ld_b;
-    n = (vis + kBlk - 1) / kBlk;
-    K = kCandBlocks;
-  }
-  SelState* st = p.state + 2 * row + which;
-  const int Q = ((n + kSelSplit - 1) / kSelSplit + 31) & ~31;   // quarter length, a multiple of 32
-  const int lo = min(n, rank * Q), hi = min(n, lo + Q);
-  const int nwq = Q >> 5;                              // bitmap words of a quarter
-  uint32_t* bitmap = fsm;                              // [nwq]
-  uint32_t* shist = fsm + ((nwq + 3) & ~3);           // [4096] second-level bins, then radix digits
-  int* scratch = reinterpret_cast<int*>(shist + kHistBins);   // [64]
-  uint64_t* cst = reinterpret_cast<uint64_t*>(scratch + 64);   // [kSelStage] candidate composites
-  // candidate indices of CTA c: the workspace's candidate row, split in quarters
-  int* cand_row = p.cand + (size_t)row * p.ld_cand + (which ? p.ld_s : 0);
-  int* xcnt = p.sure + (size_t)row * p.ld_sure + 8 * which;   // [4 CTAs][taken, candidates]
+struct SelShared {
+  uint32_t hist[kHistBins];
+  uint64_t rk[kSelRankMax];
+  int scr[128];
+  uint64_t cut;
+  int ncand[1];
+  int n_rk;
+};
 
-  __shared__ int s_thr, s_nvalid, s_ready, s_ncand, s_nsure;
-  __shared__ int s_digit, s_above, s_cnt;
-  __shared__ int s_taken[kSelSplit];
-  __shared__ __align__(8) uint64_t s_cut;
-  __shared__ __align__(8) uint64_t s_rk[kSelRankMax];   // candidates ranked by counting
-  __shared__ int s_out[2], s_nrk;
-  if (tid == 0) {
-    volatile SelState* vs = st;
-    s_ready = vs->ready;
-    s_thr = vs->thr_bin;
-    s_nvalid = vs->nvalid;
-    s_ncand = 0;
-    s_nsure = 0;
-  }
-  if (tid < kSelSplit) s_taken[tid] = 0;
-  if (tid == 0) s_nrk = 0;
-  for (int i = tid; i < nwq; i += kSelThreads) bitmap[i] = 0;
+// Completes an exact top-`need` among the C candidates comp(0..C-1) (distinct 64-bit
+// composites, larger = better) whose bits under `mask` all equal `prefix`; on return a candidate
+// c is taken iff (c & mask) >= prefix. Levels: a 4096-bin histogram of composite bits 51..40,
+// then counting when at most kSelRankMax remain tied, else a radix select over bits 39..0 in
+// 11-bit digits. All kSelThreads threads call it.
+template <typename CompFn>
+__device__ void cut_candidates(CompFn comp, int C, int need, SelShared& S, uint64_t& prefix, uint64_t& mask,
+                               int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
+  if (need >= C) return;             // every candidate is taken
+  for (int i = tid; i < kHistBins; i += kSelThreads) S.hist[i] = 0u;
   __syncthreads();
-  const int thr = s_ready ? s_thr : -1;
-  const int Keff = min(K, s_ready ? s_nvalid : 0);
-
-  // 1. one pass over the quarter: 8 float4 loads in flight per thread
-  const float f_lo = (thr < 0) ? -INFINITY : key_to_float((uint32_t)thr << kHistShift);
-  int* my_cand = cand_row + (size_t)rank * Q;
-  for (int base = lo; base < hi; base += 32 * kSelThreads) {
-    float4 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e0 = base + 4 * (u * kSelThreads + tid);
-      v[u] = (e0 < hi) ? __ldcg(reinterpret_cast<const float4*>(data + e0))
-                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e0 = base + 4 * (u * kSelThreads + tid);
-      const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = e0 + j;
-        if (!(f[j] >= f_lo) || f[j] == -INFINITY || e >= hi) continue;
-        const uint32_t key = order_key(f[j]);
-        const int bin = (int)(key >> kHistShift);
-        if (thr < 0 || bin > thr) {
-          atomicOr(bitmap + ((e - lo) >> 5), 1u << ((e - lo) & 31));
-          atomicAdd(&s_nsure, 1);
-        } else if (bin == thr) {
-          my_cand[atomicAdd(&s_ncand, 1)] = e;          // at most Q per quarter
-        }
-      }
-    }
+  for (int i = tid; i < C; i += kSelThreads) {
+    const uint64_t c = comp(i);
+    if ((c & mask) == prefix) atomicAdd(S.hist + ((c >> 40) & 0xFFFu), 1u);
   }
   __syncthreads();
-  if (tid == 0) {
-    __stcg(xcnt + 2 * rank, s_nsure);
-    __stcg(xcnt + 2 * rank + 1, s_ncand);
+  const int tied = smem_threshold<kSelThreads>(S.hist, need, S.scr, S.scr + 64, tid);
+  if (tied <= need) {                // every tied candidate is taken
+    __syncthreads();
+    return;
   }
-  cluster_sync_all();                 // every quarter's counts and candidates are in L2
-
-  // 2. the cut among the candidates: candidate i is taken iff (comp & mask) >= prefix
-  int sure_c[kSelSplit], cbase[kSelSplit], S = 0, C = 0;
-#pragma unroll
-  for (int c = 0; c < kSelSplit; ++c) {
-    sure_c[c] = __ldcg(xcnt + 2 * c);
-    cbase[c] = C;
-    C += __ldcg(xcnt + 2 * c + 1);
-    S += sure_c[c];
-  }
-  const int need = Keff - S;
-  auto cta_of = [&](int i) {
-    int c = 0;
-#pragma unroll
-    for (int d = 1; d < kSelSplit; ++d) c += (i >= cbase[d]) ? 1 : 0;
-    return c;
-  };
-  // composite of candidate i (global index over the four lists): low key bits, inverted index
-  auto comp_at = [&](int i) -> uint64_t {
-    const int c = cta_of(i);
-    const int e = __ldcg(cand_row + (size_t)c * Q + (i - cbase[c]));
-    return ((uint64_t)(order_key(__ldcg(data + e)) & 0xFFFFFu) << 32) | (uint64_t)(~(uint32_t)e);
-  };
-  const bool none = (thr < 0) || (need <= 0);
-  uint64_t prefix = none ? ~0ull : 0ull, mask = none ? ~0ull : 0ull;   // none: no composite reaches ~0
-  if (!none && need < C) {
-    const bool staged = C <= kSelStage;
-    if (staged) {
-      for (int i = tid; i < C; i += kSelThreads) cst[i] = comp_at(i);
-      named_bar_sync(1, kSelThreads);
-    }
-    auto comp = [&](int i) -> uint64_t { return staged ? cst[i] : comp_at(i); };
-    // level 2: a 4096-bin histogram of the next 12 key bits (composite bits 51..40) narrows the
-    // candidates still to be ranked to those sharing 24 key bits
-    for (int i = tid; i < kHistBins; i += kSelThreads) shist[i] = 0u;
-    named_bar_sync(1, kSelThreads);
-    for (int i = tid; i < C; i += kSelThreads) atomicAdd(shist + ((comp(i) >> 40) & 0xFFFu), 1u);
-    named_bar_sync(1, kSelThreads);
-    smem_threshold<kSelThreads>(shist, need, scratch, s_out, tid);
-    const int thr2 = s_out[0];
-    const int need_r = need - s_out[1];
-    prefix = (uint64_t)thr2 << 40;
-    mask = 0xFFFull << 40;
-    const int C2 = (int)shist[thr2];
-    if (need_r < C2 && C2 <= kSelRankMax) {
-      // few left: the need_r-th largest of them by counting (composites are distinct)
-      for (int i0 = warp * 32; i0 < C; i0 += kSelThreads) {
-        const int i = i0 + lane;
-        const uint64_t c64 = (i < C) ? comp(i) : 0ull;
-        const bool in = (i < C) && (c64 & mask) == prefix;
-        const int j = warp_append(in, &s_nrk, lane);
-        if (in) s_rk[j] = c64;
-      }
-      named_bar_sync(1, kSelThreads);
-      for (int i = tid; i < C2; i += kSelThreads) {
-        const uint64_t ci = s_rk[i];
-        int better = 0;
-        for (int j = 0; j < C2; ++j) better += (s_rk[j] > ci) ? 1 : 0;
-        if (better == need_r - 1) s_cut = ci;
-      }
-      named_bar_sync(1, kSelThreads);
-      prefix = s_cut;
-      mask = ~0ull;
-    } else if (need_r < C2) {
-      // many left (ties in 24 key bits): radix select, 11-bit digits over composite bits 39..0
-      int remaining = need_r;
-      const int shifts[4] = {29, 18, 7, 0};
-      const int widths[4] = {11, 11, 11, 7};
-      constexpr int kPerD = 2048 / kSelThreads;        // 4 digit bins per thread, high first
-      for (int d = 0; d < 4; ++d) {
-        const int sh = shifts[d];
-        const uint32_t wm = (1u << widths[d]) - 1u;
-        named_bar_sync(1, kSelThreads);
-        for (int i = tid; i < 2048; i += kSelThreads) shist[i] = 0u;
-        named_bar_sync(1, kSelThreads);
-        for (int i = tid; i < C; i += kSelThreads) {
-          const uint64_t c64 = comp(i);
-          if ((c64 & mask) == prefix) atomicAdd(shist + ((c64 >> sh) & wm), 1u);
-        }
-        named_bar_sync(1, kSelThreads);
-        const int dtop = 2048 - kPerD * (tid + 1);
-        int dc[kPerD], dl = 0;
-#pragma unroll
-        for (int i = 0; i < kPerD; ++i) {
-          dc[i] = (int)shist[dtop + kPerD - 1 - i];
-          dl += dc[i];
-        }
-        int dtot;
-        const int dex = excl_scan(dl, scratch, 1, kSelThreads, &dtot, tid);
-        if (dex < remaining && dex + dl >= remaining) {
-          int run = dex;
-#pragma unroll
-          for (int i = 0; i < kPerD; ++i) {
-            if (run + dc[i] >= remaining) {
-              s_digit = dtop + kPerD - 1 - i;
-              s_above = run;
-              s_cnt = dc[i];
-              break;
-            }
-            run += dc[i];
-          }
-        }
-        named_bar_sync(1, kSelThreads);
-        remaining -= s_above;
-        prefix |= (uint64_t)s_digit << sh;
-        mask |= (uint64_t)wm << sh;
-        const bool all_in = (s_cnt == remaining);
-        named_bar_sync(1, kSelThreads);
-        if (all_in) break;
-      }
-    }
-  }
-  if (!none) {
-    // mark this quarter's taken candidates; count every CTA's
-    int taken_c[kSelSplit] = {0, 0, 0, 0};
+  const int thr2 = S.scr[64];
+  int need_r = need - S.scr[65];
+  prefix |= (uint64_t)thr2 << 40;
+  mask |= 0xFFFull << 40;
+  const int C2 = (int)S.hist[thr2];
+  __syncthreads();                   // S.scr and S.hist read everywhere
+  if (need_r >= C2) return;          // the whole bin is taken
+  if (C2 <= kSelRankMax) {
+    // few left: the need_r-th largest of them by counting
+    if (tid == 0) S.n_rk = 0;
+    __syncthreads();
     for (int i0 = warp * 32; i0 < C; i0 += kSelThreads) {
       const int i = i0 + lane;
-      const uint64_t c64 = (i < C) ? (C <= kSelStage && need < C ? cst[i] : comp_at(i)) : 0ull;
-      const bool taken = (i < C) && (c64 & mask) >= prefix;
-      const int c = cta_of(i);
+      const uint64_t c = (i < C) ? comp(i) : 0ull;
+      const bool in = (i < C) && (c & mask) == prefix;
+      const int j = warp_append(in, &S.n_rk, lane);
+      if (in) S.rk[j] = c;
+    }
+    __syncthreads();
+    for (int i = tid; i < C2; i += kSelThreads) {
+      const uint64_t ci = S.rk[i];
+      int better = 0;
+      for (int j = 0; j < C2; ++j) better += (S.rk[j] > ci) ? 1 : 0;
+      if (better == need_r - 1) S.cut = ci;
+    }
+    __syncthreads();
+    prefix = S.cut;
+    mask = ~0ull;
+    return;
+  }
+  // many tied in 24 key bits: radix select over composite bits 39..0
+  const int shifts[4] = {29, 18, 7, 0};
+  const int widths[4] = {11, 11, 11, 7};
+  constexpr int kPerD = 2048 / kSelThreads;        // 4 digit bins per thread, high first
+  for (int d = 0; d < 4; ++d) {
+    const int sh = shifts[d];
+    const uint32_t wm = (1u << widths[d]) - 1u;
+    for (int i = tid; i < 2048; i += kSelThreads) S.hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < C; i += kSelThreads) {
+      const uint64_t c = comp(i);
+      if ((c & mask) == prefix) atomicAdd(S.hist + ((c >> sh) & wm), 1u);
+    }
+    __syncthreads();
+    const int dtop = 2048 - kPerD * (tid + 1);
+    int dc[kPerD], dl = 0;
 #pragma unroll
-      for (int d = 0; d < kSelSplit; ++d) taken_c[d] += __popc(__ballot_sync(0xffffffffu, taken && c == d));
-      if (taken && c == rank) {
-        const int e = (int)(~(uint32_t)c64) - lo;
-        atomicOr(bitmap + (e >> 5), 1u << (e & 31));
+    for (int k = 0; k < kPerD; ++k) {
+      dc[k] = (int)S.hist[dtop + kPerD - 1 - k];
+      dl += dc[k];
+    }
+    int dtot;
+    const int dex = excl_scan(dl, S.scr, 1, kSelThreads, &dtot, tid);
+    if (dex < need_r && dex + dl >= need_r) {
+      int run = dex;
+#pragma unroll
+      for (int k = 0; k < kPerD; ++k) {
+        if (run + dc[k] >= need_r) {
+          S.scr[80] = dtop + kPerD - 1 - k;
+          S.scr[81] = run;
+          S.scr[82] = dc[k];
+          break;
+        }
+        run += dc[k];
       }
     }
-    if (lane < kSelSplit) {
-      const int v = (lane == 0) ? taken_c[0] : (lane == 1) ? taken_c[1] : (lane == 2) ? taken_c[2] : taken_c[3];
-      if (v) atomicAdd(s_taken + lane, v);
+    __syncthreads();
+    need_r -= S.scr[81];
+    prefix |= (uint64_t)S.scr[80] << sh;
+    mask |= (uint64_t)wm << sh;
+    const bool all_in = (S.scr[82] == need_r);
+    __syncthreads();
+    if (all_in) break;
+  }
+}
+
+// Ascending emission of a bitmap's set bits (bit i = element i): each thread owns the words
+// [w0, w1); returns the output offset of its first set bit and the total in *total.
+__device__ __forceinline__ int bitmap_offsets(const uint32_t* bitmap, int w0, int w1, int* scr, int tid,
+                                              int* total) {
+  int cnt = 0;
+  for (int i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
+  return excl_scan(cnt, scr, 1, kSelThreads, total, tid);
+}
+
+// Slots in a shared list for `n` items per lane, from one atomic per warp; every lane calls it.
+__device__ __forceinline__ int warp_append_n(int n, int* counter, int lane) {
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int base = 0;
+  if (lane == 31 && incl) base = atomicAdd(counter, incl);
+  base = __shfl_sync(0xffffffffu, base, 31);
+  return base + incl - n;
+}
+
+// One 2-CTA cluster per (request, query) row. CTA 0 selects the block top-2048 and writes the
+// pool; CTA 1 selects the block top-512 and then the position top-512 among their positions.
+// Both read the row's block-max histogram; CTA 1 clears it once CTA 0 has read it (the cluster
+// barrier's arrive and wait are split around the work).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) uint8_t fsm_raw[];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int rank = (int)cluster_rank();
+  const int row = blockIdx.x >> 1;
+  __shared__ SelShared S;
+  __shared__ int s_thr, s_above, s_total;
+  __shared__ int s_tblk[kTopBlocks];
+  __shared__ uint32_t s_psel[kPosCand / 32];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int vis = (int)imin64(imax64(__ldg(p.vis + row), 0), p.max_vis);
+  const int nb = (vis + kBlk - 1) / kBlk;
+  const int nwb = (nb + 31) >> 5;                     // bitmap words
+  const int K = rank ? kTopBlocks : kCandBlocks;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(fsm_raw);                 // [nwb4] selected blocks
+  const int nwb4 = (nwb + 3) & ~3;
+  uint64_t* cst = reinterpret_cast<uint64_t*>(bits + nwb4);             // [kSelStage] staged candidates
+  const float* bm = p.blkmax + (size_t)row * p.ld_b;
+  int32_t* gcand = p.cand + (size_t)row * p.ld_cand + (size_t)rank * p.ld_b;   // candidates past the stage
+  uint32_t* gh = p.hist + (size_t)row * kHistBins;
+
+  // ---------------------------------------------------------------- 1. threshold bin of this CTA's block top-K
+  {
+    constexpr int kPer = kHistBins / kSelThreads;     // 8 bins per thread, high first
+    const int top = kHistBins - kPer * (tid + 1);
+    int cnt[kPer], local = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      cnt[k] = (int)__ldcg(gh + top + kPer - 1 - k);
+      local += cnt[k];
+    }
+    int total;
+    const int excl = excl_scan(local, S.scr, 1, kSelThreads, &total, tid);
+    if (total <= K) {
+      if (tid == 0) {
+        s_thr = -1;
+        s_above = total;
+      }
+    } else if (excl < K && excl + local >= K) {
+      int run = excl;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        if (run + cnt[k] >= K) {
+          s_thr = top + kPer - 1 - k;
+          s_above = run;
+          break;
+        }
+        run += cnt[k];
+      }
+    }
+    if (tid == 0) {
+      s_total = total;
+      S.ncand[0] = 0;
+    }
+    for (int i = tid; i < nwb4; i += kSelThreads) bits[i] = 0u;
+  }
+  cluster_arrive();                   // this CTA has read the histogram
+  __syncthreads();
+  if (rank == 0 && tid == 0 && s_total != nb) flag_status(p.status, HSA_FLAG_INDEX_RANGE);
+
+  // ---------------------------------------------------------------- 2. one pass over the block maxima
+  // Blocks above the threshold bin are taken at once; blocks in it are listed as candidates
+  // (composites staged in shared memory, block indices in the workspace past the stage). Eight
+  // float4 loads per thread are in flight at a time.
+  {
+    const int thr = s_thr;
+    const int nq4 = (nb + 3) >> 2;                    // float4 chunks
+    constexpr int kIlp = 8;
+    for (int c0 = 0; c0 < nq4; c0 += kIlp * kSelThreads) {
+      float4 v[kIlp];
+#pragma unroll
+      for (int u = 0; u < kIlp; ++u) {
+        const int c = c0 + u * kSelThreads + tid;
+        v[u] = (c < nq4) ? __ldcg(reinterpret_cast<const float4*>(bm) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kIlp; ++u) {
+        const int c = c0 + u * kSelThreads + tid;
+        const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t take = 0u, candm = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int b = 4 * c + k;
+          const int bin = (int)(order_key(f[k]) >> kHistShift);
+          if (b < nb) {
+            if (thr < 0 || bin > thr) take |= 1u << k;
+            else if (bin == thr) candm |= 1u << k;
+          }
+        }
+        if (take) atomicOr(bits + ((4 * c) >> 5), take << ((4 * c) & 31));
+        const int n = __popc(candm);
+        int j = warp_append_n(n, &S.ncand[0], lane);
+        while (candm) {
+          const int k = __ffs(candm) - 1;
+          candm &= candm - 1u;
+          const int b = 4 * c + k;
+          if (j < kSelStage) cst[j] = sel_comp(f[k], (uint32_t)b);
+          else gcand[j - kSelStage] = b;
+          ++j;
+        }
+      }
     }
   }
   __syncthreads();
 
-  // 3. ascending emission at this quarter's offset
-  int off = 0;
-#pragma unroll
-  for (int c = 0; c < kSelSplit; ++c) off += (c < rank) ? sure_c[c] + s_taken[c] : 0;
-  const int per = (nwq + kSelThreads - 1) / kSelThreads;
-  const int w0 = min(nwq, tid * per), w1 = min(nwq, w0 + per);
-  int cnt = 0;
-  for (int i = w0; i < w1; ++i) cnt += __popc(bitmap[i]);
-  int total;
-  int o = off + excl_scan(cnt, scratch, 1, kSelThreads, &total, tid);
-  if (which == 0) {
-    int32_t* out = p.topk_out + (size_t)row * kTopK;
-    for (int i = w0; i < w1; ++i) {
-      uint32_t m = bitmap[i];
-      while (m) {
-        const int b = __ffs(m) - 1;
-        m &= m - 1;
-        if (o < kTopK) out[o] = lo + i * 32 + b;
-        ++o;
+  // ---------------------------------------------------------------- 3. cut the threshold bin, mark its taken blocks
+  if (s_thr >= 0) {
+    const int C = S.ncand[0];
+    const int need = K - s_above;
+    auto comp = [&](int i) -> uint64_t {
+      if (i < kSelStage) return cst[i];
+      const int b = __ldcg(gcand + (i - kSelStage));
+      return sel_comp(__ldcg(bm + b), (uint32_t)b);
+    };
+    uint64_t prefix = (uint64_t)s_thr << 52, mask = 0xFFFull << 52;
+    cut_candidates(comp, C, need, S, prefix, mask, tid);
+    for (int i = tid; i < C; i += kSelThreads) {
+      const uint64_t c = comp(i);
+      if ((c & mask) >= prefix) {
+        const uint32_t b = ~(uint32_t)c;
+        atomicOr(bits + (b >> 5), 1u << (b & 31));
       }
     }
-    if (rank == 0)
-      for (int j = Keff + tid; j < kTopK; j += kSelThreads) out[j] = -1;
-  } else {
+    __syncthreads();
+  }
+
+  const int per = (nwb + kSelThreads - 1) / kSelThreads;
+  const int w0 = min(nwb, tid * per), w1 = min(nwb, w0 + per);
+  if (rank == 0) {
+    // ---------------------------------------------------------------- 4a. the pool, ascending
+    int totp;
+    int o = bitmap_offsets(bits, w0, w1, S.scr, tid, &totp);
     int32_t* out = p.pool_out + (size_t)row * kPool;
     for (int i = w0; i < w1; ++i) {
-      uint32_t m = bitmap[i];
+      uint32_t m = bits[i];
       while (m) {
-        const int b = __ffs(m) - 1;
+        const int blk = i * 32 + __ffs(m) - 1;
         m &= m - 1;
-        const int blk = lo + i * 32 + b;
         if (o < kCandBlocks) {
-          int4 lo4, hi4;
           const int q0 = blk * 8;
+          int4 lo4, hi4;
           lo4.x = (q0 + 0 < vis) ? q0 + 0 : -1;
           lo4.y = (q0 + 1 < vis) ? q0 + 1 : -1;
           lo4.z = (q0 + 2 < vis) ? q0 + 2 : -1;
@@ -589,22 +575,89 @@ __global__ void __cluster_dims__(kSelSplit, 1, 1) __launch_bounds__(kSelThreads)
         ++o;
       }
     }
-    if (rank == 0)
-      for (int j = 8 * min(Keff, kCandBlocks) + tid; j < kPool; j += kSelThreads) out[j] = -1;
+    for (int j = 8 * min(totp, kCandBlocks) + tid; j < kPool; j += kSelThreads) out[j] = -1;
+    cluster_wait();
+    return;
   }
-  // clear this row's histogram and state for the next call (every CTA read the state before the
-  // cluster barrier above)
-  if (rank == 0) {
-    uint32_t* gh = p.hist + (size_t)(2 * row + which) * kHistBins;
-    for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0;
-    if (tid == 0) {
-      st->thr_bin = 0;
-      st->above = 0;
-      st->nvalid = 0;
-      st->nsure = 0;
-      st->ncand = 0;
-      st->ready = 0;
+
+  // ---------------------------------------------------------------- 4b. the top-512 blocks, ascending
+  {
+    int tott;
+    int ot = bitmap_offsets(bits, w0, w1, S.scr, tid, &tott);
+    for (int i = w0; i < w1; ++i) {
+      uint32_t m = bits[i];
+      while (m) {
+        const int blk = i * 32 + __ffs(m) - 1;
+        m &= m - 1;
+        if (ot < kTopBlocks) s_tblk[ot] = blk;
+        ++ot;
+      }
     }
+    if (tid == 0) S.ncand[0] = min(tott, kTopBlocks);
+    for (int j = tid; j < kPosCand / 32; j += kSelThreads) s_psel[j] = 0u;
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- 5. the position top-512 among those blocks
+  // Candidate i is position 8 tblk[i / 8] + i % 8, so the list is in ascending position order.
+  // Positions at or past vis get composite 0, below every score's.
+  const int nt = S.ncand[0];
+  const int U = nt * kBlk;
+  uint64_t* pc = cst;                 // [4096] position composites (the stage is free now)
+  {
+    const float* sc = p.scores + (size_t)row * p.ld_s;
+    if (tid < nt) {
+      const int q0 = 8 * s_tblk[tid];
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(sc + q0));
+      const float4 c = __ldcg(reinterpret_cast<const float4*>(sc + q0 + 4));
+      const float f[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        pc[8 * tid + j] = (q0 + j < vis) ? sel_comp(f[j], (uint32_t)(q0 + j)) : 0ull;
+    }
+  }
+  cluster_wait();                     // CTA 0 has read the histogram: clear it for the next call
+#pragma unroll
+  for (int k = 0; k < kHistBins / kSelThreads; ++k) gh[tid + k * kSelThreads] = 0u;
+  __syncthreads();
+  const int K2 = min(kTopK, vis);
+  {
+    auto comp = [&](int i) -> uint64_t { return pc[i]; };
+    uint64_t prefix = 0ull, mask = 0ull;
+    if (K2 < U) {
+      // level 1 over the composites' top 12 bits, then cut_candidates inside the threshold bin
+      for (int i = tid; i < kHistBins; i += kSelThreads) S.hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < U; i += kSelThreads) atomicAdd(S.hist + (int)(pc[i] >> 52), 1u);
+      __syncthreads();
+      smem_threshold<kSelThreads>(S.hist, K2, S.scr, S.scr + 64, tid);
+      const int thr1 = S.scr[64], above1 = S.scr[65];
+      __syncthreads();
+      prefix = (uint64_t)thr1 << 52;
+      mask = 0xFFFull << 52;
+      cut_candidates(comp, U, K2 - above1, S, prefix, mask, tid);
+    }
+    for (int i = tid; i < U; i += kSelThreads)
+      if (pc[i] != 0ull && (pc[i] & mask) >= prefix) atomicOr(s_psel + (i >> 5), 1u << (i & 31));
+  }
+  __syncthreads();
+  {
+    // 128 words of selection bits; thread tid < 128 owns word tid
+    const int nw = (U + 31) >> 5;
+    const int v0 = min(nw, tid), v1 = min(nw, tid + 1);
+    int tot;
+    int o = bitmap_offsets(s_psel, v0, v1, S.scr, tid, &tot);
+    int32_t* out = p.topk_out + (size_t)row * kTopK;
+    for (int i = v0; i < v1; ++i) {
+      uint32_t m = s_psel[i];
+      while (m) {
+        const int k = i * 32 + __ffs(m) - 1;
+        m &= m - 1;
+        if (o < kTopK) out[o] = 8 * s_tblk[k >> 3] + (k & 7);
+        ++o;
+      }
+    }
+    for (int j = min(tot, kTopK) + tid; j < kTopK; j += kSelThreads) out[j] = -1;
   }
 }
 }  // namespace
@@ -632,12 +685,13 @@ cudaError_t launch_index_scan(const ScanParams& p, int num_sms, cudaStream_t s) 
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t s) {
   const int rows = p.batch * p.nq;
-  const int64_t q = ((std::max<int64_t>(p.max_vis, 1) + kSelSplit - 1) / kSelSplit + 31) / 32;   // bitmap words of a quarter
-  const size_t smem = (size_t)((q + 3) & ~3) * 4 + kHistBins * 4 + 64 * 4 + (size_t)kSelStage * 8;
+  const int64_t nb = (std::max<int64_t>(p.max_vis, 1) + kBlk - 1) / kBlk;
+  const int64_t nwb4 = ((nb + 31) / 32 + 3) & ~3;   // bitmap words
+  const size_t smem = (size_t)nwb4 * 4 + (size_t)kSelStage * 8;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), smem);
   if (e != cudaSuccess) return e;
-  // one cluster of 4 CTAs per (row, selection): the position top-512, then the block top-2048
-  return launch_pdl(select_kernel, dim3((unsigned)(rows * 2 * kSelSplit)), dim3(kSelThreads), smem, s, p);
+  // one 2-CTA cluster per (request, query) row
+  return launch_pdl(select_kernel, dim3((unsigned)(2 * rows)), dim3(kSelThreads), smem, s, p);
 }
 
 }  // namespace hsa

@@ -272,6 +272,23 @@ def test_full_topk_inside_pool_block_max_is_upper_bound():
         assert set(topk.tolist()) <= set(pool[pool >= 0].tolist())
 
 
+def test_full_topk_inside_top512_blocks_with_ties():
+    """The position top-512 lies inside the 8-position blocks ranked in the top 512 by block max
+    ([ARCH] §3.3: the block max is an upper bound), with both orders breaking ties towards the
+    lower index. Scores drawn from a few integers force ties at every level."""
+    rng = np.random.default_rng(61)
+    for T in (4100, 9001, 40000):
+        for levels in (3, 7, 1000):
+            s = rng.integers(0, levels, T).astype(np.float64)
+            top = O.topk_ascending(s, T, 512)
+            m = O.block_maxima(s, T)
+            blocks = O.topk_ascending(m, len(m), 512)
+            inside = set((blocks[:, None] * 8 + np.arange(8)[None, :]).ravel().tolist())
+            assert set(top.tolist()) <= inside, (T, levels)
+            # and the 512th block max never exceeds the 512th position score
+            assert m[blocks].min() <= s[top].min()
+
+
 def test_reindex_over_whole_context_equals_full():
     rng = np.random.default_rng(8)
     T = 12000                                   # ceil(T/8) <= 2048: the pool is everything
