@@ -11,11 +11,14 @@
 //     the query in place to f16 after a per-head power-of-two shift (exact within f16; each
 //     warp owns 4 whole heads, so no block barrier), and dequantise the rows to f16
 //     (E2M1 x scale, or E4M3 for SWA) into a 128B-swizzled K-major tile, 128 dims at a time;
-//  2. the MMA warp runs S^T = K . Q^T on tcgen05 (TMEM accumulators) in two M=128 passes
-//     (rows 0..127, then rows 32..159, of which only keys 128..159 are used), each 128-dim step
-//     as soon as all workers have converted it;
-//  3. the workers run a softmax local to the 160 keys (own max m_c and sum l_c per head) and
-//     write P^T (f16) as the next B operand; no cluster exchange is needed before PV;
+//  2. the MMA warp runs S = Q . K^T on tcgen05 as M = 64 heads by N = 160 keys (TMEM
+//     accumulators), each 128-dim step as soon as all workers have converted it. The tensor
+//     core takes 2 N-columns per clock whatever M is, so this costs 32 x 80 clocks, against
+//     64 x 48 (shared-memory bound) for S^T in two M = 128, N = 64 passes;
+//  3. the workers run a softmax local to the 160 keys (own max m_c and sum l_c per head): in
+//     the M = 64 accumulator layout each head is one TMEM lane, so a thread holds 40 of its
+//     head's logits and four warps merge (max, sum) through shared memory. P (f16) is written
+//     as the next B operand; no cluster exchange is needed before PV;
 //  4. the MMA warp runs O^T[512 dims][64 heads] = V^T . P^T, reading the same tile as an
 //     MN-major A operand (K = V = the 512-d latent), one 128-dim M-tile at a time;
 //  5. each worker drains one output dimension of a finished M-tile, normalised by l_c: the 48
@@ -49,12 +52,13 @@ constexpr uint32_t kOffK = 0, kOffQ = kTileBytes, kOffMisc = kOffQ + kQBytes;
 constexpr uint32_t kMiscBytes = 1792;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;   // + alignment slack
 constexpr size_t kPartFloats = (size_t)kHAtt * kDLat + 2 * kHAtt;   // one CTA's partial in the workspace
-constexpr int kSStride = kRows;                          // fp32 logit staging [64 heads][160 keys]
-constexpr uint32_t kOffPinQ = 40960;                     // P^T after the staging rows, inside the Q region
+constexpr uint32_t kOffPinQ = 40960;                     // P inside the Q region (the softmax exchange sits below it)
 constexpr int kTmemCols = 512;
-constexpr int kColS0 = 0, kColS1 = 64, kColO = 256;
+constexpr int kColS = 0, kColO = 256;                    // S [64 heads][160 keys], O^T [4 x 128 dims][64 heads]
+constexpr int kKeysPerWarp = kRows / 4;                  // softmax: the 4 warps of a TMEM lane quadrant split the keys
 static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kHAtt * kSStride * 4 <= (int)kOffPinQ && kOffPinQ % 1024 == 0, "logit staging");
+static_assert(kOffPinQ % 1024 == 0 && 512 * 4 <= (int)kOffPinQ, "softmax exchange below P");
+static_assert(kKeysPerWarp == 40 && kColS + kRows <= kColO, "S columns");
 static_assert(kOffPinQ + 3 * kHAtt * 128 <= kQBytes, "P^T (160 keys in three 64-key blocks)");
 
 
@@ -180,13 +184,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   if (warp == kWorkWarps) {
     // ---------------------------------------------------------------- MMA warp
     if (lane == 0) {
-      // S^T = K . Q^T in two M=128 passes (rows 0..127 -> columns 0..63, rows 32..159 -> 64..127),
-      // 64-dim block by block as the worker warps finish converting them. Descriptors are formed
+      // S = Q . K^T: M = 64 heads (A = the query, K-major), N = 160 keys (B = the tile, K-major),
+      // 128-dim step by step as the worker warps finish converting them. Descriptors are formed
       // once; a k-step only moves the start-address field (address >> 4), which cannot carry out
       // of its 14 bits because every operand lies below 256 KB.
-      const uint32_t id = idesc_f16(128, 64, false, false);
-      const uint64_t a0 = sdesc(sK, 16u, 1024u), a1 = sdesc(sK + 32u * 128u, 16u, 1024u);
-      const uint64_t b0 = sdesc(sQ, 16u, 1024u);
+      const uint32_t id = idesc_f16(64, kRows, false, false);
+      const uint64_t a0 = sdesc(sQ, 16u, 1024u), b0 = sdesc(sK, 16u, 1024u);
       bool ok = true;
 #pragma unroll
       for (int st = 0; st < 4; ++st) {
@@ -197,8 +200,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
           const int k = 8 * st + kk;
           const uint32_t ko = ((uint32_t)(k >> 2) * kKbStride + (uint32_t)(k & 3) * 32u) >> 4;
           const uint32_t qo = ((uint32_t)(k >> 2) * (kHAtt * 128u) + (uint32_t)(k & 3) * 32u) >> 4;
-          umma_f16(tmem + kColS0, a0 + ko, b0 + qo, id, k > 0);
-          umma_f16(tmem + kColS1, a1 + ko, b0 + qo, id, k > 0);
+          umma_f16(tmem + kColS, a0 + qo, b0 + ko, id, k > 0);
         }
       }
       umma_commit(bar);
@@ -357,56 +359,36 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   tc_fence_after();
   named_bar_sync(1, kWorkThreads);    // s_valid, s_scale visible
 
-  // ---------------------------------------------------------------- logits -> staging [h][key] (Q region)
-  // Key group kg: 0..3 = pass-0 rows 32 kg + lane (TMEM lane quadrant kg), 4 = keys 128 + lane
-  // (pass-1 rows 96 + lane, quadrant 3). Warp w stages group w & 3, heads 16 (w >> 2) .. +15;
-  // the quadrant-3 warps also stage group 4.
-  float* stg = reinterpret_cast<float*>(sm + kOffQ);
+  // ---------------------------------------------------------------- softmax, one head per TMEM lane
+  // S[h][key] lies in TMEM lane 32 (h / 16) + h % 16 (the M = 64 accumulator layout), column key.
+  // Warp w reads lane quadrant sq = w & 3 (heads 16 sq .. 16 sq + 15 in its lanes 0..15) and the
+  // 40 keys 40 sj .. 40 sj + 39, sj = w >> 2; lanes 16..31 hold no head and only take part in the
+  // collective loads and the barriers. The four warps of a quadrant merge their (max, sum)
+  // through shared memory (below P in the query region, which QK has consumed).
+  const int sq = warp & 3, sj = warp >> 2;
+  const bool hl = lane < 16;
+  const int hh = 16 * sq + (lane & 15);
+  float* s_red = reinterpret_cast<float*>(sm + kOffQ);   // [2][4 key quarters][64 heads]: max, then sum
+  float x[kKeysPerWarp];
   {
-    auto stage = [&](int kg, int hq) {
-      const int qd = kg < 4 ? kg : 3;
-      const int key = kg < 4 ? 32 * kg + lane : kTopRows + lane;
-      const uint32_t col = (kg < 4 ? (uint32_t)kColS0 : (uint32_t)kColS1) + 16u * hq;
-      uint32_t r[16];
-      TMEM_LD16(tmem + ((uint32_t)(32 * qd) << 16) + col, r);
-      tmem_wait_ld();
-      const bool kv = s_valid[key] != 0;
+    uint32_t r[kKeysPerWarp];
+    const uint32_t ta = tmem + ((uint32_t)(32 * sq) << 16) + (uint32_t)(kColS + kKeysPerWarp * sj);
+    TMEM_LD32(ta, r);
+    TMEM_LD8(ta + 32u, (r + 32));
+    tmem_wait_ld();
+    const float scl = s_scale[hh];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int h = 16 * hq + j;
-        stg[h * kSStride + key] = kv ? __uint_as_float(r[j]) * s_scale[h] : -INFINITY;
-      }
-    };
-    stage(warp & 3, warp >> 2);
-    if ((warp & 3) == 3) stage(4, warp >> 2);
+    for (int i = 0; i < kKeysPerWarp; ++i)
+      x[i] = s_valid[kKeysPerWarp * sj + i] ? __uint_as_float(r[i]) * scl : -INFINITY;
   }
-  named_bar_sync(1, kWorkThreads);
-  // per head: 8 threads; thread kq takes the 8-key runs kq, kq + 8 and (kq < 4) kq + 16. The
-  // softmax is local to this CTA's 160 keys: its own max m_c and sum l_c; the cluster combine
-  // below rescales the four partials.
-  const int hh = tid >> 3, kq = tid & 7;
-  float x[3][8];
   float mloc = -INFINITY;
 #pragma unroll
-  for (int u = 0; u < 3; ++u) {
-    const int ch = kq + 8 * u;
-    if (ch < kRows / 8) {
-      const float4 a = *reinterpret_cast<const float4*>(stg + hh * kSStride + 8 * ch);
-      const float4 c = *reinterpret_cast<const float4*>(stg + hh * kSStride + 8 * ch + 4);
-      x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
-      x[u][4] = c.x; x[u][5] = c.y; x[u][6] = c.z; x[u][7] = c.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) mloc = fmaxf(mloc, x[u][e]);
-  }
-  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-  // P^T (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys; one 8-key
-  // run is one 16-byte unit
+  for (int i = 0; i < kKeysPerWarp; ++i) mloc = fmaxf(mloc, x[i]);
+  if (hl) s_red[sj * kHAtt + hh] = mloc;
+  named_bar_sync(1, kWorkThreads);
+  mloc = fmaxf(fmaxf(s_red[hh], s_red[kHAtt + hh]), fmaxf(s_red[2 * kHAtt + hh], s_red[3 * kHAtt + hh]));
+  // P (f16) into the B operand [keys/64][64 heads][128 B]: rows = heads, K = keys; one 8-key run
+  // is one 16-byte unit.
   // p = 2^(x log2 e - m log2 e); a head with no valid key has m = -inf and every x = -inf, so
   // its offset is 0 and every p is 0. Values below 2^-126 flush to zero (f16 P rounds everything
   // below 2^-25 to zero anyway). Key pairs run as packed fp32 pairs.
@@ -415,22 +397,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const uint64_t l2e2 = f2_pack(kLog2e, kLog2e), nml2 = f2_pack(-ml2, -ml2);
   uint64_t ls2 = f2_pack(0.f, 0.f);
 #pragma unroll
-  for (int u = 0; u < 3; ++u) {
-    const int ch = kq + 8 * u;
-    if (ch < kRows / 8) {
-      uint32_t pk[4];
+  for (int u = 0; u < kKeysPerWarp / 8; ++u) {
+    uint32_t pk[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float z0, z1;
-        f2_unpack(f2_fma(f2_pack(x[u][2 * e], x[u][2 * e + 1]), l2e2, nml2), z0, z1);
-        const float p0 = ex2_ftz(z0), p1 = ex2_ftz(z1);
-        ls2 = f2_add(ls2, f2_pack(p0, p1));
-        const __half2 h = __floats2half2_rn(p0, p1);
-        pk[e] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      const int key = 8 * ch;
-      sts128(sP + (uint32_t)(key >> 6) * (kHAtt * 128u) + sw128(hh, (key & 63) >> 3), pk[0], pk[1], pk[2], pk[3]);
+    for (int e = 0; e < 4; ++e) {
+      float z0, z1;
+      f2_unpack(f2_fma(f2_pack(x[8 * u + 2 * e], x[8 * u + 2 * e + 1]), l2e2, nml2), z0, z1);
+      const float p0 = ex2_ftz(z0), p1 = ex2_ftz(z1);
+      ls2 = f2_add(ls2, f2_pack(p0, p1));
+      const __half2 h = __floats2half2_rn(p0, p1);
+      pk[e] = *reinterpret_cast<const uint32_t*>(&h);
     }
+    const int key = kKeysPerWarp * sj + 8 * u;
+    if (hl) sts128(sP + (uint32_t)(key >> 6) * (kHAtt * 128u) + sw128(hh, (key & 63) >> 3), pk[0], pk[1], pk[2], pk[3]);
   }
   float lsum;
   {
@@ -438,16 +417,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     f2_unpack(ls2, a, c);
     lsum = a + c;
   }
-  lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-  lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-  lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
-  if (kq == 0) s_invl[hh] = (lsum > 0.f) ? 1.f / lsum : 0.f;
+  if (hl) s_red[(4 + sj) * kHAtt + hh] = lsum;
+  named_bar_sync(1, kWorkThreads);
+  lsum = (s_red[4 * kHAtt + hh] + s_red[5 * kHAtt + hh]) + (s_red[6 * kHAtt + hh] + s_red[7 * kHAtt + hh]);
+  const bool hown = hl && sj == 0;    // one thread per head publishes its (m, l)
+  if (hown) s_invl[hh] = (lsum > 0.f) ? 1.f / lsum : 0.f;
   fence_async_smem();
-  named_bar_sync(2, kAttnThreads);    // P^T ready for the MMA warp; s_invl visible to every worker
+  named_bar_sync(2, kAttnThreads);    // P ready for the MMA warp; s_invl visible to every worker
   // (m_c, l_c) of head hh go to the CTA that owns it (slot [rank][hh % 16]); read after phase A.
   // Every peer has started (setup barrier).
   cluster_wait();
-  if (kq == 0) st_cluster_f2(smem_u32(s_ml + rank * 16 + (hh & 15)), (uint32_t)(hh >> 4), mloc, lsum);
+  if (hown) st_cluster_f2(smem_u32(s_ml + rank * 16 + (hh & 15)), (uint32_t)(hh >> 4), mloc, lsum);
   uint32_t* mine = part + (size_t)rank * kPartFloats;
   cluster_arrive();                   // phase A
 
