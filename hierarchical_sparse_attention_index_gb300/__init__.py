@@ -21,6 +21,8 @@ HSA_NOALLOC_SCRATCH_BYTES = 64 << 20
 HSA_SCALE_E8M0, HSA_SCALE_E4M3 = 0, 1
 HSA_MODE_FULL, HSA_MODE_REINDEX, HSA_MODE_REUSE = 0, 1, 2
 HSA_FLAG_INDEX_RANGE, HSA_FLAG_WRITE_RANGE, HSA_FLAG_TIMEOUT = 1, 2, 4
+HSA_CACHE_ROPE = 1
+HSA_ROPE_DIMS, HSA_ROPE_THETA = 64, 160000.0
 
 STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_SHAPE", 3: "HSA_ERR_ALIGN",
           4: "HSA_ERR_WORKSPACE", 5: "HSA_ERR_CUDA", 6: "HSA_ERR_TIMEOUT", 7: "HSA_ERR_UNSUPPORTED"}
@@ -38,7 +40,7 @@ class HsaError(RuntimeError):
 
 class hsa_cache(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("ratio", ctypes.c_int32), ("capacity", ctypes.c_int64),
-                ("kv_scale_fmt", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("kv_scale_fmt", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("kv_q", ctypes.c_void_p), ("kv_s", ctypes.c_void_p), ("ik_q", ctypes.c_void_p),
                 ("ik_s", ctypes.c_void_p)]
 
@@ -113,17 +115,19 @@ def _check(fn, code):
 
 class Cache:
     """Caller-owned FP4 cache of one KV-source layer: four uint8 device tensors
-    (kv_q [B][cap][256], kv_s [B][cap][32], ik_q [B][cap][64], ik_s [B][cap][4])."""
+    (kv_q [B][cap][256], kv_s [B][cap][32], ik_q [B][cap][64], ik_s [B][cap][4]); `flags` holds
+    HSA_CACHE_* bits (HSA_CACHE_ROPE: the writer applies RoPE to the main-KV latent)."""
 
-    def __init__(self, batch, capacity, ratio=1, kv_scale_fmt=HSA_SCALE_E8M0, device="cuda", tensors=None):
+    def __init__(self, batch, capacity, ratio=1, kv_scale_fmt=HSA_SCALE_E8M0, device="cuda", tensors=None, flags=0):
         import torch
         self.batch, self.capacity, self.ratio, self.kv_scale_fmt = batch, capacity, ratio, kv_scale_fmt
+        self.flags = flags
         if tensors is None:
             z = dict(dtype=torch.uint8, device=device)
             tensors = (torch.zeros(batch, capacity, 256, **z), torch.zeros(batch, capacity, 32, **z),
                        torch.zeros(batch, capacity, 64, **z), torch.zeros(batch, capacity, 4, **z))
         self.kv_q, self.kv_s, self.ik_q, self.ik_s = tensors
-        self.desc = hsa_cache(batch, ratio, capacity, kv_scale_fmt, 0, _ptr(self.kv_q), _ptr(self.kv_s),
+        self.desc = hsa_cache(batch, ratio, capacity, kv_scale_fmt, flags, _ptr(self.kv_q), _ptr(self.kv_s),
                               _ptr(self.ik_q), _ptr(self.ik_s))
 
     @property

@@ -1,5 +1,6 @@
 // C ABI of libhsa (include/hsa.h): argument validation, workspace carve-up, launches and the
 // decode-step schedule. Everything here is host code; it launches kernels only.
+#include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -58,6 +59,7 @@ hsa_status check_cache(const hsa_cache* c) {
   if (c->capacity > (int64_t)INT32_MAX) return HSA_ERR_SHAPE;
   if (c->ratio != 1 && c->ratio != 2) return HSA_ERR_INVALID_ARG;
   if (c->kv_scale_fmt != HSA_SCALE_E8M0 && c->kv_scale_fmt != HSA_SCALE_E4M3) return HSA_ERR_INVALID_ARG;
+  if ((uint32_t)c->flags & ~HSA_CACHE_ROPE) return HSA_ERR_INVALID_ARG;
   if (!aligned16(c->kv_q) || !aligned16(c->kv_s) || !aligned16(c->ik_q) || !aligned16(c->ik_s)) return HSA_ERR_ALIGN;
   return HSA_OK;
 }
@@ -276,6 +278,15 @@ hsa_status hsa_cache_write_compress(const hsa_cache* cache, const void* wkv, con
   p.ik_q = cache->ik_q;
   p.ik_s = cache->ik_s;
   p.status = status;
+  if (cache->flags & HSA_CACHE_ROPE) {
+    // RoPE turns per position of pair k, theta^(-k/32) / 2 pi, as a 64-bit binary fraction: the
+    // phase of entry e is then the wrapping product e * turns (mod one turn, exactly)
+    p.rope = 1;
+    for (int k = 0; k < HSA_ROPE_DIMS / 2; ++k) {
+      const double f = pow(HSA_ROPE_THETA, -2.0 * k / HSA_ROPE_DIMS) / (2.0 * 3.14159265358979323846);
+      p.rope_turns[k] = (uint64_t)ldexp(f, 64);
+    }
+  }
   if (p.n_entries == 0) return HSA_OK;
   return cuda_fail(launch_cache_write(p, (cudaStream_t)stream), "cache write launch");
 }

@@ -139,6 +139,8 @@ struct WriteParams {
   uint8_t* ik_q;
   uint8_t* ik_s;
   uint32_t* status;
+  int32_t rope;                              // 1: rotate the main-KV latent's last 64 dims
+  uint64_t rope_turns[HSA_ROPE_DIMS / 2];    // turns per position of pair k, a 64-bit binary fraction
 };
 cudaError_t launch_cache_write(const WriteParams& p, cudaStream_t s);
 

@@ -11,8 +11,9 @@
 //     unit gain) as one correctly rounded 1 / rms. The
 //     lane's 16 channels are one main-KV group, so its scale (the smallest E8M0 or E4M3 value s
 //     with 6 s >= amax, an exact bit computation) and its codes (RNE E2M1 of x / s from the
-//     hardware cvt, -0 cleared to +0) come straight from registers. The raw inputs of the
-//     warp's next entries are loaded while it works;
+//     hardware cvt, -0 cleared to +0) come straight from registers; with RoPE, of a copy whose
+//     last 64 dims are rotated by the entry's position. The raw inputs of the warp's next
+//     entries are loaded while it works;
 //  2. the normalised latent is split into three bf16 terms, hi + mid + lo = x exactly (each
 //     term the bf16 rounding of what the previous ones left), stacked as the 96 rows (term t,
 //     entry r -> row 32 t + r) of one 128B-swizzled K-major tile;
@@ -116,6 +117,30 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float a, float b) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
   return r;
+}
+
+// RoPE on the main-KV copy of an entry's latent ([ARCH] §3.2 压缩 RoPE, theta = 160000): lane l
+// holds dims 16 l .. 16 l + 15, so the rotary dims 448..511 are lanes 28..31, pairs
+// (448 + 2k, 449 + 2k) with k = 8 (l - 28) + u. Every lane computes the (cos, sin) of pair
+// k = lane: the phase pos * turns[k] wraps modulo one turn exactly in 64-bit integers, and its top
+// 24 bits (rounded) give 2 * phase for sincospif, within 2^-23 pi of the exact angle. Lanes 28..31
+// then fetch their pairs' values by shuffle. All 32 lanes call it.
+__device__ __forceinline__ void rope_rotate16(float (&xm)[16], int64_t pos, int lane, const uint64_t* turns) {
+  const uint64_t ph = (uint64_t)pos * turns[lane];
+  const float t2 = (float)(uint32_t)((ph + (1ull << 39)) >> 40) * 0x1p-23f;
+  float sn, cs;
+  sincospif(t2, &sn, &cs);
+  const int src0 = (8 * (lane - 28)) & 31;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float c = __shfl_sync(0xffffffffu, cs, src0 + u);
+    const float sv = __shfl_sync(0xffffffffu, sn, src0 + u);
+    if (lane >= 28) {
+      const float a = xm[2 * u], b = xm[2 * u + 1];
+      xm[2 * u] = fmaf(a, c, -(b * sv));
+      xm[2 * u + 1] = fmaf(a, sv, b * c);
+    }
+  }
 }
 
 // (request b, index i) of an entry; entries are numbered request-major
@@ -313,10 +338,15 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
         if (entry < 0 || entry >= p.cap) {
           if (lane == 0) flag_status(p.status, HSA_FLAG_WRITE_RANGE);
         } else {
-          // main KV: this lane's 16 channels are group `lane`
+          // main KV: this lane's 16 channels are group `lane`; with RoPE, of the rotated copy
+          // (the indexer K below is projected from the latent before RoPE)
+          float xm[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) xm[u] = x[u];
+          if (p.rope) rope_rotate16(xm, entry, lane, p.rope_turns);
           float amax = 0.f;
 #pragma unroll
-          for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(x[u]));
+          for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(xm[u]));
           uint32_t sb, c8[8];
           if (p.scale_fmt == HSA_SCALE_E8M0) {
             sb = e8m0_byte_for(amax);
@@ -324,16 +354,16 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
             e8m0_inv(sb, f1, f2);
             if (sb < 254u) {                // f2 = 1
 #pragma unroll
-              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(x[2 * u] * f1, x[2 * u + 1] * f1);
+              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(xm[2 * u] * f1, xm[2 * u + 1] * f1);
             } else {
 #pragma unroll
-              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair((x[2 * u] * f1) * f2, (x[2 * u + 1] * f1) * f2);
+              for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair((xm[2 * u] * f1) * f2, (xm[2 * u + 1] * f1) * f2);
             }
           } else {
             sb = e4m3_byte_for(amax);
             const float s = e4m3_to_f32(sb);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(__fdiv_rn(x[2 * u], s), __fdiv_rn(x[2 * u + 1], s));
+            for (int u = 0; u < 8; ++u) c8[u] = e2m1_pair(__fdiv_rn(xm[2 * u], s), __fdiv_rn(xm[2 * u + 1], s));
           }
           const size_t eo = (size_t)b * p.cap + entry;
           uint2 codes;

@@ -57,7 +57,7 @@ extern "C" {
 #define HSA_API
 #endif
 
-#define HSA_ABI_VERSION 1
+#define HSA_ABI_VERSION 2
 
 #define HSA_D_LATENT 512      /* main-KV latent width (head_dim)          [890B] §三 */
 #define HSA_D_INDEX 128       /* indexer head dim (index_head_dim)        [890B] §三 */
@@ -70,6 +70,8 @@ extern "C" {
 #define HSA_SWA_W 128         /* sliding_window                           [890B] §二 */
 #define HSA_MAX_NQ 8          /* query tokens per request per call (draft block 5 fits) */
 #define HSA_MAX_VIS (1 << 20) /* longest visible context per query (1M, [ARCH] §1 table) */
+#define HSA_ROPE_DIMS 64      /* rotary dims of the latent: its last 64 ([ARCH] §7: 448 NoPE + 128 B RoPE) */
+#define HSA_ROPE_THETA 160000.0 /* RoPE base of the compressed latent       [ARCH] §3.2 */
 
 typedef struct CUstream_st* hsa_stream_t; /* identical to cudaStream_t */
 
@@ -94,13 +96,16 @@ typedef enum { HSA_MODE_FULL = 0, HSA_MODE_REINDEX = 1, HSA_MODE_REUSE = 2 } hsa
 #define HSA_FLAG_WRITE_RANGE 2u   /* a cache write past capacity was skipped                         */
 #define HSA_FLAG_TIMEOUT 4u       /* a bounded device wait gave up                                  */
 
+/* Cache flags (hsa_cache.flags) */
+#define HSA_CACHE_ROPE 1u         /* the writer applies RoPE to the main-KV latent (see hsa_cache_write_compress) */
+
 /* Caller-owned cache descriptor. All four buffers are device memory, 16-byte aligned. */
 typedef struct {
   int32_t batch;        /* requests                                     */
   int32_t ratio;        /* compression ratio m of the writer: 1 or 2    */
   int64_t capacity;     /* entries per request; a multiple of 8         */
   int32_t kv_scale_fmt; /* hsa_scale_fmt of kv_s                        */
-  int32_t reserved;
+  int32_t flags;        /* HSA_CACHE_* bits; unknown bits are rejected  */
   uint8_t* kv_q;
   uint8_t* kv_s;
   uint8_t* ik_q;
@@ -147,8 +152,13 @@ HSA_API hsa_status hsa_workspace_init(void* ws, size_t ws_bytes, hsa_stream_t st
  * start_entry[b] + i:
  *   m = 2: per channel c, p = softmax(wgate[2i][c], wgate[2i+1][c]), latent = p0 x0 + p1 x1 (fp32);
  *   m = 1: latent = wkv[i] (there is no gating path);
- *   latent <- RMSNorm(latent) (eps 1e-6, unit gain); main KV <- FP4 group-16 with the cache's
- *   scale format; K = latent . w_idx (512x128, fp32 accumulate) <- FP4 group-32 E8M0.
+ *   latent <- RMSNorm(latent) (eps 1e-6, unit gain); K = latent . w_idx (512x128, fp32
+ *   accumulate) <- FP4 group-32 E8M0; main KV <- FP4 group-16 with the cache's scale format, of
+ *   the latent itself or, with HSA_CACHE_ROPE, of the latent with its last 64 dims rotated
+ *   ([ARCH] §3.2: RMSNorm, then the no-RoPE version, then compressed RoPE with theta = 160000,
+ *   then FP4; the indexer K is projected from the no-RoPE version): pair (448 + 2k, 449 + 2k),
+ *   k = 0..31, turns by the entry's position (start_entry[b] + i) times theta^(-k/32) radians,
+ *   (a, b) -> (a cos - b sin, a sin + b cos).
  * Scale rule: the smallest scale s (a power of two for E8M0, an E4M3 value otherwise) with
  * 6 s >= group amax. Codes are E2M1, round to nearest even, and -0 is stored as +0.
  *   wkv        bf16 [B][n_tokens][512]

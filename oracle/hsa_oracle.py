@@ -49,6 +49,8 @@ CAND_BLOCK = 8          # candidate_block_size                          [890B] å
 POOL_SLOTS = CAND_BLOCKS * CAND_BLOCK   # 16,384                        [CED] Figure 5
 SWA_W = 128             # sliding_window                                [890B] Â§äºŒ table
 RMS_EPS = 1e-6
+ROPE_THETA = 160000.0   # RoPE base of the compressed latent           [ARCH] Â§3.2 åŽ‹ç¼© RoPE
+ROPE_DIMS = 64          # rotary dims: the last 64 of 512 (the 448 B NoPE + 128 B RoPE page layout) [ARCH] Â§7
 
 SCALE_E8M0 = 0
 SCALE_E4M3 = 1
@@ -435,18 +437,40 @@ def rms_norm(x, eps=RMS_EPS):
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
 
 
-def cache_write_compress(wkv, wgate, w_idx, m, scale_fmt=SCALE_E8M0):
+def rope_rotate(lat, positions, theta=ROPE_THETA):
+    """RoPE on the last ROPE_DIMS dims of each row ([ARCH] Â§3.2: RMSNorm, the no-RoPE version,
+    then compressed RoPE with theta = 160000; [ARCH] Â§7: RoPE preserves the norm). Pair
+    (448 + 2k, 449 + 2k), k = 0..31, turns by positions[row] * theta^(-2k/64) radians:
+    (a, b) -> (a cos - b sin, a sin + b cos). The interleaved pairing and the position (the
+    entry's index in the request's cache) are readings; the pages give neither."""
+    x = np.array(lat, np.float64, copy=True)
+    lo = D_LATENT - ROPE_DIMS
+    k = np.arange(ROPE_DIMS // 2, dtype=np.float64)
+    freq = theta ** (-2.0 * k / ROPE_DIMS)
+    ang = np.asarray(positions, np.float64)[:, None] * freq[None, :]
+    c, s_ = np.cos(ang), np.sin(ang)
+    a = x[:, lo::2].copy()
+    b = x[:, lo + 1::2].copy()
+    x[:, lo::2] = a * c - b * s_
+    x[:, lo + 1::2] = a * s_ + b * c
+    return x
+
+
+def cache_write_compress(wkv, wgate, w_idx, m, scale_fmt=SCALE_E8M0, rope_pos=None):
     """Entries of one request: pooled latent -> RMSNorm -> FP4 main KV (group 16), and
     indexer K = latent . W_idx -> FP4 (group 32, E8M0)
     ([890B] Â§ä¸‰; [CED] CSA2 "indexer K ç›´æŽ¥ç”±ä¸» KV æŠ•å½±"; [ARCH] Â§3.1).
 
-    RoPE on the compressed latent is not applied (the rotary dims are not given).
-    Returns (kv_q [n,256], kv_s [n,32], ik_q [n,64], ik_s [n,4], latent fp64, K fp64)."""
+    With rope_pos (the entries' positions) the main KV holds the latent after RoPE and the
+    indexer K is still projected from the latent before it ([ARCH] Â§3.2 names the no-RoPE
+    version before the compressed RoPE step; that K comes from it is a reading).
+    Returns (kv_q [n,256], kv_s [n,32], ik_q [n,64], ik_s [n,4], main-KV latent fp64, K fp64)."""
     lat = rms_norm(compress_pool(wkv, wgate, m))
-    kv_q, kv_s = quantise_groups(lat.astype(np.float32), MAIN_GROUP, scale_fmt)
+    main = lat if rope_pos is None else rope_rotate(lat, rope_pos)
+    kv_q, kv_s = quantise_groups(main.astype(np.float32), MAIN_GROUP, scale_fmt)
     K = lat @ np.asarray(w_idx, np.float64)
     ik_nat, ik_s = quantise_groups(K.astype(np.float32), INDEX_GROUP, SCALE_E8M0)
-    return kv_q, kv_s, index_k_to_stored(ik_nat), ik_s, lat, K
+    return kv_q, kv_s, index_k_to_stored(ik_nat), ik_s, main, K
 
 
 # ---------------------------------------------------------------------------------------

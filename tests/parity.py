@@ -8,7 +8,8 @@ Tolerances:
 - attention: max|o - o_ref| / max|o_ref| <= ATTN_REL (2e-3, the required bound);
 - cache write: codes equal, except elements within WRITE_REL of a rounding midpoint or a
   scale boundary. The fp32 pipeline (expf, a correctly rounded sqrt and division, 512-term
-  fp32 sums) stays within about 1e-6 of the fp64 values, so 1e-5 leaves a 10x margin.
+  fp32 sums) stays within about 1e-6 of the fp64 values, so 1e-5 leaves a 10x margin. The
+  excluded fraction itself is bounded (5e-4 of main-KV, 2e-3 of indexer-K elements).
 """
 from __future__ import annotations
 
@@ -150,7 +151,9 @@ def check_write(oc_lat, oc_bytes, gpu, entries, fmt, name):
     assert not bad.any(), f"{name}: {bad.sum()} main-KV codes differ outside the band"
     bad_s = (gpu[1][entries] != oc_bytes[1]) & ~grp_ex
     assert not bad_s.any(), f"{name}: {bad_s.sum()} main-KV scales differ"
-    assert ex.mean() < 1e-3, f"{name}: band excludes {ex.mean():.2e} of the elements"
+    # the band is derived from the fp32 pipeline's error; on the seeded workloads it covers about
+    # 1e-4 of the main-KV elements and 4e-4 of the indexer-K elements
+    assert ex.mean() < 5e-4, f"{name}: the band excludes {ex.mean():.2e} of the main-KV elements"
     # indexer K (compare element codes in natural order)
     kerr = 4e-6 * (np.abs(lat) @ np.abs(W)) + WRITE_REL * np.abs(K)
     exk = write_exclusions(K, 32, O.SCALE_E8M0, kerr)
@@ -160,7 +163,8 @@ def check_write(oc_lat, oc_bytes, gpu, entries, fmt, name):
     assert not bad.any(), f"{name}: {bad.sum()} indexer-K codes differ outside the band"
     bad_s = (gpu[3][entries] != oc_bytes[3]) & ~exk.reshape(n, 4, 32).any(axis=2)
     assert not bad_s.any(), f"{name}: {bad_s.sum()} indexer-K scales differ"
-    assert exk.mean() < 1e-2
+    assert exk.mean() < 2e-3, f"{name}: the band excludes {exk.mean():.2e} of the indexer-K elements"
+    return float(ex.mean()), float(exk.mean())
 
 
 # ------------------------------------------------------------------ oracle writer in a process pool

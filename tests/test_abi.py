@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     import hierarchical_sparse_attention_index_gb300 as H
-    assert H.hsa_abi_version() == 1
+    assert H.hsa_abi_version() == 2
     for code, name in H.STATUS.items():
         assert H.hsa_status_string(code).startswith(name)
     assert H.hsa_status_string(99) == "HSA_ERR_UNKNOWN"

@@ -81,6 +81,32 @@ def test_cache_write_m2(hsa, fmt):
     assert not g[0][2048:].any()
 
 
+@pytest.mark.parametrize("m", [1, 2])
+def test_cache_write_rope(hsa, m):
+    """HSA_CACHE_ROPE: main KV holds the latent with its last 64 dims turned by the entry's
+    position (positions up to about 2^20, where a float32 angle would be off by ~0.06 rad);
+    indexer K is the no-RoPE projection. Both against the oracle's writer with rope_pos."""
+    H = hsa
+    seed, n, B = 13, 1600, 2
+    ne = n // m
+    cap = 1 << 20
+    starts = np.array([0, cap - ne - 8], np.int64)
+    wkv = np.stack([synth.latents_bf16(seed, 20, b, n) for b in range(B)])
+    wg = np.stack([synth.gates_bf16(seed, 20, b, n) for b in range(B)]) if m == 2 else None
+    W = synth.w_idx_bf16(seed, 20)
+    cache = H.Cache(B, cap, m, flags=H.HSA_CACHE_ROPE)
+    H.hsa_cache_write_compress(cache, dev_bf16(wkv), dev_bf16(wg) if m == 2 else None, dev_bf16(W), n, dev(starts))
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    for b in range(B):
+        ent = np.arange(starts[b], starts[b] + ne)
+        kv_q, kv_s, ik_q, ik_s, lat, K = O.cache_write_compress(P.f32(wkv[b]), None if m == 1 else P.f32(wg[b]),
+                                                                P.f32(W), m, rope_pos=ent)
+        g = [t[b, starts[b]:starts[b] + ne].cpu().numpy() for t in (cache.kv_q, cache.kv_s, cache.ik_q, cache.ik_s)]
+        P.check_write((lat, K, P.f32(W).astype(np.float64)), (kv_q, kv_s, ik_q, ik_s), g, np.arange(ne),
+                      O.SCALE_E8M0, f"rope m{m} b{b}")
+
+
 def test_cache_write_rejects_bad_args(hsa):
     H = hsa
     cache = H.Cache(1, 64, 2)

@@ -436,3 +436,65 @@ def test_decode_step_reuse_inherits():
         else:
             assert np.array_equal(res[lay][0], res[producer][0])
     assert not np.array_equal(res[20][0], res[24][0])
+
+
+# ------------------------------------------------------------------ RoPE on the compressed latent
+def _rot2(angle):
+    """2-D rotation by `angle` radians, from scipy's rotation about the z axis."""
+    from scipy.spatial.transform import Rotation
+    return Rotation.from_rotvec([0.0, 0.0, angle]).as_matrix()[:2, :2]
+
+
+def test_rope_preserves_norm_and_leaves_nope_dims():
+    """[ARCH] §7: RoPE preserves the norm; only the last 64 of the 512 dims turn, and position 0
+    is the identity."""
+    rng = np.random.default_rng(71)
+    x = rng.standard_normal((6, 512))
+    pos = np.array([0, 1, 7, 400, 65535, 1048575])
+    y = O.rope_rotate(x, pos)
+    assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    pairs = lambda v: v[:, 448:].reshape(len(v), 32, 2)  # noqa: E731
+    assert np.allclose(np.linalg.norm(pairs(y), axis=2), np.linalg.norm(pairs(x), axis=2), rtol=1e-13)
+    assert np.array_equal(y[:, :448], x[:, :448])
+    assert np.array_equal(y[0], x[0])
+
+
+def test_rope_pairs_turn_like_library_rotations():
+    """Pair k of dims (448 + 2k, 449 + 2k) turns counter-clockwise by pos * 160000^(-k/32): pair
+    0 by pos radians, pair 16 by pos / 400 (160000^(-1/2) = 1/400), against scipy's rotations."""
+    rng = np.random.default_rng(72)
+    x = rng.standard_normal((1, 512))
+    for pos, k, angle in ((3, 0, 3.0), (400, 16, 1.0), (1000, 16, 2.5), (123457, 0, 123457.0)):
+        y = O.rope_rotate(x, [pos])
+        want = _rot2(angle) @ x[0, 448 + 2 * k:450 + 2 * k]
+        assert np.allclose(y[0, 448 + 2 * k:450 + 2 * k], want, atol=1e-9), (pos, k)
+    # the 32 frequencies fall geometrically from 1 by the ratio 160000^(-1/32) per pair
+    e = np.zeros((1, 512))
+    e[0, 448::2] = 1.0
+    ang = np.arctan2(O.rope_rotate(e, [1])[0, 449::2], O.rope_rotate(e, [1])[0, 448::2])
+    assert np.allclose(ang[1:] / ang[:-1], 160000.0 ** (-1.0 / 32), rtol=1e-12) and abs(ang[0] - 1.0) < 1e-15
+
+
+def test_rope_depends_on_relative_position_only():
+    """The defining property: the dot product of two rotated rows depends on the position
+    difference only, and rotations compose additively."""
+    rng = np.random.default_rng(73)
+    x, y = rng.standard_normal((2, 1, 512))
+    for p, q, s in ((5, 17, 1000), (70000, 3, 12345), (0, 1048575, 7)):
+        a = O.rope_rotate(x, [p])[0] @ O.rope_rotate(y, [q])[0]
+        b = O.rope_rotate(x, [p + s])[0] @ O.rope_rotate(y, [q + s])[0]
+        assert abs(a - b) <= 1e-9 * np.linalg.norm(x) * np.linalg.norm(y)
+        assert np.allclose(O.rope_rotate(O.rope_rotate(x, [p]), [q]), O.rope_rotate(x, [p + q]), atol=1e-9)
+
+
+def test_writer_rope_touches_main_kv_tail_only():
+    """With RoPE, the indexer K is the no-RoPE projection and main-KV groups 0..27 (dims < 448)
+    keep their codes; the rotated groups differ somewhere."""
+    rng = np.random.default_rng(74)
+    wkv = rng.standard_normal((64, 512)).astype(np.float32)
+    W = (rng.standard_normal((512, 128)) / np.sqrt(512)).astype(np.float32)
+    a = O.cache_write_compress(wkv, None, W, 1)
+    b = O.cache_write_compress(wkv, None, W, 1, rope_pos=np.arange(1000, 1064))
+    assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])
+    assert np.array_equal(a[0][:, :224], b[0][:, :224]) and np.array_equal(a[1][:, :28], b[1][:, :28])
+    assert not np.array_equal(a[0][:, 224:], b[0][:, 224:])
