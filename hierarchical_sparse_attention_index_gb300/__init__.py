@@ -21,15 +21,18 @@ HSA_NOALLOC_SCRATCH_BYTES = 64 << 20
 HSA_SCALE_E8M0, HSA_SCALE_E4M3 = 0, 1
 HSA_MODE_FULL, HSA_MODE_REINDEX, HSA_MODE_REUSE = 0, 1, 2
 HSA_FLAG_INDEX_RANGE, HSA_FLAG_WRITE_RANGE, HSA_FLAG_TIMEOUT = 1, 2, 4
-HSA_CACHE_ROPE = 1
+HSA_CACHE_ROPE, HSA_CACHE_POOL_TAIL = 1, 2
+HSA_POOL_TAIL_SLOTS = 160
 HSA_ROPE_DIMS, HSA_ROPE_THETA = 64, 160000.0
 
 STATUS = {0: "HSA_OK", 1: "HSA_ERR_INVALID_ARG", 2: "HSA_ERR_SHAPE", 3: "HSA_ERR_ALIGN",
           4: "HSA_ERR_WORKSPACE", 5: "HSA_ERR_CUDA", 6: "HSA_ERR_TIMEOUT", 7: "HSA_ERR_UNSUPPORTED"}
+STATUS_CODES = {v: k for k, v in STATUS.items()}
 
 EXPORTS = ("hsa_abi_version", "hsa_status_string", "hsa_workspace_bytes", "hsa_workspace_init",
            "hsa_cache_write_compress", "hsa_index_full", "hsa_index_reindex", "hsa_sparse_attn_decode",
-           "hsa_schedule_step", "hsa_get_device_status", "hsa_index_full_noalloc")
+           "hsa_schedule_step", "hsa_get_device_status", "hsa_index_full_noalloc", "hsa_set_wait_limit",
+           "hsa_debug_stall_next_scan")
 
 
 class HsaError(RuntimeError):
@@ -80,6 +83,8 @@ def load_library(path: str = LIB_PATH):
         "hsa_schedule_step": (I32, [C, ctypes.POINTER(hsa_step_args), P, SZ, P]),
         "hsa_get_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32)]),
         "hsa_index_full_noalloc": (I32, [C, P, P, P, I32, I64, P, P, P]),
+        "hsa_set_wait_limit": (I32, [ctypes.c_uint64]),
+        "hsa_debug_stall_next_scan": (I32, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -215,6 +220,17 @@ class StepArgs:
 def hsa_schedule_step(cache: Cache, step: StepArgs, ws, stream=None):
     _check("hsa_schedule_step", load_library().hsa_schedule_step(
         cache.ref, ctypes.byref(step.args), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def hsa_set_wait_limit(ns):
+    """Limit of the kernels' bounded waits for later launches, in ns (0: the default, 2 s)."""
+    _check("hsa_set_wait_limit", load_library().hsa_set_wait_limit(int(ns)))
+
+
+def hsa_debug_stall_next_scan():
+    """Test hook: the next hsa_index_full withholds one copy of its scan, so a bounded wait runs
+    out (HSA_FLAG_TIMEOUT); that call's outputs are invalid, later calls are unaffected."""
+    _check("hsa_debug_stall_next_scan", load_library().hsa_debug_stall_next_scan())
 
 
 def hsa_get_device_status(stream=None):

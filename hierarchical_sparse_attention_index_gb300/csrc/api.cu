@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "hsa_common.cuh"
@@ -59,7 +60,7 @@ hsa_status check_cache(const hsa_cache* c) {
   if (c->capacity > (int64_t)INT32_MAX) return HSA_ERR_SHAPE;
   if (c->ratio != 1 && c->ratio != 2) return HSA_ERR_INVALID_ARG;
   if (c->kv_scale_fmt != HSA_SCALE_E8M0 && c->kv_scale_fmt != HSA_SCALE_E4M3) return HSA_ERR_INVALID_ARG;
-  if ((uint32_t)c->flags & ~HSA_CACHE_ROPE) return HSA_ERR_INVALID_ARG;
+  if ((uint32_t)c->flags & ~(HSA_CACHE_ROPE | HSA_CACHE_POOL_TAIL)) return HSA_ERR_INVALID_ARG;
   if (!aligned16(c->kv_q) || !aligned16(c->kv_s) || !aligned16(c->ik_q) || !aligned16(c->ik_s)) return HSA_ERR_ALIGN;
   return HSA_OK;
 }
@@ -71,6 +72,13 @@ hsa_status check_query(const hsa_cache* c, int32_t nq, int64_t max_vis) {
 }
 
 bool device_status_ptr(uint32_t** status, int* sms) { return device_info(status, sms); }
+
+namespace {
+std::atomic<uint64_t> g_wait_ns{kWaitLimitNs};   // bounded-wait limit of the next launches
+std::atomic<int> g_stall_next_scan{0};           // test hook, consumed by the next Full call
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 namespace {
 struct SmemLimit {
@@ -156,6 +164,8 @@ hsa_status launch_index_full(const hsa_cache* cache, const void* q, const float*
   sp.blkmax = reinterpret_cast<float*>(W + L.off_blkmax);
   sp.ld_b = L.ld_b;
   sp.hist = reinterpret_cast<uint32_t*>(W + L.off_hist_full);
+  sp.wait_ns = wait_limit_ns();
+  sp.stall_last = g_stall_next_scan.exchange(0);
   SelectParams se;
   memset(&se, 0, sizeof(se));
   se.batch = cache->batch;
@@ -172,6 +182,8 @@ hsa_status launch_index_full(const hsa_cache* cache, const void* q, const float*
   se.hist = sp.hist;
   se.cand = reinterpret_cast<int32_t*>(W + L.off_cand_full);
   se.ld_cand = 2 * L.ld_b;
+  se.tail = (cache->flags & HSA_CACHE_POOL_TAIL) ? 1 : 0;
+  se.pool_ld = kPool + (se.tail ? HSA_POOL_TAIL_SLOTS : 0);
   hsa_status r = cuda_fail(launch_index_scan(sp, sms, s), "index scan launch");
   if (r != HSA_OK) return r;
   return cuda_fail(launch_select(se, s), "select launch");
@@ -215,6 +227,7 @@ hsa_status attn_common(const hsa_cache* cache, const void* q, const int32_t* top
   p.out = out;
   p.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.off_attn);
   p.status = status;
+  p.wait_ns = wait_limit_ns();
   return cuda_fail(launch_attention(p, (cudaStream_t)stream), "attention launch");
 }
 }  // namespace hsa
@@ -278,6 +291,7 @@ hsa_status hsa_cache_write_compress(const hsa_cache* cache, const void* wkv, con
   p.ik_q = cache->ik_q;
   p.ik_s = cache->ik_s;
   p.status = status;
+  p.wait_ns = wait_limit_ns();
   if (cache->flags & HSA_CACHE_ROPE) {
     // RoPE turns per position of pair k, theta^(-k/32) / 2 pi, as a 64-bit binary fraction: the
     // phase of entry e is then the wrapping product e * turns (mod one turn, exactly)
@@ -327,6 +341,8 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
     rp.w = w;
     rp.vis = vis;
     rp.pool = pool;
+    rp.tail = (cache->flags & HSA_CACHE_POOL_TAIL) ? 1 : 0;
+    rp.pool_ld = kPool + (rp.tail ? HSA_POOL_TAIL_SLOTS : 0);
     rp.topk_out = topk_out;
     rp.status = status;
     rp.inputs_ready = inputs_ready ? 1 : 0;
@@ -389,6 +405,16 @@ hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, voi
                                 a->out[l], ws, ws_bytes, stream, true, m == HSA_MODE_REUSE);
     if (st != HSA_OK) return st;
   }
+  return HSA_OK;
+}
+
+hsa_status hsa_set_wait_limit(uint64_t ns) {
+  g_wait_ns.store(ns ? ns : kWaitLimitNs, std::memory_order_relaxed);
+  return HSA_OK;
+}
+
+hsa_status hsa_debug_stall_next_scan(void) {
+  g_stall_next_scan.store(1);
   return HSA_OK;
 }
 

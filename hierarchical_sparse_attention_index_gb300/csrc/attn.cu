@@ -193,7 +193,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       bool ok = true;
 #pragma unroll
       for (int st = 0; st < 4; ++st) {
-        ok = mbar_wait(kb_bar + 8u * st, 0) && ok;
+        ok = mbar_wait(kb_bar + 8u * st, 0, p.wait_ns) && ok;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -269,7 +269,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   {
     const int qh = 4 * warp + (lane >> 3), c = lane & 7;
     const uint32_t a0 = sQ + sw128((uint32_t)qh, (uint32_t)c);
-    if (!mbar_wait(q_bar, 0) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    if (!mbar_wait(q_bar, 0, p.wait_ns) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
     uint4 qv[8];
 #pragma unroll
     for (int kb = 0; kb < 8; ++kb) qv[kb] = lds128(a0 + (uint32_t)kb * (kHAtt * 128u));
@@ -355,7 +355,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   }
   if (qq == 0) s_valid[krow] = kval ? 1 : 0;
 
-  if (!mbar_wait(bar, 0) && tid == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+  if (!mbar_wait(bar, 0, p.wait_ns) && tid == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
   tc_fence_after();
   named_bar_sync(1, kWorkThreads);    // s_valid, s_scale visible
 
@@ -440,7 +440,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   const int dim = 128 * mtile + 32 * qd + lane;
   float own[16];
   {
-    if (!mbar_wait(bar + 8u * (1 + mtile), 0) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    if (!mbar_wait(bar + 8u * (1 + mtile), 0, p.wait_ns) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
     tc_fence_after();
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
@@ -490,7 +490,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   cluster_arrive();                   // phase B: this CTA's partial is published
   cluster_wait();
   tc_fence_after();
-  if (warp == 0) tmem_free(tmem, kTmemCols);
+  if (warp == 0) {
+    // Nothing of this CTA may still be in flight when it frees its tensor memory and exits, even
+    // if a wait above gave up: the last PV commit covers every MMA the CTA issued, q_bar the
+    // query copy (both waits are bounded, and immediate when nothing timed out).
+    if (!mbar_wait(bar + 8u * 4, 0, p.wait_ns) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    if (!mbar_wait(q_bar, 0, p.wait_ns) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    tc_fence_after();
+    tmem_free(tmem, kTmemCols);
+  }
 
   // ---------------------------------------------------------------- out[h][dim] = sum_c w_c[h] O_c[h][dim], c in rank order
   {

@@ -28,7 +28,8 @@ constexpr int kHistShift = 20;
 constexpr int kAttnSplit = 4;          // attention CTAs (one cluster) per (request, query)
 constexpr int kRxSplit = 4;            // fused Reindex CTAs (one cluster) per (request, query)
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
+// A bounded wait gives up after this many nanoseconds of %globaltimer unless the launch passes
+// another limit (hsa_set_wait_limit).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -67,14 +68,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for phase `parity` of the barrier to complete; false if kWaitLimitNs ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier to complete; false if limit_ns ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -43,6 +43,9 @@ hsa_status launch_index_full(const hsa_cache* cache, const void* q, const float*
 // false on a non-sm_100-family device.
 bool device_status_ptr(uint32_t** status, int* sms);
 
+// Limit of the kernels' bounded waits for the next launches (hsa_set_wait_limit), in ns.
+uint64_t wait_limit_ns();
+
 // Raise the dynamic shared-memory limit of kernel `func` to `bytes` on the current device. The
 // attribute belongs to the device's context, so it is set once per (device, kernel) and again
 // whenever a larger size is asked for; thread-safe.
@@ -66,6 +69,8 @@ struct ScanParams {         // Full mode: a segment is one request, its nq queri
   int64_t ld_b;
   uint32_t* hist;        // [rows][4096] counts of the block maxima's top 12 key bits
   uint32_t* status;
+  uint64_t wait_ns;      // bounded-wait limit
+  int32_t stall_last;    // test hook: CTA 0's producer withholds the copy of its last stage
 };
 
 struct SelectParams {       // the Full step's block top-2048 (pool) and position top-512
@@ -80,7 +85,9 @@ struct SelectParams {       // the Full step's block top-2048 (pool) and positio
   int32_t* cand;         // [rows][2 * ld_b] threshold-bin candidates past the shared-memory stage
   int64_t ld_cand;
   int32_t* topk_out;     // [rows][512]
-  int32_t* pool_out;     // [rows][16384]
+  int32_t* pool_out;     // [rows][pool_ld]
+  int64_t pool_ld;       // 16384, or 16384 + 160 with the window tail
+  int32_t tail;          // 1: the window's blocks join the pool
   uint32_t* status;
 };
 
@@ -96,7 +103,9 @@ struct ReindexParams {
   const uint16_t* q;     // bf16 [B][nq][16][128]
   const float* w;        // [B][nq][16]
   const int32_t* vis;    // [B][nq]
-  const int32_t* pool;   // [B][nq][16384]
+  const int32_t* pool;   // [B][nq][pool_ld]
+  int64_t pool_ld;       // 16384, or 16384 + 160 with the window tail
+  int32_t tail;          // 1: CTA rank 3 also scores the 160 slots past 16384
   int32_t* topk_out;     // [B][nq][512]
   uint32_t* status;
   int32_t inputs_ready;  // 1: q, w, vis and pool are complete at launch (schedule_step); the kernel then waits
@@ -123,6 +132,7 @@ struct AttnParams {
   float* out;             // [B][nq][64][512]
   float* partial;         // workspace: [B*nq][4][64*512 outputs, then 64 (max, sum) pairs]
   uint32_t* status;
+  uint64_t wait_ns;       // bounded-wait limit
 };
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t s);
 
@@ -139,6 +149,7 @@ struct WriteParams {
   uint8_t* ik_q;
   uint8_t* ik_s;
   uint32_t* status;
+  uint64_t wait_ns;                          // bounded-wait limit
   int32_t rope;                              // 1: rotate the main-KV latent's last 64 dims
   uint64_t rope_turns[HSA_ROPE_DIMS / 2];    // turns per position of pair k, a 64-bit binary fraction
 };

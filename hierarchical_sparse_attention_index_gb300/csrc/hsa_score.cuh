@@ -180,15 +180,26 @@ __device__ __forceinline__ float score_rows32(uint32_t codes, int row_off, uint3
 }
 
 // One warp gathers its 32 pool slots (lane l holds slot l's pool value pv): run u (slots
-// 8u .. 8u+7) starts at the pool value of lane 8u and is fetched (64-byte codes of 8 entries and
-// their 4-byte scales, with cp.async, into dc / ds) only if that start is an 8-aligned in-range
-// entry; slot l is scored (slots[l] = its position) only if it holds start + l % 8 and is
-// visible, else slots[l] = -1; anything inconsistent is flagged. Ends with a commit.
+// 8u .. 8u+7) covers the 8-position block its first (else its last) slot names (a run may start
+// with empty slots: a window block of the pool tail keeps only its newest positions) and is fetched
+// (64-byte codes of 8 entries and their 4-byte scales, with cp.async, into dc / ds) only if that
+// block is in range; slot l is scored (slots[l] = its position) only if it holds
+// block + l % 8 and is visible, else slots[l] = -1; anything inconsistent is flagged. Ends with
+// a commit.
+template <bool kPoolTail>
 __device__ __forceinline__ void gather_runs(const uint8_t* ik_q, const uint8_t* ik_s, int64_t ebase, int64_t cap,
                                             int vis, int pv, int lane, uint32_t dc, uint32_t ds, int* slots,
                                             uint32_t* status) {
   const int j = lane & 7;
-  const int base = __shfl_sync(0xffffffffu, pv, lane & ~7);
+  // the run's block: its first slot's position or, with a pool tail, when that slot is empty
+  // (only the first window block starts with empty slots, and its last slot is live), its last
+  // slot's position - 7
+  const int v0 = __shfl_sync(0xffffffffu, pv, lane & ~7);
+  int base = v0;
+  if (kPoolTail) {
+    const int v7 = __shfl_sync(0xffffffffu, pv, lane | 7);
+    base = v0 >= 0 ? v0 : (v7 >= 0 ? v7 - 7 : -1);
+  }
   const bool bok = (base >= 0) && ((base & 7) == 0) && (base < cap);
   int outv = -1;
   if (bok && pv >= 0) {

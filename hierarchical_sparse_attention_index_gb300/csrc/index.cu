@@ -109,25 +109,33 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
+    // filled[s] / fph[s]: whether stage s was ever filled and the parity of its last fill. A wait
+    // that gives up flags the status, stops the stream and falls through to the drain: the CTA
+    // never exits with one of its copies still in flight.
+    bool filled[kMaxStages] = {false, false, false, false};
+    uint32_t fph[kMaxStages] = {0u, 0u, 0u, 0u};
     int s = 0, round = 0, seg = i0 / cps, c = i0 % cps;
     for (int it = i0; it < i1; ++it) {
       if (round > 0) {
-        if (!mbar_wait(empty0 + 8 * s, (round - 1) & 1)) {
+        if (!mbar_wait(empty0 + 8 * s, (round - 1) & 1, p.wait_ns)) {
           flag_status(p.status, HSA_FLAG_TIMEOUT);
           *reinterpret_cast<volatile int*>(misc) = 1;
-          return;
+          break;
         }
       }
       const uint32_t full = full0 + 8 * s;
       const uint32_t dcodes = smem_u32(smem + L.codes + (size_t)s * kCodesBytes);
       const uint32_t dscales = smem_u32(smem + L.scales + (size_t)s * kScaleBytes);
+      // test hook (hsa_debug_stall_next_scan): CTA 0 withholds its last stage, whose consumers
+      // then wait in vain until the limit runs out
+      const bool withhold = p.stall_last && blockIdx.x == 0 && it == i1 - 1;
       {
         int vmax = 0;
         for (int q = 0; q < p.nq; ++q) vmax = max(vmax, __ldg(p.vis + seg * p.nq + q));
         vmax = (int)imin64(vmax, p.cap);
         const int p0 = c * kChunk;
         const int n = max(0, min(kChunk, vmax - p0));
-        if (lane == 0) {
+        if (lane == 0 && !withhold) {
           if (n > 0) {
             const int nc = (int)imin64((n + 7) & ~7, p.cap - p0);
             mbar_arrive_expect_tx(full, (uint32_t)nc * 68u);
@@ -141,6 +149,10 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
             mbar_arrive(full);
           }
         }
+        if (!withhold) {
+          filled[s] = true;
+          fph[s] = (uint32_t)round & 1u;
+        }
       }
       if (++s == nst) {
         s = 0;
@@ -151,6 +163,9 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
         ++seg;
       }
     }
+    // drain: every copy this warp issued has landed (immediate unless a consumer gave up early)
+    for (int st = 0; st < nst; ++st)
+      if (filled[st] && !mbar_wait(full0 + 8 * st, fph[st], p.wait_ns)) flag_status(p.status, HSA_FLAG_TIMEOUT);
     return;
   }
 
@@ -220,7 +235,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     }
     ++since_flush;
     if (!dead && *reinterpret_cast<volatile int*>(misc) != 0) dead = true;
-    if (!dead && !mbar_wait(full0 + 8 * s, ph)) {
+    if (!dead && !mbar_wait(full0 + 8 * s, ph, p.wait_ns)) {
       flag_status(p.status, HSA_FLAG_TIMEOUT);
       *reinterpret_cast<volatile int*>(misc) = 1;
       dead = true;
@@ -550,32 +565,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
   const int w0 = min(nwb, tid * per), w1 = min(nwb, w0 + per);
   if (rank == 0) {
     // ---------------------------------------------------------------- 4a. the pool, ascending
+    // With the window tail ([ARCH] §3.3 旁路与边界) the blocks of positions [vis - W, vis) join
+    // the selected ones; a window block the selection did not pick keeps only its window
+    // positions. They are the row's last blocks, so ascending block order puts them at the tail.
+    const int wlo = p.tail ? max(0, vis - kSwa) : vis;
+    const int wb0 = p.tail ? wlo / kBlk : nb;         // first window block
+    auto wmask = [&](int i) -> uint32_t {             // window blocks inside bitmap word i
+      const int lo = max(wb0, 32 * i), hi = min(nb, 32 * i + 32);
+      if (lo >= hi) return 0u;
+      const uint32_t m = (hi - lo == 32) ? 0xFFFFFFFFu : ((1u << (hi - lo)) - 1u);
+      return m << (lo - 32 * i);
+    };
+    int cnt = 0;
+    for (int i = w0; i < w1; ++i) cnt += __popc(bits[i] | wmask(i));
     int totp;
-    int o = bitmap_offsets(bits, w0, w1, S.scr, tid, &totp);
-    int32_t* out = p.pool_out + (size_t)row * kPool;
+    int o = excl_scan(cnt, S.scr, 1, kSelThreads, &totp, tid);
+    const int max_runs = (int)(p.pool_ld / kBlk);
+    int32_t* out = p.pool_out + (size_t)row * p.pool_ld;
     for (int i = w0; i < w1; ++i) {
-      uint32_t m = bits[i];
+      const uint32_t selw = bits[i];
+      uint32_t m = selw | wmask(i);
       while (m) {
-        const int blk = i * 32 + __ffs(m) - 1;
+        const int bi = __ffs(m) - 1;
         m &= m - 1;
-        if (o < kCandBlocks) {
+        const int blk = i * 32 + bi;
+        const int lo = ((selw >> bi) & 1u) ? 0 : wlo;  // first position the run keeps
+        if (o < max_runs) {
           const int q0 = blk * 8;
           int4 lo4, hi4;
-          lo4.x = (q0 + 0 < vis) ? q0 + 0 : -1;
-          lo4.y = (q0 + 1 < vis) ? q0 + 1 : -1;
-          lo4.z = (q0 + 2 < vis) ? q0 + 2 : -1;
-          lo4.w = (q0 + 3 < vis) ? q0 + 3 : -1;
-          hi4.x = (q0 + 4 < vis) ? q0 + 4 : -1;
-          hi4.y = (q0 + 5 < vis) ? q0 + 5 : -1;
-          hi4.z = (q0 + 6 < vis) ? q0 + 6 : -1;
-          hi4.w = (q0 + 7 < vis) ? q0 + 7 : -1;
+          lo4.x = (q0 + 0 < vis && q0 + 0 >= lo) ? q0 + 0 : -1;
+          lo4.y = (q0 + 1 < vis && q0 + 1 >= lo) ? q0 + 1 : -1;
+          lo4.z = (q0 + 2 < vis && q0 + 2 >= lo) ? q0 + 2 : -1;
+          lo4.w = (q0 + 3 < vis && q0 + 3 >= lo) ? q0 + 3 : -1;
+          hi4.x = (q0 + 4 < vis && q0 + 4 >= lo) ? q0 + 4 : -1;
+          hi4.y = (q0 + 5 < vis && q0 + 5 >= lo) ? q0 + 5 : -1;
+          hi4.z = (q0 + 6 < vis && q0 + 6 >= lo) ? q0 + 6 : -1;
+          hi4.w = (q0 + 7 < vis && q0 + 7 >= lo) ? q0 + 7 : -1;
           reinterpret_cast<int4*>(out + 8 * o)[0] = lo4;
           reinterpret_cast<int4*>(out + 8 * o)[1] = hi4;
         }
         ++o;
       }
     }
-    for (int j = 8 * min(totp, kCandBlocks) + tid; j < kPool; j += kSelThreads) out[j] = -1;
+    for (int64_t j = 8 * (int64_t)min(totp, max_runs) + tid; j < p.pool_ld; j += kSelThreads) out[j] = -1;
     cluster_wait();
     return;
   }

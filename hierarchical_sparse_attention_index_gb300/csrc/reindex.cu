@@ -3,7 +3,9 @@
 // 16,384 pool slots s = sum_h w_h ReLU(q_h . k) and emit the exact top-512 (ties to the lower
 // slot), ascending, in one launch.
 //
-// One thread-block cluster of 4 CTAs per row; CTA r owns slots [4096 r, 4096 r + 4096):
+// One thread-block cluster of 4 CTAs per row; CTA r owns slots [4096 r, 4096 r + 4096) (with
+// the window tail, CTA 3 also owns the 160 slots past 16,384, scored as a 9th group by its warps
+// 0..4, so the slot order stays the position order):
 //  1. 16 warps score 256 slots each: 8 groups of 32 slots (four 8-entry runs) gathered with
 //     cp.async into a per-warp ring 4 groups ahead, scored with warp MMAs (shared with the scan
 //     kernel); scores stay in shared memory with a 4096-bin histogram of their top 12 key bits;
@@ -37,6 +39,9 @@ constexpr int kRxRing = 5;                                // gathers run 4 group
 constexpr uint32_t kGrpCodes = 32 * 64, kGrpScales = 32 * 4;
 constexpr int kRankMax = 512;                             // threshold-bin elements ranked by counting up to this many
 constexpr int kPerT = kHistBins / kRxThreads;             // 8 bins (or slots) per thread
+constexpr int kTail = HSA_POOL_TAIL_SLOTS;                // slots past kPool with the window tail (CTA 3)
+constexpr int kTailGroups = kTail / 32;                   // 5 groups of 32: warps 0..4 of CTA 3
+constexpr int kLocMax = kSlotsPerCta + kTail;             // local slots of CTA 3 with the tail
 
 // shared-memory layout (bytes)
 constexpr uint32_t kOffRing = 0;                                                  // [16 warps][5][codes|scales]
@@ -45,16 +50,20 @@ constexpr uint32_t kOffSlots = kOffRing + kRingBytes;                           
 constexpr uint32_t kOffBfrag = kOffSlots + kRxWarps * kRxRing * 32 * 4;
 constexpr uint32_t kOffWsc = kOffBfrag + kQFragWords * 4;
 constexpr uint32_t kOffSfl = kOffWsc + kQWeights * 4;                              // [16 warps][512 B]
-constexpr uint32_t kOffSc = kOffSfl + kRxWarps * 512;                              // [4096] scores
-constexpr uint32_t kOffHist = kOffSc + kSlotsPerCta * 4;                           // [4096] counts
-constexpr uint32_t kOffSel = kOffHist + kHistBins * 4;                             // [4096 bits] taken slots
-constexpr uint32_t kOffScr = kOffSel + kSlotsPerCta / 8;                           // scratch ints
+constexpr uint32_t kOffSc = kOffSfl + kRxWarps * 512;                              // [4256] scores
+constexpr uint32_t kOffHist = kOffSc + kLocMax * 4;                                // [4096] counts
+constexpr uint32_t kOffSel = kOffHist + kHistBins * 4;                             // [4256 bits] taken slots
+constexpr uint32_t kSelBytes = (kLocMax / 8 + 15) / 16 * 16;                     // bitmap bytes, 16-aligned
+constexpr uint32_t kOffScr = kOffSel + kSelBytes;                                  // scratch ints
 constexpr uint32_t kScrInts = 128;
 constexpr uint32_t kRxSmem = kOffScr + kScrInts * 4;
 static_assert(kRxSmem <= 232448, "shared memory");
 // after scoring, the rings hold the union (64-bit composites) and the score array the ranked
 // threshold-bin elements
-static_assert((uint32_t)kPool * 8 + kSlotsPerCta * 8 <= kRingBytes, "union staging and own list fit the rings");
+static_assert((uint32_t)(kPool + kTail) * 8 + kLocMax * 8 <= kRingBytes, "union staging and own list fit the rings");
+static_assert(kTail % 32 == 0 && kTailGroups <= kRxWarps, "tail groups");
+// scr + 84 holds a 64-bit composite: every region starts 16-byte aligned
+static_assert(kOffSc % 16 == 0 && kOffHist % 16 == 0 && kOffSel % 16 == 0 && kOffScr % 16 == 0, "alignment");
 static_assert(kRankMax * 8 <= kSlotsPerCta * 4, "ranked elements fit the score array");
 
 // (order key, inverted row slot): larger = better, ties to the lower slot
@@ -69,6 +78,7 @@ __device__ __forceinline__ int find_threshold(const uint32_t* hist, int K, int* 
   return smem_threshold<kRxThreads>(hist, K, scr, scr + 64, tid);
 }
 
+template <bool kPoolTail>
 __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads, 1)
     reindex_kernel(const ReindexParams p) {
   extern __shared__ __align__(1024) uint8_t rsm[];
@@ -83,7 +93,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   float* wsc = reinterpret_cast<float*>(rsm + kOffWsc);
 
   for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;
-  for (int i = tid; i < kSlotsPerCta / 32; i += kRxThreads) sel[i] = 0u;
+  for (int i = tid; i < kLocMax / 32; i += kRxThreads) sel[i] = 0u;
   if (tid < kScrInts) scr[tid] = 0;
   // Inside schedule_step everything this kernel reads was complete before it was launched (the
   // pool two or more kernels earlier, q, w and vis before the step), so it scores while the
@@ -92,19 +102,26 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   griddep_launch_dependents();
 
   const int vis = __ldg(p.vis + row);
-  const int32_t* pool_row = p.pool + (size_t)row * kPool;
+  const int32_t* pool_row = p.pool + (size_t)row * p.pool_ld;
+  const bool has_tail = kPoolTail && rank == kRxCluster - 1;
 
   // ---------------------------------------------------------------- 1. score this warp's 256 slots
   const int slot0 = kSlotsPerCta * rank + kSlotsPerWarp * warp;   // first slot (row-relative) of the warp
+  // group g < 8: the warp's own slots; group 8 (CTA 3's warps 0..4 with the tail): slots
+  // kPool + 32 warp .. + 31, local kSlotsPerCta + 32 warp
+  const int ngroups = kGroups + ((has_tail && warp < kTailGroups) ? 1 : 0);
   const int64_t ebase = (int64_t)(row / p.nq) * p.cap;
   const uint32_t ring = smem_u32(rsm + kOffRing) + (uint32_t)(warp * kRxRing) * (kGrpCodes + kGrpScales);
   int* slots = reinterpret_cast<int*>(rsm + kOffSlots) + warp * kRxRing * 32;
   // a group's pool values are loaded one gather ahead, so a gather never waits for them
-  auto pool_val = [&](int grp) { return (grp < kGroups) ? __ldg(pool_row + slot0 + 32 * grp + lane) : -1; };
+  auto pool_val = [&](int grp) {
+    if (grp >= ngroups) return -1;
+    return __ldg(pool_row + (grp < kGroups ? slot0 + 32 * grp : kPool + 32 * warp) + lane);
+  };
   auto gather = [&](int grp, int pv) {
     const int rs = grp % kRxRing;
     const uint32_t dc = ring + (uint32_t)rs * (kGrpCodes + kGrpScales);
-    gather_runs(p.ik_q, p.ik_s, ebase, p.cap, vis, pv, lane, dc, dc + kGrpCodes, slots + rs * 32, p.status);
+    gather_runs<kPoolTail>(p.ik_q, p.ik_s, ebase, p.cap, vis, pv, lane, dc, dc + kGrpCodes, slots + rs * 32, p.status);
   };
   {
     // the prologue's pool values go in flight before the query is staged
@@ -123,8 +140,8 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   const uint32_t sf_base = smem_u32(rsm + kOffSfl) + (uint32_t)warp * 512u;
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll 1
-  for (int k = 0; k < kGroups; ++k) {
-    if (k + kRxRing - 1 < kGroups) {
+  for (int k = 0; k < ngroups; ++k) {
+    if (k + kRxRing - 1 < ngroups) {
       gather(k + kRxRing - 1, pv_next);
       pv_next = pool_val(k + kRxRing);
     } else {
@@ -138,7 +155,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     float v = score_rows32(codes, 0, sf_base, true, B, wr, lane);
     const bool ok = slots[rs * 32 + 8 * t + g] >= 0;
     v = ok ? v : -INFINITY;
-    const int ls = kSlotsPerWarp * warp + 32 * k + 8 * t + g;   // CTA-local slot
+    const int ls = (k < kGroups ? kSlotsPerWarp * warp + 32 * k : kSlotsPerCta + 32 * warp) + 8 * t + g;   // CTA-local slot
     sc[ls] = v;
     if (ok) atomicAdd(hist + (order_key(v) >> kHistShift), 1u);
     __syncwarp();                     // ring buffer rs is free for the gather 4 groups ahead
@@ -156,7 +173,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   // the count and the number of valid elements at scr[90], scr[91]; the peers read them over
   // distributed shared memory after the cluster barrier. The union is staged at ust.
   uint64_t* ust = reinterpret_cast<uint64_t*>(rsm + kOffRing);
-  uint64_t* lst = reinterpret_cast<uint64_t*>(rsm + kOffRing + kPool * 8);
+  uint64_t* lst = reinterpret_cast<uint64_t*>(rsm + kOffRing + (kPool + kTail) * 8);
   {
     // the warp's 8 rounds of appends take one atomic: round i's lanes follow rounds 0..i-1
     uint32_t keys[kPerT], bal[kPerT];
@@ -178,6 +195,14 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
         lst[base + __popc(bal[i] & lt)] = comp_of(keys[i], (uint32_t)(kSlotsPerCta * rank + kPerT * tid + i));
       base += __popc(bal[i]);
     }
+  }
+  if (has_tail) {
+    // CTA 3's tail slots kSlotsPerCta + tid, tid < 160
+    const float v = (tid < kTail) ? sc[kSlotsPerCta + tid] : -INFINITY;
+    const uint32_t key = order_key(v);
+    const bool in = (v != -INFINITY) && (int)(key >> kHistShift) >= lthr;
+    const int j = warp_append(in, scr + 72, lane);
+    if (in) lst[j] = comp_of(key, (uint32_t)(kSlotsPerCta * rank + kSlotsPerCta + tid));
   }
   for (int i = tid; i < kHistBins; i += kRxThreads) hist[i] = 0u;   // read by find_threshold above
   named_bar_sync(1, kRxThreads);
@@ -354,6 +379,19 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     if (at < kTopK) out[at] = __ldg(pl + i);
     ++at;
   }
+  if (has_tail) {
+    // the tail slots follow the CTA's main slots: local kSlotsPerCta + 8 tid .. + 7, tid < 20
+    uint32_t mt = (tid < kTail / 8) ? (sel[kSlotsPerCta / 32 + (tid >> 2)] >> (kPerT * (tid & 3))) & 0xFFu : 0u;
+    int tt;
+    int at2 = off + total + excl_scan(__popc(mt), scr, 1, kRxThreads, &tt, tid);
+    const int32_t* plt = pool_row + kPool + kPerT * tid;
+    while (mt) {
+      const int i = __ffs(mt) - 1;
+      mt &= mt - 1u;
+      if (at2 < kTopK) out[at2] = __ldg(plt + i);
+      ++at2;
+    }
+  }
   if (rank == 0)
     for (int j = K + tid; j < kTopK; j += kRxThreads) out[j] = -1;
   cluster_wait();                     // no peer still reads this CTA's list
@@ -362,10 +400,11 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
 }  // namespace
 
 cudaError_t launch_reindex(const ReindexParams& p, cudaStream_t s) {
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(reindex_kernel), kRxSmem);
+  auto kern = p.tail ? reindex_kernel<true> : reindex_kernel<false>;
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), kRxSmem);
   if (e != cudaSuccess) return e;
   const int rows = p.batch * p.nq;
-  return launch_pdl(reindex_kernel, dim3(rows * kRxCluster), dim3(kRxThreads), kRxSmem, s, p);
+  return launch_pdl(kern, dim3(rows * kRxCluster), dim3(kRxThreads), kRxSmem, s, p);
 }
 
 }  // namespace hsa

@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
       }
     }
   };
+  bool mma_ok = true;                 // every MMA-completion wait of this thread succeeded
   int db = 0;                         // accumulator buffer of the tile being computed
   bool have_prev = false;
   int64_t prev_tile = 0;
@@ -417,7 +418,10 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
     }
     // ------------------------------------------------------------ 4: the previous tile's indexer K
     if (have_prev) epilogue(prev_tile, prev_cur, dcol ^ kDCols);
-    if (!mbar_wait(mma_bar, phase) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+    if (!mbar_wait(mma_bar, phase, p.wait_ns)) {
+      if (lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+      mma_ok = false;
+    }
     phase ^= 1u;
     tc_fence_after();                 // this tile's accumulators (read next iteration) and B tile are done
     prev_tile = tile;
@@ -427,6 +431,11 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
     cur = nxt;
   }
   if (have_prev) epilogue(prev_tile, prev_cur, (uint32_t)(db ^ 1) * kDCols);
+  // a wait that gave up may have left this CTA's last MMAs running: wait again (bounded) before
+  // the tensor memory is freed
+  if (__syncthreads_or(!mma_ok) && have_prev && warp == 0) {
+    if (!mbar_wait(mma_bar, phase ^ 1u, p.wait_ns) && lane == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

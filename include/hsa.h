@@ -67,6 +67,7 @@ extern "C" {
 #define HSA_CAND_BLOCKS 2048  /* candidate_topk_blocks                    [890B] §二 */
 #define HSA_BLOCK 8           /* candidate_block_size                     [890B] §二 */
 #define HSA_POOL_SLOTS 16384  /* 2048 x 8 candidate positions             [CED] Figure 5 */
+#define HSA_POOL_TAIL_SLOTS 160 /* extra pool slots with HSA_CACHE_POOL_TAIL (<= 17 window blocks) */
 #define HSA_SWA_W 128         /* sliding_window                           [890B] §二 */
 #define HSA_MAX_NQ 8          /* query tokens per request per call (draft block 5 fits) */
 #define HSA_MAX_VIS (1 << 20) /* longest visible context per query (1M, [ARCH] §1 table) */
@@ -98,6 +99,7 @@ typedef enum { HSA_MODE_FULL = 0, HSA_MODE_REINDEX = 1, HSA_MODE_REUSE = 2 } hsa
 
 /* Cache flags (hsa_cache.flags) */
 #define HSA_CACHE_ROPE 1u         /* the writer applies RoPE to the main-KV latent (see hsa_cache_write_compress) */
+#define HSA_CACHE_POOL_TAIL 2u    /* index pools of this cache carry the window tail (see hsa_index_full) */
 
 /* Caller-owned cache descriptor. All four buffers are device memory, 16-byte aligned. */
 typedef struct {
@@ -125,7 +127,7 @@ typedef struct {
   float* const* out;            /* [n_layers] -> f32 [B][nq][64][512]                      */
   int32_t* const* topk;         /* [n_layers] -> i32 [B][nq][512] for Full/Reindex slots;
                                    ignored for Reuse slots, which read the latest producer  */
-  int32_t* pool;                /* i32 [B][nq][16384], written by the Full slot            */
+  int32_t* pool;                /* i32 [B][nq][16384] (16544 with HSA_CACHE_POOL_TAIL), written by the Full slot */
   const int32_t* vis;           /* i32 [B][nq] visible lengths                              */
   int64_t max_vis;              /* host upper bound of vis                                  */
   float sm_scale;               /* softmax scale applied to q.k                             */
@@ -180,6 +182,11 @@ HSA_API hsa_status hsa_cache_write_compress(const hsa_cache* cache, const void* 
  *   with the largest block max, in ascending block order. Each block contributes 8 slots
  *   8b..8b+7, positions >= vis are -1, and unused slots are -1.
  * Ties go to the lower position or block. Scores are fp32 (tensor-core f16 products, fp32 sums).
+ * With HSA_CACHE_POOL_TAIL in cache->flags ([ARCH] §3.3 旁路与边界: the newest tokens of the
+ * sliding window skip the funnel and join the expanded pool at its tail), pool rows have
+ * HSA_POOL_SLOTS + HSA_POOL_TAIL_SLOTS slots: the blocks holding positions [vis - 128, vis) join
+ * the selected blocks, still as ascending 8-slot runs, and a window block the selection did not
+ * pick keeps only its positions >= vis - 128 (its other slots are -1).
  *   q      bf16 [B][nq][16][128]      w   f32 [B][nq][16]      vis  i32 [B][nq]
  *   ws     workspace of at least hsa_workspace_bytes(B, nq, max_vis) bytes */
 HSA_API hsa_status hsa_index_full(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis,
@@ -189,7 +196,7 @@ HSA_API hsa_status hsa_index_full(const hsa_cache* cache, const void* q, const f
 /* Reindex-mode indexer ([CED] Figure 5 right; [ARCH] §3.3 池内过滤; [COST] §3.2).
  * Scores only the pool slots (pool[b][i][j] in [0, vis), others skipped) with this layer's
  * q and w, and writes the positions of the min(512, #valid) best, ascending, -1 padded.
- *   pool   i32 [B][nq][16384] as written by hsa_index_full
+ *   pool   i32 [B][nq][16384] as written by hsa_index_full ([B][nq][16544] with HSA_CACHE_POOL_TAIL)
  *   ws     workspace of at least hsa_workspace_bytes(B, nq, max_vis) bytes, checked like the
  *          other calls' so that one workspace serves every call; this call does not touch it
  *          (its CTAs exchange their candidates through distributed shared memory) */
@@ -247,6 +254,20 @@ HSA_API hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q,
  * pool rows, while the previous kernel of the step drains. */
 HSA_API hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* args, void* ws,
                              size_t ws_bytes, hsa_stream_t stream);
+
+/* Limit of the kernels' bounded waits (for a copy or a tensor-core result that does not arrive),
+ * in nanoseconds, for launches made after the call from any thread, on every device. A wait that
+ * runs out sets HSA_FLAG_TIMEOUT; the kernel then skips the work that needed it, waits (again
+ * bounded) for its own copies and tensor-core work in flight, frees its tensor memory and
+ * finishes, so the context stays usable. 0 restores the default, 2 s. Host only; no error. */
+HSA_API hsa_status hsa_set_wait_limit(uint64_t ns);
+
+/* Test hook for failure detection. The next hsa_index_full call (on any device or thread)
+ * withholds one indexer-K copy of its scan kernel: the first CTA's last pipeline stage is never
+ * filled, so that stage's consumer warps wait until the limit of hsa_set_wait_limit runs out,
+ * set HSA_FLAG_TIMEOUT, skip the stage and finish with no copy or tensor-core work in flight.
+ * That call's outputs are invalid; the workspace and every later call are unaffected. Host only. */
+HSA_API hsa_status hsa_debug_stall_next_scan(void);
 
 /* Synchronise `stream`, return the device status flags (HSA_FLAG_*) in *flags and clear them.
  * Returns HSA_ERR_TIMEOUT if HSA_FLAG_TIMEOUT is set, else HSA_OK or HSA_ERR_CUDA. */

@@ -48,6 +48,7 @@ CAND_BLOCKS = 2048      # candidate_topk_blocks                         [890B] ¬
 CAND_BLOCK = 8          # candidate_block_size                          [890B] ÂÄôÈÄâÊ±†ËÆ©Ê∑±Â±ÇÁ¥¢ÂºïÂô®‚Ä¶
 POOL_SLOTS = CAND_BLOCKS * CAND_BLOCK   # 16,384                        [CED] Figure 5
 SWA_W = 128             # sliding_window                                [890B] ¬ß‰∫å table
+POOL_TAIL_SLOTS = 160   # pool slots past POOL_SLOTS with the window tail: the <= 17 window blocks, as 5 x 32
 RMS_EPS = 1e-6
 ROPE_THETA = 160000.0   # RoPE base of the compressed latent           [ARCH] ¬ß3.2 ÂéãÁº© RoPE
 ROPE_DIMS = 64          # rotary dims: the last 64 of 512 (the 448 B NoPE + 128 B RoPE page layout) [ARCH] ¬ß7
@@ -328,31 +329,45 @@ def block_maxima(s, vis):
     return m
 
 
-def expand_pool(blocks, vis):
+def expand_pool(blocks, vis, tail=False):
     """Candidate pool: each selected block (ascending) contributes 8 slots 8b..8b+7, with
     positions >= vis written as -1. Slots beyond the selected blocks are -1. The size is
-    min(2048, ceil(vis/8))*8 live slots out of 16,384 ([CED] Figure 5; [ARCH] ¬ß3.3)."""
-    pool = np.full(POOL_SLOTS, -1, np.int64)
-    for i, b in enumerate(np.sort(blocks)):
+    min(2048, ceil(vis/8))*8 live slots out of 16,384 ([CED] Figure 5; [ARCH] ¬ß3.3).
+
+    With tail ([ARCH] ¬ß3.3 ÊóÅË∑Ø‰∏éËæπÁïå: the newest tokens of the sliding window skip the funnel
+    and are merged at the tail of the expanded pool, so they are not lost while their block is
+    still filling): the blocks holding positions [vis - 128, vis) join the selected ones, and a
+    window block the selection did not pick contributes only its positions >= vis - 128. The
+    union stays in ascending block order (the window blocks are the last ones, at the tail), in
+    POOL_SLOTS + POOL_TAIL_SLOTS slots. That the window joins by whole 8-slot runs, deduplicated
+    against the selected blocks, is a reading."""
+    vis = int(vis)
+    sel = set(int(b) for b in blocks)
+    wlo = max(0, vis - SWA_W)
+    run_blocks = sel | (set(range(wlo // CAND_BLOCK, -(-vis // CAND_BLOCK))) if tail else set())
+    pool = np.full(POOL_SLOTS + (POOL_TAIL_SLOTS if tail else 0), -1, np.int64)
+    for i, b in enumerate(sorted(run_blocks)):
         p = b * CAND_BLOCK + np.arange(CAND_BLOCK)
-        pool[i * CAND_BLOCK:(i + 1) * CAND_BLOCK] = np.where(p < vis, p, -1)
+        keep = (p < vis) & ((p >= wlo) | (b in sel))
+        pool[i * CAND_BLOCK:(i + 1) * CAND_BLOCK] = np.where(keep, p, -1)
     return pool
 
 
-def index_full(q, w, K, vis, topk=INDEX_TOPK, n_blocks=CAND_BLOCKS):
+def index_full(q, w, K, vis, topk=INDEX_TOPK, n_blocks=CAND_BLOCKS, tail=False):
     """Full layer: one score pass over every visible entry, then two top-k's side by side
     on the same scores: a position top-512 for its own attention and a block top-2048
     (block max) whose blocks expand into the shared candidate pool
     ([ARCH] ¬ß3.3 Êó∂Â∫èÊæÑÊ∏Ö; [CED] Figure 5 left/middle).
 
-    Returns (topk positions [512] ascending, -1 padded; pool [16384]; scores; block maxima)."""
+    Returns (topk positions [512] ascending, -1 padded; pool [16384, or 16544 with the window
+    tail]; scores; block maxima)."""
     s = index_scores(q, w, K, vis)
     pos = topk_ascending(s, vis, topk)
     out = np.full(topk, -1, np.int64)
     out[:len(pos)] = pos
     m = block_maxima(s, vis)
     blk = topk_ascending(m, len(m), n_blocks)
-    pool = expand_pool(blk, vis)
+    pool = expand_pool(blk, vis, tail)
     return out, pool, s, m
 
 

@@ -97,6 +97,41 @@ def check_pool(gpu_pool, s, vis, name="pool"):
     return check_set_band(blocks, o, m, name)
 
 
+def check_pool_tail(gpu_pool, s, vis, name="pool tail"):
+    """A pool with the window tail: ascending 8-slot runs; every window block (positions
+    [vis - 128, vis)) present, whole or keeping only its window positions; every other run a whole
+    selected block; the non-window selected blocks agree with the oracle's block top-2048 within
+    the band, and so do window blocks whose run shows whether they were selected."""
+    m = O.block_maxima(s, vis)
+    nblk = len(m)
+    wlo = max(0, vis - 128)
+    wb = set(range(wlo // 8, nblk))
+    runs = gpu_pool.reshape(-1, 8)
+    live = (runs >= 0).any(axis=1)
+    nl = int(live.sum())
+    assert live[:nl].all() and not live[nl:].any(), f"{name}: runs not contiguous"
+    blocks = np.array([r[r >= 0][0] // 8 for r in runs[:nl]], np.int64)
+    assert np.all(np.diff(blocks) > 0), f"{name}: blocks not ascending"
+    assert wb <= set(blocks.tolist()), f"{name}: window blocks missing"
+    picked, known = [], []
+    for r, b in zip(runs[:nl], blocks):
+        p = 8 * b + np.arange(8)
+        whole = np.where(p < vis, p, -1)
+        part = np.where((p < vis) & (p >= wlo), p, -1)
+        if b in wb:
+            assert np.array_equal(r, whole) or np.array_equal(r, part), f"{name}: window run {b}"
+            if not np.array_equal(whole, part):
+                known.append(int(b))
+                if np.array_equal(r, whole):
+                    picked.append(int(b))
+        else:
+            assert np.array_equal(r, whole), f"{name}: run {b}"
+            picked.append(int(b))
+    o = O.topk_ascending(m, nblk, 2048)
+    o_vis = [int(b) for b in o if b not in wb or b in known]
+    return check_set_band(np.array(picked), np.array(o_vis), m, name)
+
+
 def check_attention(o_gpu, o_ref, name="attn"):
     denom = np.max(np.abs(o_ref))
     err = np.max(np.abs(o_gpu.astype(np.float64) - o_ref)) / (denom if denom > 0 else 1.0)

@@ -89,3 +89,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.hsa_cache_write_compress(ctypes.byref(c), 0x10, null, 0x20, 4, null, null) == 1
     flags = ctypes.c_uint32(0)
     assert lib.hsa_get_device_status(null, None) == 1
+
+
+def test_wait_limit_and_stall_hook_are_host_only(lib):
+    """The wait limit and the stall hook only set host state (no CUDA call, no device needed)."""
+    import hierarchical_sparse_attention_index_gb300 as H
+    assert lib.hsa_set_wait_limit(1000) == 0
+    assert lib.hsa_set_wait_limit(0) == 0
+    assert H.STATUS_CODES["HSA_ERR_TIMEOUT"] == 6

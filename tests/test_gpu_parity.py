@@ -182,6 +182,36 @@ def test_index_full_ties(hsa):
     assert pool.cpu().numpy()[0, 0].tolist() == list(range(16384))
 
 
+def test_index_full_wait_timeout_and_recovery(hsa):
+    """Failure detection without a GPU fault: the test hook withholds one indexer-K copy of the
+    Full scan, so its consumers' bounded wait (limit lowered to 2 ms) runs out. The call reports
+    HSA_ERR_TIMEOUT through hsa_get_device_status, and the next call on the same workspace is
+    clean and matches the oracle."""
+    H = hsa
+    B, T = 2, 20000
+    oc, q, w, vis, cache, ws, topk, pool = _full_case(H, B, T, 1)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    try:
+        H.hsa_set_wait_limit(2_000_000)
+        H.hsa_debug_stall_next_scan()
+        H.hsa_index_full(cache, dev_bf16(q), dev(w), dev(vis), 1, T, topk, pool, ws)
+        code, flags = H.hsa_get_device_status()
+        assert code == H.STATUS_CODES["HSA_ERR_TIMEOUT"] and flags & H.HSA_FLAG_TIMEOUT, (code, flags)
+    finally:
+        H.hsa_set_wait_limit(0)
+    topk.fill_(-7)
+    pool.fill_(-7)
+    H.hsa_index_full(cache, dev_bf16(q), dev(w), dev(vis), 1, T, topk, pool, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0, (code, flags)
+    topk, pool = topk.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        s = O.index_scores(P.f32(q[b, 0]), w[b, 0], P.dequant_index(oc, b, T), int(vis[b, 0]))
+        P.check_topk(topk[b, 0], s, int(vis[b, 0]), name=f"after timeout topk b{b}")
+        P.check_pool(pool[b, 0], s, int(vis[b, 0]), name=f"after timeout pool b{b}")
+
+
 # ------------------------------------------------------------------ Reindex
 @pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 3000, 1), (1, 200000, 1), (1, 300, 1),
                                     (1, 50, 2)])
@@ -259,6 +289,81 @@ def test_index_reindex_three_score_classes(hsa):
     got = _reindex_direct(H, cache, dev_bf16(qb), dev(wv), T, pool)
     want = np.nonzero(cls[:16384] == best)[0][:512]
     assert got.tolist() == want.tolist()
+
+
+@pytest.mark.parametrize("B,T,nq", [(2, 40000, 1), (1, 16391, 1), (1, 1000, 1), (1, 200000, 2)])
+def test_index_pool_tail(hsa, B, T, nq):
+    """HSA_CACHE_POOL_TAIL ([ARCH] §3.3 旁路与边界): the Full call's pool gains the window blocks
+    (16,544 slots per row) and the Reindex call scores them: the position top-512 is unchanged,
+    the pool is checked by check_pool_tail, and Reindex over the kernel's pool against the oracle."""
+    H = hsa
+    cap = round8(T)
+    oc = P.oracle_cache(2, 20, B, T, cap)
+    q, w = synth.index_q_bf16(2, 20, B, nq), synth.index_w(2, 20, B, nq)
+    q2, w2 = synth.index_q_bf16(2, 24, B, nq), synth.index_w(2, 24, B, nq)
+    vis = synth.visibility(B, nq, T)
+    cache = H.Cache(B, cap, 1, tensors=(dev(oc["kv_q"]), dev(oc["kv_s"]), dev(oc["ik_q"]), dev(oc["ik_s"])),
+                    flags=H.HSA_CACHE_POOL_TAIL)
+    ws = H.new_workspace(B, nq, T)
+    n = 16384 + H.HSA_POOL_TAIL_SLOTS
+    topk = torch.full((B, nq, 512), -7, dtype=torch.int32, device="cuda")
+    pool = torch.full((B, nq, n), -7, dtype=torch.int32, device="cuda")
+    out = torch.full((B, nq, 512), -7, dtype=torch.int32, device="cuda")
+    H.hsa_index_full(cache, dev_bf16(q), dev(w), dev(vis), nq, T, topk, pool, ws)
+    H.hsa_index_reindex(cache, dev_bf16(q2), dev(w2), dev(vis), nq, T, pool, out, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0, (code, flags)
+    topk, pool, out = topk.cpu().numpy(), pool.cpu().numpy(), out.cpu().numpy()
+    for b in range(B):
+        K = P.dequant_index(oc, b, T)
+        for i in range(nq):
+            v = int(vis[b, i])
+            s = O.index_scores(P.f32(q[b, i]), w[b, i], K, v)
+            P.check_topk(topk[b, i], s, v, name=f"tail topk b{b} q{i}")
+            P.check_pool_tail(pool[b, i], s, v, name=f"tail pool b{b} q{i}")
+            ref, _ = O.index_reindex(P.f32(q2[b, i]), w2[b, i], K, pool[b, i], v)
+            s2 = O.index_scores(P.f32(q2[b, i]), w2[b, i], K, v)
+            g = out[b, i]
+            kk = min(512, int(((pool[b, i] >= 0) & (pool[b, i] < v)).sum()))
+            assert (g >= 0).sum() == kk and np.all(g[kk:] == -1) and np.all(np.diff(g[:kk]) > 0)
+            P.check_set_band(g[:kk], ref[ref >= 0], s2, f"tail reindex b{b} q{i}")
+
+
+def test_index_pool_tail_window_survives(hsa):
+    """The newest positions score far below every block the Full query picks, yet with the tail
+    they reach the pool and a Reindex query that favours them selects them."""
+    H = hsa
+    T = 60000
+    oc = P.oracle_cache(9, 20, 1, T, T)
+    K = P.dequant_index(oc, 0, T)
+    q = synth.index_q_bf16(9, 20, 1, 1)
+    w = synth.index_w(9, 20, 1, 1)
+    s = O.index_scores(P.f32(q[0, 0]), w[0, 0], K, T)
+    m = O.block_maxima(s, T)
+    blk = O.topk_ascending(m, len(m), 2048)
+    assert not set(range((T - 128) // 8, T // 8)) <= set(blk.tolist())   # the plain pool misses the window
+    cache = H.Cache(1, T, 1, tensors=(dev(oc["kv_q"]), dev(oc["kv_s"]), dev(oc["ik_q"]), dev(oc["ik_s"])),
+                    flags=H.HSA_CACHE_POOL_TAIL)
+    vis = torch.tensor([[T]], dtype=torch.int32, device="cuda")
+    ws = H.new_workspace(1, 1, T)
+    topk = torch.empty(1, 1, 512, dtype=torch.int32, device="cuda")
+    pool = torch.empty(1, 1, 16384 + H.HSA_POOL_TAIL_SLOTS, dtype=torch.int32, device="cuda")
+    H.hsa_index_full(cache, dev_bf16(q), dev(w), vis, 1, T, topk, pool, ws)
+    pl = pool.cpu().numpy()[0, 0]
+    assert set(range(T - 128, T)) <= set(pl.tolist())
+    # a Reindex query whose heads all favour the newest entry's own direction
+    qn = np.tile(np.sign(K[T - 1]).astype(np.float32), (16, 1))[None, None]
+    qn_bits = (qn.view(np.uint32) >> 16).astype(np.uint16)
+    wn = np.ones((1, 1, 16), np.float32)
+    out = torch.empty(1, 1, 512, dtype=torch.int32, device="cuda")
+    H.hsa_index_reindex(cache, dev_bf16(qn_bits), dev(wn), vis, 1, T, pool, out, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0
+    g = out.cpu().numpy()[0, 0]
+    s2 = O.index_scores(P.f32(qn_bits[0, 0]), wn[0, 0], K, T)
+    ref, _ = O.index_reindex(P.f32(qn_bits[0, 0]), wn[0, 0], K, pl, T)
+    P.check_set_band(g[g >= 0], ref[ref >= 0], s2, "tail reindex, window query")
+    assert T - 1 in set(g.tolist())
 
 
 # ------------------------------------------------------------------ attention

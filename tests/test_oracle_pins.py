@@ -498,3 +498,30 @@ def test_writer_rope_touches_main_kv_tail_only():
     assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])
     assert np.array_equal(a[0][:, :224], b[0][:, :224]) and np.array_equal(a[1][:, :28], b[1][:, :28])
     assert not np.array_equal(a[0][:, 224:], b[0][:, 224:])
+
+
+# ------------------------------------------------------------------ pool with the window tail
+def test_pool_tail_keeps_the_window():
+    """[ARCH] §3.3 旁路与边界: with the window tail every one of the newest 128 positions is in
+    the pool whatever its block scored; the plain pool is a subset; at most 128 positions are
+    added; runs stay 8-aligned and ascending; with every block selected nothing changes."""
+    rng = np.random.default_rng(81)
+    for vis in (5, 130, 16383, 16385, 16391, 40000, 100001):
+        s = rng.standard_normal(vis)
+        s[max(0, vis - 200):] -= 100.0           # the newest positions score worst
+        m = O.block_maxima(s, vis)
+        blk = O.topk_ascending(m, len(m), 2048)
+        plain, tail = O.expand_pool(blk, vis), O.expand_pool(blk, vis, tail=True)
+        assert len(tail) == 16384 + 160
+        ps, ts = set(plain[plain >= 0].tolist()), set(tail[tail >= 0].tolist())
+        window = set(range(max(0, vis - 128), vis))
+        assert window <= ts and ps <= ts and ts == ps | window
+        runs = tail.reshape(-1, 8)
+        live = runs[(runs >= 0).any(axis=1)]
+        first = np.array([r[r >= 0][0] // 8 for r in live])
+        assert np.all(np.diff(first) > 0)
+        assert all(((r < 0) | (r // 8 == b)).all() for r, b in zip(live, first))
+        if -(-vis // 8) <= 2048:
+            assert np.array_equal(tail[:16384], plain) and (tail[16384:] == -1).all()
+        elif vis > 20000:
+            assert not window <= ps                # the low-scoring window needed the tail
