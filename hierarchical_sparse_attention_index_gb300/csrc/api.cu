@@ -9,10 +9,35 @@
 #include <atomic>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "hsa_common.cuh"
 #include "hsa_internal.h"
 
 namespace hsa {
+
+// NVTX range of one C-ABI call (or one layer slot of a step) in the "libhsa" domain, so that a
+// timeline tool attributes the call's host time and its launches; costs a pointer test when no
+// tool is attached.
+class NvtxRange {
+ public:
+  explicit NvtxRange(const char* name) {
+    static const nvtxDomainHandle_t domain = nvtxDomainCreateA("libhsa");
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    domain_ = domain;
+    nvtxDomainRangePushEx(domain_, &a);
+  }
+  ~NvtxRange() { nvtxDomainRangePop(domain_); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+
+ private:
+  nvtxDomainHandle_t domain_;
+};
 
 // Per-device status word (HSA_FLAG_*), written by kernels with atomicOr.
 __device__ uint32_t g_status_word;
@@ -265,6 +290,7 @@ hsa_status hsa_workspace_init(void* ws, size_t ws_bytes, hsa_stream_t stream) {
 
 hsa_status hsa_cache_write_compress(const hsa_cache* cache, const void* wkv, const void* wgate, const void* w_idx,
                                     int64_t n_tokens, const int64_t* start_entry, hsa_stream_t stream) {
+  NvtxRange range("hsa_cache_write_compress");
   hsa_status st = check_cache(cache);
   if (st != HSA_OK) return st;
   if (!wkv || !w_idx) return HSA_ERR_INVALID_ARG;
@@ -355,12 +381,14 @@ static hsa_status index_common(bool pool_mode, const hsa_cache* cache, const voi
 hsa_status hsa_index_full(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,
                           int64_t max_vis, int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
                           hsa_stream_t stream) {
+  NvtxRange range("hsa_index_full");
   return index_common(false, cache, q, w, vis, nq, max_vis, nullptr, topk_out, pool_out, ws, ws_bytes, stream);
 }
 
 hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, const float* w, const int32_t* vis, int32_t nq,
                              int64_t max_vis, const int32_t* pool, int32_t* topk_out, void* ws, size_t ws_bytes,
                              hsa_stream_t stream) {
+  NvtxRange range("hsa_index_reindex");
   return index_common(true, cache, q, w, vis, nq, max_vis, pool, topk_out, nullptr, ws, ws_bytes, stream);
 }
 
@@ -368,11 +396,13 @@ hsa_status hsa_index_reindex(const hsa_cache* cache, const void* q, const float*
 hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const int32_t* topk, const uint8_t* swa,
                                   const int32_t* vis, int32_t nq, int64_t max_vis, float sm_scale, float* out,
                                   void* ws, size_t ws_bytes, hsa_stream_t stream) {
+  NvtxRange range("hsa_sparse_attn_decode");
   return attn_common(cache, q, topk, swa, vis, nq, max_vis, sm_scale, out, ws, ws_bytes, stream, false, false);
 }
 
 hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, void* ws, size_t ws_bytes,
                              hsa_stream_t stream) {
+  NvtxRange range("hsa_schedule_step");
   hsa_status st = check_cache(cache);
   if (st != HSA_OK) return st;
   if (!a || !a->modes || !a->q_attn || !a->swa || !a->out || !a->topk || !a->pool || !a->vis)
@@ -387,8 +417,11 @@ hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, voi
     if (!a->q_attn[l] || !a->swa[l] || !a->out[l]) return HSA_ERR_INVALID_ARG;
   }
   const int32_t* latest = nullptr;
+  static const char* const kSlotName[3] = {"layer slot: Full + attention", "layer slot: Reindex + attention",
+                                           "layer slot: Reuse + attention"};
   for (int l = 0; l < a->n_layers; ++l) {
     const int m = a->modes[l];
+    NvtxRange slot(kSlotName[m]);
     if (m == HSA_MODE_FULL) {
       st = hsa_index_full(cache, a->q_idx[l], a->w_idx[l], a->vis, a->nq, a->max_vis, a->topk[l], a->pool, ws,
                           ws_bytes, stream);
