@@ -85,6 +85,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// cluster barrier arrive without release semantics: for a thread that published nothing, or
+// that already ordered what it published with fence_cluster()
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -138,8 +144,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   __syncthreads();
   tc_fence_after();
   // Peers store into this CTA's (m, l) slots only once it runs: the matching wait comes right
-  // before each thread's first store into a peer (or, for the MMA warp, before phase A).
-  cluster_arrive();
+  // before each thread's first store into a peer (or, for the MMA warp, before phase A). The
+  // arrive publishes nothing (the barriers are CTA-local), so it is relaxed.
+  cluster_arrive_relaxed();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
   // query: all 64 heads, 8 boxes of 64 dims x 64 heads (8 KB each), into this CTA's own shared
   // memory
@@ -227,9 +234,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     }
     __syncwarp();
     cluster_wait();                   // setup barrier (arrived at the top)
-    cluster_arrive();                 // phase A: (m, l) published
+    cluster_arrive_relaxed();         // phase A: (m, l) published (this warp stored none)
     cluster_wait();
-    cluster_arrive();                 // phase B: partials published
+    cluster_arrive_relaxed();         // phase B: partials published (this warp stored none)
     cluster_wait();
     return;
   }
@@ -429,7 +436,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   cluster_wait();
   if (hown) st_cluster_f2(smem_u32(s_ml + rank * 16 + (hh & 15)), (uint32_t)(hh >> 4), mloc, lsum);
   uint32_t* mine = part + (size_t)rank * kPartFloats;
-  cluster_arrive();                   // phase A
+  // phase A: only warps 0..3 stored into peers ((m, l) of their heads); they release it with a
+  // cluster-scope fence, so every thread's arrive can be relaxed
+  if (warp < 4) fence_cluster();
+  cluster_arrive_relaxed();
 
   // ---------------------------------------------------------------- partial O / l -> L2
   // Warp (quadrant qd = w & 3, tile mt = w >> 2) owns output dimension d = 128 mt + 32 qd + lane
