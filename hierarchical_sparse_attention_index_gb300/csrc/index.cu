@@ -295,6 +295,10 @@ constexpr int kSelRankMax = 512;    // elements ranked by counting up to this ma
 constexpr int kTopBlocks = kTopK;   // the position top-512 lies inside the top-512 blocks
 constexpr int kPosCand = kTopBlocks * kBlk;   // 4096 position candidates
 
+// the smallest float whose order key is `key` (inverse of order_key)
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
 // (order key, inverted index): larger = better, ties to the lower index
 __device__ __forceinline__ uint64_t sel_comp(float v, uint32_t idx) {
   return ((uint64_t)order_key(v) << 32) | (uint64_t)(~idx);
@@ -416,27 +420,13 @@ __device__ __forceinline__ int bitmap_offsets(const uint32_t* bitmap, int w0, in
   return excl_scan(cnt, scr, 1, kSelThreads, total, tid);
 }
 
-// Slots in a shared list for `n` items per lane, from one atomic per warp; every lane calls it.
-__device__ __forceinline__ int warp_append_n(int n, int* counter, int lane) {
-  int incl = n;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  int base = 0;
-  if (lane == 31 && incl) base = atomicAdd(counter, incl);
-  base = __shfl_sync(0xffffffffu, base, 31);
-  return base + incl - n;
-}
-
 // One 2-CTA cluster per (request, query) row. CTA 0 selects the block top-2048 and writes the
 // pool; CTA 1 selects the block top-512 and then the position top-512 among their positions.
 // Both read the row's block-max histogram; CTA 1 clears it once CTA 0 has read it (the cluster
 // barrier's arrive and wait are split around the work).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
   extern __shared__ __align__(16) uint8_t fsm_raw[];
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int rank = (int)cluster_rank();
   const int row = blockIdx.x >> 1;
   __shared__ SelShared S;
@@ -497,12 +487,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
 
   // ---------------------------------------------------------------- 2. one pass over the block maxima
   // Blocks above the threshold bin are taken at once; blocks in it are listed as candidates
-  // (composites staged in shared memory, block indices in the workspace past the stage). Eight
-  // float4 loads per thread are in flight at a time.
+  // (composites staged in shared memory, block indices in the workspace past the stage). Per
+  // batch of 2,048 float4 (eight loads per thread in flight), each thread counts its
+  // candidates and one block-wide exclusive scan places them: no shared counter is contended.
   {
     const int thr = s_thr;
+    // f_lo, the smallest float of the threshold bin: a block max below it is neither taken nor
+    // listed, which one float compare decides for most blocks. The compare only filters: the
+    // bin of a block that passes is decided on its order key (which tells -0 from +0)
+    const float f_lo = (thr < 0) ? -INFINITY : key_to_float((uint32_t)thr << kHistShift);
     const int nq4 = (nb + 3) >> 2;                    // float4 chunks
     constexpr int kIlp = 8;
+    int listed = 0;                                   // candidates of earlier batches (same in every thread)
     for (int c0 = 0; c0 < nq4; c0 += kIlp * kSelThreads) {
       float4 v[kIlp];
 #pragma unroll
@@ -510,26 +506,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
         const int c = c0 + u * kSelThreads + tid;
         v[u] = (c < nq4) ? __ldcg(reinterpret_cast<const float4*>(bm) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      uint32_t candm[kIlp];
+      int n = 0;
 #pragma unroll
       for (int u = 0; u < kIlp; ++u) {
         const int c = c0 + u * kSelThreads + tid;
         const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        uint32_t take = 0u, candm = 0u;
+        uint32_t take = 0u;
+        candm[u] = 0u;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int b = 4 * c + k;
-          const int bin = (int)(order_key(f[k]) >> kHistShift);
-          if (b < nb) {
+          if (4 * c + k < nb && (f[k] >= f_lo || f[k] == 0.f)) {
+            const int bin = (int)(order_key(f[k]) >> kHistShift);
             if (thr < 0 || bin > thr) take |= 1u << k;
-            else if (bin == thr) candm |= 1u << k;
+            else if (bin == thr) candm[u] |= 1u << k;
           }
         }
         if (take) atomicOr(bits + ((4 * c) >> 5), take << ((4 * c) & 31));
-        const int n = __popc(candm);
-        int j = warp_append_n(n, &S.ncand[0], lane);
-        while (candm) {
-          const int k = __ffs(candm) - 1;
-          candm &= candm - 1u;
+        n += __popc(candm[u]);
+      }
+      int total;
+      int j = listed + excl_scan(n, S.scr, 1, kSelThreads, &total, tid);
+      listed += total;
+#pragma unroll
+      for (int u = 0; u < kIlp; ++u) {
+        const int c = c0 + u * kSelThreads + tid;
+        const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t m = candm[u];
+        while (m) {
+          const int k = __ffs(m) - 1;
+          m &= m - 1u;
           const int b = 4 * c + k;
           if (j < kSelStage) cst[j] = sel_comp(f[k], (uint32_t)b);
           else gcand[j - kSelStage] = b;
@@ -537,6 +543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
         }
       }
     }
+    if (tid == 0) S.ncand[0] = listed;
   }
   __syncthreads();
 
