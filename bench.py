@@ -6,11 +6,15 @@ at 131,072 visible positions, FP4 main KV + FP4 indexer K, one GB300 per rank.
 
 Prints one JSON line (rank 0). `value` is decode steps/s summed over ranks (weak scaling: each
 rank runs its own batch of 32 requests; no collective on the data path). The step runs through
-hsa_schedule_step, captured once in a CUDA graph and replayed. Inputs are resident in HBM and
-larger than L2 (the 1.49 GB cache). `e2e` repeats the measurement through the same public call,
-with every step's inputs copied from pinned host memory and its outputs copied back inside the
-timed region, two steps in flight (upload, compute and download on three streams). `--impl reference` times the fp64 CPU oracle on a bounded sample of the
-same workload.
+hsa_schedule_step, captured once in a CUDA graph and replayed. Every layer owns its cache, as in
+a decoder: layer 20's is written by the m=1 cache writer, and each other layer's is a device copy
+of it with every request's entries rotated by a layer-specific offset (the entries are i.i.d.
+over positions, so the distribution is the same, but no layer finds another layer's row at a
+position). Inputs are resident in HBM and larger than L2 (20 caches of 1.49 GB). `e2e` repeats
+the measurement through the same public call, with every step's inputs copied from pinned host
+memory and its outputs copied back inside the timed region, two steps in flight (upload, compute
+and download on three streams). `--impl reference` times the fp64 CPU oracle on a bounded sample
+of the same workload.
 """
 from __future__ import annotations
 
@@ -121,8 +125,10 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def build_inputs(H, torch, seed, rank):
-    """Device-resident step inputs for one rank (its own batch of 32 requests)."""
+def build_inputs(H, torch, seed, rank, one_cache=False):
+    """Device-resident step inputs for one rank (its own batch of 32 requests). With `one_cache`
+    (profiling captures, which must keep the device footprint small) every layer slot reads
+    layer 20's cache."""
     B, T, nq = CFG.batch, CFG.T, CFG.nq
     s = rank_seed(seed, rank)
     cache = H.Cache(B, T, 1)
@@ -136,6 +142,12 @@ def build_inputs(H, torch, seed, rank):
     torch.cuda.synchronize()
     code, flags = H.hsa_get_device_status()
     assert code == 0 and flags == 0, ("cache write", code, flags)
+    caches = [cache] * len(LAYERS) if one_cache else [cache]
+    for l in ([] if one_cache else LAYERS[1:]):
+        shift = layer_shift(l, T)
+        caches.append(H.Cache(B, T, 1, tensors=tuple(torch.roll(t, shift, dims=1)
+                                                    for t in (cache.kv_q, cache.kv_s, cache.ik_q, cache.ik_s))))
+    torch.cuda.synchronize()
 
     host = {}
     for l in INDEX_LAYERS:
@@ -158,7 +170,13 @@ def build_inputs(H, torch, seed, rank):
     step = H.StepArgs(modes, [dev.get(("qi", l)) for l in LAYERS], [dev.get(("wi", l)) for l in LAYERS],
                       [dev[("qa", l)] for l in LAYERS], [dev[("sw", l)] for l in LAYERS], outs, topk, pool,
                       vis, nq, T, 1.0)
-    return dict(cache=cache, dev=dev, host=host, vis=vis, outs=outs, topk=topk, pool=pool, ws=ws, step=step)
+    return dict(caches=caches, dev=dev, host=host, vis=vis, outs=outs, topk=topk, pool=pool, ws=ws, step=step)
+
+
+def layer_shift(layer, T):
+    """Rotation (in entries) of layer `layer`'s cache against layer 20's: distinct per layer and
+    3 mod 8, so the 8-entry blocks of different layers do not line up either."""
+    return ((layer - LAYERS[0]) * 5237 * 8 + 3) % T
 
 
 def per_kernel_times(H, torch, I, reps=10):
@@ -177,18 +195,18 @@ def per_kernel_times(H, torch, I, reps=10):
 
     def attn(s):
         for l, j, tk in att:
-            H.hsa_sparse_attn_decode(I["cache"], d[("qa", l)], tk, d[("sw", l)], I["vis"], nq, T, 1.0,
+            H.hsa_sparse_attn_decode(I["caches"][j], d[("qa", l)], tk, d[("sw", l)], I["vis"], nq, T, 1.0,
                                      I["outs"][j], ws, stream=s)
 
     def full(s):
         j = LAYERS.index(20)
-        H.hsa_index_full(I["cache"], d[("qi", 20)], d[("wi", 20)], I["vis"], nq, T, I["topk"][j], I["pool"], ws,
+        H.hsa_index_full(I["caches"][j], d[("qi", 20)], d[("wi", 20)], I["vis"], nq, T, I["topk"][j], I["pool"], ws,
                          stream=s)
 
     def reindex(s):
         for l in INDEX_LAYERS[1:]:
             j = LAYERS.index(l)
-            H.hsa_index_reindex(I["cache"], d[("qi", l)], d[("wi", l)], I["vis"], nq, T, I["pool"], I["topk"][j],
+            H.hsa_index_reindex(I["caches"][j], d[("qi", l)], d[("wi", l)], I["vis"], nq, T, I["pool"], I["topk"][j],
                                 ws, stream=s)
 
     out = {}
@@ -248,18 +266,18 @@ def run_hsa(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     H.load_library()
-    I = build_inputs(H, torch, CFG.seed, rank)
+    I = build_inputs(H, torch, CFG.seed, rank, args.one_cache)
 
     st = torch.cuda.current_stream()
     # one eager step (sets up per-device state), then capture the step as a CUDA graph
-    H.hsa_schedule_step(I["cache"], I["step"], I["ws"])
+    H.hsa_schedule_step(I["caches"], I["step"], I["ws"])
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     s2 = torch.cuda.Stream()
     s2.wait_stream(st)
     with torch.cuda.stream(s2):
         with torch.cuda.graph(g, stream=s2):
-            H.hsa_schedule_step(I["cache"], I["step"], I["ws"], stream=s2)
+            H.hsa_schedule_step(I["caches"], I["step"], I["ws"], stream=s2)
     torch.cuda.synchronize()
 
     def barrier():
@@ -427,7 +445,7 @@ def run_e2e(H, torch, I, args, world, barrier, st):
             sl["ev_in"].record(s_in)
         st.wait_event(sl["ev_in"])
         st.wait_event(sl["ev_out"])             # step i - 2's results have left this slot
-        H.hsa_schedule_step(I["cache"], sl["step"], I["ws"], stream=st)
+        H.hsa_schedule_step(I["caches"], sl["step"], I["ws"], stream=st)
         sl["ev_comp"].record(st)
         s_out.wait_event(sl["ev_comp"])
         with torch.cuda.stream(s_out):
@@ -451,7 +469,7 @@ def run_e2e(H, torch, I, args, world, barrier, st):
     if code != 0 or flags != 0:
         raise RuntimeError(f"device status after the end-to-end steps: code {code} flags {flags}")
     # the results that came back must be those of the device-resident step on the same inputs
-    H.hsa_schedule_step(I["cache"], I["step"], I["ws"], stream=st)
+    H.hsa_schedule_step(I["caches"], I["step"], I["ws"], stream=st)
     torch.cuda.synchronize()
     ref = torch.cat([o.reshape(-1) for o in I["outs"]] + [I["topk"][j].reshape(-1).view(torch.float32) for j in idx_j])
     if not torch.equal(slots[(e2e_steps - 1) % 2]["hres"], ref.cpu()):
@@ -474,11 +492,15 @@ def make_line(args, world, value, tmax, clocks, e2e, roofline):
     return {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * tmax / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp4-e2m1 cache; f16 tensor-core MMA, fp32 accumulate",
-            "data": "synthetic (seeded N(0,1) latents through the m=1 cache writer; bf16 queries)",
+            "data": "synthetic (seeded N(0,1) latents through the m=1 cache writer for layer 20; each other "
+                    "layer's cache is that one with every request's entries rotated by a layer-specific "
+                    "offset; bf16 queries)",
             "config": {"workload": CFG.name, "batch_per_gpu": B, "ctx": T, "nq": CFG.nq,
                        "layers": "20..39 (1 Full, 4 Reindex, 15 Reuse, 20 attention)",
                        "parallelism": f"replicas x{world} (requests sharded, no collective)",
-                       "l2": "inputs larger than L2 (1.49 GB FP4 cache per step)",
+                       "l2": ("inputs larger than L2 (one 1.49 GB FP4 cache for every layer: profiling mode)"
+                              if args.one_cache else
+                              "inputs larger than L2 (one 1.49 GB FP4 cache per layer, 29.8 GB)"),
                        "step": "hsa_schedule_step captured in one CUDA graph"},
             "clocks": clocks, "gpu_launches": args.steps * kernels_per_step(), "e2e": e2e, "roofline": roofline}
 
@@ -605,12 +627,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=CFG.batch, help="requests per GPU (profiling runs)")
     ap.add_argument("--ctx", type=int, default=CFG.T, help="visible positions (profiling runs)")
+    ap.add_argument("--one-cache", action="store_true",
+                    help="profiling runs: every layer slot reads layer 20's cache (1.49 GB on the device "
+                         "instead of 29.8 GB)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.batch != CFG.batch or args.ctx != CFG.T:
-        CFG = synth.DecodeConfig(f"b{args.batch}_t{args.ctx}_20layers", CFG.seed, args.batch, args.ctx, CFG.nq,
-                                 CFG.layers)
+    if args.batch != CFG.batch or args.ctx != CFG.T or args.one_cache:
+        name = f"b{args.batch}_t{args.ctx}_20layers" + ("_one_cache" if args.one_cache else "")
+        CFG = synth.DecodeConfig(name, CFG.seed, args.batch, args.ctx, CFG.nq, CFG.layers)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -217,9 +217,16 @@ class StepArgs:
                                   _ptr(pool), _ptr(vis), max_vis, float(sm_scale))
 
 
-def hsa_schedule_step(cache: Cache, step: StepArgs, ws, stream=None):
+def hsa_schedule_step(caches, step: StepArgs, ws, stream=None):
+    """`caches`: one Cache per layer slot (a list), or one Cache that every slot uses."""
+    n = step.args.n_layers
+    if isinstance(caches, Cache):
+        caches = [caches] * n
+    if len(caches) != n:
+        raise ValueError(f"{len(caches)} caches for {n} layer slots")
+    descs = (hsa_cache * n)(*[c.desc for c in caches])
     _check("hsa_schedule_step", load_library().hsa_schedule_step(
-        cache.ref, ctypes.byref(step.args), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        descs, ctypes.byref(step.args), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def hsa_set_wait_limit(ns):

@@ -400,15 +400,23 @@ hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q, const i
   return attn_common(cache, q, topk, swa, vis, nq, max_vis, sm_scale, out, ws, ws_bytes, stream, false, false);
 }
 
-hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, void* ws, size_t ws_bytes,
+hsa_status hsa_schedule_step(const hsa_cache* caches, const hsa_step_args* a, void* ws, size_t ws_bytes,
                              hsa_stream_t stream) {
   NvtxRange range("hsa_schedule_step");
-  hsa_status st = check_cache(cache);
-  if (st != HSA_OK) return st;
-  if (!a || !a->modes || !a->q_attn || !a->swa || !a->out || !a->topk || !a->pool || !a->vis)
+  if (!caches || !a || !a->modes || !a->q_attn || !a->swa || !a->out || !a->topk || !a->pool || !a->vis)
     return HSA_ERR_INVALID_ARG;
   if (a->n_layers < 1) return HSA_ERR_SHAPE;
   if (a->modes[0] != HSA_MODE_FULL) return HSA_ERR_INVALID_ARG;
+  // every slot's cache is checked before anything is launched; the pool's row length follows
+  // the pool-tail flag, so all slots must agree on it
+  for (int l = 0; l < a->n_layers; ++l) {
+    const hsa_status cs = check_cache(caches + l);
+    if (cs != HSA_OK) return cs;
+    if (caches[l].batch != caches[0].batch || caches[l].ratio != caches[0].ratio ||
+        ((caches[l].flags ^ caches[0].flags) & HSA_CACHE_POOL_TAIL) || a->max_vis > caches[l].capacity)
+      return HSA_ERR_SHAPE;
+  }
+  hsa_status st = HSA_OK;
   for (int l = 0; l < a->n_layers; ++l) {
     const int m = a->modes[l];
     if (m != HSA_MODE_FULL && m != HSA_MODE_REINDEX && m != HSA_MODE_REUSE) return HSA_ERR_INVALID_ARG;
@@ -422,6 +430,7 @@ hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* a, voi
   for (int l = 0; l < a->n_layers; ++l) {
     const int m = a->modes[l];
     NvtxRange slot(kSlotName[m]);
+    const hsa_cache* cache = caches + l;
     if (m == HSA_MODE_FULL) {
       st = hsa_index_full(cache, a->q_idx[l], a->w_idx[l], a->vis, a->nq, a->max_vis, a->topk[l], a->pool, ws,
                           ws_bytes, stream);

@@ -57,7 +57,7 @@ extern "C" {
 #define HSA_API
 #endif
 
-#define HSA_ABI_VERSION 2
+#define HSA_ABI_VERSION 3
 
 #define HSA_D_LATENT 512      /* main-KV latent width (head_dim)          [890B] §三 */
 #define HSA_D_INDEX 128       /* indexer head dim (index_head_dim)        [890B] §三 */
@@ -246,13 +246,18 @@ HSA_API hsa_status hsa_sparse_attn_decode(const hsa_cache* cache, const void* q,
 
 /* One decode step over consecutive layer slots ([ARCH] §3.3: 1 full score + 4 pool rescores +
  * 15 inherits; [COST] §3.1; [CED] Figure 4). Slot l runs its indexer if FULL (which also
- * writes the pool) or REINDEX, then attention with the latest indices. Everything is
- * stream-ordered, with no host synchronisation. The step's inputs (q_attn, swa, q_idx, w_idx,
+ * writes the pool) or REINDEX, then attention with the latest indices. Every layer owns its
+ * cache: `caches` is a HOST array of n_layers descriptors, and slot l scores caches[l]'s
+ * indexer K (Full, Reindex) and attends over caches[l]'s main KV. Indices are positions, so an
+ * inherited top-k or the Full slot's pool addresses the same tokens in every layer's cache.
+ * The caches share batch and ratio and each holds at least max_vis entries (HSA_ERR_SHAPE
+ * otherwise); a slot may repeat another's descriptor. Everything is stream-ordered, with no
+ * host synchronisation. The step's inputs (q_attn, swa, q_idx, w_idx,
  * vis, pool when the first slot is not FULL) must be complete before the call's work starts on
  * `stream` and must not alias anything the step writes (out, topk, pool, ws): the attention
  * kernels fetch their queries and SWA rows, and the Reindex kernels their queries, weights and
  * pool rows, while the previous kernel of the step drains. */
-HSA_API hsa_status hsa_schedule_step(const hsa_cache* cache, const hsa_step_args* args, void* ws,
+HSA_API hsa_status hsa_schedule_step(const hsa_cache* caches, const hsa_step_args* args, void* ws,
                              size_t ws_bytes, hsa_stream_t stream);
 
 /* Limit of the kernels' bounded waits (for a copy or a tensor-core result that does not arrive),

@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     import hierarchical_sparse_attention_index_gb300 as H
-    assert H.hsa_abi_version() == 2
+    assert H.hsa_abi_version() == 3
     for code, name in H.STATUS.items():
         assert H.hsa_status_string(code).startswith(name)
     assert H.hsa_status_string(99) == "HSA_ERR_UNKNOWN"
@@ -97,3 +97,29 @@ def test_wait_limit_and_stall_hook_are_host_only(lib):
     assert lib.hsa_set_wait_limit(1000) == 0
     assert lib.hsa_set_wait_limit(0) == 0
     assert H.STATUS_CODES["HSA_ERR_TIMEOUT"] == 6
+
+
+def test_schedule_step_checks_every_slot_cache_without_gpu(lib):
+    """hsa_schedule_step takes one cache per layer slot and refuses, before any launch, slots
+    whose caches disagree on batch, ratio or the pool-tail flag, or hold fewer than max_vis
+    entries (fake, never dereferenced pointers)."""
+    import hierarchical_sparse_attention_index_gb300 as H
+    n = 2
+    modes = (ctypes.c_int32 * n)(H.HSA_MODE_FULL, H.HSA_MODE_REUSE)
+    ptrs = lambda *v: (ctypes.c_void_p * n)(*v)  # noqa: E731
+    keep = [ptrs(0x100, None), ptrs(0x200, None), ptrs(0x300, 0x310), ptrs(0x400, 0x410), ptrs(0x500, 0x510),
+            ptrs(0x600, None)]
+    vp = ctypes.POINTER(ctypes.c_void_p)
+    args = H.hsa_step_args(n, 1, ctypes.cast(modes, ctypes.POINTER(ctypes.c_int32)),
+                           *[ctypes.cast(k, vp) for k in keep], 0x700, 0x800, 1000, 1.0)
+
+    def caches(*specs):
+        return (H.hsa_cache * n)(*[H.hsa_cache(b, 1, cap, 0, fl, 0x1000, 0x2000, 0x3000, 0x4000)
+                                   for b, cap, fl in specs])
+
+    step = lambda cs: lib.hsa_schedule_step(cs, ctypes.byref(args), 0x900, 1 << 30, None)  # noqa: E731
+    assert step(caches((2, 1024, 0), (1, 1024, 0))) == 2                          # batch differs
+    assert step(caches((2, 1024, 0), (2, 1024, H.HSA_CACHE_POOL_TAIL))) == 2      # pool-tail flag differs
+    assert step(caches((2, 1024, 0), (2, 512, 0))) == 2                           # slot 1 holds < max_vis
+    assert step(caches((2, 1024, 0), (2, 1020, 0))) == 2                          # slot 1 capacity invalid
+    assert step(None) == 1

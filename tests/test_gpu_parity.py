@@ -428,13 +428,15 @@ def test_sparse_attention_flags_bad_index(hsa):
 
 # ------------------------------------------------------------------ schedule
 def test_schedule_step(hsa):
+    """Each layer slot owns its cache: the Full slot scores layer 20's indexer K, the Reindex slot
+    rescores the pool over layer 24's, and every slot attends over its own main KV."""
     H = hsa
     B, T, nq, seed = 2, 12345, 1, 0
     layers = [20, 21, 24, 25]
     modes = [H.HSA_MODE_FULL, H.HSA_MODE_REUSE, H.HSA_MODE_REINDEX, H.HSA_MODE_REUSE]
     cap = round8(T)
-    oc = P.oracle_cache(seed, 20, B, T, cap)
-    cache = gpu_cache(H, oc, cap)
+    oc = {l: P.oracle_cache(seed, l, B, T, cap) for l in layers}
+    caches = [gpu_cache(H, oc[l], cap) for l in layers]
     vis = synth.visibility(B, nq, T)
     qi = {l: synth.index_q_bf16(seed, l, B, nq) for l in (20, 24)}
     wi = {l: synth.index_w(seed, l, B, nq) for l in (20, 24)}
@@ -450,22 +452,22 @@ def test_schedule_step(hsa):
     d_vis = dev(vis)
     ws = H.new_workspace(B, nq, T)
     step = H.StepArgs(modes, d_qi, d_wi, d_qa, d_sw, outs, tk, pool, d_vis, nq, T, 1.0)
-    H.hsa_schedule_step(cache, step, ws)
+    H.hsa_schedule_step(caches, step, ws)
     code, flags = H.hsa_get_device_status()
     assert code == 0 and flags == 0
     pool_h = pool.cpu().numpy()
     t20, t24 = tk[0].cpu().numpy(), tk[2].cpu().numpy()
     for b in range(B):
-        K = P.dequant_index(oc, b, T)
-        s20 = O.index_scores(P.f32(qi[20][b, 0]), wi[20][b, 0], K, T)
+        K20, K24 = P.dequant_index(oc[20], b, T), P.dequant_index(oc[24], b, T)
+        s20 = O.index_scores(P.f32(qi[20][b, 0]), wi[20][b, 0], K20, T)
         P.check_topk(t20[b, 0], s20, T, name="step L20")
         P.check_pool(pool_h[b, 0], s20, T, name="step pool")
-        ref24, _ = O.index_reindex(P.f32(qi[24][b, 0]), wi[24][b, 0], K, pool_h[b, 0], T)
-        s24 = O.index_scores(P.f32(qi[24][b, 0]), wi[24][b, 0], K, T)
+        ref24, _ = O.index_reindex(P.f32(qi[24][b, 0]), wi[24][b, 0], K24, pool_h[b, 0], T)
+        s24 = O.index_scores(P.f32(qi[24][b, 0]), wi[24][b, 0], K24, T)
         P.check_set_band(t24[b, 0][t24[b, 0] >= 0], ref24[ref24 >= 0], s24, "step L24")
         for j, l in enumerate(layers):
             idx = t20 if l < 24 else t24
-            ref = _attn_ref(oc, b, 0, T, idx[b, 0], sw[l][b], qa[l][b, 0], T, 1.0)
+            ref = _attn_ref(oc[l], b, 0, T, idx[b, 0], sw[l][b], qa[l][b, 0], T, 1.0)
             P.check_attention(outs[j].cpu().numpy()[b, 0], ref, f"step attn L{l}")
 
 
@@ -473,14 +475,14 @@ def test_schedule_step_matches_standalone_calls(hsa):
     """Inside hsa_schedule_step the kernels read step inputs before their dependency wait and a
     Reindex or Reuse-slot attention kernel waits only before its first global write; the
     arithmetic is that of the standalone calls, so the step's indices and outputs equal theirs
-    bit for bit (two requests, a ragged length, slots Full, Reuse, Reindex, Reuse, Reuse)."""
+    bit for bit (two requests, a ragged length, slots Full, Reuse, Reindex, Reuse, Reuse, each
+    slot over its own layer's cache)."""
     H = hsa
     B, T, nq, seed = 2, 12345, 1, 3
     layers = [20, 21, 24, 25, 26]
     modes = [H.HSA_MODE_FULL, H.HSA_MODE_REUSE, H.HSA_MODE_REINDEX, H.HSA_MODE_REUSE, H.HSA_MODE_REUSE]
     cap = round8(T)
-    oc = P.oracle_cache(seed, 20, B, T, cap)
-    cache = gpu_cache(H, oc, cap)
+    cache = {l: gpu_cache(H, P.oracle_cache(seed, l, B, T, cap), cap) for l in layers}
     d_vis = dev(synth.visibility(B, nq, T))
     d_qi = {l: dev_bf16(synth.index_q_bf16(seed, l, B, nq)) for l in (20, 24)}
     d_wi = {l: dev(synth.index_w(seed, l, B, nq)) for l in (20, 24)}
@@ -492,12 +494,12 @@ def test_schedule_step_matches_standalone_calls(hsa):
 
     # standalone calls, one after the other
     t20, pool, t24 = new_idx(), torch.empty(B, nq, 16384, dtype=torch.int32, device="cuda"), new_idx()
-    H.hsa_index_full(cache, d_qi[20], d_wi[20], d_vis, nq, T, t20, pool, ws)
-    H.hsa_index_reindex(cache, d_qi[24], d_wi[24], d_vis, nq, T, pool, t24, ws)
+    H.hsa_index_full(cache[20], d_qi[20], d_wi[20], d_vis, nq, T, t20, pool, ws)
+    H.hsa_index_reindex(cache[24], d_qi[24], d_wi[24], d_vis, nq, T, pool, t24, ws)
     ref = {}
     for l in layers:
         ref[l] = new_out()
-        H.hsa_sparse_attn_decode(cache, d_qa[l], t20 if l < 24 else t24, d_sw[l], d_vis, nq, T, 1.0, ref[l], ws)
+        H.hsa_sparse_attn_decode(cache[l], d_qa[l], t20 if l < 24 else t24, d_sw[l], d_vis, nq, T, 1.0, ref[l], ws)
 
     # the same work as one step
     outs = [new_out() for _ in layers]
@@ -505,7 +507,7 @@ def test_schedule_step_matches_standalone_calls(hsa):
     s_pool = torch.empty_like(pool)
     step = H.StepArgs(modes, [d_qi.get(l) for l in layers], [d_wi.get(l) for l in layers],
                       [d_qa[l] for l in layers], [d_sw[l] for l in layers], outs, tk, s_pool, d_vis, nq, T, 1.0)
-    H.hsa_schedule_step(cache, step, ws)
+    H.hsa_schedule_step([cache[l] for l in layers], step, ws)
     code, flags = H.hsa_get_device_status()
     assert code == 0 and flags == 0
     assert torch.equal(tk[0], t20) and torch.equal(s_pool, pool) and torch.equal(tk[2], t24)
