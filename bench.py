@@ -237,6 +237,14 @@ def per_kernel_times(H, torch, I, reps=10):
 # null.
 NCU_TRAFFIC = {
     # call: (sources its kernels are built from, sha256 over them in order, dram read + write bytes)
+    "sparse_attn_decode": (("attn.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
+                           "16e485aba3ebb21b0917c457c52a70f349b9bac3842a660e90aecd6963da8e89", 10547112),
+    "index_full": (("index.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
+                   "4c03750f6c3c86404916c6f979bef52ff56fa06b08b17e01bbb334078c54d648", 295772562),
+    "index_reindex": (("reindex.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
+                      "6a8b38b5b283d54ba583627962c902e2050c3c800249cafd8c0330b3795fed47", 42806473),
+    "cache_write_m2": (("write.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
+                       "811576158514fa7a2bded13b3c4e8fd8a23e6120363588ffb541b6d88456eebb", 139557120),
 }
 
 
