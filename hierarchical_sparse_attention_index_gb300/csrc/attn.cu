@@ -383,6 +383,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     TMEM_LD32(ta, r);
     TMEM_LD8(ta + 32u, (r + 32));
     tmem_wait_ld();
+    tmem_regs_ready(r);
     const float scl = s_scale[hh];
 #pragma unroll
     for (int i = 0; i < kKeysPerWarp; ++i)
@@ -457,6 +458,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       uint32_t r[32];
       TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mtile + 32 * hc), r);
       tmem_wait_ld();
+      tmem_regs_ready(r);
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int h = 32 * hc + j;

@@ -245,6 +245,9 @@ __global__ void __launch_bounds__(kWThreads, 1) cache_write_kernel(const WritePa
     TMEM_LD8(ta + kTileE, vm);
     TMEM_LD8(ta + 2 * kTileE, vl);
     tmem_wait_ld();
+    tmem_regs_ready(vh);
+    tmem_regs_ready(vm);
+    tmem_regs_ready(vl);
     // the 8 entries as independent chains: value, group max, scale, codes, fragment-order word
     uint32_t word[8], sbs[8];
 #pragma unroll
