@@ -612,7 +612,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_req, 3),
             "step_unit": f"one request's decode step (1/{B} of a batch-{B} step); value is batch-{B} steps/s",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (same seeded workload)",
+            "data": "synthetic (same seeded workload; the oracle reads layer 20's cache for every layer, "
+                    "which does not change its cost)",
             "config": {"workload": CFG.name, "batch_per_gpu": B, "ctx": CFG.T, "nq": CFG.nq,
                        "layers": "20..39 (1 Full, 4 Reindex, 15 Reuse, 20 attention)"},
             "cpu_baseline": {"value": round(value, 4), "unit": "steps/s", "cores": _threads_used(),
