@@ -74,6 +74,9 @@ def check_topk(gpu_row, s, vis, k=512, name="topk"):
     kk = min(k, vis)
     g = gpu_row[gpu_row >= 0]
     assert len(g) == kk, f"{name}: {len(g)} indices, expected {kk}"
+    if kk <= 0:                                    # an empty request: every slot is -1
+        assert np.all(gpu_row == -1), f"{name}: empty request not -1 filled"
+        return 0
     assert np.all(gpu_row[kk:] == -1) and np.all(np.diff(g) > 0), f"{name}: not ascending/-1 padded"
     assert g.min() >= 0 and g.max() < vis
     o = O.topk_ascending(s, vis, k)

@@ -123,7 +123,7 @@ def test_cache_write_rejects_bad_args(hsa):
 # ------------------------------------------------------------------ Full indexer
 FULL_CASES = [  # (B, T, nq)
     (1, 32768, 1), (3, 5000, 1), (1, 1, 1), (1, 7, 1), (1, 9, 1), (1, 511, 1), (1, 513, 1),
-    (1, 16385, 1), (2, 4100, 5), (1, 20000, 2),
+    (1, 16385, 1), (2, 4100, 5), (1, 20000, 2), (1, 3000, 8),
 ]
 
 
@@ -214,7 +214,7 @@ def test_index_full_wait_timeout_and_recovery(hsa):
 
 # ------------------------------------------------------------------ Reindex
 @pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 3000, 1), (1, 200000, 1), (1, 300, 1),
-                                    (1, 50, 2)])
+                                    (1, 50, 2), (1, 3000, 8)])
 def test_index_reindex(hsa, B, T, nq):
     H = hsa
     oc, q, w, vis, cache, ws, topk, pool = _full_case(H, B, T, nq)
@@ -373,7 +373,8 @@ def _attn_ref(oc, b, i, T, topk_row, swa_rows, q, vis, scale, fmt=O.SCALE_E8M0):
     return O.sparse_attention(P.f32(q), rows, scale)
 
 
-@pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 300, 1), (1, 50, 1), (3, 2000, 2)])
+@pytest.mark.parametrize("B,T,nq", [(1, 32768, 1), (2, 4100, 5), (1, 300, 1), (1, 50, 1), (3, 2000, 2),
+                                    (1, 3000, 8)])
 def test_sparse_attention(hsa, B, T, nq):
     H = hsa
     oc, q, w, vis, cache, ws, topk, pool = _full_case(H, B, T, nq)
@@ -388,6 +389,48 @@ def test_sparse_attention(hsa, B, T, nq):
         for i in range(nq):
             ref = _attn_ref(oc, b, i, T, topk[b, i], swa[b], qa[b, i], int(vis[b, i]), 1.0)
             P.check_attention(out[b, i], ref, f"attn b{b} q{i}")
+
+
+def test_ragged_batch_with_empty_request(hsa):
+    """Requests of 0, 5000, 37 and 1 visible positions in one batch, through the Full, Reindex
+    and attention calls: the empty request gets -1 indices, an all -1 pool and a zero output;
+    the others match the oracle."""
+    H = hsa
+    T, seed = 5000, 7
+    vis_h = np.array([[0], [T], [37], [1]], np.int32)
+    B, nq = vis_h.shape
+    cap = round8(T)
+    oc = P.oracle_cache(seed, 20, B, T, cap)
+    cache = gpu_cache(H, oc, cap)
+    q, w = synth.index_q_bf16(seed, 20, B, nq), synth.index_w(seed, 20, B, nq)
+    q2, w2 = synth.index_q_bf16(seed, 24, B, nq), synth.index_w(seed, 24, B, nq)
+    qa, swa = synth.attn_q_bf16(seed, 20, B, nq), synth.swa_e4m3(seed, 20, B, nq)
+    vis = dev(vis_h)
+    ws = H.new_workspace(B, nq, T)
+    topk = torch.full((B, nq, 512), -7, dtype=torch.int32, device="cuda")
+    pool = torch.full((B, nq, 16384), -7, dtype=torch.int32, device="cuda")
+    top2 = torch.full_like(topk, -7)
+    out = torch.full((B, nq, 64, 512), float("nan"), device="cuda")
+    H.hsa_index_full(cache, dev_bf16(q), dev(w), vis, nq, T, topk, pool, ws)
+    H.hsa_index_reindex(cache, dev_bf16(q2), dev(w2), vis, nq, T, pool, top2, ws)
+    H.hsa_sparse_attn_decode(cache, dev_bf16(qa), top2, dev(swa), vis, nq, T, 1.0, out, ws)
+    code, flags = H.hsa_get_device_status()
+    assert code == 0 and flags == 0, (code, flags)
+    topk, pool, top2, out = topk.cpu().numpy(), pool.cpu().numpy(), top2.cpu().numpy(), out.cpu().numpy()
+    assert np.all(topk[0] == -1) and np.all(pool[0] == -1) and np.all(top2[0] == -1) and np.all(out[0] == 0)
+    for b in range(B):
+        v = int(vis_h[b, 0])
+        K = P.dequant_index(oc, b, T)
+        s = O.index_scores(P.f32(q[b, 0]), w[b, 0], K, v)
+        P.check_topk(topk[b, 0], s, v, name=f"ragged topk b{b}")
+        P.check_pool(pool[b, 0], s, v, name=f"ragged pool b{b}")
+        ref2, _ = O.index_reindex(P.f32(q2[b, 0]), w2[b, 0], K, pool[b, 0], v)
+        s2 = O.index_scores(P.f32(q2[b, 0]), w2[b, 0], K, v)
+        assert np.sum(top2[b, 0] >= 0) == np.sum(ref2 >= 0), f"ragged reindex b{b}: count"
+        if v > 0:
+            P.check_set_band(top2[b, 0][top2[b, 0] >= 0], ref2[ref2 >= 0], s2, f"ragged reindex b{b}")
+        ref = _attn_ref(oc, b, 0, T, top2[b, 0], swa[b], qa[b, 0], v, 1.0)
+        P.check_attention(out[b, 0], ref, f"ragged attn b{b}")
 
 
 def test_sparse_attention_scale_and_e4m3_scales(hsa):
