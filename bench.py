@@ -240,7 +240,7 @@ NCU_TRAFFIC = {
     "sparse_attn_decode": (("attn.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
                            "857e717595da7bccd52c19f4fdc7a904a0346b7bd664fe2f00a939fbdff89edf", 10546904),
     "index_full": (("index.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                   "4c03750f6c3c86404916c6f979bef52ff56fa06b08b17e01bbb334078c54d648", 295772562),
+                   "688c80d06741483b09545e536f337a7a50cfccc2d92e4f98650248f043fb4a30", 296137152),
     "index_reindex": (("reindex.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
                       "6a8b38b5b283d54ba583627962c902e2050c3c800249cafd8c0330b3795fed47", 42806473),
     "cache_write_m2": (("write.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),

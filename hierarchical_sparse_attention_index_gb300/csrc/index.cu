@@ -494,8 +494,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
     const int thr = s_thr;
     // f_lo, the smallest float of the threshold bin: a block max below it is neither taken nor
     // listed, which one float compare decides for most blocks. The compare only filters: the
-    // bin of a block that passes is decided on its order key (which tells -0 from +0)
-    const float f_lo = (thr < 0) ? -INFINITY : key_to_float((uint32_t)thr << kHistShift);
+    // bin of a block that passes is decided on its order key (which tells -0 from +0). The
+    // lowest keys of bins 0..7 are NaN patterns (-inf lies in bin 7): there the filter passes
+    // everything, and NaN block maxima always pass, so the filter never changes a decision
+    float f_lo = (thr < 0) ? -INFINITY : key_to_float((uint32_t)thr << kHistShift);
+    if (f_lo != f_lo) f_lo = -INFINITY;
     const int nq4 = (nb + 3) >> 2;                    // float4 chunks
     constexpr int kIlp = 8;
     int listed = 0;                                   // candidates of earlier batches (same in every thread)
@@ -516,7 +519,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
         candm[u] = 0u;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          if (4 * c + k < nb && (f[k] >= f_lo || f[k] == 0.f)) {
+          if (4 * c + k < nb && (f[k] >= f_lo || f[k] == 0.f || f[k] != f[k])) {
             const int bin = (int)(order_key(f[k]) >> kHistShift);
             if (thr < 0 || bin > thr) take |= 1u << k;
             else if (bin == thr) candm[u] |= 1u << k;
