@@ -238,7 +238,7 @@ def per_kernel_times(H, torch, I, reps=10):
 NCU_TRAFFIC = {
     # call: (sources its kernels are built from, sha256 over them in order, dram read + write bytes)
     "sparse_attn_decode": (("attn.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
-                           "857e717595da7bccd52c19f4fdc7a904a0346b7bd664fe2f00a939fbdff89edf", 10546904),
+                           "69b9fdcf90f316f622ebc1d4ae85f1d2e057cfa9d8d1ed6e9bf250111c3758d4", 10548787),
     "index_full": (("index.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
                    "688c80d06741483b09545e536f337a7a50cfccc2d92e4f98650248f043fb4a30", 296137152),
     "index_reindex": (("reindex.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),

@@ -22,8 +22,9 @@
 //  4. the MMA warp runs O^T[512 dims][64 heads] = V^T . P^T, reading the same tile as an
 //     MN-major A operand (K = V = the 512-d latent), one 128-dim M-tile at a time;
 //  5. each worker drains one output dimension of a finished M-tile, normalised by l_c: the 48
-//     heads the other CTAs combine go to the workspace (L2) as f16 pairs, this CTA's own 16
-//     stay in registers in fp32. (m_c, l_c) of the 16 heads a peer owns go straight into the
+//     heads the other CTAs combine go to the workspace (L2) as f16, 8 heads per 16-byte unit
+//     (a warp stores 32 consecutive dimensions of a unit: 512 contiguous bytes), this CTA's own
+//     16 stay in registers in fp32. (m_c, l_c) of the 16 heads a peer owns go straight into the
 //     peer's shared memory before PV (cluster barrier phase A), the partials after (phase B);
 //     each CTA then forms its 16 heads as sum_c w_c (O_c / l_c), w_c = exp(m_c - M) l_c /
 //     sum_c' exp(m_c' - M) l_c', over c in rank order (deterministic). L2 moves the partials
@@ -444,8 +445,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 
   // ---------------------------------------------------------------- partial O / l -> L2
   // Warp (quadrant qd = w & 3, tile mt = w >> 2) owns output dimension d = 128 mt + 32 qd + lane
-  // for all 64 heads: it sends the 48 heads other CTAs combine to the workspace (L2) as f16
-  // pairs [h / 2][d] and keeps this CTA's own 16 heads in registers (fp32).
+  // for all 64 heads: it sends the 48 heads other CTAs combine to the workspace (L2) as f16,
+  // [h / 8][d] units of 8 heads, and keeps this CTA's own 16 heads in registers (fp32).
   if (p.topk_ready) griddep_wait();   // the previous kernel may still read the partials workspace
   const int qd = warp & 3, mtile = warp >> 2;
   const int dim = 128 * mtile + 32 * qd + lane;
@@ -459,6 +460,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       TMEM_LD32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kColO + 64 * mtile + 32 * hc), r);
       tmem_wait_ld();
       tmem_regs_ready(r);
+      uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int h = 32 * hc + j;
@@ -468,10 +470,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
         if ((h >> 4) == (int)rank) {
           own[h & 15] = o0;
           own[(h & 15) + 1] = o1;
-        } else {
-          const __half2 v = __floats2half2_rn(o0, o1);
-          __stcg(mine + (size_t)(h >> 1) * kDLat + dim, *reinterpret_cast<const uint32_t*>(&v));
         }
+        const __half2 v = __floats2half2_rn(o0, o1);
+        pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+      // 8 heads (4 pairs) per 16-byte unit: group G = 4 hc + u covers heads 8G .. 8G + 7
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int G = 4 * hc + u;
+        if ((G >> 1) != (int)rank)
+          __stcg(reinterpret_cast<uint4*>(mine) + (size_t)G * kDLat + dim,
+                 make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
       }
     }
   }
@@ -524,13 +533,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = own[j];
       } else {
-        const uint32_t* src = part + (size_t)c * kPartFloats + (size_t)(8 * rank) * kDLat + dim;
+        // this CTA's heads 16 rank .. + 15 are groups 2 rank and 2 rank + 1 of peer c's partial
+        const uint4* src = reinterpret_cast<const uint4*>(part + (size_t)c * kPartFloats) + (size_t)(2 * rank) * kDLat + dim;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t u = __ldcg(src + (size_t)j * kDLat);
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
-          v[2 * j] = f.x;
-          v[2 * j + 1] = f.y;
+        for (int g2 = 0; g2 < 2; ++g2) {
+          const uint4 u4 = __ldcg(src + (size_t)g2 * kDLat);
+          const uint32_t uu[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&uu[j]));
+            v[8 * g2 + 2 * j] = f.x;
+            v[8 * g2 + 2 * j + 1] = f.y;
+          }
         }
       }
 #pragma unroll
