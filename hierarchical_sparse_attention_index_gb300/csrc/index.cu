@@ -435,6 +435,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
   __shared__ uint32_t s_psel[kPosCand / 32];
   griddep_wait();
   griddep_launch_dependents();
+  const float* bm = p.blkmax + (size_t)row * p.ld_b;
+  // The block pass's first batch of block maxima (eight float4 per thread) goes in flight with
+  // the histogram loads instead of after the threshold is known. Its bound comes from max_vis
+  // (the row stride ld_b covers it, rounded up to 64 blocks); chunks past this row's vis hold
+  // values of no block and are masked by the block bound in the pass.
+  constexpr int kIlp = 8;
+  float4 v[kIlp];
+  {
+    const int nq4_max = (int)(((p.max_vis + kBlk - 1) / kBlk + 3) >> 2);
+#pragma unroll
+    for (int u = 0; u < kIlp; ++u) {
+      const int c = u * kSelThreads + tid;
+      v[u] = (c < nq4_max) ? __ldcg(reinterpret_cast<const float4*>(bm) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   const int vis = (int)imin64(imax64(__ldg(p.vis + row), 0), p.max_vis);
   const int nb = (vis + kBlk - 1) / kBlk;
   const int nwb = (nb + 31) >> 5;                     // bitmap words
@@ -442,7 +457,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
   uint32_t* bits = reinterpret_cast<uint32_t*>(fsm_raw);                 // [nwb4] selected blocks
   const int nwb4 = (nwb + 3) & ~3;
   uint64_t* cst = reinterpret_cast<uint64_t*>(bits + nwb4);             // [kSelStage] staged candidates
-  const float* bm = p.blkmax + (size_t)row * p.ld_b;
   int32_t* gcand = p.cand + (size_t)row * p.ld_cand + (size_t)rank * p.ld_b;   // candidates past the stage
   uint32_t* gh = p.hist + (size_t)row * kHistBins;
 
@@ -488,8 +502,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
   // ---------------------------------------------------------------- 2. one pass over the block maxima
   // Blocks above the threshold bin are taken at once; blocks in it are listed as candidates
   // (composites staged in shared memory, block indices in the workspace past the stage). Per
-  // batch of 2,048 float4 (eight loads per thread in flight), each thread counts its
-  // candidates and one block-wide exclusive scan places them: no shared counter is contended.
+  // batch of 4,096 float4 (eight loads per thread; the next batch's loads are issued before this
+  // one is classified), each thread counts its candidates and one block-wide exclusive scan
+  // places them: no shared counter is contended.
   {
     const int thr = s_thr;
     // f_lo, the smallest float of the threshold bin: a block max below it is neither taken nor
@@ -500,21 +515,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
     float f_lo = (thr < 0) ? -INFINITY : key_to_float((uint32_t)thr << kHistShift);
     if (f_lo != f_lo) f_lo = -INFINITY;
     const int nq4 = (nb + 3) >> 2;                    // float4 chunks
-    constexpr int kIlp = 8;
     int listed = 0;                                   // candidates of earlier batches (same in every thread)
     for (int c0 = 0; c0 < nq4; c0 += kIlp * kSelThreads) {
-      float4 v[kIlp];
+      float4 cur[kIlp];
 #pragma unroll
-      for (int u = 0; u < kIlp; ++u) {
-        const int c = c0 + u * kSelThreads + tid;
-        v[u] = (c < nq4) ? __ldcg(reinterpret_cast<const float4*>(bm) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kIlp; ++u) cur[u] = v[u];
+      if (c0 + kIlp * kSelThreads < nq4) {
+#pragma unroll
+        for (int u = 0; u < kIlp; ++u) {
+          const int c = c0 + (kIlp + u) * kSelThreads + tid;
+          v[u] = (c < nq4) ? __ldcg(reinterpret_cast<const float4*>(bm) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
       uint32_t candm[kIlp];
       int n = 0;
 #pragma unroll
       for (int u = 0; u < kIlp; ++u) {
         const int c = c0 + u * kSelThreads + tid;
-        const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const float f[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
         uint32_t take = 0u;
         candm[u] = 0u;
 #pragma unroll
@@ -534,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSelThreads) select_
 #pragma unroll
       for (int u = 0; u < kIlp; ++u) {
         const int c = c0 + u * kSelThreads + tid;
-        const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const float f[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
         uint32_t m = candm[u];
         while (m) {
           const int k = __ffs(m) - 1;
