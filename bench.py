@@ -238,11 +238,11 @@ def per_kernel_times(H, torch, I, reps=10):
 NCU_TRAFFIC = {
     # call: (sources its kernels are built from, sha256 over them in order, dram read + write bytes)
     "sparse_attn_decode": (("attn.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
-                           "69b9fdcf90f316f622ebc1d4ae85f1d2e057cfa9d8d1ed6e9bf250111c3758d4", 10548787),
+                           "40083dc6f295b9e1a349f456a5cc471ef7001d2b6a6132386329ea5e1938c154", 10546564),
     "index_full": (("index.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                   "688c80d06741483b09545e536f337a7a50cfccc2d92e4f98650248f043fb4a30", 296137152),
+                   "1cf8cfe0ee487801efaa13dd63d40e95467acc8eb7dc056fc91864c057a349b0", 295708453),
     "index_reindex": (("reindex.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                      "6a8b38b5b283d54ba583627962c902e2050c3c800249cafd8c0330b3795fed47", 42806473),
+                      "f2d0d5dd739ba42aa76d8597a831362a09851aa24ee9f136b241bcceffd08153", 42805495),
     "cache_write_m2": (("write.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
                        "11bf0e4150a5857cff883df2eccf414441b0b5ba87cbadd9c2331a00caf53070", 139710720),
 }

@@ -182,8 +182,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   }
   // A Reuse slot of schedule_step reads nothing the previous kernel wrote (its top-k is two or
   // more kernels old): it waits only before its first global write, the partials drain.
+  // The next kernel is released once the key tile is converted (worker warps) and QK is issued
+  // (MMA warp), not here: released at the top, its early CTAs' loads compete with this kernel's
+  // gathers while its later CTAs still wait for SMs (measured: 0.5 % slower per step; with no
+  // release before exit, 6 % slower).
   if (!p.topk_ready) griddep_wait();
-  griddep_launch_dependents();
   if (!p.inputs_ready) {
     issue_query();
     load_swa();
@@ -215,6 +218,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       if (!ok) flag_status(p.status, HSA_FLAG_TIMEOUT);
     }
     __syncwarp();
+    griddep_launch_dependents();
     named_bar_sync(2, kAttnThreads);  // P^T written by the worker warps
     if (lane == 0) {
       tc_fence_after();
@@ -362,6 +366,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
     if (lane == 0) mbar_arrive(kb_bar + 8u * s4);
   }
   if (qq == 0) s_valid[krow] = kval ? 1 : 0;
+  griddep_launch_dependents();
 
   if (!mbar_wait(bar, 0, p.wait_ns) && tid == 0) flag_status(p.status, HSA_FLAG_TIMEOUT);
   tc_fence_after();

@@ -97,9 +97,9 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   if (tid < kScrInts) scr[tid] = 0;
   // Inside schedule_step everything this kernel reads was complete before it was launched (the
   // pool two or more kernels earlier, q, w and vis before the step), so it scores while the
-  // previous kernel drains and waits for it only before its first global write.
+  // previous kernel drains and waits for it only before its first global write. The next
+  // kernel is released after the scoring, whose gathers it would otherwise slow down.
   if (!p.inputs_ready) griddep_wait();
-  griddep_launch_dependents();
 
   const int vis = __ldg(p.vis + row);
   const int32_t* pool_row = p.pool + (size_t)row * p.pool_ld;
@@ -162,6 +162,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   }
   __syncthreads();
 
+  griddep_launch_dependents();
   if (p.inputs_ready) griddep_wait();
   // ---------------------------------------------------------------- 2. publish this CTA's own top region
   // scr: [0, 32) scan scratch; 64, 65 threshold bin and count above it; 72 published count;
