@@ -218,16 +218,21 @@ def per_kernel_times(H, torch, I, reps=10):
             with torch.cuda.graph(g, stream=st):
                 fn(st)
         torch.cuda.synchronize()
-        for _ in range(2):
-            g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # warm-up and timed replays on the one stream: replays of the same calls on two streams
+        # would run at once on the shared workspace
         with torch.cuda.stream(st):
+            for _ in range(2):
+                g.replay()
             e0.record(st)
             for _ in range(reps):
                 g.replay()
             e1.record(st)
         torch.cuda.synchronize()
         out[key] = 1e-3 * e0.elapsed_time(e1) / (reps * calls)       # seconds per call
+    code, flags = H.hsa_get_device_status()
+    if code != 0 or flags != 0:
+        raise RuntimeError(f"device status after the per-call timing: code {code} flags {flags}")
     return out
 
 
