@@ -92,6 +92,19 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Plain global loads (coherent, cached in L1) for the gathered cache rows, which the cache
+// writer may have produced: unlike ld.global.nc they cannot be served before the dependency wait
+// (the L2-only ld.global.cg costs 6 % of the decode step here)
+__device__ __forceinline__ uint4 ld_global_v4(const uint4* ptr) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_global_u16(const uint16_t* ptr) {
+  unsigned short v;
+  asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(ptr));
+  return v;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -253,9 +266,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   // 64 contiguous bytes (4 lanes q x 16 B), so every sector fetched is used whole, and in the
   // shared-memory stores that follow, the 8 lanes of each store phase write 8 different rows.
   // top-k rows: warp w owns rows 8w + rr; step s takes code chunk j = 4 s + qq (dims 32j..32j+31).
-  // The row index goes first: the row loads depend on it.
+  // The row index goes first: the row loads depend on it. The indices and the cache rows are
+  // other kernels' outputs: coherent loads only (see griddep_wait)
   const int krow = 8 * warp + rr;
-  const int kidx = __ldg(p.topk + (size_t)row * kTopK + rank * kTopRows + krow);
+  const int kidx = __ldcg(p.topk + (size_t)row * kTopK + rank * kTopRows + krow);
   const bool sval = (vis - kSwa + 32 * (int)rank + srow) >= 0;
   uint4 kc[4];
   uint32_t ks2[4];
@@ -266,8 +280,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) {
       const int j = 4 * s4 + qq;
-      kc[s4] = __ldg(reinterpret_cast<const uint4*>(p.kv_q + e * 256) + j);
-      ks2[s4] = __ldg(reinterpret_cast<const uint16_t*>(p.kv_s + e * 32) + j);
+      kc[s4] = ld_global_v4(reinterpret_cast<const uint4*>(p.kv_q + e * 256) + j);
+      ks2[s4] = ld_global_u16(reinterpret_cast<const uint16_t*>(p.kv_s + e * 32) + j);
     }
   }
 

@@ -214,6 +214,12 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 // Programmatic dependent launch: wait for the preceding kernel in the stream (and its memory),
 // and let the next kernel start its own setup early.
+// Anything another kernel of a programmatic-launch chain writes (the cache, a top-k, the pool)
+// is read with coherent loads (ld.global, ld.global.cg), never through the non-coherent path
+// (ld.global.nc, __ldg): that path requires the data to stay unchanged for the reading kernel's
+// whole lifetime, and under programmatic launch the reader starts while the writer may still be
+// running, so a non-coherent load may be served before this wait has returned. Only data no
+// kernel of the library writes (queries, weights, lengths, window rows) goes through __ldg.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -113,10 +113,11 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   const int64_t ebase = (int64_t)(row / p.nq) * p.cap;
   const uint32_t ring = smem_u32(rsm + kOffRing) + (uint32_t)(warp * kRxRing) * (kGrpCodes + kGrpScales);
   int* slots = reinterpret_cast<int*>(rsm + kOffSlots) + warp * kRxRing * 32;
-  // a group's pool values are loaded one gather ahead, so a gather never waits for them
+  // a group's pool values are loaded one gather ahead, so a gather never waits for them. The
+  // pool is another kernel's output: coherent loads only (see griddep_wait)
   auto pool_val = [&](int grp) {
     if (grp >= ngroups) return -1;
-    return __ldg(pool_row + (grp < kGroups ? slot0 + 32 * grp : kPool + 32 * warp) + lane);
+    return __ldcg(pool_row + (grp < kGroups ? slot0 + 32 * grp : kPool + 32 * warp) + lane);
   };
   auto gather = [&](int grp, int pv) {
     const int rs = grp % kRxRing;
@@ -377,7 +378,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
   while (mine) {
     const int i = __ffs(mine) - 1;
     mine &= mine - 1u;
-    if (at < kTopK) out[at] = __ldg(pl + i);
+    if (at < kTopK) out[at] = __ldcg(pl + i);
     ++at;
   }
   if (has_tail) {
@@ -389,7 +390,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     while (mt) {
       const int i = __ffs(mt) - 1;
       mt &= mt - 1u;
-      if (at2 < kTopK) out[at2] = __ldg(plt + i);
+      if (at2 < kTopK) out[at2] = __ldcg(plt + i);
       ++at2;
     }
   }

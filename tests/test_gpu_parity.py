@@ -514,6 +514,106 @@ def test_schedule_step(hsa):
             P.check_attention(outs[j].cpu().numpy()[b, 0], ref, f"step attn L{l}")
 
 
+def test_chained_calls_read_fresh_outputs(hsa):
+    """Every call is launched with programmatic dependent launch: a kernel starts while its
+    predecessor may still run, and must read what the predecessor writes (cache rows, the pool,
+    a top-k) only after its dependency wait and through coherent loads. Before each chained
+    round, every index buffer is filled with the other query's valid, different result (plain
+    copies, which complete before the chain starts), so a read that overtakes its producer
+    returns another in-range index set; the latent sets alternate, so an early row read returns
+    other rows. Each reader directly follows its producer: cache write -> attention, Full ->
+    Reindex (pool), Reindex -> attention (top-k), Full -> attention (top-k); then the same work
+    as one schedule_step. Every round must equal the same calls separated by synchronisations,
+    bit for bit, with no device flag. Batch 16 at 65,536 positions keeps each producer running
+    long enough for an early read to land before its writes."""
+    H = hsa
+    B, T, nq = 16, 65536, 1
+    torch.manual_seed(11)
+    W = (torch.randn(512, 128, device="cuda") / 22.6).to(torch.bfloat16)
+    lat = [torch.randn(B, T, 512, device="cuda").to(torch.bfloat16) for _ in range(2)]
+    qi = [torch.randn(B, nq, 16, 128, device="cuda").to(torch.bfloat16) for _ in range(2)]
+    wi = torch.rand(B, nq, 16, device="cuda")
+    qi2 = torch.randn(B, nq, 16, 128, device="cuda").to(torch.bfloat16)
+    qa = (torch.randn(B, nq, 64, 512, device="cuda") / 22.6).to(torch.bfloat16)
+    swa = torch.randn(B, 128 + nq - 1, 512, device="cuda").to(torch.float8_e4m3fn).view(torch.uint8)
+    vis = torch.full((B, nq), T, dtype=torch.int32, device="cuda")
+    fixed = torch.randint(0, T, (B, nq, 512), dtype=torch.int32, device="cuda")
+    cache = H.Cache(B, T, 1)
+    ws = H.new_workspace(B, nq, T)
+    topk = torch.empty(B, nq, 512, dtype=torch.int32, device="cuda")
+    top2 = torch.empty_like(topk)
+    pool = torch.empty(B, nq, 16384, dtype=torch.int32, device="cuda")
+    out = [torch.empty(B, nq, 64, 512, device="cuda") for _ in range(3)]
+
+    def flags_clear(tag):
+        code, flags = H.hsa_get_device_status()
+        assert code == 0 and flags == 0, (tag, code, flags)
+
+    def calls(c, q, sync, stale=None):
+        fence = torch.cuda.synchronize if sync else (lambda: None)
+        if stale is not None:
+            topk.copy_(stale[1])
+            pool.copy_(stale[2])
+            top2.copy_(stale[3])
+        H.hsa_cache_write_compress(cache, lat[c], None, W, T, None)
+        fence()
+        H.hsa_sparse_attn_decode(cache, qa, fixed, swa, vis, nq, T, 1.0, out[0], ws)
+        fence()
+        H.hsa_index_full(cache, qi[q], wi, vis, nq, T, topk, pool, ws)
+        fence()
+        H.hsa_index_reindex(cache, qi2, wi, vis, nq, T, pool, top2, ws)
+        fence()
+        H.hsa_sparse_attn_decode(cache, qa, top2, swa, vis, nq, T, 1.0, out[1], ws)
+        torch.cuda.synchronize()
+        res = [out[0].clone(), topk.clone(), pool.clone(), top2.clone(), out[1].clone()]
+        if stale is not None:
+            topk.copy_(stale[1])
+        H.hsa_index_full(cache, qi[q], wi, vis, nq, T, topk, pool, ws)
+        fence()
+        H.hsa_sparse_attn_decode(cache, qa, topk, swa, vis, nq, T, 1.0, out[2], ws)
+        torch.cuda.synchronize()
+        flags_clear(("calls", c, q, sync))
+        return res + [out[2].clone()]
+
+    modes = [H.HSA_MODE_FULL, H.HSA_MODE_REUSE, H.HSA_MODE_REINDEX, H.HSA_MODE_REUSE]
+    s_out = [torch.empty_like(out[0]) for _ in modes]
+    s_tk = [torch.empty_like(topk), None, torch.empty_like(topk), None]
+    s_pool = torch.empty_like(pool)
+    q_step = torch.empty_like(qi[0])
+    step = H.StepArgs(modes, [q_step, None, qi2, None], [wi, None, wi, None], [qa] * 4, [swa] * 4, s_out, s_tk,
+                      s_pool, vis, nq, T, 1.0)
+
+    def stepped(c, q, stale):
+        s_tk[0].copy_(stale[1])
+        s_pool.copy_(stale[2])
+        s_tk[2].copy_(stale[3])
+        q_step.copy_(qi[q])
+        H.hsa_cache_write_compress(cache, lat[c], None, W, T, None)
+        H.hsa_schedule_step(cache, step, ws)
+        torch.cuda.synchronize()
+        flags_clear(("step", c, q))
+        return [s_tk[0].clone(), s_pool.clone(), s_out[0].clone(), s_out[1].clone(), s_tk[2].clone(),
+                s_out[2].clone(), s_out[3].clone()]
+
+    ref = {(c, q): calls(c, q, True) for c in (0, 1) for q in (0, 1)}
+    # the queries give different index sets and the latent sets different rows, else the
+    # rounds would show nothing
+    assert not torch.equal(ref[(0, 0)][2], ref[(0, 1)][2]) and not torch.equal(ref[(0, 0)][3], ref[(0, 1)][3])
+    assert not torch.equal(ref[(0, 0)][0], ref[(1, 0)][0])
+    names = ("attention after the cache write", "Full top-k", "pool", "Reindex top-k",
+             "attention on the Reindex top-k", "attention on the Full top-k")
+    slots = ("Full top-k", "pool", "Full slot output", "Reuse slot output", "Reindex top-k",
+             "Reindex slot output", "second Reuse slot output")
+    for c, q in [(0, 0), (1, 1), (0, 1), (1, 0)] * 2:
+        want = ref[(c, q)]
+        stale = ref[(c, 1 - q)]
+        for name, x, y in zip(names, calls(c, q, False, stale), want):
+            assert torch.equal(x, y), f"chained calls, latents {c}, query {q}: {name} differs"
+        o0, tk_r, pool_r, t2_r, o2_r, o1_r = want
+        for name, x, y in zip(slots, stepped(c, q, stale), (tk_r, pool_r, o1_r, o1_r, t2_r, o2_r, o2_r)):
+            assert torch.equal(x, y), f"schedule_step, latents {c}, query {q}: {name} differs"
+
+
 def test_schedule_step_matches_standalone_calls(hsa):
     """Inside hsa_schedule_step the kernels read step inputs before their dependency wait and a
     Reindex or Reuse-slot attention kernel waits only before its first global write; the
