@@ -243,13 +243,13 @@ def per_kernel_times(H, torch, I, reps=10):
 NCU_TRAFFIC = {
     # call: (sources its kernels are built from, sha256 over them in order, dram read + write bytes)
     "sparse_attn_decode": (("attn.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
-                           "40083dc6f295b9e1a349f456a5cc471ef7001d2b6a6132386329ea5e1938c154", 10546564),
+                           "d3c96c7934b41319b8b30475ef29bab357a86f3288bbd01a318cc1c3658a8859", 10546634),
     "index_full": (("index.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                   "1cf8cfe0ee487801efaa13dd63d40e95467acc8eb7dc056fc91864c057a349b0", 295708453),
+                   "aa44542a0133d086c5c9a0541b0792f1345628e4da393ae7c494504b8eb7165f", 295804453),
     "index_reindex": (("reindex.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                      "f2d0d5dd739ba42aa76d8597a831362a09851aa24ee9f136b241bcceffd08153", 42805495),
+                      "b0eb3a2205aca687845efab617211742fd00c9134e181d281c2ebeb2ae5a2251", 42805568),
     "cache_write_m2": (("write.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
-                       "11bf0e4150a5857cff883df2eccf414441b0b5ba87cbadd9c2331a00caf53070", 139710720),
+                       "09da3a295656c1422482be72e3ac22d90af198f2189e757a27951607244f3312", 137599573),
 }
 
 
