@@ -238,12 +238,30 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     for (int d = 1; d < kRxCluster; ++d) c += (i >= ubase[d]) ? 1 : 0;
     return c;
   };
+  // thread tid stages union entries tid, tid + 512, ...: a round issues all eight of its remote
+  // loads before it uses any, so their latencies overlap
+  constexpr int kUnionRound = 8;
+  for (int i0 = 0; i0 < U; i0 += kUnionRound * kRxThreads) {
+    uint64_t v[kUnionRound];
 #pragma unroll
-  for (int c = 0; c < kRxCluster; ++c) {
-    for (int j = tid; j < cnt[c]; j += kRxThreads) {
-      const uint64_t comp = ld_cluster_u64(lst_c[c] + 8u * (uint32_t)j);
-      ust[ubase[c] + j] = comp;
-      atomicAdd(hist + bin_of(comp), 1u);
+    for (int k = 0; k < kUnionRound; ++k) {
+      const int i = i0 + k * kRxThreads + tid;
+      if (i < U) {
+        const int c = cta_of(i);
+        uint32_t at = lst_c[0] + 8u * (uint32_t)(i - ubase[0]);
+#pragma unroll
+        for (int d = 1; d < kRxCluster; ++d)
+          if (c == d) at = lst_c[d] + 8u * (uint32_t)(i - ubase[d]);
+        v[k] = ld_cluster_u64(at);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kUnionRound; ++k) {
+      const int i = i0 + k * kRxThreads + tid;
+      if (i < U) {
+        ust[i] = v[k];
+        atomicAdd(hist + bin_of(v[k]), 1u);
+      }
     }
   }
   cluster_arrive();                   // done with the peers' lists (waited for before exit)
