@@ -247,7 +247,7 @@ NCU_TRAFFIC = {
     "index_full": (("index.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
                    "aa44542a0133d086c5c9a0541b0792f1345628e4da393ae7c494504b8eb7165f", 295804453),
     "index_reindex": (("reindex.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                      "b0eb3a2205aca687845efab617211742fd00c9134e181d281c2ebeb2ae5a2251", 42805568),
+                      "b953591c5d782a32b7b4c992d0aa318acd3f74847202b420ec057cf711e27ef2", 42810871),
     "cache_write_m2": (("write.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
                        "09da3a295656c1422482be72e3ac22d90af198f2189e757a27951607244f3312", 137599573),
 }
