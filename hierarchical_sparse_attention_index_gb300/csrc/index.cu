@@ -246,7 +246,6 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
     const int nrows = dead ? 0 : max(0, min(kChunk, vmax_seg - c * kChunk));
 
     if (warp * 32 < nrows) {
-      const bool two = warp * 32 + 16 < nrows;        // the warp's second 16-row tile holds data
       const uint32_t sf_base = smem_u32(smem + L.sfl) + (uint32_t)warp * 512u;
       stage_group_scales(scales, row_off, sf_base, lane);
       // this lane's row after the reduce-scatter: rows 8t .. 8t+7 of the warp's 32 are the
@@ -254,7 +253,10 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
       const int r_mine = warp * 32 + 8 * t + g;
       for (int ql = 0; ql < nql; ++ql) {
         if (nql > 1) load_query_regs(ql);
-        float v = score_rows32(codes, row_off, sf_base, two, B, wr, lane);
+        // both 16-row tiles are always scored, so the compiler can interleave their independent
+        // convert and MMA chains (a conditional second tile serialised them: Full call 92.2 ->
+        // 89.4 us); rows past the stage's data hold stale bytes and are masked just below
+        float v = score_rows32(codes, row_off, sf_base, true, B, wr, lane);
         const bool ok = c * kChunk + r_mine < svis[ql];
         v = ok ? v : -INFINITY;
         {
