@@ -113,10 +113,11 @@ __device__ __forceinline__ void stage_group_scales(uint32_t scales, int row_off,
   __syncwarp();
 }
 
-// Scores of the warp's 32 rows (codes: 64 bytes per row in fragment order, rows from row_off;
-// `two`: the second 16-row tile holds data). Returns the score of row 8t + g (g = lane / 4,
-// t = lane % 4), i.e. the 16-head ReLU-weighted sum before any visibility mask.
-__device__ __forceinline__ float score_rows32(uint32_t codes, int row_off, uint32_t sf_base, bool two,
+// Scores of the warp's 32 rows (codes: 64 bytes per row in fragment order, rows from row_off).
+// Returns the score of row 8t + g (g = lane / 4, t = lane % 4), i.e. the 16-head ReLU-weighted
+// sum before any visibility mask. Both 16-row tiles are always scored (their independent chains
+// interleave); the caller masks rows that hold no data.
+__device__ __forceinline__ float score_rows32(uint32_t codes, int row_off, uint32_t sf_base,
                                               const uint32_t (&B)[2][8][2], const float (&wr)[2][2], int lane) {
   const int g = lane >> 2, t = lane & 3;
   const uint32_t a_base = codes + (uint32_t)(row_off + g) * 64u + 16u * t;
@@ -124,7 +125,6 @@ __device__ __forceinline__ float score_rows32(uint32_t codes, int row_off, uint3
   float vp[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
-    if (mt == 1 && !two) break;
     const uint4 A0 = lds128_u(a_base + (uint32_t)mt * 1024u);
     const uint4 A1 = lds128_u(a_base + (uint32_t)mt * 1024u + 512u);
     const uint4 SF0 = lds128_u(sf_base + (uint32_t)(16 * mt + g) * 16u);

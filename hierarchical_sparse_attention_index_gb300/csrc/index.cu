@@ -256,7 +256,7 @@ __global__ void __maxnreg__(96) index_scan_kernel(const ScanParams p) {
         // both 16-row tiles are always scored, so the compiler can interleave their independent
         // convert and MMA chains (a conditional second tile serialised them: Full call 92.2 ->
         // 89.4 us); rows past the stage's data hold stale bytes and are masked just below
-        float v = score_rows32(codes, row_off, sf_base, true, B, wr, lane);
+        float v = score_rows32(codes, row_off, sf_base, B, wr, lane);
         const bool ok = c * kChunk + r_mine < svis[ql];
         v = ok ? v : -INFINITY;
         {

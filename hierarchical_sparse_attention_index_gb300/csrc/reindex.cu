@@ -153,7 +153,7 @@ __global__ void __cluster_dims__(kRxCluster, 1, 1) __launch_bounds__(kRxThreads,
     const int rs = k % kRxRing;
     const uint32_t codes = ring + (uint32_t)rs * (kGrpCodes + kGrpScales);
     stage_group_scales(codes + kGrpCodes, 0, sf_base, lane);
-    float v = score_rows32(codes, 0, sf_base, true, B, wr, lane);
+    float v = score_rows32(codes, 0, sf_base, B, wr, lane);
     const bool ok = slots[rs * 32 + 8 * t + g] >= 0;
     v = ok ? v : -INFINITY;
     const int ls = (k < kGroups ? kSlotsPerWarp * warp + 32 * k : kSlotsPerCta + 32 * warp) + 8 * t + g;   // CTA-local slot
