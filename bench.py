@@ -245,9 +245,9 @@ NCU_TRAFFIC = {
     "sparse_attn_decode": (("attn.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
                            "d3c96c7934b41319b8b30475ef29bab357a86f3288bbd01a318cc1c3658a8859", 10546634),
     "index_full": (("index.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                   "aa44542a0133d086c5c9a0541b0792f1345628e4da393ae7c494504b8eb7165f", 295804453),
+                   "e7e1832045c8493913a3565d22f087db7648e34d44756010821da641e438ff60", 295897271),
     "index_reindex": (("reindex.cu", "hsa_common.cuh", "hsa_hist.cuh", "hsa_score.cuh", "hsa_internal.h"),
-                      "b953591c5d782a32b7b4c992d0aa318acd3f74847202b420ec057cf711e27ef2", 42810871),
+                      "2760977bd93d9ece40d12dc5b97e5e53fead391fe7c30c38651cde7d308e5b6b", 42809335),
     "cache_write_m2": (("write.cu", "hsa_common.cuh", "hsa_tc.cuh", "hsa_internal.h"),
                        "09da3a295656c1422482be72e3ac22d90af198f2189e757a27951607244f3312", 137599573),
 }
